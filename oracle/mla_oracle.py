@@ -1,0 +1,219 @@
+"""fp64 CPU oracle for absorbed MLA decode.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  It shares no code with
+the CUDA path (``mla_latent_kv_absorbed_gb300``) and imports nothing from it:
+inputs arrive as plain numpy arrays (bf16 values as uint16 bit patterns) and are
+widened to float64 exactly before any arithmetic.
+
+What it computes (the plain definition; the kernel reaches the same result up
+to rounding order):
+
+  for request b and head h, with K_b = the cache rows named by
+  kv_indices[kv_indptr[b]:kv_indptr[b+1]] (shape [L_b, 576]) and
+  q = [q_nope[b,h], q_rope[b,h]] (576 wide):
+      s_t  = sm_scale * (q_nope . c_t + q_rope . k_rope_t)           (dual-path score)
+      lse  = ln sum_t exp(s_t)                                        (natural log, of the SCALED scores)
+      out  = sum_t softmax(s)_t * c_t                                 (the latent is the value)
+
+Sources, by page and section:
+  * "实现差距：MLA 与 DeepSeek V3", section 2.4 "MLA Pallas Kernel (V2 生产版本)",
+    core computation: s = (s_nope + s_pe) * sm_scale, an FA2-style online
+    softmax, then p times kv_c with kv_c serving as the value.  The oracle
+    takes the softmax in one pass (max, then exp) instead of online.
+  * same page, section 2.1 "Absorbed MLA 投影流程": kv_a_proj_with_mqa gives a
+    576-wide row split as kv_latent (512) then k_rope (64) -- the row layout.
+  * "Attention backends", paragraph "MLA": one 576-wide vector per token, 576
+    wide for k and 512 for v, shared by all query heads.
+  * "Attention backends", paragraph "FlashAttention": Flash-Decoding splits the
+    keys across blocks and merges partial results with the same rescaling --
+    ``merge_states``.
+  * "MLA and torch.compile: v0.3's two sources", section "MLA: starting from a
+    439-line commit": kv_b_proj split into w_kc and w_vc; decode multiplies
+    q_nope by w_kc before attention and the latent output by w_vc after it --
+    ``absorb_weights``, ``absorbed_attention``, ``decompressed_attention``.
+  * same page, "Exercises", exercise 1: multiply-accumulate counts of the
+    absorbing and decompressing paths -- ``mac_counts``.
+
+Pins (tests/test_oracle_pins.py, CPU only): the absorption identity against a
+decompressed multi-head attention evaluated with scipy's softmax; brute-force
+closed forms for 1-3 tokens; split-and-merge equals the unsplit result;
+invariance under relabelling cache slots; all-equal rows and q = 0 closed
+forms; the MAC counts printed in exercise 1 (tests/golden/).  Every function
+here is pinned by at least one of them.
+
+Readings taken where the pages are silent: the rope key sits at columns
+[512, 576) of a row; the LSE is natural-log and of the scaled scores; an empty
+request gives out = 0 and lse = -inf; merging skips partials whose lse is -inf;
+a slot named twice in one request counts twice.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+KV_LORA_RANK = 512
+QK_ROPE_HEAD_DIM = 64
+KV_ROW = KV_LORA_RANK + QK_ROPE_HEAD_DIM
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def gather_rows(kv_cache_bits: np.ndarray, kv_indices: np.ndarray, begin: int, end: int) -> np.ndarray:
+    """Rows kv_cache[kv_indices[begin:end]] as float64, shape [end-begin, 576].
+
+    Page size 1: a request's cache is its list of slot numbers in token order
+    ("Attention backends", paragraph "Paged, ragged batches").
+    """
+    idx = np.asarray(kv_indices[begin:end], dtype=np.int64)
+    return bf16_bits_to_f64(kv_cache_bits[idx])
+
+
+def partial_state(q_nope: np.ndarray, q_rope: np.ndarray, rows: np.ndarray, sm_scale: float):
+    """Attention of one request's heads over a set of cache rows.
+
+    q_nope [H,512], q_rope [H,64], rows [n,576] (all float64).
+    Returns (o [H,512], lse [H]); o is already divided by the softmax sum.
+    With n == 0: o = 0 and lse = -inf.
+    """
+    H = q_nope.shape[0]
+    if rows.shape[0] == 0:
+        return np.zeros((H, KV_LORA_RANK)), np.full(H, -np.inf)
+    latent = rows[:, :KV_LORA_RANK]
+    k_rope = rows[:, KV_LORA_RANK:]
+    # dual-path score, scaled after the sum (section 2.4 of the sglang-jax gap page)
+    s = (q_nope @ latent.T + q_rope @ k_rope.T) * sm_scale          # [H, n]
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    denom = e.sum(axis=1, keepdims=True)
+    lse = (m + np.log(denom))[:, 0]
+    o = (e / denom) @ latent                                          # latent reused as value
+    return o, lse
+
+
+def decode_attention(q_nope_bits, q_rope_bits, kv_cache_bits, kv_indptr, kv_indices, sm_scale,
+                     requests=None):
+    """Absorbed MLA decode over a CSR batch.
+
+    Returns (out [B,H,512], lse [B,H]) in float64.  With ``requests`` given,
+    only those rows are computed; the others stay NaN.
+    """
+    qn = np.asarray(q_nope_bits)
+    qr = np.asarray(q_rope_bits)
+    B, H = qn.shape[0], qn.shape[1]
+    out = np.full((B, H, KV_LORA_RANK), np.nan)
+    lse = np.full((B, H), np.nan)
+    todo = range(B) if requests is None else requests
+    for b in todo:
+        rows = gather_rows(kv_cache_bits, kv_indices, int(kv_indptr[b]), int(kv_indptr[b + 1]))
+        o, l = partial_state(bf16_bits_to_f64(qn[b]), bf16_bits_to_f64(qr[b]), rows, sm_scale)
+        out[b], lse[b] = o, l
+    return out, lse
+
+
+def merge_states(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """Combine partial states of disjoint key sets by LSE rescaling.
+
+    o_parts [P,H,512] (each already normalised), lse_parts [P,H].
+      M = max_i lse_i;  w_i = exp(lse_i - M);
+      out = sum_i w_i o_i / sum_i w_i;  lse = M + ln sum_i w_i.
+    Partials with lse = -inf carry no weight; if every partial is empty the
+    result is out = 0, lse = -inf.
+    ("Attention backends", paragraph "FlashAttention": Flash-Decoding merges
+    partial results with the same rescaling; the EAGLE tree-verify PR page
+    merges prefix and suffix attention by LSE in its introduction.)
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    P, H = lse_parts.shape
+    out = np.zeros((H, o_parts.shape[2]))
+    lse = np.full(H, -np.inf)
+    for h in range(H):
+        l = lse_parts[:, h]
+        live = np.isfinite(l)
+        if not live.any():
+            continue
+        M = l[live].max()
+        w = np.exp(l[live] - M)
+        out[h] = (w[:, None] * o_parts[live, h, :]).sum(axis=0) / w.sum()
+        lse[h] = M + np.log(w.sum())
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# Weight absorption: used only to pin the decode definition above against an
+# ordinary multi-head attention over decompressed keys and values.
+# ----------------------------------------------------------------------------
+
+def absorb_weights(kv_b_proj: np.ndarray, qk_nope_head_dim: int, v_head_dim: int):
+    """Split kv_b_proj [H*(nope+v), 512] into per-head w_kc and w_vc.
+
+    Following "MLA and torch.compile: v0.3's two sources", section "MLA:
+    starting from a 439-line commit": unflatten dim 0 to [H, nope+v, 512] and
+    split along dim 1.  Returns
+      w_kc [H, nope, 512]  (used as bmm(q_nope[H,B,nope], w_kc) -> [H,B,512])
+      w_vc [H, 512, v]     (used as bmm(attn[H,B,512], w_vc)   -> [H,B,v])
+    """
+    rank = kv_b_proj.shape[1]
+    w = kv_b_proj.reshape(-1, qk_nope_head_dim + v_head_dim, rank)
+    w_kc = w[:, :qk_nope_head_dim, :]
+    w_vc = np.transpose(w[:, qk_nope_head_dim:, :], (0, 2, 1))
+    return w_kc, w_vc
+
+
+def absorbed_attention(q_nope_heads, q_rope_heads, latents, k_rope, kv_b_proj, sm_scale,
+                       qk_nope_head_dim, v_head_dim):
+    """Decode for one request on the absorbing path, in float64.
+
+    q_nope_heads [H, nope] (before absorption), q_rope_heads [H, 64],
+    latents [L, 512], k_rope [L, 64].  q_nope is moved into the latent space by
+    w_kc, attention runs on the latent rows (``partial_state``), and the latent
+    output is moved to the value space by w_vc.  Returns [H, v].
+    """
+    w_kc, w_vc = absorb_weights(kv_b_proj, qk_nope_head_dim, v_head_dim)
+    q_lat = np.einsum("hn,hnr->hr", q_nope_heads, w_kc)              # bmm(q_nope, w_kc)
+    rows = np.concatenate([latents, k_rope], axis=1)
+    o_lat, _ = partial_state(q_lat, q_rope_heads, rows, sm_scale)
+    return np.einsum("hr,hrv->hv", o_lat, w_vc)                      # bmm(attn, w_vc)
+
+
+def decompressed_attention(q_nope_heads, q_rope_heads, latents, k_rope, kv_b_proj, sm_scale,
+                           qk_nope_head_dim, v_head_dim):
+    """Decode for one request on the decompressing path, in float64.
+
+    Every head gets its own keys k_{h,t} = [W_UK[h] c_t ; k_rope_t] and values
+    v_{h,t} = W_UV[h] c_t, expanded from the latent rows with the kv_b_proj
+    weights, and ordinary attention runs per head (scipy's softmax).  This is
+    the path the absorbing one must equal ("MLA and torch.compile", self-test
+    answer 2 and section "MLA: starting from a 439-line commit").  Returns [H, v].
+    """
+    from scipy.special import softmax
+
+    H = q_nope_heads.shape[0]
+    rank = kv_b_proj.shape[1]
+    w = kv_b_proj.reshape(H, qk_nope_head_dim + v_head_dim, rank)
+    out = np.empty((H, v_head_dim))
+    for h in range(H):
+        k_nope = latents @ w[h, :qk_nope_head_dim, :].T             # [L, nope]
+        v = latents @ w[h, qk_nope_head_dim:, :].T                   # [L, v]
+        keys = np.concatenate([k_nope, k_rope], axis=1)               # [L, nope+64]
+        q = np.concatenate([q_nope_heads[h], q_rope_heads[h]])
+        p = softmax(sm_scale * (keys @ q))
+        out[h] = p @ v
+    return out
+
+
+def mac_counts(num_heads: int, qk_nope_head_dim: int, kv_lora_rank: int, history: int):
+    """Multiply-accumulates to bring one decode query against the history.
+
+    Absorbing path: each head maps its q_nope (nope) through w_kc (nope x rank):
+    H * nope * rank, independent of the history.  Decompressing path: every
+    historical latent is mapped back to H heads of nope dims:
+    history * rank * H * nope.  ("MLA and torch.compile", "Exercises", 1.)
+    """
+    absorbing = num_heads * qk_nope_head_dim * kv_lora_rank
+    decompressing = history * kv_lora_rank * num_heads * qk_nope_head_dim
+    return absorbing, decompressing

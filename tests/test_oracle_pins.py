@@ -1,0 +1,292 @@
+"""Pins for the fp64 oracle: facts fixed by the pages and by the mathematics,
+none of them a retyping of the oracle's own formula.  CPU only.
+
+Each check is chosen so that a plausible mistake in the oracle (dropped rope
+term, scale applied to one path only, wrong value columns, transposed operand,
+log base, merge weight sign) fails at least one of them; the planted-mistake
+tests at the bottom show that.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import mla_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+SM = 1.0 / math.sqrt(192.0)
+
+
+def _rows(rng, n):
+    return rng.standard_normal((n, 576))
+
+
+def _dot(a, b):
+    return math.fsum(float(x) * float(y) for x, y in zip(a, b))
+
+
+def _score(qn, qr, row, scale):
+    # plain python dual-path score, element by element
+    return scale * (_dot(qn, row[:512]) + _dot(qr, row[512:]))
+
+
+# --------------------------------------------------------------------------
+# 1. absorption identity vs decompressed multi-head attention (scipy softmax)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,L", [(2, 1), (3, 5), (4, 17)])
+def test_absorption_identity_matches_decompressed_mha(H, L):
+    rng = np.random.default_rng(7 + H * 31 + L)
+    nope, vdim = 128, 128
+    kv_b_proj = rng.standard_normal((H * (nope + vdim), 512)) / math.sqrt(512)
+    q_nope = rng.standard_normal((H, nope))
+    q_rope = rng.standard_normal((H, 64))
+    lat = rng.standard_normal((L, 512))
+    k_rope = rng.standard_normal((L, 64))
+    a = O.absorbed_attention(q_nope, q_rope, lat, k_rope, kv_b_proj, SM, nope, vdim)
+    d = O.decompressed_attention(q_nope, q_rope, lat, k_rope, kv_b_proj, SM, nope, vdim)
+    assert a.shape == (H, vdim)
+    np.testing.assert_allclose(a, d, rtol=1e-11, atol=1e-12)
+
+
+def test_absorb_weights_layout():
+    # kv_b_proj rows are [head][nope + v]; w_kc must pick the first nope rows
+    # of each head's block, w_vc the remaining v rows, transposed.
+    H, nope, vdim, R = 3, 4, 5, 6
+    w = np.arange(H * (nope + vdim) * R, dtype=np.float64).reshape(H * (nope + vdim), R)
+    w_kc, w_vc = O.absorb_weights(w, nope, vdim)
+    assert w_kc.shape == (H, nope, R) and w_vc.shape == (H, R, vdim)
+    for h in range(H):
+        for i in range(nope):
+            assert np.array_equal(w_kc[h, i], w[h * (nope + vdim) + i])
+        for j in range(vdim):
+            assert np.array_equal(w_vc[h, :, j], w[h * (nope + vdim) + nope + j])
+
+
+# --------------------------------------------------------------------------
+# 2. brute force on 1-3 tokens
+# --------------------------------------------------------------------------
+
+def test_one_token_closed_form():
+    rng = np.random.default_rng(11)
+    H = 3
+    qn, qr, rows = rng.standard_normal((H, 512)), rng.standard_normal((H, 64)), _rows(rng, 1)
+    o, lse = O.partial_state(qn, qr, rows, SM)
+    for h in range(H):
+        assert np.array_equal(o[h], rows[0, :512])          # softmax of one score is 1
+        assert lse[h] == pytest.approx(_score(qn[h], qr[h], rows[0], SM), abs=1e-12)
+
+
+def test_two_token_closed_form():
+    rng = np.random.default_rng(12)
+    H = 4
+    qn, qr, rows = rng.standard_normal((H, 512)), rng.standard_normal((H, 64)), _rows(rng, 2)
+    o, lse = O.partial_state(qn, qr, rows, SM)
+    for h in range(H):
+        s0 = _score(qn[h], qr[h], rows[0], SM)
+        s1 = _score(qn[h], qr[h], rows[1], SM)
+        p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        want = p0 * rows[0, :512] + (1.0 - p0) * rows[1, :512]
+        np.testing.assert_allclose(o[h], want, rtol=1e-12, atol=1e-13)
+        assert lse[h] == pytest.approx(max(s0, s1) + math.log1p(math.exp(-abs(s1 - s0))), abs=1e-12)
+
+
+def test_three_token_brute_force():
+    rng = np.random.default_rng(13)
+    H = 2
+    qn, qr, rows = rng.standard_normal((H, 512)), rng.standard_normal((H, 64)), _rows(rng, 3)
+    o, lse = O.partial_state(qn, qr, rows, SM)
+    for h in range(H):
+        s = [_score(qn[h], qr[h], rows[t], SM) for t in range(3)]
+        e = [math.exp(x) for x in s]
+        z = math.fsum(e)
+        for d in range(0, 512, 37):
+            want = math.fsum(e[t] / z * rows[t, d] for t in range(3))
+            assert o[h, d] == pytest.approx(want, rel=1e-12, abs=1e-13)
+        assert lse[h] == pytest.approx(math.log(z), abs=1e-12)
+
+
+def test_scale_applies_to_both_paths():
+    # with q_nope = 0 the score is sm_scale * rope part only; a scale applied to
+    # one path only (or none) changes lse for a single token
+    rng = np.random.default_rng(14)
+    qr = rng.standard_normal((1, 64))
+    rows = _rows(rng, 1)
+    _, lse = O.partial_state(np.zeros((1, 512)), qr, rows, 0.25)
+    assert lse[0] == pytest.approx(0.25 * _dot(qr[0], rows[0, 512:]), abs=1e-12)
+    _, lse = O.partial_state(rng.standard_normal((1, 512)) * 0 + 1.0, np.zeros((1, 64)), rows, 0.5)
+    assert lse[0] == pytest.approx(0.5 * math.fsum(rows[0, :512]), abs=1e-12)
+
+
+# --------------------------------------------------------------------------
+# 3. split-KV + LSE merge equals the unsplit result
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_split_merge_equals_unsplit(seed):
+    rng = np.random.default_rng(100 + seed)
+    H, L = 5, 97
+    qn, qr, rows = rng.standard_normal((H, 512)), rng.standard_normal((H, 64)), _rows(rng, L) * 2.0
+    ref_o, ref_l = O.partial_state(qn, qr, rows, SM)
+    ncut = int(rng.integers(2, 6))
+    cuts = sorted(set(int(c) for c in rng.integers(1, L, size=ncut)) | {0}) + [L]
+    pieces, start = [], 0
+    for c in cuts:
+        pieces.append((start, c))        # may be empty
+        start = c
+    parts = [O.partial_state(qn, qr, rows[a:b], SM) for a, b in pieces]
+    o, l = O.merge_states(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    np.testing.assert_allclose(o, ref_o, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_merge_all_empty_and_single():
+    o, l = O.merge_states(np.zeros((2, 3, 512)), np.full((2, 3), -np.inf))
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((1, 3, 512))
+    lx = rng.standard_normal((1, 3))
+    o, l = O.merge_states(x, lx)
+    np.testing.assert_allclose(o, x[0], rtol=1e-15)
+    np.testing.assert_allclose(l, lx[0], rtol=1e-15)
+
+
+def test_empty_request():
+    o, l = O.partial_state(np.ones((2, 512)), np.ones((2, 64)), np.zeros((0, 576)), SM)
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+# --------------------------------------------------------------------------
+# 4. relabelling the physical slots changes nothing (bit for bit)
+# --------------------------------------------------------------------------
+
+def test_slot_permutation_invariance():
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    bt = W.make_batch([3, 0, 40, 129], heads=16, pool=300, seed=3)
+    out1, lse1 = O.decode_attention(bt.q_nope, bt.q_rope, bt.kv_cache, bt.kv_indptr, bt.kv_indices, SM)
+    perm = np.random.default_rng(9).permutation(bt.pool)
+    kv2 = np.empty_like(bt.kv_cache)
+    kv2[perm] = bt.kv_cache                      # kv'[pi(s)] = kv[s]
+    idx2 = perm[bt.kv_indices].astype(np.int32)  # indices' = pi(indices)
+    out2, lse2 = O.decode_attention(bt.q_nope, bt.q_rope, kv2, bt.kv_indptr, idx2, SM)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+# --------------------------------------------------------------------------
+# 5. closed forms
+# --------------------------------------------------------------------------
+
+def test_all_rows_equal():
+    rng = np.random.default_rng(21)
+    H, L = 3, 50
+    row = rng.standard_normal(576)
+    rows = np.tile(row, (L, 1))
+    qn, qr = rng.standard_normal((H, 512)), rng.standard_normal((H, 64))
+    o, lse = O.partial_state(qn, qr, rows, SM)
+    for h in range(H):
+        np.testing.assert_allclose(o[h], row[:512], rtol=1e-13)
+        assert lse[h] == pytest.approx(_score(qn[h], qr[h], row, SM) + math.log(L), abs=1e-11)
+
+
+def test_zero_query_is_uniform_mean():
+    rng = np.random.default_rng(22)
+    L = 33
+    rows = _rows(rng, L)
+    o, lse = O.partial_state(np.zeros((2, 512)), np.zeros((2, 64)), rows, SM)
+    for h in range(2):
+        want = [math.fsum(rows[:, d]) / L for d in range(512)]
+        np.testing.assert_allclose(o[h], want, rtol=1e-12, atol=1e-14)
+        assert lse[h] == pytest.approx(math.log(L), abs=1e-13)
+
+
+def test_bf16_widening_is_exact():
+    bits = np.array([0x3F80, 0xBF80, 0x0000, 0x8000, 0x3F81, 0x7F7F, 0x0001, 0x4049], dtype=np.uint16)
+    want = [1.0, -1.0, 0.0, -0.0, 1.0 + 2.0 ** -7, (2 - 2.0 ** -7) * 2.0 ** 127, 2.0 ** -133, 3.140625]
+    got = O.bf16_bits_to_f64(bits)
+    assert [float(x) for x in got] == want
+
+
+def test_mac_counts_golden():
+    with open(os.path.join(GOLDEN, "mac_counts.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for H, nope, rank, hist, absorb, decomp, p_abs, p_dec in rows:
+        a, d = O.mac_counts(int(H), int(nope), int(rank), int(hist))
+        assert (a, d) == (int(absorb), int(decomp))
+        assert round(a / 1e6, 1) == float(p_abs.rstrip("M"))        # "~8.4M"
+        assert round(d / 1e9) == int(p_dec.rstrip("G"))              # "~34G"
+
+
+def test_row_width_golden():
+    with open(os.path.join(GOLDEN, "row_widths.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for rank, rope, width, mha, padded, ratio in rows:
+        assert O.KV_LORA_RANK == int(rank) and O.QK_ROPE_HEAD_DIM == int(rope)
+        assert O.KV_ROW == int(width)
+        assert 128 * 128 * 2 == int(mha)
+        assert round(int(mha) / int(padded)) == int(ratio)
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each plausible oracle bug is caught by some pin above
+# --------------------------------------------------------------------------
+
+def _mutant_partial(kind):
+    def f(q_nope, q_rope, rows, sm_scale):
+        H = q_nope.shape[0]
+        if rows.shape[0] == 0:
+            return np.zeros((H, 512)), np.full(H, -np.inf)
+        lat, kr = rows[:, :512], rows[:, 512:]
+        if kind == "drop_rope":
+            s = (q_nope @ lat.T) * sm_scale
+        elif kind == "scale_nope_only":
+            s = q_nope @ lat.T * sm_scale + q_rope @ kr.T
+        elif kind == "value_offset":
+            lat_v = rows[:, 64:]
+            s = (q_nope @ lat.T + q_rope @ kr.T) * sm_scale
+            m = s.max(1, keepdims=True); e = np.exp(s - m); z = e.sum(1, keepdims=True)
+            return (e / z) @ lat_v, (m + np.log(z))[:, 0]
+        elif kind == "log2_lse":
+            s = (q_nope @ lat.T + q_rope @ kr.T) * sm_scale
+            m = s.max(1, keepdims=True); e = np.exp(s - m); z = e.sum(1, keepdims=True)
+            return (e / z) @ lat, (m + np.log2(z))[:, 0]
+        else:
+            raise ValueError(kind)
+        m = s.max(1, keepdims=True); e = np.exp(s - m); z = e.sum(1, keepdims=True)
+        return (e / z) @ lat, (m + np.log(z))[:, 0]
+    return f
+
+
+PIN_TESTS = [
+    lambda: test_absorption_identity_matches_decompressed_mha(3, 5),
+    test_one_token_closed_form, test_two_token_closed_form, test_three_token_brute_force,
+    test_scale_applies_to_both_paths, test_all_rows_equal, test_zero_query_is_uniform_mean,
+]
+
+
+@pytest.mark.parametrize("kind", ["drop_rope", "scale_nope_only", "value_offset", "log2_lse"])
+def test_planted_partial_mistakes_are_caught(kind, monkeypatch):
+    monkeypatch.setattr(O, "partial_state", _mutant_partial(kind))
+    failures = 0
+    for t in PIN_TESTS:
+        try:
+            t()
+        except AssertionError:
+            failures += 1
+    assert failures >= 1, f"mutant {kind} passed every pin"
+
+
+def test_planted_merge_mistake_is_caught(monkeypatch):
+    real = O.merge_states
+
+    def bad(o_parts, lse_parts):       # weights exp(M - lse) instead of exp(lse - M)
+        o_parts = np.asarray(o_parts); lse_parts = np.asarray(lse_parts)
+        M = np.max(np.where(np.isfinite(lse_parts), lse_parts, -1e300), axis=0)
+        w = np.where(np.isfinite(lse_parts), np.exp(M - lse_parts), 0.0)
+        return (w[..., None] * o_parts).sum(0) / w.sum(0)[:, None], M + np.log(w.sum(0))
+
+    monkeypatch.setattr(O, "merge_states", bad)
+    for seed in range(3):
+        with pytest.raises(AssertionError):
+            test_split_merge_equals_unsplit(seed)
+    monkeypatch.setattr(O, "merge_states", real)
