@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark of absorbed MLA decode on GB300 (one JSON line on stdout).
+
+A step is one whole decode pass (mla_decode_attend + mla_decode_merge) over one
+synthetic batch whose inputs are already resident in HBM.  Default workload:
+the DeepSeek-V2-Lite-shaped batch (B=64, H=16, contexts uniform in
+[512, 4096], page size 1, 2^19-slot pool); ``--workload 1..5`` picks another.
+
+Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA
+events on the launching stream; L2 is flushed by a 256 MiB write before every
+timed step (outside the events).  The K steps are bracketed by a barrier and
+torch.cuda.synchronize() on both sides; the max over ranks is reported.
+``--gpus N`` under torchrun runs N independent replicas (the path needs no
+collective).  ``--impl reference`` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/step and latent-KV GB/s as % of GB300 HBM roofline (1 GPU)"
+UNIT = "us/step"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_work(batch):
+    """Bytes and flops the path must move / compute for one step (not the
+    decompressed work absorption avoids): every cache row once, the indices,
+    q, the fp32 output and lse; flops 2*576 (QK) + 2*512 (PV) per head-token."""
+    B, H, nnz = batch.batch, batch.heads, batch.nnz
+    bytes_ = nnz * 1152 + nnz * 4 + B * H * 576 * 2 + B * H * 512 * 4 + B * H * 4 + (B + 1) * 4
+    flops = nnz * H * 2 * (576 + 512)
+    return bytes_, flops
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_absorbed_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name):
+    """DRAM bytes per decode-kernel launch from the committed ncu summary, or
+    None when absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload_name]
+        if e.get("source_sha") != kernel_source_sha():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(value, pg, device=None):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(batch, budget_s):
+    """Time the fp64 oracle on the first requests of the batch until about
+    budget_s of CPU work, and scale to the whole batch by tokens."""
+    from oracle import mla_oracle as O
+    reqs, t_total, tok = [], 0.0, 0
+    order = list(range(batch.batch))
+    for b in order:
+        t0 = time.perf_counter()
+        O.decode_attention(batch.q_nope, batch.q_rope, batch.kv_cache, batch.kv_indptr, batch.kv_indices,
+                           batch.sm_scale, requests=[b])
+        t_total += time.perf_counter() - t0
+        reqs.append(b)
+        tok += int(batch.kv_indptr[b + 1] - batch.kv_indptr[b])
+        if t_total >= budget_s:
+            break
+    scale = batch.nnz / max(tok, 1)
+    return t_total * scale * 1e6, len(reqs), tok
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, batch, rank, pg):
+    """--impl reference: the fp64 oracle on the host cores, bounded sample per step."""
+    if pg is not None and rank != 0:
+        return 0
+    per_step_budget = max(0.5, args.reference_budget_s / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(batch, per_step_budget)
+    vals, samples = [], None
+    for _ in range(args.steps):
+        us, nreq, tok = cpu_oracle_sample(batch, per_step_budget)
+        vals.append(us)
+        samples = (nreq, tok)
+    value = statistics.mean(vals)
+    cores = oracle_threads()
+    sample = f"first {samples[0]} requests ({samples[1]} of {batch.nnz} tokens) per step, scaled by tokens"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(batch, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(batch, args):
+    spec = batch.spec
+    return {"workload": spec.name if spec else "custom", "batch": batch.batch, "heads": batch.heads,
+            "kv_lora_rank": 512, "qk_rope_head_dim": 64, "nnz": batch.nnz, "pool_slots": batch.pool,
+            "max_context": int(batch.lengths.max()), "page_size": 1, "out_dtype": "fp32",
+            "l2": "flushed before every timed step (256 MiB write, outside the events)",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+def run_ours(args, batch, world, rank, local, pg):
+    import numpy as np
+    import torch
+    from mla_latent_kv_absorbed_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if pg is not None:
+        pg.barrier()
+    B.build()
+    from mla_latent_kv_absorbed_gb300 import binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    q_nope, q_rope, kv = bf(batch.q_nope), bf(batch.q_rope), bf(batch.kv_cache)
+    indptr_d = torch.from_numpy(batch.kv_indptr).to(dev)
+    indices_d = torch.from_numpy(batch.kv_indices).to(dev)
+    Bn, H = batch.batch, batch.heads
+    out = torch.empty((Bn, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((Bn, H), dtype=torch.float32, device=dev)
+    t0 = time.perf_counter()
+    dec = binding.Decoder(batch.kv_indptr, H, device=dev)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        dec.attend(q_nope, q_rope, kv, indptr_d, indices_d, batch.sm_scale, out, lse, stream)
+        dec.merge(out, lse, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    st = dec.check(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {binding.status_string(st)}")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            e0, e1, e2 = evs[k]
+            e0.record(stream)
+            dec.attend(q_nope, q_rope, kv, indptr_d, indices_d, batch.sm_scale, out, lse, stream)
+            e1.record(stream)
+            dec.merge(out, lse, stream)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if pg is not None:
+        pg.barrier()
+    st = dec.check(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {binding.status_string(st)}")
+    step_ms = [a.elapsed_time(c) for a, b_, c in evs]
+    attend_ms = [a.elapsed_time(b_) for a, b_, c in evs]
+    ms = max_over_ranks(statistics.mean(step_ms), pg, dev)
+    attend_avg = max_over_ranks(statistics.mean(attend_ms), pg, dev)
+
+    # ---------------------------------------------------------------- e2e
+    # Public API end to end, host buffers: plan on the host, pinned H2D of the
+    # step's inputs (q, indptr, indices, plan words), run, D2H of out and lse.
+    h_qn = torch.from_numpy(np.ascontiguousarray(batch.q_nope).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_qr = torch.from_numpy(np.ascontiguousarray(batch.q_rope).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_ptr = torch.from_numpy(batch.kv_indptr).pin_memory()
+    h_idx = torch.from_numpy(batch.kv_indices).pin_memory()
+    h_out = torch.empty((Bn, H, 512), dtype=torch.float32).pin_memory()
+    h_lse = torch.empty((Bn, H), dtype=torch.float32).pin_memory()
+    d_qn, d_qr = torch.empty_like(q_nope), torch.empty_like(q_rope)
+    d_ptr, d_idx = torch.empty_like(indptr_d), torch.empty_like(indices_d)
+    plan_pin = torch.empty(dec.plan_host.shape[0], dtype=torch.int32).pin_memory()
+    d_plan = torch.empty(dec.plan_host.shape[0], dtype=torch.int32, device=dev)
+    ws = dec.workspace
+
+    def e2e_step():
+        ph, _ = binding.decode_plan(h_ptr.numpy(), H)
+        plan_pin[:ph.shape[0]].copy_(torch.from_numpy(ph))
+        d_plan[:ph.shape[0]].copy_(plan_pin[:ph.shape[0]], non_blocking=True)
+        d_qn.copy_(h_qn, non_blocking=True)
+        d_qr.copy_(h_qr, non_blocking=True)
+        d_ptr.copy_(h_ptr, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        binding.decode_run(ph, d_plan, d_qn, d_qr, kv, d_ptr, d_idx, batch.sm_scale, out, lse, ws, stream)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        stream.synchronize()
+        return ph
+
+    for _ in range(max(2, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    e2e_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ph = e2e_step()
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_us = max_over_ranks(statistics.mean(e2e_times) * 1e6, pg, dev)
+    h2d = (h_qn.numel() * 2 + h_qr.numel() * 2 + h_ptr.numel() * 4 + h_idx.numel() * 4 + ph.shape[0] * 4)
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    st = dec.check(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after e2e: {binding.status_string(st)}")
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    bytes_alg, flops_alg = algorithmic_work(batch)
+    gbs_attend = bytes_alg / (attend_avg * 1e-3) / 1e9
+    tflops_attend = flops_alg / (attend_avg * 1e-3) / 1e12
+    t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops_alg / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": gbs_attend, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs_attend / peaks["hbm_gbs"]}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops_attend, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tflops_attend / peaks["bf16_tflops"]}
+    roof["traffic"] = ncu_traffic(batch.spec.name if batch.spec else "custom")
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = "mla_decode (swab)" if H <= 32 else "mla_decode (pair)"
+    roof["kernel_ms"] = attend_avg
+    roof["algorithmic_bytes"] = bytes_alg
+    roof["algorithmic_flops"] = flops_alg
+    roof["roofline_us"] = max(t_hbm, t_tc) * 1e6
+    roof["step_frac_of_roofline"] = max(t_hbm, t_tc) * 1e3 / ms
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        us, nreq, tok = cpu_oracle_sample(batch, args.cpu_budget_s)
+        cpu = {"value": us, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"first {nreq} requests ({tok} of {batch.nnz} tokens), fp64 numpy, scaled by tokens"}
+    launches = args.steps * (1 + (1 if dec.has_merge else 0))
+    line = {
+        "metric": METRIC, "value": ms * 1e3, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random slots)",
+        "config": workload_config(batch, args),
+        "latent_kv_gbs": batch.nnz * 1152 / (ms * 1e-3) / 1e9 * world,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "includes": "host plan + pinned H2D (q, indptr, indices, plan) + kernels + D2H (out, lse)"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "plan_ms_host": plan_ms,
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local, pg = dist_setup(args)
+    from mla_latent_kv_absorbed_gb300 import workloads
+    batch = workloads.make_workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, batch, rank, pg)
+    return run_ours(args, batch, world, rank, local, pg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

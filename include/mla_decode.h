@@ -1,0 +1,170 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode.so: absorbed multi-head latent
+ * attention (MLA) decode on GB300 (sm_103a).
+ *
+ * The operation (one query token per request, per head):
+ *
+ *   for request b with context rows K_b = kv_cache[kv_indices[kv_indptr[b] .. kv_indptr[b+1])]
+ *   and head h with q = [q_nope[b,h,0:512], q_rope[b,h,0:64]]:
+ *       s_t        = sm_scale * (q_nope . c_t + q_rope . k_rope_t)     c_t = row[0:512], k_rope_t = row[512:576]
+ *       lse[b,h]   = ln sum_t exp(s_t)
+ *       out[b,h,:] = sum_t softmax(s)_t * c_t                            (the latent is also the value)
+ *
+ * Sources: "实现差距：MLA 与 DeepSeek V3", section 2.4 (MLA Pallas kernel V2,
+ * core computation: dual-path score, FA2-style online softmax, kv_c reused as
+ * the value) and section 2.1 (the 576-wide row: kv_latent 512 then k_rope 64);
+ * "Attention backends", paragraphs "MLA" (one 576-wide vector per token shared
+ * by all heads) and "Paged, ragged batches" (page size 1, kv_indptr /
+ * kv_indices CSR, a host-side plan() that picks split-KV chunking and balances
+ * long and short contexts across SMs); "Attention backends", paragraph
+ * "FlashAttention" (Flash-Decoding: keys split across blocks, partial results
+ * merged with the same rescaling).
+ *
+ * Conventions for every entry point:
+ *   - All memory is owned by the caller; the library never allocates.
+ *   - Device pointers must be 16-byte aligned; tensors are dense row-major.
+ *   - bf16 means IEEE bfloat16 (the bits of the upper half of an fp32).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - No function throws or aborts; each returns an mla_status.  Arguments are
+ *     checked on the host before any launch; on a bad argument nothing is
+ *     launched and nothing is written.
+ *   - Supported head counts: 16 and 32 (one CTA per SM, 128-token tiles) and
+ *     48..128 in steps of 16 (a two-CTA cluster per worker, 64-token tiles).
+ *     kv_lora_rank is 512 and qk_rope_head_dim is 64; nothing else is built.
+ *   - The natural log is used for every LSE.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, malformed kv_indptr, bad plan */
+  MLA_ERR_UNSUPPORTED = 2,   /* head count or dtype the library does not build */
+  MLA_ERR_WORKSPACE = 3,     /* plan or workspace buffer too small */
+  MLA_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, attribute, device query) */
+  MLA_ERR_TIMEOUT = 5,       /* a device-side wait exceeded its limit (~1 s); the kernel returned early */
+  MLA_ERR_INDEX_OOB = 6,     /* a kv_indices value was outside [0, num_slots); row 0 was read instead */
+  MLA_ERR_PLAN_MISMATCH = 7  /* a plan work item does not lie inside its request's kv_indptr range */
+} mla_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_status_string(int status);
+
+/* Library ABI version (currently 1). */
+int mla_abi_version(void);
+
+/* mla_decode_plan -- host only, no device work, deterministic.
+ *
+ * Builds the split-KV work plan for one decode batch ("Attention backends",
+ * paragraph "Paged, ragged batches": plan() rebuilt on the CPU per batch,
+ * choosing per-request chunking and balancing long and short contexts).
+ *
+ *   kv_indptr          host int32[batch+1]; kv_indptr[0] == 0, non-decreasing.
+ *   batch              number of requests B >= 0.
+ *   num_heads          H (see supported head counts above).
+ *   num_sms            SMs to plan for; 0 = query the current CUDA device.
+ *   plan               host int32 buffer of plan_words words that receives the
+ *                      plan, or NULL to only report the sizes.
+ *   plan_words_needed  out: words the plan takes (always written when non-NULL).
+ *   workspace_bytes    out: device workspace bytes mla_decode_run needs for this
+ *                      plan (fp32 partial states plus a 256-byte status header).
+ *
+ * Rule: tiles of T tokens (T = 128 for H <= 32, 64 otherwise); W workers =
+ * SMs (H <= 32) or SMs/2; candidate chunk sizes ceil(ceil(total_tiles/W)/k)
+ * for k = 1..8; requests cut into chunks; chunks placed longest-first on the
+ * least-loaded worker; the candidate with the smallest makespan (plus a fixed
+ * merge cost if any request is cut) wins.  Requests left whole are written
+ * straight to out/lse; cut or empty requests go through the LSE merge.
+ *
+ * Returns MLA_OK, MLA_ERR_INVALID_ARG (malformed kv_indptr, negative batch),
+ * MLA_ERR_UNSUPPORTED (head count), MLA_ERR_WORKSPACE (plan too small; sizes
+ * are still reported) or MLA_ERR_CUDA (num_sms == 0 and no device).
+ */
+int mla_decode_plan(const int32_t* kv_indptr, int32_t batch, int32_t num_heads, int32_t num_sms,
+                    int32_t* plan, size_t plan_words, size_t* plan_words_needed,
+                    size_t* workspace_bytes);
+
+/* mla_decode_run -- asynchronous on `stream`.
+ *
+ *   plan_host     host copy of the plan words from mla_decode_plan (read now).
+ *   plan_dev      device copy of the same words (read by the kernels).
+ *   q_nope        device bf16 [batch, H, 512]: q_nope already multiplied by W_UK.
+ *   q_rope        device bf16 [batch, H, 64]: the rotary part of the query.
+ *   kv_cache      device bf16 [num_slots, 576]: latent [0,512) then rope key [512,576).
+ *   num_slots     rows in kv_cache (1 .. 2^31-1).
+ *   kv_indptr     device int32 [batch+1], equal to the host array the plan was built from.
+ *   kv_indices    device int32 [kv_indptr[batch]]: slot of every context token.
+ *   sm_scale      softmax scale applied to the summed score.
+ *   out           device [batch, H, 512], fp32 (out_dtype 0) or bf16 (out_dtype 1).
+ *   lse           device fp32 [batch, H] (natural log), or NULL to skip it.
+ *   workspace     device buffer of at least the planned workspace_bytes; must be
+ *                 zero-filled before its first use (its first 256 bytes hold the
+ *                 sticky device status read by mla_check_errors).
+ *
+ * Launches the decode kernel and, when the plan cut or left empty any request,
+ * the merge kernel.  Device-side faults are not possible from bad indices: an
+ * index outside [0, num_slots) reads row 0 and sets MLA_ERR_INDEX_OOB in the
+ * workspace status.  The call does not synchronise; read device-side status
+ * with mla_check_errors.  Safe to capture in a CUDA graph (no host sync, no
+ * allocation) as long as the plan words stay unchanged.
+ */
+int mla_decode_run(const int32_t* plan_host, const int32_t* plan_dev,
+                   const void* q_nope, const void* q_rope,
+                   const void* kv_cache, int64_t num_slots,
+                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                   float sm_scale, void* out, int32_t out_dtype, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* mla_decode_attend / mla_decode_merge -- the two launches of mla_decode_run,
+ * callable separately (same arguments and checks).  mla_decode_attend runs
+ * the decode kernel: requests the plan left whole get their out/lse, cut
+ * requests leave fp32 partial states in the workspace.  mla_decode_merge then
+ * combines the partials of every cut request (and writes out = 0, lse = -inf
+ * for empty requests); it launches nothing when the plan has no such request.
+ * mla_decode_run == mla_decode_attend followed by mla_decode_merge. */
+int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev,
+                      const void* q_nope, const void* q_rope,
+                      const void* kv_cache, int64_t num_slots,
+                      const int32_t* kv_indptr, const int32_t* kv_indices,
+                      float sm_scale, void* out, int32_t out_dtype, float* lse,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+int mla_decode_merge(const int32_t* plan_host, const int32_t* plan_dev, void* out,
+                     int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* mla_merge_states -- asynchronous on `stream`.
+ *
+ * Flash-Decoding merge ("Attention backends", paragraph "FlashAttention"):
+ * for request b, partial states i in [merge_indptr[b], merge_indptr[b+1]):
+ *   M = max_i s_i;  w_i = exp(s_i - M);  out = sum_i w_i v_i / sum_i w_i;
+ *   lse = M + ln sum_i w_i.
+ * Partials with s_i = -inf carry no weight; a request with no live partial
+ * gets out = 0 and lse = -inf.
+ *
+ *   v_partial     device fp32 [P, H, 512], each partial already normalised.
+ *   s_partial     device fp32 [P, H], the partial LSEs (natural log).
+ *   merge_indptr  device int32 [batch+1], non-decreasing, merge_indptr[0] == 0.
+ *   out, lse      as for mla_decode_run (lse may be NULL).
+ */
+int mla_merge_states(const float* v_partial, const float* s_partial, const int32_t* merge_indptr,
+                     int32_t batch, int32_t num_heads, void* out, int32_t out_dtype, float* lse,
+                     void* stream);
+
+/* mla_check_errors -- synchronises `stream`, reads the workspace status word,
+ * clears it, and returns it (MLA_OK when the kernels found nothing wrong), or
+ * MLA_ERR_CUDA if the stream reports a CUDA error. */
+int mla_check_errors(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

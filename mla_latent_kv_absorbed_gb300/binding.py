@@ -1,0 +1,192 @@
+"""Thin ctypes binding of libmla_decode.so (include/mla_decode.h).
+
+Argument marshalling only: every step of the decode path runs in the
+library's kernels.  torch is used for device memory and streams.  Importing
+this module loads the library and raises if it has not been built (there is
+no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla_decode.so")
+
+MLA_OK = 0
+STATUS_NAMES = {
+    0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
+    4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT", 6: "MLA_ERR_INDEX_OOB", 7: "MLA_ERR_PLAN_MISMATCH",
+}
+EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
+           "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with mla_latent_kv_absorbed_gb300.build.build()")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
+_c_szp = ctypes.POINTER(ctypes.c_size_t)
+_vp = ctypes.c_void_p
+
+_lib.mla_status_string.restype = ctypes.c_char_p
+_lib.mla_status_string.argtypes = [ctypes.c_int]
+_lib.mla_abi_version.restype = ctypes.c_int
+_lib.mla_decode_plan.restype = ctypes.c_int
+_lib.mla_decode_plan.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
+                                 ctypes.c_size_t, _c_szp, _c_szp]
+_lib.mla_decode_run.restype = ctypes.c_int
+_lib.mla_decode_run.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, ctypes.c_float,
+                                _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.mla_decode_attend.restype = ctypes.c_int
+_lib.mla_decode_attend.argtypes = _lib.mla_decode_run.argtypes
+_lib.mla_decode_merge.restype = ctypes.c_int
+_lib.mla_decode_merge.argtypes = [_vp, _vp, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.mla_merge_states.restype = ctypes.c_int
+_lib.mla_merge_states.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, _vp, ctypes.c_int32,
+                                  _vp, _vp]
+_lib.mla_check_errors.restype = ctypes.c_int
+_lib.mla_check_errors.argtypes = [_vp, _vp]
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def status_string(status: int) -> str:
+    return _lib.mla_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(_lib.mla_abi_version())
+
+
+def library():
+    return _lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return int(t.data_ptr())
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    h = getattr(stream, "cuda_stream", stream)
+    return int(h) if h else None
+
+
+def decode_plan(kv_indptr_host, num_heads: int, num_sms: int = 0):
+    """Host plan for a batch.  Returns (plan words as int32 numpy array, workspace bytes)."""
+    indptr = np.ascontiguousarray(np.asarray(kv_indptr_host), dtype=np.int32)
+    B = indptr.shape[0] - 1
+    need = ctypes.c_size_t(0)
+    ws = ctypes.c_size_t(0)
+    st = _lib.mla_decode_plan(indptr.ctypes.data, B, int(num_heads), int(num_sms), None, 0,
+                              ctypes.byref(need), ctypes.byref(ws))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_plan")
+    plan = np.zeros(need.value, dtype=np.int32)
+    st = _lib.mla_decode_plan(indptr.ctypes.data, B, int(num_heads), int(num_sms), plan.ctypes.data,
+                              plan.shape[0], ctypes.byref(need), ctypes.byref(ws))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_plan")
+    return plan, int(ws.value)
+
+
+def _out_dtype(out, where):
+    import torch
+    code = {torch.float32: 0, torch.bfloat16: 1}.get(out.dtype)
+    if code is None:
+        raise MLAError(2, where + ": out dtype")
+    return code
+
+
+def decode_run(plan_host: np.ndarray, plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
+               sm_scale: float, out, lse, workspace, stream=None, _entry="mla_decode_run") -> None:
+    """Launch the decode (and merge) kernels.  Tensors are torch CUDA tensors:
+    q_nope bf16 [B,H,512], q_rope bf16 [B,H,64], kv_cache bf16 [slots,576],
+    kv_indptr/kv_indices int32, out fp32 or bf16 [B,H,512], lse fp32 [B,H] or
+    None, workspace uint8 (zero-filled before first use)."""
+    out_dtype = _out_dtype(out, _entry)
+    plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    st = getattr(_lib, _entry)(plan_host.ctypes.data, _ptr(plan_dev), _ptr(q_nope), _ptr(q_rope),
+                             _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(kv_indptr), _ptr(kv_indices),
+                             float(sm_scale), _ptr(out), out_dtype, _ptr(lse), _ptr(workspace),
+                             int(workspace.numel() * workspace.element_size()), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, _entry)
+
+
+def decode_attend(plan_host, plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse,
+                  workspace, stream=None) -> None:
+    """The decode kernel alone (whole requests to out/lse, cut ones to partials)."""
+    decode_run(plan_host, plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse,
+               workspace, stream, _entry="mla_decode_attend")
+
+
+def decode_merge(plan_host, plan_dev, out, lse, workspace, stream=None) -> None:
+    """The plan's LSE merge of partial states (no launch if nothing was cut)."""
+    out_dtype = _out_dtype(out, "mla_decode_merge")
+    plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    st = _lib.mla_decode_merge(plan_host.ctypes.data, _ptr(plan_dev), _ptr(out), out_dtype, _ptr(lse),
+                               _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                               _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_merge")
+
+
+def merge_states(v_partial, s_partial, merge_indptr, out, lse, stream=None) -> None:
+    out_dtype = _out_dtype(out, "mla_merge_states")
+    B = int(merge_indptr.shape[0]) - 1
+    H = int(v_partial.shape[1])
+    st = _lib.mla_merge_states(_ptr(v_partial), _ptr(s_partial), _ptr(merge_indptr), B, H, _ptr(out),
+                               out_dtype, _ptr(lse), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_merge_states")
+
+
+def check_errors(workspace, stream=None) -> int:
+    """Synchronise, read and clear the device status; returns the status code."""
+    return int(_lib.mla_check_errors(_ptr(workspace), _stream_handle(stream)))
+
+
+class Decoder:
+    """Convenience holder: plan once per batch shape, then run on device tensors."""
+
+    def __init__(self, kv_indptr_host, num_heads: int, device="cuda", num_sms: int = 0):
+        import torch
+        self.plan_host, self.workspace_bytes = decode_plan(kv_indptr_host, num_heads, num_sms)
+        self.plan_dev = torch.from_numpy(self.plan_host).to(device)
+        self.workspace = torch.zeros(max(self.workspace_bytes, 256), dtype=torch.uint8, device=device)
+        self.num_heads = num_heads
+
+    @property
+    def header(self):
+        return self.plan_host[:16]
+
+    def run(self, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse, stream=None):
+        decode_run(self.plan_host, self.plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
+                   sm_scale, out, lse, self.workspace, stream)
+
+    def attend(self, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse, stream=None):
+        decode_attend(self.plan_host, self.plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
+                      sm_scale, out, lse, self.workspace, stream)
+
+    def merge(self, out, lse, stream=None):
+        decode_merge(self.plan_host, self.plan_dev, out, lse, self.workspace, stream)
+
+    @property
+    def has_merge(self) -> bool:
+        return int(self.plan_host[10]) > 0
+
+    def check(self, stream=None) -> int:
+        return check_errors(self.workspace, stream)

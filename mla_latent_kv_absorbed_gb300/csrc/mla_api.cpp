@@ -1,0 +1,256 @@
+// The C ABI of libmla_decode.so (declared in include/mla_decode.h): argument
+// checks, the host plan, TMA descriptor encoding and kernel dispatch.  Nothing
+// here allocates device memory or synchronises except mla_check_errors.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "mla_launch.h"
+#include "mla_plan.h"
+
+using namespace mla;
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] array, box {box_cols, box_rows},
+// 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool plan_header_ok(const int32_t* h) {
+  if (!h || h[kHMagic] != kPlanMagic || h[kHVersion] != kPlanVersion) return false;
+  int T = 0, cpw = 0;
+  const int v = variant_for_heads(h[kHHeads], &T, &cpw);
+  if (!v || v != h[kHVariant] || T != h[kHTile] || cpw != h[kHCtasPerWorker]) return false;
+  if (h[kHBatch] < 0 || h[kHWorkers] < 1 || h[kHItems] < 0 || h[kHPartials] < 0 || h[kHMerges] < 0)
+    return false;
+  const long long words = kHeaderWords + (static_cast<long long>(h[kHWorkers]) + 1) +
+                          4ll * h[kHItems] + 3ll * h[kHMerges];
+  return words == h[kHTotalWords];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_INDEX_OOB: return "MLA_ERR_INDEX_OOB";
+    case MLA_ERR_PLAN_MISMATCH: return "MLA_ERR_PLAN_MISMATCH";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_abi_version(void) { return 1; }
+
+int mla_decode_plan(const int32_t* kv_indptr, int32_t batch, int32_t num_heads, int32_t num_sms,
+                    int32_t* plan, size_t plan_words, size_t* plan_words_needed,
+                    size_t* workspace_bytes) {
+  if (batch < 0 || !kv_indptr) return MLA_ERR_INVALID_ARG;
+  if (kv_indptr[0] != 0) return MLA_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b)
+    if (kv_indptr[b + 1] < kv_indptr[b]) return MLA_ERR_INVALID_ARG;
+  int T = 0, cpw = 0;
+  if (!variant_for_heads(num_heads, &T, &cpw)) return MLA_ERR_UNSUPPORTED;
+  if (num_sms < 0) return MLA_ERR_INVALID_ARG;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+  }
+  std::vector<int32_t> words;
+  size_t ws = 0;
+  const int st = build_plan(kv_indptr, batch, num_heads, num_sms, words, &ws);
+  if (st != MLA_OK) return st;
+  if (plan_words_needed) *plan_words_needed = words.size();
+  if (workspace_bytes) *workspace_bytes = ws;
+  if (!plan) return MLA_OK;
+  if (plan_words < words.size()) return MLA_ERR_WORKSPACE;
+  std::memcpy(plan, words.data(), words.size() * sizeof(int32_t));
+  return MLA_OK;
+}
+
+namespace {
+
+int check_run_args(const int32_t* plan_host, const int32_t* plan_dev, int32_t out_dtype, void* workspace,
+                   size_t workspace_bytes) {
+  if (!plan_header_ok(plan_host) || !plan_dev) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != 0 && out_dtype != 1) return MLA_ERR_UNSUPPORTED;
+  const size_t need = kWsHeaderBytes +
+                      static_cast<size_t>(plan_host[kHPartials]) * plan_host[kHHeads] * (kLatent + 1) * 4;
+  if (!workspace || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+}  // namespace
+
+int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope,
+                      const void* q_rope, const void* kv_cache, int64_t num_slots,
+                      const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale, void* out,
+                      int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  const int rc0 = check_run_args(plan_host, plan_dev, out_dtype, workspace, workspace_bytes);
+  if (rc0 != MLA_OK) return rc0;
+  if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+  const int B = plan_host[kHBatch], H = plan_host[kHHeads];
+  if (B == 0 || plan_host[kHItems] == 0) return MLA_OK;
+  if (!q_nope || !q_rope || !kv_cache || !kv_indptr || !kv_indices || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(kv_cache) || !aligned16(out) ||
+      !aligned16(kv_indices) || (lse && !aligned16(lse)))
+    return MLA_ERR_INVALID_ARG;
+  if (num_slots < 1 || num_slots > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p{};
+  p.plan = plan_dev;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.out = out;
+  p.lse = lse;
+  p.part_o = reinterpret_cast<float*>(ws + ws_part_o_offset());
+  p.part_lse = reinterpret_cast<float*>(ws + ws_part_lse_offset(plan_host));
+  p.status = reinterpret_cast<int*>(ws);
+  p.num_slots = num_slots;
+  p.batch = B;
+  p.heads = H;
+  p.out_bf16 = out_dtype;
+  p.items_off = plan_items_off(plan_host);
+  p.num_workers = plan_host[kHWorkers];
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+
+  CUtensorMap tm_kv, tm_qn, tm_qr;
+  const uint64_t qrows = static_cast<uint64_t>(B) * H;
+  if (!make_map(&tm_kv, kv_cache, kRow, static_cast<uint64_t>(num_slots), 64, 1) ||
+      !make_map(&tm_qr, q_rope, kRope, qrows, 64, static_cast<uint32_t>(H)))
+    return MLA_ERR_CUDA;
+  if (plan_host[kHVariant] == kVariantSwab) {
+    if (!make_map(&tm_qn, q_nope, kLatent, qrows, 64, static_cast<uint32_t>(H))) return MLA_ERR_CUDA;
+    return launch_swab(H, tm_kv, tm_qn, tm_qr, p, plan_host[kHWorkers], st);
+  }
+  if (!make_map(&tm_qn, q_nope, kLatent, qrows, 64, 1)) return MLA_ERR_CUDA;
+  return launch_pair(H, tm_kv, tm_qn, tm_qr, p, plan_host[kHWorkers], st);
+}
+
+int mla_decode_merge(const int32_t* plan_host, const int32_t* plan_dev, void* out, int32_t out_dtype,
+                     float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc0 = check_run_args(plan_host, plan_dev, out_dtype, workspace, workspace_bytes);
+  if (rc0 != MLA_OK) return rc0;
+  if (plan_host[kHBatch] == 0 || plan_host[kHMerges] == 0) return MLA_OK;
+  if (!out || !aligned16(out) || (lse && !aligned16(lse))) return MLA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  MergeParams m{};
+  m.part_o = reinterpret_cast<const float*>(ws + ws_part_o_offset());
+  m.part_lse = reinterpret_cast<const float*>(ws + ws_part_lse_offset(plan_host));
+  m.list = plan_dev + plan_merge_off(plan_host);
+  m.indptr = nullptr;
+  m.n_entries = plan_host[kHMerges];
+  m.heads = plan_host[kHHeads];
+  m.out = out;
+  m.out_bf16 = out_dtype;
+  m.lse = lse;
+  return launch_merge(m, m.n_entries, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_decode_run(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope,
+                   const void* q_rope, const void* kv_cache, int64_t num_slots,
+                   const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale, void* out,
+                   int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  const int rc = mla_decode_attend(plan_host, plan_dev, q_nope, q_rope, kv_cache, num_slots, kv_indptr,
+                                   kv_indices, sm_scale, out, out_dtype, lse, workspace, workspace_bytes,
+                                   stream);
+  if (rc != MLA_OK) return rc;
+  return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_merge_states(const float* v_partial, const float* s_partial, const int32_t* merge_indptr,
+                     int32_t batch, int32_t num_heads, void* out, int32_t out_dtype, float* lse,
+                     void* stream) {
+  if (batch < 0 || num_heads < 1 || num_heads > 65535) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != 0 && out_dtype != 1) return MLA_ERR_UNSUPPORTED;
+  if (batch == 0) return MLA_OK;
+  if (!v_partial || !s_partial || !merge_indptr || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(v_partial) || !aligned16(out) || (lse && !aligned16(lse))) return MLA_ERR_INVALID_ARG;
+  MergeParams m{};
+  m.part_o = v_partial;
+  m.part_lse = s_partial;
+  m.list = nullptr;
+  m.indptr = merge_indptr;
+  m.n_entries = batch;
+  m.heads = num_heads;
+  m.out = out;
+  m.out_bf16 = out_dtype;
+  m.lse = lse;
+  return launch_merge(m, batch, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_check_errors(void* workspace, void* stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  int status = 0;
+  if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (status != 0) {
+    if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+  }
+  return status;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Shared between the host shim and the kernels: status codes, the plan word
+// layout and the launch parameter blocks.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+constexpr int kLatent = 512;       // kv_lora_rank
+constexpr int kRope = 64;          // qk_rope_head_dim
+constexpr int kRow = kLatent + kRope;  // 576 bf16 per cache row
+
+// ---- plan words --------------------------------------------------------
+constexpr int32_t kPlanMagic = 0x4D4C4131;
+constexpr int32_t kPlanVersion = 1;
+constexpr int kHeaderWords = 16;
+enum PlanHeader : int {
+  kHMagic = 0, kHVersion, kHBatch, kHHeads, kHVariant, kHTile, kHWorkers, kHChunkTiles,
+  kHItems, kHPartials, kHMerges, kHHeadGroups, kHCtasPerWorker, kHTotalWords, kHNumSms,
+  kHReserved
+};
+constexpr int kVariantSwab = 1;  // H in {16, 32}: one CTA per worker, 128-token tiles
+constexpr int kVariantPair = 2;  // H in 48..128: a 2-CTA cluster per worker, 64-token tiles
+constexpr int kItemOverheadTiles = 1;
+constexpr int kMergeCostTiles = 4;
+constexpr int kNumCandidates = 8;
+constexpr size_t kWsHeaderBytes = 256;
+
+// offsets of the plan arrays, from the header
+inline int plan_wptr_off(const int32_t* h) { (void)h; return kHeaderWords; }
+inline int plan_items_off(const int32_t* h) { return kHeaderWords + h[kHWorkers] + 1; }
+inline int plan_merge_off(const int32_t* h) { return plan_items_off(h) + 4 * h[kHItems]; }
+
+// ---- kernel parameters -------------------------------------------------
+struct DecodeParams {
+  const int32_t* plan;        // device plan words
+  const int32_t* kv_indptr;   // device [B+1]
+  const int32_t* kv_indices;  // device [nnz]
+  const uint16_t* q_nope;     // device bf16 [B, H, 512] (read directly by the pair kernel)
+  void* out;                  // [B, H, 512] fp32 or bf16
+  float* lse;                 // [B, H] or null
+  float* part_o;              // [P, H, 512]
+  float* part_lse;            // [P, H]
+  int* status;                // workspace status word
+  long long num_slots;
+  int batch;
+  int heads;
+  int out_bf16;
+  int items_off;
+  int num_workers;
+  float scale_log2;           // sm_scale * log2(e)
+};
+
+struct MergeParams {
+  const float* part_o;
+  const float* part_lse;
+  const int32_t* list;        // plan merge entries (b, p0, p1) x n, or null
+  const int32_t* indptr;      // CSR partial ranges [B+1] (when list is null)
+  int n_entries;
+  int heads;
+  void* out;
+  int out_bf16;
+  float* lse;
+};
+
+}  // namespace mla

@@ -1,0 +1,143 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports
+every entry point include/*.h declares, its plan matches the restatement in
+oracle/plan_ref.py word for word, and bad arguments are rejected on the host
+before any launch."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from mla_latent_kv_absorbed_gb300 import build
+    build.build()
+    from mla_latent_kv_absorbed_gb300 import binding
+    return binding
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(mla_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(B):
+    declared = _declared_functions()
+    assert "mla_decode_run" in declared and "mla_decode_plan" in declared
+    lib = B.library()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(B.EXPORTS) <= set(declared)
+    assert B.abi_version() == 1
+
+
+def test_status_strings(B):
+    for code, name in B.STATUS_NAMES.items():
+        assert B.status_string(code) == name
+    assert B.status_string(99) == "MLA_ERR_UNKNOWN"
+
+
+def _cases():
+    rng = np.random.default_rng(5)
+    out = [([0], 16), ([0, 0, 0], 128), ([0, 1], 16), ([0, 1], 128), ([0, 131072], 128),
+           ([0, 65536, 196608], 128), ([0, 7, 7, 40, 2000], 32), ([0, 4096] * 1, 64)]
+    for H in (16, 32, 48, 64, 96, 112, 128):
+        for _ in range(6):
+            Bn = int(rng.integers(1, 260))
+            L = rng.integers(0, 6000, size=Bn)
+            if rng.random() < 0.4:
+                L[rng.integers(0, Bn)] = int(rng.integers(30000, 140000))
+            out.append((np.concatenate([[0], np.cumsum(L)]).tolist(), H))
+    return out
+
+
+@pytest.mark.parametrize("sms", [152, 148, 7])
+def test_plan_matches_restatement_bit_exact(B, sms):
+    from oracle import plan_ref as PR
+    for indptr, H in _cases():
+        words, ws = B.decode_plan(np.asarray(indptr, dtype=np.int32), H, num_sms=sms)
+        ref_words, ref_ws = PR.build_plan(indptr, H, sms)
+        assert words.tolist() == ref_words, (indptr[:5], H)
+        assert ws == ref_ws
+
+
+def test_plan_workloads_bit_exact(B):
+    from oracle import plan_ref as PR
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    for n, spec in W.WORKLOADS.items():
+        rng = np.random.default_rng(spec.seed)
+        L = W.draw_lengths(spec, rng)
+        indptr = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+        words, ws = B.decode_plan(indptr, spec.heads, num_sms=152)
+        ref, ref_ws = PR.build_plan(indptr.tolist(), spec.heads, 152)
+        assert words.tolist() == ref and ws == ref_ws
+
+
+def _plan_raw(B, indptr, H, sms=152, plan_words=None):
+    lib = B.library()
+    arr = np.ascontiguousarray(indptr, dtype=np.int32)
+    need, ws = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    buf = None if plan_words is None else np.zeros(plan_words, dtype=np.int32)
+    st = lib.mla_decode_plan(arr.ctypes.data, arr.shape[0] - 1, H, sms,
+                             None if buf is None else buf.ctypes.data, 0 if buf is None else plan_words,
+                             ctypes.byref(need), ctypes.byref(ws))
+    return st, need.value, ws.value
+
+
+def test_plan_rejects_bad_input(B):
+    assert _plan_raw(B, [1, 5], 16)[0] == 1            # indptr[0] != 0
+    assert _plan_raw(B, [0, 5, 3], 16)[0] == 1         # decreasing
+    assert _plan_raw(B, [0, 5], 8)[0] == 2             # unsupported heads
+    assert _plan_raw(B, [0, 5], 136)[0] == 2
+    assert _plan_raw(B, [0, 5], 16, sms=-1)[0] == 1
+    st, need, _ = _plan_raw(B, [0, 5, 9], 16)
+    assert st == 0 and need > 16
+    st2, need2, _ = _plan_raw(B, [0, 5, 9], 16, plan_words=need - 1)
+    assert st2 == 3 and need2 == need                   # too small, size still reported
+    lib = B.library()
+    assert lib.mla_decode_plan(None, 1, 16, 152, None, 0, None, None) == 1
+
+
+def test_run_rejects_bad_arguments_before_launch(B):
+    lib = B.library()
+    plan, ws_bytes = B.decode_plan(np.array([0, 100, 300], dtype=np.int32), 16, num_sms=152)
+    fake = 1 << 20   # never dereferenced: every case below fails its host check first
+
+    def run(plan_host=plan, plan_dev=fake, ws=fake, ws_bytes=ws_bytes, out_dtype=0, slots=1000, q=fake,
+            scale=0.1):
+        ph = None if plan_host is None else np.ascontiguousarray(plan_host, dtype=np.int32)
+        return lib.mla_decode_run(None if ph is None else ph.ctypes.data, plan_dev, q, fake, fake, slots,
+                                  fake, fake, ctypes.c_float(scale), fake, out_dtype, fake, ws, ws_bytes,
+                                  None)
+
+    assert run(plan_host=None) == 1
+    bad = plan.copy(); bad[0] = 0
+    assert run(plan_host=bad) == 1                       # magic
+    bad = plan.copy(); bad[13] += 1
+    assert run(plan_host=bad) == 1                       # word count
+    assert run(plan_dev=None) == 1
+    assert run(out_dtype=3) == 2
+    assert run(ws=None) == 1
+    assert run(ws=fake + 4) == 1                         # misaligned workspace
+    assert run(ws_bytes=0) == 3 if plan[9] > 0 else True
+    assert run(slots=0) == 1
+    assert run(q=fake + 2) == 1                          # misaligned q_nope
+    assert run(scale=float("nan")) == 1
+
+
+def test_merge_rejects_bad_arguments(B):
+    lib = B.library()
+    assert lib.mla_merge_states(None, None, None, -1, 16, None, 0, None, None) == 1
+    assert lib.mla_merge_states(None, None, None, 2, 16, None, 5, None, None) == 2
+    assert lib.mla_merge_states(None, None, None, 2, 16, None, 0, None, None) == 1
+    assert lib.mla_merge_states(None, None, None, 0, 16, None, 0, None, None) == 0
+    assert lib.mla_check_errors(None, None) == 1
