@@ -28,8 +28,8 @@
  *   - No function throws or aborts; each returns an mla_status.  Arguments are
  *     checked on the host before any launch; on a bad argument nothing is
  *     launched and nothing is written.
- *   - Supported head counts: 16 and 32 (one CTA per SM, 128-token tiles) and
- *     48..128 in steps of 16 (a two-CTA cluster per worker, 64-token tiles).
+ *   - Supported head counts: 16 and 32 (one CTA per SM) and 48..128 in steps
+ *     of 16 (a two-CTA cluster per worker); both work in 64-token tiles.
  *     kv_lora_rank is 512 and qk_rope_head_dim is 64; nothing else is built.
  *   - The natural log is used for every LSE.
  */
@@ -76,7 +76,7 @@ int mla_abi_version(void);
  *   workspace_bytes    out: device workspace bytes mla_decode_run needs for this
  *                      plan (fp32 partial states plus a 256-byte status header).
  *
- * Rule: tiles of T tokens (T = 128 for H <= 32, 64 otherwise); W workers =
+ * Rule: tiles of T = 64 tokens; W workers =
  * SMs (H <= 32) or SMs/2; candidate chunk sizes ceil(ceil(total_tiles/W)/k)
  * for k = 1..8; requests cut into chunks; chunks placed longest-first on the
  * least-loaded worker; the candidate with the smallest makespan (plus a fixed

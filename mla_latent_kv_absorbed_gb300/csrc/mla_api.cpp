@@ -153,6 +153,7 @@ int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev, const v
   p.kv_indptr = kv_indptr;
   p.kv_indices = kv_indices;
   p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.kv_cache = static_cast<const uint8_t*>(kv_cache);
   p.out = out;
   p.lse = lse;
   p.part_o = reinterpret_cast<float*>(ws + ws_part_o_offset());

@@ -5,7 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/mla_decode.h"
+#include "mla_decode.h"
 
 namespace mla {
 
@@ -40,6 +40,7 @@ struct DecodeParams {
   const int32_t* kv_indptr;   // device [B+1]
   const int32_t* kv_indices;  // device [nnz]
   const uint16_t* q_nope;     // device bf16 [B, H, 512] (read directly by the pair kernel)
+  const uint8_t* kv_cache;    // device [num_slots, 576] bf16 rows (for whole-row L2 prefetch)
   void* out;                  // [B, H, 512] fp32 or bf16
   float* lse;                 // [B, H] or null
   float* part_o;              // [P, H, 512]

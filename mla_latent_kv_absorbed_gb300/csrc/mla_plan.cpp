@@ -4,9 +4,8 @@
 // chunking per request and balances long and short contexts across SMs.  The
 // page states the goal, not a rule; the rule below is this library's.)
 //
-//   * variant by head count: H in {16, 32} -> 128-token tiles, one CTA per
-//     worker; H in 48..128 (step 16) -> 64-token tiles, a 2-CTA cluster per
-//     worker;
+//   * variant by head count: H in {16, 32} -> one CTA per worker; H in
+//     48..128 (step 16) -> a 2-CTA cluster per worker; 64-token tiles for both;
 //   * W workers = SMs / CTAs-per-worker;
 //   * candidate chunk sizes c_k = max(1, ceil(ceil(total_tiles / W) / k)),
 //     k = 1..8, duplicates dropped;
@@ -78,7 +77,7 @@ long long place(std::vector<Chunk> chunks, int W, std::vector<std::vector<Chunk>
 
 int variant_for_heads(int H, int* tile, int* ctas_per_worker) {
   if (H == 16 || H == 32) {
-    *tile = 128;
+    *tile = 64;
     *ctas_per_worker = 1;
     return kVariantSwab;
   }

@@ -1,64 +1,76 @@
 // Absorbed MLA decode for few heads (H = 16 or 32) on sm_103a.
 //
-// With only 16 or 32 query heads the tensor core's 128-row M side cannot be
-// the heads, so both products run "swapped": tokens (or latent dims) on M,
-// heads on N.
+// With only 16 or 32 query heads the tensor core's M side cannot be the
+// heads, so both products run "swapped": tokens (or latent dims) on M, heads
+// on N.
 //
-//   QK:  S^T[128 tok x H]   = K_tile[128 tok x 576] . Q[H x 576]^T       (K-major A and B)
-//   PV:  O^T[128 dim x H]  += V^T[128 dim x 128 tok] . P^T[128 tok x H]   (A read MN-major
-//                                                                          from the same tile)
+//   QK:  S^T[64 tok x H]    = K_tile[64 tok x 576] . Q[H x 576]^T        (M = 64, K-major A and B)
+//   PV:  O^T[128 dim x H]  += V^T[128 dim x 64 tok] . P^T[64 tok x H]    (M = 128, A read MN-major
+//                                                                         from the same tile)
 //
-// The latent rows are gathered from the page-size-1 cache with TMA gather4
-// (four slots per instruction) into 128-byte-swizzled "atoms" of 128 tokens x
-// 64 dims (16 KB): 8 latent atoms and 1 rope atom per 128-token tile.  Each
-// latent atom is read twice by the tensor core -- once as part of the key
-// (score over 576) and once as the value (latent reused as V) -- and leaves
-// shared memory after its PV, so every cache byte crosses HBM once.
+// The rows of a request are gathered from the page-size-1 cache with TMA
+// gather4 (four slots per instruction) into 128-byte-swizzled "atoms" of 64
+// tokens x 64 dims (8 KB): 8 latent atoms and 1 rope atom per 64-token tile.
+// Latent atoms travel in pairs (16 KB ring units, the 128 latent dims one PV
+// block consumes), one 32-lane gather4 instruction per unit.
+// Each latent atom is read twice by the tensor core -- as part of the key
+// (score over 576) and as the value (latent reused as V) -- and is released
+// after its PV, so every cache byte crosses HBM once.
 // ("实现差距：MLA 与 DeepSeek V3", section 2.4: dual-path score, FA2-style
 // online softmax, kv_c reused as the value; "Attention backends", paragraph
 // "MLA": 576 wide for k and 512 for v, one shared vector per token.)
 //
-// Warp roles (256 threads, one CTA per SM, persistent over the plan's items):
-//   warp 0     gather producer (32 lanes, 4 tokens each, one gather4 per atom)
-//   warp 1     MMA issuer (one thread)
-//   warp 2     TMEM allocator and query loader (TMA)
-//   warps 4-7  softmax / epilogue: thread t owns token row t of S^T and latent
-//              row t of every O^T block.
+// The shared-memory ring holds 2.5 (H=16) or 2 (H=32) tiles, so the gather of
+// the next tile runs while the current one is scored.  A single warp issuing
+// gather4 saturates near a fifth of HBM bandwidth, so four producer warps
+// split each tile's units between them.
+//
+// Warp roles (one CTA per SM, persistent over the plan's work items):
+//   warps 0-3   softmax / epilogue (TMEM lane quadrants 0-3)
+//   warp 4      MMA issuer (one thread)
+//   warp 5      TMEM allocator and query loader (TMA)
+//   warp 6      index stager: slot numbers to shared memory, rows prefetched into L2
+//   warps 7-10  gather producers
+// With M = 64 the score tile S^T puts token rows 16q..16q+15 in TMEM lanes
+// 32q..32q+15 (q = lane quadrant); O^T (M = 128) puts latent dim r in lane r.
 //
 // Softmax: scores are scaled into log2 units; each head keeps a reference
 // maximum m_ref that only moves when a tile exceeds it by more than 8 (a
-// group vote per tile).  Then O and the running sums are rescaled once; so
+// group vote per tile); then O and the running sums are rescaled once.  So
 // P = 2^(s - m_ref) <= 256 always fits bf16 and the fp32 sums.
-#include <cstdio>
-
 #include "mla_device.cuh"
 #include "mla_launch.h"
 
 namespace mla {
 namespace swab {
 
+constexpr int kProducers = 4;
+constexpr int kIdxSlots = 4;              // tiles of slot indices staged ahead (also the L2 prefetch distance)
+constexpr int kProducerWarp0 = 7;
+constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
+
 template <int NH>
 struct Cfg {
-  static constexpr int T = 128;                    // tokens per tile
-  static constexpr int kLatSlots = (NH == 16) ? 10 : 8;  // even: atom pairs never wrap
-  static constexpr int kRopeSlots = 2;
-  static constexpr int kAtom = T * 128;            // 16 KB
+  static constexpr int T = 64;                           // tokens per tile
+  static constexpr int kPairSlots = (NH == 16) ? 10 : 8;  // ring of latent atom pairs (16 KB each)
+  static constexpr int kRopeSlots = 4;
+  static constexpr int kAtom = T * 128;                  // 8 KB: 64 tokens x 64 dims
+  static constexpr int kPair = 2 * kAtom;                // dims 128u .. 128u+127
   static constexpr int kQAtom = NH * 128;
   static constexpr int kQBytes = 9 * kQAtom;
-  static constexpr int kPAtom = NH * 128;          // NH heads x 64 tokens
-  static constexpr int kPBytes = 2 * kPAtom;       // 128 tokens
+  static constexpr int kPBytes = NH * 128;               // P^T: NH heads x 64 tokens
   static constexpr int kOffLat = 0;
-  static constexpr int kOffRope = kOffLat + kLatSlots * kAtom;
+  static constexpr int kOffRope = kOffLat + kPairSlots * kPair;
   static constexpr int kOffQ = kOffRope + kRopeSlots * kAtom;
   static constexpr int kOffP = kOffQ + kQBytes;
-  static constexpr int kOffRed = kOffP + 2 * kPBytes;   // [2][4][NH] floats
+  static constexpr int kOffRed = kOffP + 2 * kPBytes;    // [2][4][NH] floats
   static constexpr int kOffBar = kOffRed + 2 * 4 * NH * 4;
   // barrier indices
   static constexpr int bLatFull = 0;
-  static constexpr int bLatEmpty = kLatSlots;
-  static constexpr int bRopeFull = 2 * kLatSlots;
-  static constexpr int bRopeEmpty = bRopeFull + 2;
-  static constexpr int bQFull = bRopeEmpty + 2;
+  static constexpr int bLatEmpty = kPairSlots;
+  static constexpr int bRopeFull = 2 * kPairSlots;
+  static constexpr int bRopeEmpty = bRopeFull + kRopeSlots;
+  static constexpr int bQFull = bRopeEmpty + kRopeSlots;
   static constexpr int bQEmpty = bQFull + 1;
   static constexpr int bSFull = bQEmpty + 1;
   static constexpr int bSEmpty = bSFull + 2;
@@ -68,16 +80,21 @@ struct Cfg {
   static constexpr int bOFull = bPvDone + 1;
   static constexpr int bOEmpty = bOFull + 1;
   static constexpr int bDrain = bOEmpty + 1;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bIdxFull = bDrain + 1;
+  static constexpr int bIdxEmpty = bIdxFull + kIdxSlots;
+  static constexpr int kNumBars = bIdxEmpty + kIdxSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+  static constexpr int kOffLast = kOffMisc + 16;           // [kPairSlots + kRopeSlots] ints
+  static constexpr int kOffIdx = (kOffLast + 4 * (kPairSlots + kRopeSlots) + 15) / 16 * 16;   // [kIdxSlots][T] ints
+  static constexpr int kSmemBytes = kOffIdx + 4 * kIdxSlots * T + 1024;   // + alignment slack
   static constexpr int kTmemCols = (6 * NH <= 128) ? 128 : 256;
   static constexpr int kTmS = 0;       // S^T buffers: columns [0,NH) and [NH,2NH)
   static constexpr int kTmO = 2 * NH;  // O^T blocks: columns 2NH + mb*NH
-  static constexpr uint32_t kIdescQK = idesc_bf16(128, NH, false, false);
+  static constexpr uint32_t kIdescQK = idesc_bf16(64, NH, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(128, NH, true, false);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "atoms must be 1024-byte aligned");
+  static_assert(kOffIdx % 16 == 0, "index ring alignment");
 };
 
 __device__ __forceinline__ bool item_ok(const DecodeParams& p, int b, int s, int e) {
@@ -147,8 +164,38 @@ __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&r)[
   }
 }
 
+// A tile is five ring units: latent atom pairs u = 0..3 (dims 128u..128u+127,
+// 16 KB) and the rope atom u = 4 (8 KB).  Returns the unit's ring position.
+struct UnitRef {
+  uint32_t addr, full, empty, use, slot;
+  bool rope;
+};
+
 template <int NH>
-__global__ void __launch_bounds__(256, 1)
+__device__ __forceinline__ UnitRef unit_ref(uint32_t base, uint32_t g, int u) {
+  using C = Cfg<NH>;
+  UnitRef r;
+  if (u < 4) {
+    const uint32_t seq = g * 4 + u;
+    r.slot = seq % C::kPairSlots;
+    r.use = seq / C::kPairSlots;
+    r.addr = base + C::kOffLat + r.slot * C::kPair;
+    r.full = base + C::kOffBar + 8u * (C::bLatFull + r.slot);
+    r.empty = base + C::kOffBar + 8u * (C::bLatEmpty + r.slot);
+    r.rope = false;
+  } else {
+    r.slot = g % C::kRopeSlots;
+    r.use = g / C::kRopeSlots;
+    r.addr = base + C::kOffRope + r.slot * C::kAtom;
+    r.full = base + C::kOffBar + 8u * (C::bRopeFull + r.slot);
+    r.empty = base + C::kOffBar + 8u * (C::bRopeEmpty + r.slot);
+    r.rope = true;
+  }
+  return r;
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 1)
     swab_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qn,
                 const __grid_constant__ CUtensorMap tm_qr, const DecodeParams p) {
   using C = Cfg<NH>;
@@ -160,6 +207,7 @@ __global__ void __launch_bounds__(256, 1)
   auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int* last_armed = reinterpret_cast<int*>(smem + C::kOffLast);   // per ring slot: last armed use
   const WaitCtx wc{abort_flag, p.status};
 
   const int w = blockIdx.x;
@@ -168,19 +216,21 @@ __global__ void __launch_bounds__(256, 1)
   const int32_t* items = p.plan + p.items_off;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kLatSlots; ++i) { mbar_init(bar(C::bLatFull + i), 1); mbar_init(bar(C::bLatEmpty + i), 1); }
+    for (int i = 0; i < C::kPairSlots; ++i) { mbar_init(bar(C::bLatFull + i), 1); mbar_init(bar(C::bLatEmpty + i), 1); }
+    for (int i = 0; i < C::kRopeSlots; ++i) { mbar_init(bar(C::bRopeFull + i), 1); mbar_init(bar(C::bRopeEmpty + i), 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(C::bRopeFull + i), 1); mbar_init(bar(C::bRopeEmpty + i), 1);
       mbar_init(bar(C::bSFull + i), 1); mbar_init(bar(C::bSEmpty + i), 4);
       mbar_init(bar(C::bPFull + i), 4); mbar_init(bar(C::bPEmpty + i), 1);
     }
     mbar_init(bar(C::bQFull), 1); mbar_init(bar(C::bQEmpty), 1);
     mbar_init(bar(C::bPvDone), 1); mbar_init(bar(C::bOFull), 1); mbar_init(bar(C::bOEmpty), 4);
     mbar_init(bar(C::bDrain), 1);
+    for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(C::bIdxFull + i), 1); mbar_init(bar(C::bIdxEmpty + i), kProducers); }
+    for (int i = 0; i < C::kPairSlots + C::kRopeSlots; ++i) last_armed[i] = -1;
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -189,11 +239,16 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------- gather producer
-    if (lane == 0) { tma_prefetch_desc(&tm_kv); }
-    const uint64_t pol = l2_policy_evict_first();
-    uint32_t g = 0, lat_issued = 0, rope_issued = 0;
+  if (warp == 6) {
+    // ---------------------------------------------------------- index stager
+    // Walks the tiles in plan order, loads each tile's 64 slot numbers
+    // (coalesced), replaces out-of-range ones by slot 0 (flagged) and the
+    // ragged tail by the last valid slot, publishes them in a small ring, and
+    // prefetches every row's nine 128-byte lines into L2 together (through
+    // the load/store path, leaving the TMA unit to the gathers), so the nine
+    // gather pieces of a row later hit L2.
+    int* idx_ring = reinterpret_cast<int*>(smem + C::kOffIdx);
+    uint32_t g = 0;
     bool ok = true;
     for (int it = it0; it < it1 && ok; ++it) {
       const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
@@ -202,142 +257,224 @@ __global__ void __launch_bounds__(256, 1)
         continue;
       }
       const int n = e - s;
-      for (int t0 = 0; t0 < n && ok; t0 += C::T, ++g) {
-        int y[4];
+      for (int t0 = 0; t0 < n; t0 += C::T, ++g) {
+        const uint32_t slot = g % kIdxSlots, use = g / kIdxSlots;
+        int v[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) v[k] = __ldg(p.kv_indices + s + min(t0 + lane + 32 * k, n - 1));
+        bool w_ok = true;
+        if (lane == 0 && use > 0) w_ok = mbar_wait(bar(C::bIdxEmpty + slot), (use - 1) & 1, wc);
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) { ok = false; break; }
         bool oob = false;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = min(t0 + 4 * lane + k, n - 1);   // tail rows repeat a valid slot
-          int v = __ldg(p.kv_indices + s + tok);
-          if (v < 0 || static_cast<long long>(v) >= p.num_slots) { oob = true; v = 0; }
-          y[k] = v;
+        for (int k = 0; k < 2; ++k) {
+          if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
+          idx_ring[slot * C::T + lane + 32 * k] = v[k];
+        }
+        // the 9 lines of each of the tile's rows, 18 per lane
+        for (int q = lane; q < 9 * C::T; q += 32) {
+          const int r = q / 9, line = q - 9 * (q / 9);
+          const int lo = __shfl_sync(0xffffffffu, v[0], r & 31);   // row r's slot lives in lane r%32,
+          const int hi = __shfl_sync(0xffffffffu, v[1], r & 31);   // element r/32
+          const int vr = (r >> 5) ? hi : lo;
+          if (t0 + r < n) prefetch_l2_line(p.kv_cache + static_cast<size_t>(vr) * (kRow * 2) + line * 128);
         }
         if (__any_sync(0xffffffffu, oob) && lane == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
-        for (int a = 0; a < 9; ++a) {
-          uint32_t dst, full, empty, use;
-          if (a < 8) {
-            const uint32_t seq = g * 8 + a, slot = seq % C::kLatSlots;
-            use = seq / C::kLatSlots;
-            dst = base + C::kOffLat + slot * C::kAtom;
-            full = bar(C::bLatFull + slot);
-            empty = bar(C::bLatEmpty + slot);
-          } else {
-            const uint32_t slot = g & 1;
-            use = g >> 1;
-            dst = base + C::kOffRope + slot * C::kAtom;
-            full = bar(C::bRopeFull + slot);
-            empty = bar(C::bRopeEmpty + slot);
-          }
-          bool w_ok = true;
-          if (lane == 0 && use > 0) w_ok = mbar_wait(empty, (use - 1) & 1, wc);
-          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-          if (!w_ok) { ok = false; break; }
-          if (lane == 0) mbar_arrive_expect_tx(full, C::kAtom);
-          __syncwarp();
-          tma_gather4(dst + lane * 512, &tm_kv, 64 * a, y[0], y[1], y[2], y[3], full, pol);
-          if (a < 8) ++lat_issued; else ++rope_issued;
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::bIdxFull + slot));
       }
     }
-    // drain: wait for the last armed phase of every slot (in-flight copies)
-    if (lane == 0) {
-      for (uint32_t s = 0; s < (uint32_t)C::kLatSlots; ++s)
-        if (lat_issued > s) drain_wait(bar(C::bLatFull + s), ((lat_issued - 1 - s) / C::kLatSlots) & 1);
-      for (uint32_t s = 0; s < 2; ++s)
-        if (rope_issued > s) drain_wait(bar(C::bRopeFull + s), ((rope_issued - 1 - s) / 2) & 1);
+  } else if (warp >= kProducerWarp0) {
+    // ------------------------------------------------------ gather producers
+    // Producer pw issues the ring units whose running number (5 per tile) is
+    // congruent to pw mod kProducers, one 32-lane gather4 instruction per
+    // unit, with slot numbers taken from the index ring.
+    const int pw = warp - kProducerWarp0;
+    if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
+    const uint64_t pol = l2_policy_evict_first();
+    const int* idx_ring = reinterpret_cast<const int*>(smem + C::kOffIdx);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+      if (!item_ok(p, b, s, e)) continue;
+      const int n = e - s;
+      for (int t0 = 0; t0 < n && ok; t0 += C::T, ++g) {
+        const uint32_t islot = g % kIdxSlots;
+        bool w_ok = true;
+        if (lane == 0) w_ok = mbar_wait(bar(C::bIdxFull + islot), (g / kIdxSlots) & 1, wc);
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) { ok = false; break; }
+        // lane l gathers tokens 4(l%16)..4(l%16)+3; lanes 16-31 take the
+        // second atom of a pair
+        const int4 v = *reinterpret_cast<const int4*>(idx_ring + islot * C::T + 4 * (lane & 15));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::bIdxEmpty + islot));
+        const int first = (pw - static_cast<int>((g * 5) % kProducers) + kProducers) % kProducers;
+        if (lane == 0) MLA_TRACE_EVENT(pw == 0 ? 0 : 8 + pw, g);
+        for (int u = first; u < 5; u += kProducers) {
+          const UnitRef r = unit_ref<NH>(base, g, u);
+          bool e_ok = true;
+          if (lane == 0 && r.use > 0) e_ok = mbar_wait(r.empty, (r.use - 1) & 1, wc);
+          e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+          if (!e_ok) { ok = false; break; }
+          if (lane == 0) mbar_arrive_expect_tx(r.full, r.rope ? C::kAtom : C::kPair);
+          __syncwarp();
+          if (r.rope) {
+            if (lane < 16) tma_gather4(r.addr + lane * 512, &tm_kv, 512, v.x, v.y, v.z, v.w, r.full, pol);
+          } else {
+            const int half = lane >> 4;
+            tma_gather4(r.addr + half * C::kAtom + (lane & 15) * 512, &tm_kv, 64 * (2 * u + half), v.x, v.y, v.z,
+                        v.w, r.full, pol);
+          }
+          if (lane == 0) atomicMax(last_armed + (r.rope ? C::kPairSlots : 0) + r.slot, static_cast<int>(r.use));
+        }
+        if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
+      }
+    }
+    // drain: every copy armed by any producer has landed before the CTA can
+    // exit (slots are shared between producer warps, so use the latest use)
+    named_bar_sync(3, 32 * kProducers);
+    if (pw == 0) {
+      for (int i = lane; i < C::kPairSlots + C::kRopeSlots; i += 32) {
+        const int u = last_armed[i];
+        const int bfull = i < C::kPairSlots ? C::bLatFull + i : C::bRopeFull + (i - C::kPairSlots);
+        if (u >= 0) drain_wait(bar(bfull), u & 1);
+      }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 4) {
     // ----------------------------------------------------------- MMA issuer
+    // An event loop over two cursors: the QK cursor walks (tile, unit) as
+    // ring units land; the PV cursor issues a tile's PV as soon as its P is
+    // ready (PV first: it frees ring slots for the gather).  The issue path is
+    // kept lean -- descriptors are advanced by constant offsets and ring
+    // positions by running counters -- because every instruction of this one
+    // thread sits between two tensor-core operations.
     if (lane == 0) {
-      uint32_t g = 0, nitem = 0;
-      bool ok = true;
-      const uint32_t qbase = base + C::kOffQ;
-      auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-        const uint32_t buf = gp & 1;
-        if (!mbar_wait(bar(C::bPFull + buf), (gp >> 1) & 1, wc)) return false;
-        if (first && nitem > 0 && !mbar_wait(bar(C::bOEmpty), (nitem - 1) & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t lat0 = (gp * 8) % C::kLatSlots;
-        const uint32_t pbase = base + C::kOffP + buf * C::kPBytes;
-#pragma unroll 1
-        for (int mb = 0; mb < 4; ++mb) {
-          const uint32_t slot = (lat0 + 2 * mb) % C::kLatSlots;
-          const uint32_t a_addr = base + C::kOffLat + slot * C::kAtom;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad = sdesc(a_addr + ks * 2048, C::kAtom, 1024);
-            const uint64_t bd = sdesc(pbase + (ks >> 2) * C::kPAtom + (ks & 3) * 32, 16, 1024);
-            umma_ss(tmem + C::kTmO + mb * NH, ad, bd, C::kIdescPV, (first && ks == 0) ? 0u : 1u);
-          }
-          umma_commit(bar(C::bLatEmpty + slot));
-          umma_commit(bar(C::bLatEmpty + slot + 1));
-        }
-        umma_commit(bar(C::bPEmpty + buf));
-        umma_commit(bar(C::bPvDone));
-        return true;
+      const uint64_t dq = sdesc(base + C::kOffQ, 16, 1024);        // Q atom 0 (B of QK)
+      const uint64_t dk = sdesc(base + C::kOffLat, 16, 1024);      // pair slot 0 (A of QK)
+      const uint64_t dr = sdesc(base + C::kOffRope, 16, 1024);     // rope slot 0 (A of QK)
+      const uint64_t dv = sdesc(base + C::kOffLat, C::kAtom, 1024);  // pair slot 0 (A of PV, MN-major)
+      const uint64_t dp = sdesc(base + C::kOffP, 16, 1024);        // P^T buffer 0 (B of PV)
+      const uint32_t bar0 = bar(0);
+      auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
+      auto bar_at = [&](int i) -> uint32_t { return bar0 + 8u * i; };
+      auto next_valid = [&](int it) {
+        while (it < it1 && !item_ok(p, items[4 * it], items[4 * it + 1], items[4 * it + 2])) ++it;
+        return it;
       };
-      // PV of a tile is issued after the QK of the next one (so the softmax
-      // overlaps that QK), or earlier if that QK needs a ring slot the PV frees.
-      int64_t pending = -1;        // tile whose PV is not issued yet
-      bool pending_first = false;
-      for (int it = it0; it < it1 && ok; ++it) {
-        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-        if (!item_ok(p, b, s, e)) continue;
-        const int nt = (e - s + C::T - 1) / C::T;
-        if (!mbar_wait(bar(C::bQFull), nitem & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        for (int j = 0; j < nt; ++j, ++g) {
-          const uint32_t buf = g & 1;
-          if (g >= 2 && !mbar_wait(bar(C::bSEmpty + buf), ((g >> 1) - 1) & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d_s = tmem + C::kTmS + buf * NH;
-          for (int a = 0; a < 9; ++a) {
-            uint32_t src, full, use;
-            if (a < 8) {
-              const uint32_t seq = g * 8 + a, slot = seq % C::kLatSlots;
-              use = seq / C::kLatSlots;
-              src = base + C::kOffLat + slot * C::kAtom;
-              full = bar(C::bLatFull + slot);
-              if (pending >= 0 && seq >= (uint32_t)C::kLatSlots &&
-                  (seq - C::kLatSlots) / 8 == static_cast<uint32_t>(pending)) {
-                if (!issue_pv(static_cast<uint32_t>(pending), pending_first)) { ok = false; break; }
-                pending = -1;
-              }
-            } else {
-              src = base + C::kOffRope + (g & 1) * C::kAtom;
-              use = g >> 1;
-              full = bar(C::bRopeFull + (g & 1));
-            }
-            if (!mbar_wait(full, use & 1, wc)) { ok = false; break; }
+      auto ntiles = [&](int it) { return it < it1 ? (items[4 * it + 2] - items[4 * it + 1] + C::T - 1) / C::T : 0; };
+      // QK cursor
+      int q_it = next_valid(it0), q_nt = ntiles(q_it), q_j = 0, q_u = 0;
+      uint32_t q_g = 0, q_nitem = 0, qs = 0, qph = 0, qr = 0, qrph = 0;
+      bool q_ready = false;
+      // PV cursor
+      int p_it = q_it, p_nt = q_nt, p_j = 0;
+      uint32_t p_g = 0, p_nitem = 0, ps = 0;
+      uint64_t t_last = globaltimer();
+      while (p_it < it1) {
+        bool prog = false;
+        if (p_g < q_g) {
+          const uint32_t buf = p_g & 1;
+          const bool first = p_j == 0;
+          if (mbar_test_wait(bar_at(C::bPFull + buf), (p_g >> 1) & 1) &&
+              (!first || p_nitem == 0 || mbar_test_wait(bar_at(C::bOEmpty), (p_nitem - 1) & 1))) {
             tc_fence_after();
+            MLA_TRACE_EVENT(4, p_g);
+            const uint64_t bp = D(dp, buf * C::kPBytes);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc(src + 32 * kk, 16, 1024);
-              const uint64_t bd = sdesc(qbase + a * C::kQAtom + 32 * kk, 16, 1024);
-              umma_ss(d_s, ad, bd, C::kIdescQK, (a | kk) != 0 ? 1u : 0u);
+            for (int mb = 0; mb < 4; ++mb) {
+              const uint64_t av = D(dv, ps * C::kPair);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ss(tmem + C::kTmO + mb * NH, D(av, ks * 2048), D(bp, ks * 32), C::kIdescPV,
+                        (first && ks == 0) ? 0u : 1u);
+              umma_commit(bar_at(C::bLatEmpty + ps));
+              ps = (ps + 1 == C::kPairSlots) ? 0 : ps + 1;
+            }
+            umma_commit(bar_at(C::bPEmpty + buf));
+            umma_commit(bar_at(C::bPvDone));
+            MLA_TRACE_EVENT(5, p_g);
+            if (++p_j == p_nt) {
+              umma_commit(bar_at(C::bOFull));
+              ++p_nitem;
+              p_it = next_valid(p_it + 1);
+              p_nt = ntiles(p_it);
+              p_j = 0;
+            }
+            ++p_g;
+            prog = true;
+          }
+        }
+        if (!prog && q_it < it1) {
+          if (!q_ready) {
+            q_ready = (q_j != 0 || mbar_test_wait(bar_at(C::bQFull), q_nitem & 1)) &&
+                      (q_g < 2 || mbar_test_wait(bar_at(C::bSEmpty + (q_g & 1)), ((q_g >> 1) - 1) & 1));
+            if (q_ready) MLA_TRACE_EVENT(2, q_g);
+          }
+          if (q_ready) {
+            const uint32_t d_s = tmem + C::kTmS + (q_g & 1) * NH;
+            if (q_u < 4) {
+              if (mbar_test_wait(bar_at(C::bLatFull + qs), qph)) {
+                tc_fence_after();
+                const uint64_t ak = D(dk, qs * C::kPair);
+                const uint64_t bq = D(dq, 2 * q_u * C::kQAtom);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    umma_ss(d_s, D(ak, h * C::kAtom + 32 * kk), D(bq, h * C::kQAtom + 32 * kk), C::kIdescQK,
+                            (q_u | h | kk) != 0 ? 1u : 0u);
+                if (++qs == static_cast<uint32_t>(C::kPairSlots)) { qs = 0; qph ^= 1; }
+                ++q_u;
+                prog = true;
+              }
+            } else if (mbar_test_wait(bar_at(C::bRopeFull + qr), qrph)) {
+              tc_fence_after();
+              const uint64_t ar = D(dr, qr * C::kAtom);
+              const uint64_t bq = D(dq, 8 * C::kQAtom);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) umma_ss(d_s, D(ar, 32 * kk), D(bq, 32 * kk), C::kIdescQK, 1u);
+              umma_commit(bar_at(C::bRopeEmpty + qr));
+              if (++qr == static_cast<uint32_t>(C::kRopeSlots)) { qr = 0; qrph ^= 1; }
+              umma_commit(bar_at(C::bSFull + (q_g & 1)));
+              MLA_TRACE_EVENT(3, q_g);
+              const bool last = q_j == q_nt - 1;
+              if (last) umma_commit(bar_at(C::bQEmpty));
+              q_u = 0;
+              q_ready = false;
+              ++q_g;
+              if (last) {
+                ++q_nitem;
+                q_it = next_valid(q_it + 1);
+                q_nt = ntiles(q_it);
+                q_j = 0;
+              } else {
+                ++q_j;
+              }
+              prog = true;
             }
           }
-          if (!ok) break;
-          umma_commit(bar(C::bSFull + buf));
-          umma_commit(bar(C::bRopeEmpty + (g & 1)));
-          if (j == nt - 1) umma_commit(bar(C::bQEmpty));
-          if (pending >= 0 && !issue_pv(static_cast<uint32_t>(pending), pending_first)) { ok = false; break; }
-          pending = g;
-          pending_first = (j == 0);
         }
-        if (!ok) break;
-        if (!issue_pv(static_cast<uint32_t>(pending), pending_first)) { ok = false; break; }
-        pending = -1;
-        umma_commit(bar(C::bOFull));
-        ++nitem;
+        if (prog) {
+          t_last = globaltimer();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer() - t_last > MLA_WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            record_status(p.status, MLA_ERR_TIMEOUT);
+            break;
+          }
+        }
       }
       // every MMA issued by this thread has completed before TMEM is freed
-      umma_commit(bar(C::bDrain));
-      drain_wait(bar(C::bDrain), 0);
+      umma_commit(bar_at(C::bDrain));
+      drain_wait(bar_at(C::bDrain), 0);
     }
     __syncwarp();
-  } else if (warp == 2) {
+  } else if (warp == 5) {
     // --------------------------------------------------------- query loader
     if (lane == 0) {
       tma_prefetch_desc(&tm_qn);
@@ -356,11 +493,13 @@ __global__ void __launch_bounds__(256, 1)
       if (nitem > 0) drain_wait(bar(C::bQFull), (nitem - 1) & 1);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else {
     // --------------------------------------------------- softmax + epilogue
-    const int t = threadIdx.x - 128;   // token row of S^T; latent row of O^T
-    const int wq = warp & 3;
+    const int wq = warp;                          // lane quadrant
+    const int t = 16 * wq + lane;                 // token row of S^T (lanes 0-15 only)
+    const bool row_lane = lane < 16;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const int dim_row = 32 * wq + lane;           // latent row of O^T (within a 128-dim block)
     float* red = reinterpret_cast<float*>(smem + C::kOffRed);
     int rk = 0;
     uint32_t g = 0, nitem = 0;
@@ -381,6 +520,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int j = 0; j < nt; ++j, ++g) {
         const uint32_t buf = g & 1;
         wait(bar(C::bSFull + buf), (g >> 1) & 1);
+        if (threadIdx.x == 0) MLA_TRACE_EVENT(6, g);
         tc_fence_after();
         uint32_t r[NH];
         if (!aborted) {
@@ -393,7 +533,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(bar(C::bSEmpty + buf));
-        const bool valid = t < n - j * C::T;
+        const bool valid = row_lane && t < n - j * C::T;
         float sv[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) sv[h] = valid ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
@@ -443,13 +583,12 @@ __global__ void __launch_bounds__(256, 1)
           l_part[h] += pv[h];
         }
         if (g >= 2) wait(bar(C::bPEmpty + buf), ((g >> 1) - 1) & 1);
-        if (!aborted) {
+        if (!aborted && row_lane) {
           // P^T[buf]: K-major, 128B swizzle; row = head, 64 tokens per 128-byte row
-          uint8_t* pb = smem + C::kOffP + buf * C::kPBytes + (t >> 6) * C::kPAtom;
-          const int tw = t & 63;
+          uint8_t* pb = smem + C::kOffP + buf * C::kPBytes;
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
-            const int off = (h >> 3) * 1024 + (h & 7) * 128 + ((((tw >> 3) ^ (h & 7)) & 7) << 4) + (tw & 7) * 2;
+            const int off = (h >> 3) * 1024 + (h & 7) * 128 + ((((t >> 3) ^ (h & 7)) & 7) << 4) + (t & 7) * 2;
             *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pv[h]);
           }
         }
@@ -457,6 +596,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(bar(C::bPFull + buf));
+        if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
       }
       // ------------------------------------------------------------ epilogue
       wait(bar(C::bOFull), nitem & 1);
@@ -471,7 +611,7 @@ __global__ void __launch_bounds__(256, 1)
           uint32_t o[NH];
           tmem_ld_row<NH>(tmem + lane_off + C::kTmO + mb * NH, o);
           tmem_wait_ld();
-          const int dim = 128 * mb + t;
+          const int dim = 128 * mb + dim_row;
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             const float v = __uint_as_float(o[h]) / l_tot[h];
@@ -489,9 +629,10 @@ __global__ void __launch_bounds__(256, 1)
       __syncwarp();
       if (lane == 0 && !aborted) mbar_arrive(bar(C::bOEmpty));
       if (!aborted) {
+        const int tid = threadIdx.x;
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          if (t == h) {
+          if (tid == h) {
             const float l = (m_ref[h] + __log2f(l_tot[h])) * 0.69314718055994531f;
             if (part < 0) { if (p.lse) p.lse[static_cast<size_t>(b) * p.heads + h] = l; }
             else p.part_lse[static_cast<size_t>(part) * p.heads + h] = l;
@@ -505,21 +646,21 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == 5) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 template <int NH>
 int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap& tm_qr,
            const DecodeParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<NH>;
-  static bool attr_done = false;   // per process; the attribute is per function
+  static bool attr_done = false;   // the attribute is per function, set once per process
   if (!attr_done) {
     if (cudaFuncSetAttribute(swab_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return MLA_ERR_CUDA;
     attr_done = true;
   }
-  swab_kernel<NH><<<grid, 256, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
+  swab_kernel<NH><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -531,7 +672,5 @@ int launch_swab(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_qn,
   if (heads == 32) return swab::launch<32>(tm_kv, tm_qn, tm_qr, p, grid, stream);
   return MLA_ERR_UNSUPPORTED;
 }
-
-int swab_tile_tokens() { return swab::Cfg<16>::T; }
 
 }  // namespace mla

@@ -9,9 +9,9 @@ ragged batches" -- the CSR arrays are rebuilt on the CPU for each batch and
 plan() chooses the split-KV chunking per request and balances long and short
 contexts across SMs.  They give no rule, so this is the one the library uses:
 
-  * kernel variant by head count: H in {16, 32} -> "swab" (one CTA per SM,
-    128-token tiles); H in {48, 64, ..., 128} -> "pair" (a two-CTA cluster
-    per worker, 64-token tiles);
+  * kernel variant by head count: H in {16, 32} -> "swab" (one CTA per SM);
+    H in {48, 64, ..., 128} -> "pair" (a two-CTA cluster per worker); both
+    work in 64-token tiles;
   * W workers = SMs (swab) or SMs // 2 (pair);
   * tiles_b = ceil(L_b / T); total = sum tiles_b; base = ceil(total / W);
   * candidate chunk sizes (in tiles) c_k = max(1, ceil(base / k)), k = 1..8,
@@ -53,7 +53,7 @@ VARIANT_PAIR = 2
 def variant_for_heads(H: int):
     """(variant, tile_tokens, ctas_per_worker) or None when H is unsupported."""
     if H in (16, 32):
-        return VARIANT_SWAB, 128, 1
+        return VARIANT_SWAB, 64, 1
     if 48 <= H <= 128 and H % 16 == 0:
         return VARIANT_PAIR, 64, 2
     return None

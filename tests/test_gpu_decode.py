@@ -31,7 +31,7 @@ def test_tiny_workload_full():
     assert dec.header[4] == 1   # few-heads kernel variant ran
 
 
-@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("H", [16, 32, 48, 64, 112, 128])
 def test_ragged_tails_small(H):
     # lengths around the 128-token tile edges, plus an empty request
     bt = _batch([1, 2, 3, 127, 128, 129, 0, 255, 256, 257, 1000, 64], H, seed=H)
@@ -40,7 +40,7 @@ def test_ragged_tails_small(H):
     assert_close(out, lse, ro, rl)
 
 
-@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("H", [16, 32, 128])
 def test_split_and_merge_long_request(H):
     # one long request is cut over every worker and merged by LSE
     bt = _batch([20000, 3], H, seed=7)
@@ -50,9 +50,10 @@ def test_split_and_merge_long_request(H):
     assert_close(out, lse, ro, rl)
 
 
-def test_bf16_output():
+@pytest.mark.parametrize("H", [16, 128])
+def test_bf16_output(H):
     import torch
-    bt = _batch([100, 513, 1], 16, seed=3)
+    bt = _batch([100, 513, 1], H, seed=3)
     (out, lse), _ = run_gpu(bt, out_dtype=torch.bfloat16)
     ro, rl = oracle(bt)
     assert_close(out, lse, ro, rl)
@@ -68,8 +69,9 @@ def test_lse_optional_and_duplicate_slots():
     assert_close(out, None, ro, rl)
 
 
-def test_repeat_runs_bit_identical_and_slot_relabelling():
-    bt = _batch([300, 1, 4000, 77], 16, seed=5)
+@pytest.mark.parametrize("H", [16, 128])
+def test_repeat_runs_bit_identical_and_slot_relabelling(H):
+    bt = _batch([300, 1, 4000, 77], H, seed=5)
     runs, _ = run_gpu(bt, repeat=2)
     (o1, l1), (o2, l2) = runs
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
@@ -82,12 +84,13 @@ def test_repeat_runs_bit_identical_and_slot_relabelling():
     assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
 
 
-def test_forced_chunkings_agree():
+@pytest.mark.parametrize("H", [16, 128])
+def test_forced_chunkings_agree(H):
     # different SM counts give different plans; all must match the oracle
-    bt = _batch([3000, 5000, 12, 900], 16, seed=6)
+    bt = _batch([3000, 5000, 12, 900], H, seed=6)
     ro, rl = oracle(bt)
     dev = to_device(bt)
-    for sms in (152, 40, 7, 1):
+    for sms in ((152, 40, 7, 1) if H <= 32 else (152, 40, 8, 2)):
         (out, lse), dec = run_gpu(bt, dev=dev, num_sms=sms)
         assert_close(out, lse, ro, rl)
 
@@ -117,17 +120,18 @@ def test_v2lite_workload_sampled():
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
-def test_attend_then_merge_equals_run():
+@pytest.mark.parametrize("H", [16, 128])
+def test_attend_then_merge_equals_run(H):
     import torch
     from mla_latent_kv_absorbed_gb300 import binding
-    bt = _batch([9000, 40, 3000], 16, seed=12)
+    bt = _batch([9000, 40, 3000], H, seed=12)
     dev = to_device(bt)
-    dec = binding.Decoder(bt.kv_indptr, 16)
+    dec = binding.Decoder(bt.kv_indptr, H)
     assert dec.has_merge
     outs = []
     for mode in ("run", "split"):
-        out = torch.full((bt.batch, 16, 512), float("nan"), device="cuda")
-        lse = torch.full((bt.batch, 16), float("nan"), device="cuda")
+        out = torch.full((bt.batch, H, 512), float("nan"), device="cuda")
+        lse = torch.full((bt.batch, H), float("nan"), device="cuda")
         args = (dev["q_nope"], dev["q_rope"], dev["kv_cache"], dev["kv_indptr"], dev["kv_indices"], bt.sm_scale,
                 out, lse)
         if mode == "run":
@@ -163,3 +167,24 @@ def test_public_merge_states_matches_oracle_merge():
         fin = np.isfinite(rl)
         np.testing.assert_allclose(l[b][fin], rl[fin], atol=1e-5)
         assert np.all(np.isneginf(l[b][~fin]))
+
+
+def test_pair_kernel_variant_and_empty_requests():
+    bt = _batch([0, 65, 0, 200, 0], 128, seed=13)
+    (out, lse), dec = run_gpu(bt)
+    assert dec.header[4] == 2   # two-CTA cluster variant ran
+    ro, rl = oracle(bt)
+    assert_close(out, lse, ro, rl)
+    assert np.all(out[[0, 2, 4]] == 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("number", [3, 4, 5])
+def test_many_head_workloads_sampled(number):
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    bt = W.make_workload(number)
+    (out, lse), _ = run_gpu(bt)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    req = sorted(set([0, bt.batch - 1] + list(range(0, bt.batch, max(1, bt.batch // 6)))))
+    ro, rl = oracle(bt, requests=req)
+    assert_close(out, lse, ro, rl, requests=req)
