@@ -32,7 +32,7 @@
 //   warp 4      MMA issuer (one thread, event loop)
 //   warp 5      TMEM allocator and rope-query loader (TMA)
 //   warp 6      index stager (slot numbers to shared memory, L2 row prefetch)
-//   warps 7-10  gather producers (producer pw issues tiles g = pw mod 4)
+//   warps 7-10  gather producers (every producer takes a slice of every tile)
 //
 // Softmax per head is thread-local (a head is a TMEM lane), with a lazily
 // moved reference maximum (threshold 8 in log2 units) as in the few-heads
@@ -48,7 +48,7 @@ constexpr int kProducers = 4;
 constexpr int kIdxSlots = 4;
 constexpr int kProducerWarp0 = 7;
 constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
-constexpr int kLatBlocks = 4;                // must equal kProducers (producer pw owns block pw)
+constexpr int kLatBlocks = 4;                // ring of latent blocks (all producers fill every block)
 constexpr int kRopeSlots = 4;
 constexpr int kAtom = T * 128;               // 8 KB: 64 tokens x 64 dims
 constexpr int kLatBlock = 4 * kAtom;         // 32 KB: 64 tokens x 256 dims
@@ -84,7 +84,7 @@ constexpr int kSmemBytes = kOffLast + 4 * (kLatBlocks + kRopeSlots) + 1024;
 constexpr int kTmO = 0, kTmQ = 256, kTmS = 384;
 constexpr uint32_t kIdescQK = idesc_bf16(128, T, false, false);     // M=128 heads, N=64 tokens
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // N=256 dims, B (V) MN-major
-static_assert(kLatBlocks == kProducers, "one latent ring block per producer warp");
+static_assert(kProducers == 4, "producer pw gathers latent atom pw of the CTA's four");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 16 == 0 && kOffIdx % 16 == 0, "alignment");
 
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bXFull), 1);
     mbar_init(bar(bXEmpty), 4);                  // the peer's four softmax warps
     mbar_init(bar(bDrain), 1);
-    for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(bIdxFull + i), 1); mbar_init(bar(bIdxEmpty + i), 1); }
+    for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(bIdxFull + i), 1); mbar_init(bar(bIdxEmpty + i), kProducers); }
     for (int i = 0; i < kLatBlocks + kRopeSlots; ++i) last_armed[i] = -1;
     *abort_flag = 0;
     fence_mbar_init();
@@ -207,9 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
-    // Producer pw gathers tiles g = pw (mod 4): the CTA's 256 latent dims
-    // (four atoms, two 32-lane gather4 instructions) into latent block pw,
-    // and the rope atom into rope slot g mod 4.
+    // A warp completes one gather4 only every ~70-110 cycles, so a tile's
+    // landing time is set by how many gathers one warp issues for it.  All
+    // four producers therefore share every tile: producer pw gathers latent
+    // atom pw of the CTA's half (16 gathers) and rope gathers 4pw..4pw+3.
     const int pw = warp - kProducerWarp0;
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
     const uint64_t pol = l2_policy_evict_first();
@@ -221,36 +222,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!item_ok(p, b, s, e)) continue;
       const int n = e - s;
       for (int t0 = 0; t0 < n && ok; t0 += T, ++g) {
-        if (static_cast<int>(g % kProducers) != pw) continue;
         const uint32_t islot = g % kIdxSlots;
         bool w_ok = true;
         if (lane == 0) w_ok = mbar_wait(bar(bIdxFull + islot), (g / kIdxSlots) & 1, wc);
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) { ok = false; break; }
+        // lane l < 16 holds tokens 4l..4l+3 (gather op l of an atom)
         const int4 v = *reinterpret_cast<const int4*>(idx_ring + islot * T + 4 * (lane & 15));
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bIdxEmpty + islot));
-        const int half = lane >> 4;
-        // latent block
+        if (lane == 0 && pw == 0) MLA_TRACE_EVENT(0, g);
+        // rope ops 4pw + r (r = 0..3) take the tokens of op 4pw + r
+        const int src = 4 * pw + (lane & 3);
+        const int r0 = __shfl_sync(0xffffffffu, v.x, src), r1 = __shfl_sync(0xffffffffu, v.y, src);
+        const int r2 = __shfl_sync(0xffffffffu, v.z, src), r3 = __shfl_sync(0xffffffffu, v.w, src);
+        // latent atom pw into block g mod 4
         {
-          const uint32_t use = g / kLatBlocks;
+          const uint32_t blk = g % kLatBlocks, use = g / kLatBlocks;
           bool e_ok = true;
-          if (lane == 0 && use > 0) e_ok = mbar_wait(bar(bLatEmpty + pw), (use - 1) & 1, wc);
+          if (lane == 0 && use > 0) e_ok = mbar_wait(bar(bLatEmpty + blk), (use - 1) & 1, wc);
           e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
           if (!e_ok) { ok = false; break; }
-          const uint32_t full = bar(bLatFull + pw);
-          if (lane == 0) mbar_arrive_expect_tx(full, kLatBlock);
+          const uint32_t full = bar(bLatFull + blk);
+          if (lane == 0 && pw == 0) mbar_arrive_expect_tx(full, kLatBlock);
           __syncwarp();
-          const uint32_t dst = base + kOffLat + pw * kLatBlock + (lane & 15) * 512;
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int atom = 2 * k + half;       // 0..3 within the CTA's half
-            tma_gather4(dst + atom * kAtom, &tm_kv, 64 * (4 * static_cast<int>(cta) + atom), v.x, v.y, v.z, v.w,
-                        full, pol);
-          }
-          if (lane == 0) atomicMax(last_armed + pw, static_cast<int>(use));
+          if (lane < 16)
+            tma_gather4(base + kOffLat + blk * kLatBlock + pw * kAtom + lane * 512, &tm_kv,
+                        64 * (4 * static_cast<int>(cta) + pw), v.x, v.y, v.z, v.w, full, pol);
+          if (lane == 0) atomicMax(last_armed + blk, static_cast<int>(use));
         }
-        // rope atom
+        // rope slice
         {
           const uint32_t rs = g % kRopeSlots, use = g / kRopeSlots;
           bool e_ok = true;
@@ -258,11 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
           if (!e_ok) { ok = false; break; }
           const uint32_t full = bar(bRopeFull + rs);
-          if (lane == 0) mbar_arrive_expect_tx(full, kAtom);
+          if (lane == 0 && pw == 0) mbar_arrive_expect_tx(full, kAtom);
           __syncwarp();
-          if (lane < 16)
-            tma_gather4(base + kOffRope + rs * kAtom + lane * 512, &tm_kv, 512, v.x, v.y, v.z, v.w, full, pol);
+          if (lane < 4)
+            tma_gather4(base + kOffRope + rs * kAtom + (4 * pw + lane) * 512, &tm_kv, 512, r0, r1, r2, r3, full, pol);
           if (lane == 0) atomicMax(last_armed + kLatBlocks + rs, static_cast<int>(use));
+          if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
         }
       }
     }
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (mbar_test_wait(bar_at(bPFull + buf), (p_g >> 1) & 1) &&
               (!first || p_nitem == 0 || mbar_test_wait(bar_at(bOEmpty), (p_nitem - 1) & 1))) {
             tc_fence_after();
+            MLA_TRACE_EVENT(4, p_g);
             const uint32_t blk = p_g % kLatBlocks;
             const uint64_t bv = D(dv, blk * kLatBlock);
             const uint32_t a_p = tmem + kTmS + buf * 64;           // P: 64 tokens as 32 packed columns
@@ -311,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(bar_at(bLatEmpty + blk));
             umma_commit(bar_at(bSFree + buf));
             umma_commit(bar_at(bPvDone));
+            MLA_TRACE_EVENT(5, p_g);
             if (++p_j == p_nt) {
               umma_commit(bar_at(bOFull));
               ++p_nitem;
@@ -333,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t blk = q_g % kLatBlocks;
               if (mbar_test_wait(bar_at(bLatFull + blk), (q_g / kLatBlocks) & 1)) {
                 tc_fence_after();
+                MLA_TRACE_EVENT(2, q_g);
                 const uint64_t bk = D(dk, blk * kLatBlock);
 #pragma unroll
                 for (int k = 0; k < 16; ++k)      // 256 latent dims = 16 K-steps; A (query) from TMEM
@@ -353,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(bar_at(bRopeEmpty + rs));
                 umma_commit(bar_at(bSFull + (q_g & 1)));
+                MLA_TRACE_EVENT(3, q_g);
                 const bool last = q_j == q_nt - 1;
                 if (last) umma_commit(bar_at(bQEmpty));
                 q_u = 0;
@@ -447,12 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0 && !aborted) mbar_arrive(bar(bQFull));
 
-      for (int j = 0; j < nt; ++j, ++g) {
-        const uint32_t buf = g & 1;
-        const uint32_t tm_s = tmem + lane_off + kTmS + buf * 64;
-        wait(bar(bSFull + buf), (g >> 1) & 1, false);
+      // The exchange is software-pipelined: tile j+1's partial row is sent as
+      // soon as tile j's has been read, so the transfer runs under tile j's
+      // softmax.  `sr` holds this CTA's partial row of the tile in flight.
+      uint32_t sr[64];
+      auto stage_send = [&](uint32_t gg) {
+        const uint32_t tm_s = tmem + lane_off + kTmS + (gg & 1) * 64;
+        wait(bar(bSFull + (gg & 1)), (gg >> 1) & 1, false);
+        if (threadIdx.x == 0) MLA_TRACE_EVENT(6, gg);
         tc_fence_after();
-        uint32_t sr[64];
         if (!aborted) {
           tmem_ld64(tm_s, sr);
           tmem_wait_ld();
@@ -460,36 +469,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 64; ++i) sr[i] = 0;
         }
-        // send my partial row to the peer once it has read the previous one
         if (warp == 0 && lane == 0 && !aborted) mbar_arrive_expect_tx(bar(bXFull), 128 * 64 * 4);
-        if (g > 0) wait(bar(bXEmpty), (g - 1) & 1, true);
+        if (gg > 0) wait(bar(bXEmpty), (gg - 1) & 1, true);      // the peer has read tile gg-1
         if (!aborted) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             st_async_v4(x_row_peer + 16 * i, sr[4 * i], sr[4 * i + 1], sr[4 * i + 2], sr[4 * i + 3], x_full_peer);
         }
+      };
+      stage_send(g);
+      for (int j = 0; j < nt; ++j, ++g) {
+        const uint32_t buf = g & 1;
+        const uint32_t tm_s = tmem + lane_off + kTmS + buf * 64;
         wait(bar(bXFull), g & 1, true);
+        if (threadIdx.x == 0) MLA_TRACE_EVENT(9, g);
+        // s = (CTA0 partial + CTA1 partial) in log2 units; the same sum order in both CTAs
         float sv[64];
-        const int nvalid = n - j * T;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           uint4 pv = make_uint4(0, 0, 0, 0);
-          if (!aborted) asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(pv.x), "=r"(pv.y), "=r"(pv.z), "=r"(pv.w) : "r"(x_row + 16 * i));
-          // identical sum order in both CTAs: (CTA0 partial) + (CTA1 partial)
-          const float o0 = __uint_as_float(sr[4 * i]), o1 = __uint_as_float(sr[4 * i + 1]);
-          const float o2 = __uint_as_float(sr[4 * i + 2]), o3 = __uint_as_float(sr[4 * i + 3]);
-          const float q0 = __uint_as_float(pv.x), q1 = __uint_as_float(pv.y);
-          const float q2 = __uint_as_float(pv.z), q3 = __uint_as_float(pv.w);
-          sv[4 * i] = (cta == 0 ? o0 + q0 : q0 + o0) * p.scale_log2;
-          sv[4 * i + 1] = (cta == 0 ? o1 + q1 : q1 + o1) * p.scale_log2;
-          sv[4 * i + 2] = (cta == 0 ? o2 + q2 : q2 + o2) * p.scale_log2;
-          sv[4 * i + 3] = (cta == 0 ? o3 + q3 : q3 + o3) * p.scale_log2;
-        }
+          if (!aborted)
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(pv.x), "=r"(pv.y), "=r"(pv.z), "=r"(pv.w)
+                         : "r"(x_row + 16 * i));
+          const uint32_t q[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-        for (int t = 0; t < 64; ++t)
-          if (t >= nvalid) sv[t] = -INFINITY;
+          for (int k = 0; k < 4; ++k) {
+            const float own = __uint_as_float(sr[4 * i + k]), oth = __uint_as_float(q[k]);
+            sv[4 * i + k] = (cta == 0 ? own + oth : oth + own) * p.scale_log2;
+          }
+        }
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive_cluster(bar(bXEmpty), peer);   // the peer may send again
+        if (j + 1 < nt) stage_send(g + 1);       // next partial goes out while this tile is scored
+        const int nvalid = n - j * T;
+        if (nvalid < T) {
+#pragma unroll
+          for (int t = 0; t < 64; ++t)
+            if (t >= nvalid) sv[t] = -INFINITY;
+        }
         float mt = sv[0];
 #pragma unroll
         for (int t = 1; t < 64; ++t) mt = fmaxf(mt, sv[t]);
@@ -523,12 +541,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P = 2^(s - m_ref) as bf16 pairs over the score buffer
         uint32_t pk[32];
+        float l0 = 0.f, l1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float a = ex2_approx(sv[2 * i] - m_ref), c = ex2_approx(sv[2 * i + 1] - m_ref);
-          l_sum += a + c;
+          l0 += a;
+          l1 += c;
           pk[i] = pack_bf16x2(a, c);
         }
+        l_sum += l0 + l1;
         if (!aborted) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -542,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(bar(bPFull + buf));
+        if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
       }
       // ------------------------------------------------------------ epilogue
       wait(bar(bOFull), nitem & 1, false);

@@ -22,8 +22,8 @@
 //
 // The shared-memory ring holds 2.5 (H=16) or 2 (H=32) tiles, so the gather of
 // the next tile runs while the current one is scored.  A single warp issuing
-// gather4 saturates near a fifth of HBM bandwidth, so four producer warps
-// split each tile's units between them.
+// gather4 completes one op every ~70-110 cycles, so four producer warps
+// share every tile (a tile lands in about a quarter of the time).
 //
 // Warp roles (one CTA per SM, persistent over the plan's work items):
 //   warps 0-3   softmax / epilogue (TMEM lane quadrants 0-3)
@@ -287,9 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
-    // Producer pw issues the ring units whose running number (5 per tile) is
-    // congruent to pw mod kProducers, one 32-lane gather4 instruction per
-    // unit, with slot numbers taken from the index ring.
+    // A warp completes one gather4 only every ~70-110 cycles, so a tile's
+    // landing time is set by how many gathers one warp issues for it.  All
+    // four producers share every tile: producer pw gathers latent atoms pw
+    // and pw+4 (16 gathers each) and rope gathers 4pw..4pw+3.  A pair unit
+    // is armed by the producer of its even atom; the rope by producer 0.
     const int pw = warp - kProducerWarp0;
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
     const uint64_t pol = l2_policy_evict_first();
@@ -306,27 +308,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) w_ok = mbar_wait(bar(C::bIdxFull + islot), (g / kIdxSlots) & 1, wc);
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) { ok = false; break; }
-        // lane l gathers tokens 4(l%16)..4(l%16)+3; lanes 16-31 take the
-        // second atom of a pair
+        // lane l < 16 holds tokens 4l..4l+3 (gather op l of an atom)
         const int4 v = *reinterpret_cast<const int4*>(idx_ring + islot * C::T + 4 * (lane & 15));
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::bIdxEmpty + islot));
-        const int first = (pw - static_cast<int>((g * 5) % kProducers) + kProducers) % kProducers;
         if (lane == 0) MLA_TRACE_EVENT(pw == 0 ? 0 : 8 + pw, g);
-        for (int u = first; u < 5; u += kProducers) {
-          const UnitRef r = unit_ref<NH>(base, g, u);
+        const int src = 4 * pw + (lane & 3);
+        const int r0 = __shfl_sync(0xffffffffu, v.x, src), r1 = __shfl_sync(0xffffffffu, v.y, src);
+        const int r2 = __shfl_sync(0xffffffffu, v.z, src), r3 = __shfl_sync(0xffffffffu, v.w, src);
+#pragma unroll 1
+        for (int k = 0; k < 3 && ok; ++k) {
+          const int a = k == 0 ? pw : k == 1 ? pw + 4 : 8;     // latent atom, latent atom, rope slice
+          const UnitRef r = unit_ref<NH>(base, g, a < 8 ? a >> 1 : 4);
           bool e_ok = true;
           if (lane == 0 && r.use > 0) e_ok = mbar_wait(r.empty, (r.use - 1) & 1, wc);
           e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
           if (!e_ok) { ok = false; break; }
-          if (lane == 0) mbar_arrive_expect_tx(r.full, r.rope ? C::kAtom : C::kPair);
+          const bool arms = r.rope ? pw == 0 : (a & 1) == 0;
+          if (lane == 0 && arms) mbar_arrive_expect_tx(r.full, r.rope ? C::kAtom : C::kPair);
           __syncwarp();
           if (r.rope) {
-            if (lane < 16) tma_gather4(r.addr + lane * 512, &tm_kv, 512, v.x, v.y, v.z, v.w, r.full, pol);
-          } else {
-            const int half = lane >> 4;
-            tma_gather4(r.addr + half * C::kAtom + (lane & 15) * 512, &tm_kv, 64 * (2 * u + half), v.x, v.y, v.z,
-                        v.w, r.full, pol);
+            if (lane < 4) tma_gather4(r.addr + (4 * pw + lane) * 512, &tm_kv, 512, r0, r1, r2, r3, r.full, pol);
+          } else if (lane < 16) {
+            tma_gather4(r.addr + (a & 1) * C::kAtom + lane * 512, &tm_kv, 64 * a, v.x, v.y, v.z, v.w, r.full, pol);
           }
           if (lane == 0) atomicMax(last_armed + (r.rope ? C::kPairSlots : 0) + r.slot, static_cast<int>(r.use));
         }
