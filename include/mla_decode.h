@@ -158,6 +158,39 @@ int mla_merge_states(const float* v_partial, const float* s_partial, const int32
                      int32_t batch, int32_t num_heads, void* out, int32_t out_dtype, float* lse,
                      void* stream);
 
+/* mla_decode_run_noalloc -- mla_decode_run without a caller-provided workspace.
+ *
+ * No counterpart on the pages: this entry point exists for callers that are
+ * not allowed to allocate device memory at the point of the call -- code
+ * running inside a memory arena owned by another runtime, plugins that only
+ * receive tensors they did not allocate, or a decode step that must not call
+ * cudaMalloc while it runs.  It takes the same arguments as mla_decode_run
+ * except the workspace: the split-KV partial states and the device status go
+ * to one static device buffer of MLA_NOALLOC_SCRATCH_BYTES (32 MiB) that is
+ * part of the library image, so every GPU that loads the library holds it
+ * until the process exits.
+ *
+ *   - The first call on a device looks the buffer's device address up for
+ *     that device (a runtime query, no allocation); make that first call
+ *     before any stream capture.
+ *   - Plans whose partial states do not fit (256 B + P*H*513*4 bytes larger
+ *     than MLA_NOALLOC_SCRATCH_BYTES) are rejected with MLA_ERR_WORKSPACE
+ *     and nothing is launched.
+ *   - Every call shares the one buffer: calls that overlap on the GPU (on
+ *     different streams, or from different threads) race and corrupt each
+ *     other's partial states.  Serialise them on one stream.
+ *   - Each call clears the buffer's status word before its kernels run;
+ *     device-side status (bad slot indices, timeouts) of this variant is not
+ *     readable by the caller.
+ *   - Nothing here calls cudaMalloc, cudaFree or an allocating routine. */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* plan_dev,
+                           const void* q_nope, const void* q_rope,
+                           const void* kv_cache, int64_t num_slots,
+                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                           float sm_scale, void* out, int32_t out_dtype, float* lse,
+                           void* stream);
+
 /* mla_check_errors -- synchronises `stream`, reads the workspace status word,
  * clears it, and returns it (MLA_OK when the kernels found nothing wrong), or
  * MLA_ERR_CUDA if the stream reports a CUDA error. */

@@ -22,7 +22,9 @@ STATUS_NAMES = {
     4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT", 6: "MLA_ERR_INDEX_OOB", 7: "MLA_ERR_PLAN_MISMATCH",
 }
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
-           "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors")
+           "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
+           "mla_decode_run_noalloc")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with mla_latent_kv_absorbed_gb300.build.build()")
@@ -48,6 +50,9 @@ _lib.mla_decode_merge.argtypes = [_vp, _vp, _vp, ctypes.c_int32, _vp, _vp, ctype
 _lib.mla_merge_states.restype = ctypes.c_int
 _lib.mla_merge_states.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, _vp, ctypes.c_int32,
                                   _vp, _vp]
+_lib.mla_decode_run_noalloc.restype = ctypes.c_int
+_lib.mla_decode_run_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp, ctypes.c_float, _vp,
+                                        ctypes.c_int32, _vp, _vp]
 _lib.mla_check_errors.restype = ctypes.c_int
 _lib.mla_check_errors.argtypes = [_vp, _vp]
 
@@ -142,6 +147,20 @@ def decode_merge(plan_host, plan_dev, out, lse, workspace, stream=None) -> None:
                                _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_decode_merge")
+
+
+def decode_run_noalloc(plan_host, plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse,
+                       stream=None) -> None:
+    """mla_decode_run without a workspace: for callers that cannot allocate
+    device memory.  Partial states live in the library's static 32 MiB
+    device buffer, shared by every call -- calls must not overlap on the GPU."""
+    out_dtype = _out_dtype(out, "mla_decode_run_noalloc")
+    plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    st = _lib.mla_decode_run_noalloc(plan_host.ctypes.data, _ptr(plan_dev), _ptr(q_nope), _ptr(q_rope),
+                                     _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(kv_indptr), _ptr(kv_indices),
+                                     float(sm_scale), _ptr(out), out_dtype, _ptr(lse), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_run_noalloc")
 
 
 def merge_states(v_partial, s_partial, merge_indptr, out, lse, stream=None) -> None:
