@@ -55,30 +55,38 @@ def algorithmic_work(batch):
     return bytes_, flops
 
 
-def kernel_source_sha():
+KERNEL_SOURCES = {
+    "swab": ("mla_swab.cu", "mla_device.cuh", "mla_internal.h", "mla_launch.h"),
+    "pair": ("mla_pair.cu", "mla_device.cuh", "mla_internal.h", "mla_launch.h"),
+}
+
+
+def kernel_source_sha(kernel):
+    """Digest of the sources that make up one decode kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_absorbed_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload_name):
-    """DRAM bytes per decode-kernel launch from the committed ncu summary, or
-    None when absent or taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+def ncu_traffic(workload_name, kernel):
+    """DRAM bytes (read + write) per decode-kernel launch from the committed
+    ncu summary profiles/ncu_traffic.txt, or None when there is no entry or
+    the entry was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d[workload_name]
-        if e.get("source_sha") != kernel_source_sha():
-            return None
-        return float(e["dram_bytes_per_launch"])
-    except Exception:
-        return None
+            for line in f:
+                parts = line.split()
+                if len(parts) == 4 and not line.startswith("#") and parts[0] == workload_name \
+                        and parts[1] == kernel:
+                    return float(parts[2]) if parts[3] == kernel_source_sha(kernel) else None
+    except OSError:
+        pass
+    return None
 
 
 class ClockSampler:
@@ -346,7 +354,8 @@ def run_ours(args, batch, world, rank, local, pg):
     else:
         roof = {"bound": "tensor", "achieved": tflops_attend, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": tflops_attend / peaks["bf16_tflops"]}
-    roof["traffic"] = ncu_traffic(batch.spec.name if batch.spec else "custom")
+    kernel = "swab" if H <= 32 else "pair"
+    roof["traffic"] = ncu_traffic(batch.spec.name if batch.spec else "custom", kernel)
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
     roof["kernel"] = "mla_decode (swab)" if H <= 32 else "mla_decode (pair)"
     roof["kernel_ms"] = attend_avg
