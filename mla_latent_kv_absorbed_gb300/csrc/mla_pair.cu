@@ -7,9 +7,10 @@
 // of every row and half of the rope key.
 //
 //   QK (per CTA, partial):  S_c[128 h x 64 tok] = Q[:, D_c] . K[:, D_c]^T  (+ its rope half)
-//   exchange:               S = S_0 + S_1   (each CTA sends its fp32 partial
-//                           to the other through distributed shared memory)
-//   softmax:                the same P in both CTAs (identical inputs)
+//   exchange:               each CTA sends its partial row of every head to
+//                           the other through distributed shared memory
+//   combine:                S = S_0 + S_1, identical in both CTAs
+//   softmax:                the same P in both CTAs
 //   PV (per CTA):           O_c[128 h x 256] += P[128 x 64 tok] . V[64 tok x D_c]
 //
 // so no product is computed twice and no latent byte is loaded twice.
@@ -17,26 +18,47 @@
 // FA2-style online softmax, kv_c reused as the value; "Attention backends",
 // paragraph "MLA": every KV byte used by all 128 heads.)
 //
+// The exchange is the narrow path: an SM moves only about 9 bytes per cycle
+// to its cluster peer, so the partial rows travel as 16-bit fixed point with
+// one power-of-two scale per row (64 scores: 128 B + a 4-byte exponent, half
+// of fp32).  With s_max the largest |partial| of the row, the step is at most
+// 2^-14 s_max and the rounding error at most 2^-15 s_max per partial.  Both
+// CTAs add the two DEQUANTISED partials, so S, P, the running maximum and the
+// row sums are bit-identical in the pair.
+//
 // TMEM (512 columns per CTA): O_c [0,256) fp32; the query's latent half
 // [256,384) as packed bf16 (A operand of QK, read from TMEM); two score
-// buffers [384,448), [448,512).  P (bf16) is written back over the score
-// buffer it came from and is the A operand of PV, read from TMEM.
+// buffers [384,448), [448,512) that hold this CTA's fp32 partial, then its
+// quantised row (32 packed columns and the row exponent).
 //
 // Shared memory per CTA: a ring of 4 latent blocks (64 tokens x 256 dims,
-// 32 KB, gathered with TMA gather4), 4 rope atoms (8 KB), the rope query
-// (16 KB), the exchange buffer for the peer's partial scores (34 KB) and a
-// small ring of slot indices.
+// 32 KB, gathered with TMA gather4), 3 rope atoms (8 KB), the rope query
+// (16 KB), 3 exchange slots (16 KB each: the peer's quantised partial rows,
+// later overwritten in place by P as bf16, the A operand of PV), the peer's
+// row exponents and a small ring of slot indices.
 //
-// Warp roles per CTA (352 threads):
-//   warps 0-3   softmax / epilogue; thread h owns head h (TMEM lane h)
-//   warp 4      MMA issuer (one thread, event loop)
-//   warp 5      TMEM allocator and rope-query loader (TMA)
-//   warp 6      index stager (slot numbers to shared memory, L2 row prefetch)
-//   warps 7-10  gather producers (every producer takes a slice of every tile)
+// Warp roles per CTA (512 threads):
+//   warps 0-3   softmax / epilogue: thread h owns head h (TMEM lane h); adds
+//               the two quantised partials, writes P, keeps m and l
+//   warps 4-7   sender: quantises this CTA's partial, leaves it in TMEM for
+//               the softmax and pushes it to the peer (st.async)
+//   warp 8      QK issuer and rope-query loader (one thread)
+//   warp 9      TMEM allocator and PV issuer (one thread)
+//   warp 10     index stager (slot numbers to shared memory, L2 row prefetch)
+//   warps 11-15 gather producers: latent atoms 0-3 of the CTA's half, rope
 //
-// Softmax per head is thread-local (a head is a TMEM lane), with a lazily
-// moved reference maximum (threshold 8 in log2 units) as in the few-heads
-// kernel; both CTAs take identical rescale decisions.
+// Pushing a tile's rows stalls the issuing warps for as long as the link
+// needs to carry them, so only the sender warps push; nothing on the
+// softmax -> PV -> QK chain waits behind a push.  Per tile g (S buffer
+// g mod 2, exchange slot g mod 3):
+//   QK(g) -> sender quantises, stores the int16 row over the partial in the
+//   S buffer and pushes it into the peer's slot -> softmax waits for the
+//   peer's rows, reads its own from TMEM (freeing the S buffer for
+//   QK(g+2)), adds them, writes P over the peer's rows -> PV(g) frees the
+//   latent block and, through a multicast commit, tells the PEER that its
+//   rows for tile g+3 may land in this slot.
+// The softmax moves its reference maximum lazily (threshold 8 in log2
+// units) as in the few-heads kernel.
 #include "mla_device.cuh"
 #include "mla_launch.h"
 
@@ -44,20 +66,23 @@ namespace mla {
 namespace pair {
 
 constexpr int T = 64;                        // tokens per tile
-constexpr int kProducers = 4;
+constexpr int kProducers = 5;                // latent atoms 0-3 and the rope
 constexpr int kIdxSlots = 4;
-constexpr int kProducerWarp0 = 7;
+constexpr int kMmaWarp = 8, kLoaderWarp = 9, kIdxWarp = 10, kProducerWarp0 = 11;
 constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
-constexpr int kLatBlocks = 4;                // ring of latent blocks (all producers fill every block)
-constexpr int kRopeSlots = 4;
+constexpr int kLatBlocks = 4;                // ring of latent blocks (every latent producer fills every block)
+constexpr int kRopeSlots = 3;
+constexpr int kXSlots = 3;                   // exchange slots
 constexpr int kAtom = T * 128;               // 8 KB: 64 tokens x 64 dims
 constexpr int kLatBlock = 4 * kAtom;         // 32 KB: 64 tokens x 256 dims
-constexpr int kXRow = 64 * 4 + 16;           // exchange row: 64 fp32 + pad (272 B)
+constexpr int kXSlot = 128 * 128;            // 128 rows x 128 B (64 int16 scores, then 64 bf16 P)
+constexpr int kXRowBytes = 128 + 4;          // bytes one head's row carries to the peer
 constexpr int kOffLat = 0;
 constexpr int kOffRope = kOffLat + kLatBlocks * kLatBlock;
 constexpr int kOffQR = kOffRope + kRopeSlots * kAtom;   // rope query: 128 rows x 128 B (K-major SW128)
 constexpr int kOffX = kOffQR + 128 * 128;
-constexpr int kOffIdx = kOffX + 128 * kXRow;
+constexpr int kOffXE = kOffX + kXSlots * kXSlot;        // [kXSlots][128] int32 row exponents from the peer
+constexpr int kOffIdx = kOffXE + kXSlots * 128 * 4;
 constexpr int kOffBar = kOffIdx + 4 * kIdxSlots * T;
 // barriers
 constexpr int bLatFull = 0;
@@ -66,15 +91,16 @@ constexpr int bRopeFull = bLatEmpty + kLatBlocks;
 constexpr int bRopeEmpty = bRopeFull + kRopeSlots;
 constexpr int bQFull = bRopeEmpty + kRopeSlots;
 constexpr int bQEmpty = bQFull + 1;
-constexpr int bSFull = bQEmpty + 1;          // [2]
-constexpr int bPFull = bSFull + 2;           // [2]
-constexpr int bSFree = bPFull + 2;           // [2] (PV done with the P in that buffer)
-constexpr int bPvDone = bSFree + 2;
+constexpr int bSFull = bQEmpty + 1;          // [2] this CTA's partial is in the S buffer
+constexpr int bSQuant = bSFull + 2;          // [2] the quantised row is in the S buffer
+constexpr int bSFree = bSQuant + 2;          // [2] the softmax has read the S buffer
+constexpr int bPFull = bSFree + 2;           // [kXSlots] P is in the exchange slot
+constexpr int bPvDone = bPFull + kXSlots;
 constexpr int bOFull = bPvDone + 1;
 constexpr int bOEmpty = bOFull + 1;
-constexpr int bXFull = bOEmpty + 1;          // peer's partial scores have landed here
-constexpr int bXEmpty = bXFull + 1;          // peer has read what this CTA sent
-constexpr int bDrain = bXEmpty + 1;
+constexpr int bXFull = bOEmpty + 1;          // [kXSlots] the peer's rows have landed in this CTA's slot
+constexpr int bXFree = bXFull + kXSlots;     // [kXSlots] the PEER's slot may take this CTA's next rows
+constexpr int bDrain = bXFree + kXSlots;
 constexpr int bIdxFull = bDrain + 1;
 constexpr int bIdxEmpty = bIdxFull + kIdxSlots;
 constexpr int kNumBars = bIdxEmpty + kIdxSlots;
@@ -84,9 +110,12 @@ constexpr int kSmemBytes = kOffLast + 4 * (kLatBlocks + kRopeSlots) + 1024;
 constexpr int kTmO = 0, kTmQ = 256, kTmS = 384;
 constexpr uint32_t kIdescQK = idesc_bf16(128, T, false, false);     // M=128 heads, N=64 tokens
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // N=256 dims, B (V) MN-major
-static_assert(kProducers == 4, "producer pw gathers latent atom pw of the CTA's four");
+static_assert(kProducers == 5, "producers 0-3 gather the latent atoms, producer 4 the rope");
+static_assert(kThreads == 512, "16 warps");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 16 == 0 && kOffIdx % 16 == 0, "alignment");
+static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 1024 == 0 && kXSlot % 1024 == 0 &&
+                  kOffIdx % 16 == 0,
+              "alignment");
 
 __device__ __forceinline__ bool item_ok(const DecodeParams& p, int b, int s, int e) {
   if (b < 0 || b >= p.batch) return false;
@@ -111,6 +140,22 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
   }
 }
 
+// 2^k as a float, for -126 <= k <= 127.
+__device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
+
+// 16-bit codes are offset binary: u = q + 32768 for the integer q in [-32767, 32767].
+// Rounding and decoding use full-rate float arithmetic, not conversions:
+//   encode: v + (1.5 * 2^23 + 32768) rounds v to the nearest integer (ties to
+//           even) and leaves u in the low 16 bits of the float;
+//   decode: the bits 0x4B000000 | u are the float 2^23 + u, so
+//           (2^23 + u) * step - (2^23 + 32768) * step = q * step exactly.
+// Both the sender (from its own codes) and the receiver (from the peer's)
+// form q * step exactly and then multiply by sm_scale * log2(e) once, so the
+// two CTAs hold the same scaled partials and, after one commutative add,
+// the same scores.
+constexpr float kEncBias = 12615680.0f;      // 1.5 * 2^23 + 32768
+constexpr float kDecBias = 8421376.0f;       // 2^23 + 32768
+
 __global__ void __launch_bounds__(kThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qr,
                 const DecodeParams p) {
@@ -126,6 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* last_armed = reinterpret_cast<int*>(smem + kOffLast);
   const WaitCtx wc{abort_flag, p.status};
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    MLA_TRACE_RAW(15, 0, static_cast<long long>(globaltimer()));
+    MLA_TRACE_RAW(15, 2, static_cast<long long>(smid));
+    MLA_TRACE_RAW(15, 3, clock64());
+  }
+#endif
 
   const int w = blockIdx.x >> 1;
   const int32_t* wptr = p.plan + kHeaderWords;
@@ -136,17 +190,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLatBlocks; ++i) { mbar_init(bar(bLatFull + i), 1); mbar_init(bar(bLatEmpty + i), 1); }
     for (int i = 0; i < kRopeSlots; ++i) { mbar_init(bar(bRopeFull + i), 1); mbar_init(bar(bRopeEmpty + i), 1); }
-    mbar_init(bar(bQFull), 5);                   // 4 softmax warps (latent half) + the rope TMA
+    mbar_init(bar(bQFull), 5);                   // 4 sender warps (latent half) + the rope TMA
     mbar_init(bar(bQEmpty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(bSFull + i), 1); mbar_init(bar(bPFull + i), 4); mbar_init(bar(bSFree + i), 1);
+      mbar_init(bar(bSFull + i), 1); mbar_init(bar(bSQuant + i), 4); mbar_init(bar(bSFree + i), 4);
+    }
+    for (int i = 0; i < kXSlots; ++i) {
+      mbar_init(bar(bPFull + i), 4);
+      mbar_init(bar(bXFull + i), 1);             // own expect_tx; the bytes come from the peer
+      mbar_init(bar(bXFree + i), 1);             // the peer's PV commit
     }
     mbar_init(bar(bPvDone), 1);
     mbar_init(bar(bOFull), 1);
     mbar_init(bar(bOEmpty), 4);
-    mbar_init(bar(bXFull), 1);
-    mbar_init(bar(bXEmpty), 4);                  // the peer's four softmax warps
-    mbar_init(bar(bDrain), 1);
+    mbar_init(bar(bDrain), 2);                   // both issuers' final commits
     for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(bIdxFull + i), 1); mbar_init(bar(bIdxEmpty + i), kProducers); }
     for (int i = 0; i < kLatBlocks + kRopeSlots; ++i) last_armed[i] = -1;
     *abort_flag = 0;
@@ -155,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // rope-query rows >= H stay zero (the TMA box has H rows)
   for (int i = threadIdx.x; i < (128 * 128) / 16; i += blockDim.x)
     *reinterpret_cast<uint4*>(smem + kOffQR + 16 * i) = make_uint4(0, 0, 0, 0);
-  if (warp == 5) {
+  if (warp == kLoaderWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -164,8 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();                            // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  bool aborted = false;                          // set by the softmax / sender warps only
 
-  if (warp == 6) {
+  if (warp == kIdxWarp) {
     // ---------------------------------------------------------- index stager
     int* idx_ring = reinterpret_cast<int*>(smem + kOffIdx);
     uint32_t g = 0;
@@ -208,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
     // A warp completes one gather4 only every ~70-110 cycles, so a tile's
-    // landing time is set by how many gathers one warp issues for it.  All
-    // four producers therefore share every tile: producer pw gathers latent
-    // atom pw of the CTA's half (16 gathers) and rope gathers 4pw..4pw+3.
+    // landing time is set by how many gathers one warp issues for it.  The
+    // five producers split every tile evenly: producer pw < 4 gathers latent
+    // atom pw of the CTA's half, producer 4 the rope atom; 16 gathers each.
     const int pw = warp - kProducerWarp0;
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
     const uint64_t pol = l2_policy_evict_first();
@@ -232,12 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bIdxEmpty + islot));
         if (lane == 0 && pw == 0) MLA_TRACE_EVENT(0, g);
-        // rope ops 4pw + r (r = 0..3) take the tokens of op 4pw + r
-        const int src = 4 * pw + (lane & 3);
-        const int r0 = __shfl_sync(0xffffffffu, v.x, src), r1 = __shfl_sync(0xffffffffu, v.y, src);
-        const int r2 = __shfl_sync(0xffffffffu, v.z, src), r3 = __shfl_sync(0xffffffffu, v.w, src);
-        // latent atom pw into block g mod 4
-        {
+        if (pw < 4) {
           const uint32_t blk = g % kLatBlocks, use = g / kLatBlocks;
           bool e_ok = true;
           if (lane == 0 && use > 0) e_ok = mbar_wait(bar(bLatEmpty + blk), (use - 1) & 1, wc);
@@ -250,21 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_gather4(base + kOffLat + blk * kLatBlock + pw * kAtom + lane * 512, &tm_kv,
                         64 * (4 * static_cast<int>(cta) + pw), v.x, v.y, v.z, v.w, full, pol);
           if (lane == 0) atomicMax(last_armed + blk, static_cast<int>(use));
-        }
-        // rope slice
-        {
+          if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
+        } else {
           const uint32_t rs = g % kRopeSlots, use = g / kRopeSlots;
           bool e_ok = true;
           if (lane == 0 && use > 0) e_ok = mbar_wait(bar(bRopeEmpty + rs), (use - 1) & 1, wc);
           e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
           if (!e_ok) { ok = false; break; }
           const uint32_t full = bar(bRopeFull + rs);
-          if (lane == 0 && pw == 0) mbar_arrive_expect_tx(full, kAtom);
+          if (lane == 0) mbar_arrive_expect_tx(full, kAtom);
+          if (lane == 0) MLA_TRACE_EVENT(11, g);
           __syncwarp();
-          if (lane < 4)
-            tma_gather4(base + kOffRope + rs * kAtom + (4 * pw + lane) * 512, &tm_kv, 512, r0, r1, r2, r3, full, pol);
+          if (lane < 16)
+            tma_gather4(base + kOffRope + rs * kAtom + lane * 512, &tm_kv, 512, v.x, v.y, v.z, v.w, full, pol);
           if (lane == 0) atomicMax(last_armed + kLatBlocks + rs, static_cast<int>(use));
-          if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
         }
       }
     }
@@ -275,150 +327,105 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= 0) drain_wait(bar(bfull), u & 1);
     }
     __syncwarp();
-  } else if (warp == 4) {
-    // ----------------------------------------------------------- MMA issuer
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------- QK issuer + rope-query loader
+    // One thread; it blocks on its barriers (no polling), so the warps that
+    // share its scheduler keep their issue slots.
     if (lane == 0) {
+      tma_prefetch_desc(&tm_qr);
       const uint64_t dk = sdesc(base + kOffLat, 16, 1024);         // latent block 0, K-major (B of QK)
-      const uint64_t dv = sdesc(base + kOffLat, kAtom, 1024);      // latent block 0, MN-major (B of PV)
       const uint64_t dr = sdesc(base + kOffRope, 16, 1024);        // rope slot 0 (B of QK)
       const uint64_t dqr = sdesc(base + kOffQR, 16, 1024);         // rope query (A of QK)
       auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
-      const uint32_t bar0 = bar(0);
-      auto bar_at = [&](int i) -> uint32_t { return bar0 + 8u * i; };
-      auto next_valid = [&](int it) {
-        while (it < it1 && !item_ok(p, items[4 * it], items[4 * it + 1], items[4 * it + 2])) ++it;
-        return it;
-      };
-      auto ntiles = [&](int it) { return it < it1 ? (items[4 * it + 2] - items[4 * it + 1] + T - 1) / T : 0; };
-      int q_it = next_valid(it0), q_nt = ntiles(q_it), q_j = 0, q_u = 0;
-      uint32_t q_g = 0, q_nitem = 0;
-      bool q_ready = false;
-      int p_it = q_it, p_nt = q_nt, p_j = 0;
-      uint32_t p_g = 0, p_nitem = 0;
-      uint64_t t_last = globaltimer();
-      while (p_it < it1) {
-        bool prog = false;
-        if (p_g < q_g) {
-          const uint32_t buf = p_g & 1;
-          const bool first = p_j == 0;
-          if (mbar_test_wait(bar_at(bPFull + buf), (p_g >> 1) & 1) &&
-              (!first || p_nitem == 0 || mbar_test_wait(bar_at(bOEmpty), (p_nitem - 1) & 1))) {
-            tc_fence_after();
-            MLA_TRACE_EVENT(4, p_g);
-            const uint32_t blk = p_g % kLatBlocks;
-            const uint64_t bv = D(dv, blk * kLatBlock);
-            const uint32_t a_p = tmem + kTmS + buf * 64;           // P: 64 tokens as 32 packed columns
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_ts(tmem + kTmO, a_p + 8 * ks, D(bv, ks * 2048), kIdescPV, (first && ks == 0) ? 0u : 1u);
-            umma_commit(bar_at(bLatEmpty + blk));
-            umma_commit(bar_at(bSFree + buf));
-            umma_commit(bar_at(bPvDone));
-            MLA_TRACE_EVENT(5, p_g);
-            if (++p_j == p_nt) {
-              umma_commit(bar_at(bOFull));
-              ++p_nitem;
-              p_it = next_valid(p_it + 1);
-              p_nt = ntiles(p_it);
-              p_j = 0;
-            }
-            ++p_g;
-            prog = true;
-          }
-        }
-        if (!prog && q_it < it1) {
-          if (!q_ready) {
-            q_ready = (q_j != 0 || mbar_test_wait(bar_at(bQFull), q_nitem & 1)) &&
-                      (q_g < 2 || mbar_test_wait(bar_at(bSFree + (q_g & 1)), ((q_g >> 1) - 1) & 1));
-          }
-          if (q_ready) {
-            const uint32_t d_s = tmem + kTmS + (q_g & 1) * 64;
-            if (q_u == 0) {
-              const uint32_t blk = q_g % kLatBlocks;
-              if (mbar_test_wait(bar_at(bLatFull + blk), (q_g / kLatBlocks) & 1)) {
-                tc_fence_after();
-                MLA_TRACE_EVENT(2, q_g);
-                const uint64_t bk = D(dk, blk * kLatBlock);
-#pragma unroll
-                for (int k = 0; k < 16; ++k)      // 256 latent dims = 16 K-steps; A (query) from TMEM
-                  umma_ts(d_s, tmem + kTmQ + 8 * k, D(bk, (k >> 2) * kAtom + (k & 3) * 32), kIdescQK,
-                          k != 0 ? 1u : 0u);
-                q_u = 1;
-                prog = true;
-              }
-            } else {
-              const uint32_t rs = q_g % kRopeSlots;
-              if (mbar_test_wait(bar_at(bRopeFull + rs), (q_g / kRopeSlots) & 1)) {
-                tc_fence_after();
-                const uint64_t br = D(dr, rs * kAtom);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {  // this CTA's half of the rope dims
-                  const uint32_t off = (2 * cta + kk) * 32;
-                  umma_ss(d_s, D(dqr, off), D(br, off), kIdescQK, 1u);
-                }
-                umma_commit(bar_at(bRopeEmpty + rs));
-                umma_commit(bar_at(bSFull + (q_g & 1)));
-                MLA_TRACE_EVENT(3, q_g);
-                const bool last = q_j == q_nt - 1;
-                if (last) umma_commit(bar_at(bQEmpty));
-                q_u = 0;
-                q_ready = false;
-                ++q_g;
-                if (last) {
-                  ++q_nitem;
-                  q_it = next_valid(q_it + 1);
-                  q_nt = ntiles(q_it);
-                  q_j = 0;
-                } else {
-                  ++q_j;
-                }
-                prog = true;
-              }
-            }
-          }
-        }
-        if (prog) {
-          t_last = globaltimer();
-        } else {
-          if (*abort_flag) break;
-          if (globaltimer() - t_last > MLA_WAIT_LIMIT_NS) {
-            *abort_flag = 1;
-            record_status(p.status, MLA_ERR_TIMEOUT);
-            break;
-          }
-        }
-      }
-      umma_commit(bar_at(bDrain));
-      drain_wait(bar_at(bDrain), 0);
-    }
-    __syncwarp();
-  } else if (warp == 5) {
-    // ---------------------------------------------------- rope-query loader
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_qr);
-      uint32_t nitem = 0;
-      for (int it = it0; it < it1; ++it) {
+      uint32_t g = 0, nitem = 0;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++it) {
         const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
         if (!item_ok(p, b, s, e)) continue;
+        const int nt = (e - s + T - 1) / T;
+        // the rope query of this item replaces the previous one once its last QK is done
         if (nitem > 0 && !mbar_wait(bar(bQEmpty), (nitem - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(bar(bQFull), H * 128);
         tma_load_2d(base + kOffQR, &tm_qr, 0, b * H, bar(bQFull));
+        if (!mbar_wait(bar(bQFull), nitem & 1, wc)) break;     // + the latent half in TMEM
+        for (int j = 0; j < nt; ++j, ++g) {
+          const uint32_t d_s = tmem + kTmS + (g & 1) * 64;
+          const uint32_t blk = g % kLatBlocks, rs = g % kRopeSlots;
+          if (g >= 2 && !mbar_wait(bar(bSFree + (g & 1)), ((g >> 1) - 1) & 1, wc)) { ok = false; break; }
+          if (!mbar_wait(bar(bLatFull + blk), (g / kLatBlocks) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          MLA_TRACE_EVENT(2, g);
+          const uint64_t bk = D(dk, blk * kLatBlock);
+#pragma unroll
+          for (int k = 0; k < 16; ++k)            // 256 latent dims = 16 K-steps; A (query) from TMEM
+            umma_ts(d_s, tmem + kTmQ + 8 * k, D(bk, (k >> 2) * kAtom + (k & 3) * 32), kIdescQK, k != 0 ? 1u : 0u);
+          MLA_TRACE_EVENT(10, g);
+          if (!mbar_wait(bar(bRopeFull + rs), (g / kRopeSlots) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          MLA_TRACE_EVENT(12, g);
+          const uint64_t br = D(dr, rs * kAtom);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {        // this CTA's half of the rope dims
+            const uint32_t off = (2 * cta + kk) * 32;
+            umma_ss(d_s, D(dqr, off), D(br, off), kIdescQK, 1u);
+          }
+          umma_commit(bar(bRopeEmpty + rs));
+          umma_commit(bar(bSFull + (g & 1)));
+          if (j == nt - 1) umma_commit(bar(bQEmpty));
+          MLA_TRACE_EVENT(3, g);
+        }
         ++nitem;
       }
-      if (nitem > 0) drain_wait(bar(bQFull), (nitem - 1) & 1);
+      umma_commit(bar(bDrain));
+      drain_wait(bar(bDrain), 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // --------------------------------------------------- softmax + epilogue
-    const int h = 32 * warp + lane;              // head == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp == kLoaderWarp) {
+    // ----------------------------------------------------------- PV issuer
+    if (lane == 0) {
+      const uint64_t dv = sdesc(base + kOffLat, kAtom, 1024);      // latent block 0, MN-major (B of PV)
+      const uint64_t dp = sdesc(base + kOffX, 16, 1024);           // P in exchange slot 0 (A of PV)
+      auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
+      const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
+      uint32_t g = 0, nitem = 0;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++it) {
+        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+        if (!item_ok(p, b, s, e)) continue;
+        const int nt = (e - s + T - 1) / T;
+        for (int j = 0; j < nt; ++j, ++g) {
+          const uint32_t xs = g % kXSlots, blk = g % kLatBlocks;
+          if (!mbar_wait(bar(bPFull + xs), (g / kXSlots) & 1, wc)) { ok = false; break; }
+          if (j == 0 && nitem > 0 && !mbar_wait(bar(bOEmpty), (nitem - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          MLA_TRACE_EVENT(4, g);
+          const uint64_t bv = D(dv, blk * kLatBlock);
+          const uint64_t ap = D(dp, xs * kXSlot);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)          // 64 tokens = 4 K-steps of 16
+            umma_ss(tmem + kTmO, D(ap, ks * 32), D(bv, ks * 2048), kIdescPV, (j == 0 && ks == 0) ? 0u : 1u);
+          umma_commit(bar(bLatEmpty + blk));
+          umma_commit_mc(bar(bXFree + xs), peer_mask);         // the peer may send into this slot again
+          umma_commit(bar(bPvDone));
+          if (j == nt - 1) umma_commit(bar(bOFull));
+          MLA_TRACE_EVENT(5, g);
+        }
+        ++nitem;
+      }
+      umma_commit(bar(bDrain));
+      drain_wait(bar(bDrain), 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // --------------------------------------------------------------- sender
+    const int qd = warp - 4;                     // TMEM lane quadrant of this warp
+    const int h = 32 * qd + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const bool head_ok = h < H;
-    const uint32_t x_row = base + kOffX + h * kXRow;                 // my row of the receive buffer
-    const uint32_t x_row_peer = mapa_shared(x_row, peer);            // my row in the peer's buffer
-    const uint32_t x_full_peer = mapa_shared(bar(bXFull), peer);
-    uint32_t g = 0, nitem = 0;
-    bool aborted = false;
-    float m_ref = 0.f, l_sum = 0.f;
+    const uint32_t sw = static_cast<uint32_t>(h & 7);      // 16-byte chunk c of row h sits at c ^ (h mod 8)
+    const uint32_t xrow_peer = mapa_shared(base + kOffX + h * 128, peer);
+    const uint32_t xe_peer = mapa_shared(base + kOffXE + h * 4, peer);
+    const uint32_t xfull_peer = mapa_shared(bar(bXFull), peer);
     auto wait = [&](uint32_t bb, uint32_t par, bool cluster_scope) {
       if (aborted) return;
       bool r = true;
@@ -426,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       r = __shfl_sync(0xffffffffu, r, 0);
       if (!r) aborted = true;
     };
+    uint32_t g = 0, nitem = 0;
     for (int it = it0; it < it1; ++it) {
       const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      const int part = items[4 * it + 3];
       if (!item_ok(p, b, s, e)) continue;
-      const int n = e - s, nt = (n + T - 1) / T;
+      const int nt = (e - s + T - 1) / T;
       // -- query latent half into TMEM (after the previous item's last QK)
       if (nitem > 0) wait(bar(bQEmpty), (nitem - 1) & 1, false);
       tc_fence_after();
@@ -453,64 +460,147 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0 && !aborted) mbar_arrive(bar(bQFull));
 
-      // The exchange is software-pipelined: tile j+1's partial row is sent as
-      // soon as tile j's has been read, so the transfer runs under tile j's
-      // softmax.  `sr` holds this CTA's partial row of the tile in flight.
-      uint32_t sr[64];
-      auto stage_send = [&](uint32_t gg) {
-        const uint32_t tm_s = tmem + lane_off + kTmS + (gg & 1) * 64;
-        wait(bar(bSFull + (gg & 1)), (gg >> 1) & 1, false);
-        if (threadIdx.x == 0) MLA_TRACE_EVENT(6, gg);
+      for (int j = 0; j < nt; ++j, ++g) {
+        const uint32_t sb = g & 1, xs = g % kXSlots;
+        const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64;
+        wait(bar(bSFull + sb), (g >> 1) & 1, false);
+        if (threadIdx.x == 128) MLA_TRACE_EVENT(6, g);
         tc_fence_after();
+        // quantise the partial row: 64 codes on the step 2^(e-14), where e is the
+        // exponent of max|s| nudged up by 2^-15 so that no code rounds to 32768;
+        // the scaled dequantised row goes back into the S buffer for the softmax
+        uint32_t qw[32];
+        int e_own;
+        {
+          uint32_t r[64];
+          if (!aborted) {
+            tmem_ld64(tm_s, r);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) r[i] = 0;
+          }
+          float mx = 0.f;
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) mx = max3(mx, fabsf(__uint_as_float(r[i])), fabsf(__uint_as_float(r[i + 1])));
+          mx *= 1.000030517578125f;
+          e_own = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127, -100);
+          const float inv = pow2i(min(14 - e_own, 127)), st = pow2i(max(e_own - 14, -126));
+          const uint64_t inv2 = f2_pack(inv, inv), enc2 = f2_pack(kEncBias, kEncBias);
+          const uint64_t st2 = f2_pack(st, st), dec2 = f2_pack(-kEncBias * st, -kEncBias * st);
+          const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o16[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint64_t t = f2_fma(f2_pack(__uint_as_float(r[16 * c + 2 * i]), __uint_as_float(r[16 * c + 2 * i + 1])),
+                                        inv2, enc2);
+              float t0, t1;
+              f2_unpack(t, t0, t1);
+              qw[8 * c + i] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
+              float d0, d1;
+              f2_unpack(f2_mul(f2_fma(t, st2, dec2), sl2), d0, d1);
+              o16[2 * i] = __float_as_uint(d0);
+              o16[2 * i + 1] = __float_as_uint(d1);
+            }
+            if (!aborted) tmem_st16(tm_s + 16 * c, o16);
+          }
+          if (!aborted) tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !aborted) mbar_arrive(bar(bSQuant + sb));
+        if (threadIdx.x == 128) MLA_TRACE_EVENT(13, g);
+        // push it into the peer's slot xs once the peer's PV(g - kXSlots) has read that slot
+        if (g >= kXSlots) wait(bar(bXFree + xs), ((g / kXSlots) - 1) & 1, true);
+        if (threadIdx.x == 128) MLA_TRACE_EVENT(14, g);
+        if (!aborted && head_ok) {
+          const uint32_t fb = xfull_peer + 8u * xs;
+          const uint32_t dst = xrow_peer + xs * kXSlot;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_async_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), qw[4 * c], qw[4 * c + 1], qw[4 * c + 2],
+                        qw[4 * c + 3], fb);
+          st_async_b32(xe_peer + xs * 512, static_cast<uint32_t>(e_own), fb);
+        }
+        if (threadIdx.x == 128) MLA_TRACE_EVENT(8, g);
+      }
+      ++nitem;
+    }
+  } else {
+    // --------------------------------------------------- softmax + epilogue
+    const int h = 32 * warp + lane;              // head == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const bool head_ok = h < H;
+    const uint32_t sw = static_cast<uint32_t>(h & 7);
+    uint32_t g = 0, nitem = 0;
+    float m_ref = 0.f, l_sum = 0.f;
+    auto wait = [&](uint32_t bb, uint32_t par, bool cluster_scope) {
+      if (aborted) return;
+      bool r = true;
+      if (lane == 0) r = cluster_scope ? mbar_wait<true>(bb, par, wc) : mbar_wait(bb, par, wc);
+      r = __shfl_sync(0xffffffffu, r, 0);
+      if (!r) aborted = true;
+    };
+    for (int it = it0; it < it1; ++it) {
+      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+      const int part = items[4 * it + 3];
+      if (!item_ok(p, b, s, e)) continue;
+      const int n = e - s, nt = (n + T - 1) / T;
+      for (int j = 0; j < nt; ++j, ++g) {
+        const uint32_t sb = g & 1, xs = g % kXSlots;
+        const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64;
+        if (warp == 0 && lane == 0 && !aborted) mbar_arrive_expect_tx(bar(bXFull + xs), H * kXRowBytes);
+        wait(bar(bSQuant + sb), (g >> 1) & 1, false);
+        // this CTA's scaled dequantised row; then the S buffer is free for QK(g+2)
+        uint32_t sv[64];
         if (!aborted) {
-          tmem_ld64(tm_s, sr);
+          tc_fence_after();
+          tmem_ld64(tm_s, sv);
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) sr[i] = 0;
+          for (int i = 0; i < 64; ++i) sv[i] = 0;
         }
-        if (warp == 0 && lane == 0 && !aborted) mbar_arrive_expect_tx(bar(bXFull), 128 * 64 * 4);
-        if (gg > 0) wait(bar(bXEmpty), (gg - 1) & 1, true);      // the peer has read tile gg-1
-        if (!aborted) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            st_async_v4(x_row_peer + 16 * i, sr[4 * i], sr[4 * i + 1], sr[4 * i + 2], sr[4 * i + 3], x_full_peer);
-        }
-      };
-      stage_send(g);
-      for (int j = 0; j < nt; ++j, ++g) {
-        const uint32_t buf = g & 1;
-        const uint32_t tm_s = tmem + lane_off + kTmS + buf * 64;
-        wait(bar(bXFull), g & 1, true);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !aborted) mbar_arrive(bar(bSFree + sb));
+        wait(bar(bXFull + xs), (g / kXSlots) & 1, true);
         if (threadIdx.x == 0) MLA_TRACE_EVENT(9, g);
-        // s = (CTA0 partial + CTA1 partial) in log2 units; the same sum order in both CTAs
-        float sv[64];
+        // s = own + peer (log2 units), the same in both CTAs; -inf past the item end
+        uint8_t* xrow = smem + kOffX + xs * kXSlot + h * 128;
+        const int e_peer =
+            (head_ok && !aborted) ? *reinterpret_cast<const int*>(smem + kOffXE + xs * 512 + h * 4) : -100;
+        const float st_p = pow2i(max(e_peer - 14, -126));
+        const uint64_t st2 = f2_pack(st_p, st_p), dec2 = f2_pack(-kDecBias * st_p, -kDecBias * st_p);
+        const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          uint4 pv = make_uint4(0, 0, 0, 0);
-          if (!aborted)
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(pv.x), "=r"(pv.y), "=r"(pv.z), "=r"(pv.w)
-                         : "r"(x_row + 16 * i));
-          const uint32_t q[4] = {pv.x, pv.y, pv.z, pv.w};
+        for (int c = 0; c < 8; ++c) {            // 8 tokens per 16-byte chunk
+          uint4 pv = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);   // code of 0
+          if (head_ok && !aborted) pv = *reinterpret_cast<const uint4*>(xrow + ((static_cast<uint32_t>(c) ^ sw) << 4));
+          const uint32_t pq[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float own = __uint_as_float(sr[4 * i + k]), oth = __uint_as_float(q[k]);
-            sv[4 * i + k] = (cta == 0 ? own + oth : oth + own) * p.scale_log2;
+            const int t = 8 * c + 2 * k;
+            const uint64_t f = f2_pack(__uint_as_float(__byte_perm(pq[k], 0x4B000000u, 0x7610)),
+                                       __uint_as_float(__byte_perm(pq[k], 0x4B000000u, 0x7632)));
+            const uint64_t sp = f2_mul(f2_fma(f, st2, dec2), sl2);
+            float s0, s1;
+            f2_unpack(f2_add(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), sp), s0, s1);
+            sv[t] = __float_as_uint(s0);
+            sv[t + 1] = __float_as_uint(s1);
           }
         }
-        __syncwarp();
-        if (lane == 0 && !aborted) mbar_arrive_cluster(bar(bXEmpty), peer);   // the peer may send again
-        if (j + 1 < nt) stage_send(g + 1);       // next partial goes out while this tile is scored
         const int nvalid = n - j * T;
         if (nvalid < T) {
 #pragma unroll
-          for (int t = 0; t < 64; ++t)
-            if (t >= nvalid) sv[t] = -INFINITY;
+          for (int t = 0; t < T; ++t)
+            if (t >= nvalid) sv[t] = __float_as_uint(-INFINITY);
         }
-        float mt = sv[0];
+        float mt = -INFINITY;
 #pragma unroll
-        for (int t = 1; t < 64; ++t) mt = fmaxf(mt, sv[t]);
+        for (int t = 0; t < T; t += 2) mt = max3(mt, __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
         if (j == 0) {
           m_ref = mt;
           l_sum = 0.f;
@@ -537,35 +627,38 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               tmem_wait_st();
             }
+            tc_fence_before();
           }
         }
-        // P = 2^(s - m_ref) as bf16 pairs over the score buffer
-        uint32_t pk[32];
-        float l0 = 0.f, l1 = 0.f;
+        // P = 2^(s - m_ref) as bf16, written over the peer's rows (K-major, 128-byte swizzle)
+        const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float a = ex2_approx(sv[2 * i] - m_ref), c = ex2_approx(sv[2 * i + 1] - m_ref);
-          l0 += a;
-          l1 += c;
-          pk[i] = pack_bf16x2(a, c);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float d0, d1;
+            f2_unpack(f2_add(f2_pack(__uint_as_float(sv[8 * c + 2 * i]), __uint_as_float(sv[8 * c + 2 * i + 1])), nm2),
+                      d0, d1);
+            const float a = ex2_approx(d0), d = ex2_approx(d1);
+            l2 = f2_add(l2, f2_pack(a, d));
+            pk[i] = pack_bf16x2(a, d);
+          }
+          if (!aborted)
+            *reinterpret_cast<uint4*>(xrow + ((static_cast<uint32_t>(c) ^ sw) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        float l0, l1;
+        f2_unpack(l2, l0, l1);
         l_sum += l0 + l1;
-        if (!aborted) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t r[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = pk[16 * c + i];
-            tmem_st16(tm_s + 16 * c, r);
-          }
-          tmem_wait_st();
-        }
-        tc_fence_before();
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && !aborted) mbar_arrive(bar(bPFull + buf));
+        if (lane == 0 && !aborted) mbar_arrive(bar(bPFull + xs));
         if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
       }
       // ------------------------------------------------------------ epilogue
+      if (threadIdx.x == 0 && nitem < 24) MLA_TRACE_RAW(15, 8 + 2 * nitem, clock64());
       wait(bar(bOFull), nitem & 1, false);
       tc_fence_after();
       if (!aborted) {
@@ -610,18 +703,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !aborted) mbar_arrive(bar(bOEmpty));
+      if (threadIdx.x == 0 && nitem < 24) MLA_TRACE_RAW(15, 9 + 2 * nitem, clock64());
       ++nitem;
     }
-    // If this CTA gave up, the peer may still have a partial in flight to us
-    // (it sends tile g after we release tile g-1): let it land before exit.
-    if (aborted && lane == 0 && warp == 0) drain_wait(bar(bXFull), g & 1);
   }
 
+  // A CTA that gave up may still have the peer's rows in flight towards it.
+  const bool gave_up = __syncthreads_or(aborted) != 0;
   tc_fence_before();
-  __syncthreads();
   cluster_sync_all();                            // no CTA leaves while its peer may still write to it
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (gave_up && threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 50000ull) {
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    MLA_TRACE_RAW(15, 1, static_cast<long long>(globaltimer()));
+    MLA_TRACE_RAW(15, 4, clock64());
+  }
+  if (warp == kLoaderWarp) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace pair
