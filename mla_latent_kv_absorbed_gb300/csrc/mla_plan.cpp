@@ -6,20 +6,17 @@
 //
 //   * variant by head count: H in {16, 32} -> one CTA per worker; H in
 //     48..128 (step 16) -> a 2-CTA cluster per worker; 64-token tiles for both;
-//   * W workers = SMs / CTAs-per-worker;
-//   * candidate chunk sizes c_k = max(1, ceil(ceil(total_tiles / W) / k)),
-//     k = 1..8, duplicates dropped;
-//   * a request of t tiles becomes ceil(t / c) chunks; chunk cost = tiles + 1;
-//   * longest-processing-time placement: chunks sorted by (cost desc, request,
-//     chunk index), each to the least-loaded worker (ties: lowest index);
-//   * objective = makespan + 4 if any request was cut; smallest wins, ties to
-//     the earlier (larger) candidate.
+//   * W workers = SMs / CTAs-per-worker; an item of t tiles costs t + 1;
+//   * wrap-around fill: requests, in order, are poured into workers 0, 1, ...
+//     each up to a load budget cap, so a request is cut only where a worker
+//     is full (at most W - 1 cuts, hence few partial states to merge);
+//   * no cut piece is shorter than kMinPieceTiles: with less space left the
+//     worker is closed, and a shorter tail stays with its head piece;
+//   * cap starts at ceil((total + (nonempty + W - 1)) / W) and grows by one
+//     tile until the fill fits on W workers.
 // The plan is deterministic: equal inputs give identical words.
 #include <algorithm>
 #include <cstdint>
-#include <functional>
-#include <queue>
-#include <utility>
 #include <vector>
 
 #include "mla_plan.h"
@@ -28,49 +25,42 @@ namespace mla {
 
 namespace {
 
-struct Chunk {
+struct Piece {
   int b;
-  int k;
-  int tiles;
+  long long k0;      // first tile of the piece inside its request
+  long long tiles;
 };
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-void make_chunks(const std::vector<long long>& tiles, long long c, std::vector<Chunk>& out) {
-  out.clear();
-  for (size_t b = 0; b < tiles.size(); ++b) {
-    const long long t = tiles[b];
-    if (t <= 0) continue;
-    const long long n = ceil_div(t, c);
-    for (long long k = 0; k < n; ++k)
-      out.push_back({static_cast<int>(b), static_cast<int>(k), static_cast<int>(std::min(c, t - k * c))});
-  }
-}
-
-// LPT placement; returns the makespan and fills per-worker lists.
-long long place(std::vector<Chunk> chunks, int W, std::vector<std::vector<Chunk>>& lists) {
-  std::sort(chunks.begin(), chunks.end(), [](const Chunk& x, const Chunk& y) {
-    if (x.tiles != y.tiles) return x.tiles > y.tiles;   // cost = tiles + const
-    if (x.b != y.b) return x.b < y.b;
-    return x.k < y.k;
-  });
-  using Slot = std::pair<long long, int>;   // (load, worker)
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int w = 0; w < W; ++w) heap.push({0, w});
+// Wrap-around fill with load budget cap; false when W workers do not suffice.
+bool fill(const std::vector<long long>& tiles, int W, long long cap, std::vector<std::vector<Piece>>& lists) {
   lists.assign(W, {});
-  for (const Chunk& ch : chunks) {
-    Slot s = heap.top();
-    heap.pop();
-    lists[s.second].push_back(ch);
-    s.first += ch.tiles + kItemOverheadTiles;
-    heap.push(s);
+  int w = 0;
+  long long used = 0;
+  for (size_t b = 0; b < tiles.size(); ++b) {
+    long long k0 = 0;
+    const long long t = tiles[b];
+    while (k0 < t) {
+      if (w == W) return false;
+      const long long rem = t - k0;
+      const long long space = cap - used - kItemOverheadTiles;
+      long long take;
+      if (rem <= space || (space >= 1 && rem - space < kMinPieceTiles)) {
+        take = rem;
+      } else if (space >= kMinPieceTiles) {
+        take = space;
+      } else {
+        ++w;
+        used = 0;
+        continue;
+      }
+      lists[w].push_back({static_cast<int>(b), k0, take});
+      used += take + kItemOverheadTiles;
+      k0 += take;
+    }
   }
-  long long makespan = 0;
-  while (!heap.empty()) {
-    makespan = std::max(makespan, heap.top().first);
-    heap.pop();
-  }
-  return makespan;
+  return true;
 }
 
 }  // namespace
@@ -105,46 +95,32 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
     total += tiles[b];
   }
 
-  long long c = 1;
-  std::vector<std::vector<Chunk>> lists(W);
+  long long nonempty = 0;
+  for (long long t : tiles) nonempty += t > 0 ? 1 : 0;
+  long long cap = 0;
+  std::vector<std::vector<Piece>> lists(W);
   if (total > 0) {
-    const long long base = ceil_div(total, W);
-    long long best_obj = -1;
-    std::vector<long long> seen;
-    std::vector<Chunk> chunks;
-    std::vector<std::vector<Chunk>> cand;
-    for (int k = 1; k <= kNumCandidates; ++k) {
-      const long long cc = std::max<long long>(1, ceil_div(base, k));
-      if (std::find(seen.begin(), seen.end(), cc) != seen.end()) continue;
-      seen.push_back(cc);
-      make_chunks(tiles, cc, chunks);
-      const long long makespan = place(chunks, W, cand);
-      bool cut = false;
-      for (long long t : tiles) cut = cut || t > cc;
-      const long long obj = makespan + (cut ? kMergeCostTiles : 0);
-      if (best_obj < 0 || obj < best_obj) {
-        best_obj = obj;
-        c = cc;
-        lists.swap(cand);
-      }
-    }
+    cap = ceil_div(total + (nonempty + W - 1) * kItemOverheadTiles, W);
+    while (!fill(tiles, W, cap, lists)) ++cap;
   }
 
-  std::vector<long long> nchunks(B), pstart(B);
+  std::vector<long long> npieces(B, 0), pstart(B), seen(B, 0);
+  for (const auto& lst : lists)
+    for (const Piece& pc : lst) ++npieces[pc.b];
   long long P = 0;
   for (int b = 0; b < B; ++b) {
-    nchunks[b] = tiles[b] > 0 ? ceil_div(tiles[b], c) : 0;
     pstart[b] = P;
-    if (nchunks[b] > 1) P += nchunks[b];
+    if (npieces[b] > 1) P += npieces[b];
   }
 
   std::vector<int32_t> wptr(1, 0), items;
   for (int w = 0; w < W; ++w) {
-    for (const Chunk& ch : lists[w]) {
-      const long long begin = static_cast<long long>(indptr[ch.b]) + static_cast<long long>(ch.k) * c * T;
-      const long long end = std::min<long long>(indptr[ch.b + 1], begin + c * T);
-      const long long part = nchunks[ch.b] > 1 ? pstart[ch.b] + ch.k : -1;
-      items.push_back(ch.b);
+    for (const Piece& pc : lists[w]) {
+      const long long begin = static_cast<long long>(indptr[pc.b]) + pc.k0 * T;
+      const long long end = std::min<long long>(indptr[pc.b + 1], begin + pc.tiles * T);
+      const long long part = npieces[pc.b] > 1 ? pstart[pc.b] + seen[pc.b] : -1;
+      ++seen[pc.b];
+      items.push_back(pc.b);
       items.push_back(static_cast<int32_t>(begin));
       items.push_back(static_cast<int32_t>(end));
       items.push_back(static_cast<int32_t>(part));
@@ -153,10 +129,10 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
   }
   std::vector<int32_t> merge;
   for (int b = 0; b < B; ++b) {
-    if (nchunks[b] != 1) {
+    if (npieces[b] != 1) {
       merge.push_back(b);
       merge.push_back(static_cast<int32_t>(pstart[b]));
-      merge.push_back(static_cast<int32_t>(pstart[b] + (nchunks[b] > 1 ? nchunks[b] : 0)));
+      merge.push_back(static_cast<int32_t>(pstart[b] + (npieces[b] > 1 ? npieces[b] : 0)));
     }
   }
   const long long n_items = static_cast<long long>(items.size() / 4);
@@ -172,7 +148,7 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
   words[kHVariant] = variant;
   words[kHTile] = T;
   words[kHWorkers] = W;
-  words[kHChunkTiles] = static_cast<int32_t>(c);
+  words[kHChunkTiles] = static_cast<int32_t>(cap);
   words[kHItems] = static_cast<int32_t>(n_items);
   words[kHPartials] = static_cast<int32_t>(P);
   words[kHMerges] = static_cast<int32_t>(n_merge);

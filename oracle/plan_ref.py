@@ -13,18 +13,17 @@ contexts across SMs.  They give no rule, so this is the one the library uses:
     H in {48, 64, ..., 128} -> "pair" (a two-CTA cluster per worker); both
     work in 64-token tiles;
   * W workers = SMs (swab) or SMs // 2 (pair);
-  * tiles_b = ceil(L_b / T); total = sum tiles_b; base = ceil(total / W);
-  * candidate chunk sizes (in tiles) c_k = max(1, ceil(base / k)), k = 1..8,
-    duplicates dropped, in that order;
-  * for a candidate c, request b with tiles_b > 0 is cut into
-    ceil(tiles_b / c) chunks of c tiles (the last one shorter); each chunk is a
-    work item of cost tiles + ITEM_OVERHEAD;
-  * items are placed longest-processing-time first: sorted by
-    (-cost, b, chunk), each goes to the worker with the smallest load, ties to
-    the lowest worker index;
-  * objective = makespan + (MERGE_COST if any request is cut, else 0);
-    the smallest objective wins, ties to the earlier candidate;
-  * partial slots are numbered over the cut requests in (b, chunk) order; an
+  * tiles_b = ceil(L_b / T); total = sum tiles_b; a work item of t tiles
+    costs t + ITEM_OVERHEAD;
+  * wrap-around fill: requests are walked in b order and poured into workers
+    0, 1, ... in turn, each worker up to a load budget cap; a request is cut
+    only where a worker is full, so there are at most W - 1 cuts;
+  * no cut piece is shorter than MIN_PIECE tiles: with space < MIN_PIECE left
+    the worker is closed, and a tail shorter than MIN_PIECE stays with the
+    head piece (the worker then overshoots cap by < MIN_PIECE);
+  * cap starts at ceil((total + (nonempty + W - 1) * ITEM_OVERHEAD) / W) and
+    grows by one tile until the fill fits on the W workers;
+  * partial slots are numbered over the cut requests in (b, piece) order; an
     uncut request's item writes out/lse directly (partial = -1);
   * the merge list holds every request that is cut or empty, in b order, with
     its partial range (empty requests get an empty range).
@@ -35,14 +34,11 @@ words per merge entry (b, p_begin, p_end).
 """
 from __future__ import annotations
 
-import heapq
-
 PLAN_MAGIC = 0x4D4C4131
 PLAN_VERSION = 1
 HEADER_WORDS = 16
 ITEM_OVERHEAD = 1
-MERGE_COST = 4
-NUM_CANDIDATES = 8
+MIN_PIECE = 1
 WS_HEADER_BYTES = 256
 D_LATENT = 512
 
@@ -63,26 +59,29 @@ def _ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def _chunks(tiles, c):
-    items = []
-    for b, t in enumerate(tiles):
-        n = _ceil_div(t, c) if t > 0 else 0
-        for k in range(n):
-            items.append((b, k, min(c, t - k * c)))
-    return items
-
-
-def _place(items, W):
-    """LPT placement. Returns (makespan, per-worker item lists)."""
-    order = sorted(items, key=lambda it: (-(it[2] + ITEM_OVERHEAD), it[0], it[1]))
-    heap = [(0, w) for w in range(W)]
+def _fill(tiles, W, cap):
+    """Wrap-around fill with load budget cap: per-worker lists of
+    (b, first tile, tiles), or None when W workers do not suffice."""
     lists = [[] for _ in range(W)]
-    for it in order:
-        load, w = heapq.heappop(heap)
-        lists[w].append(it)
-        heapq.heappush(heap, (load + it[2] + ITEM_OVERHEAD, w))
-    makespan = max(load for load, _ in heap) if heap else 0
-    return makespan, lists
+    w, used = 0, 0
+    for b, t in enumerate(tiles):
+        k0 = 0
+        while k0 < t:
+            if w == W:
+                return None
+            rem = t - k0
+            space = cap - used - ITEM_OVERHEAD
+            if rem <= space or (space >= 1 and rem - space < MIN_PIECE):
+                take = rem
+            elif space >= MIN_PIECE:
+                take = space
+            else:
+                w, used = w + 1, 0
+                continue
+            lists[w].append((b, k0, take))
+            used += take + ITEM_OVERHEAD
+            k0 += take
+    return lists
 
 
 def build_plan(kv_indptr, H: int, num_sms: int):
@@ -98,55 +97,52 @@ def build_plan(kv_indptr, H: int, num_sms: int):
         raise ValueError("too few SMs")
     tiles = [_ceil_div(L, T) for L in lengths]
     total = sum(tiles)
+    nonempty = sum(1 for t in tiles if t > 0)
 
-    best = None
     if total > 0:
-        base = _ceil_div(total, W)
-        seen = []
-        for k in range(1, NUM_CANDIDATES + 1):
-            c = max(1, _ceil_div(base, k))
-            if c in seen:
-                continue
-            seen.append(c)
-            items = _chunks(tiles, c)
-            makespan, lists = _place(items, W)
-            cut = any(t > c for t in tiles)
-            obj = makespan + (MERGE_COST if cut else 0)
-            if best is None or obj < best[0]:
-                best = (obj, c, lists)
-        _, c, lists = best
+        cap = _ceil_div(total + (nonempty + W - 1) * ITEM_OVERHEAD, W)
+        while True:
+            lists = _fill(tiles, W, cap)
+            if lists is not None:
+                break
+            cap += 1
     else:
-        c, lists = 1, [[] for _ in range(W)]
+        cap, lists = 0, [[] for _ in range(W)]
 
-    nchunks = [(_ceil_div(t, c) if t > 0 else 0) for t in tiles]
+    npieces = [0] * B
+    for lst in lists:
+        for (b, _k0, _t) in lst:
+            npieces[b] += 1
     pstart = []
     P = 0
     for b in range(B):
         pstart.append(P)
-        if nchunks[b] > 1:
-            P += nchunks[b]
+        if npieces[b] > 1:
+            P += npieces[b]
 
     words_items = []
     indptr_w = [0]
+    seen = [0] * B
     for w in range(W):
-        for (b, k, _t) in lists[w]:
-            begin = int(kv_indptr[b]) + k * c * T
-            end = min(int(kv_indptr[b + 1]), begin + c * T)
-            part = pstart[b] + k if nchunks[b] > 1 else -1
+        for (b, k0, t) in lists[w]:
+            begin = int(kv_indptr[b]) + k0 * T
+            end = min(int(kv_indptr[b + 1]), begin + t * T)
+            part = pstart[b] + seen[b] if npieces[b] > 1 else -1
+            seen[b] += 1
             words_items += [b, begin, end, part]
         indptr_w.append(len(words_items) // 4)
     n_items = len(words_items) // 4
 
     merge = []
     for b in range(B):
-        if nchunks[b] != 1:
+        if npieces[b] != 1:
             p0 = pstart[b]
-            p1 = p0 + (nchunks[b] if nchunks[b] > 1 else 0)
+            p1 = p0 + (npieces[b] if npieces[b] > 1 else 0)
             merge += [b, p0, p1]
     n_merge = len(merge) // 3
 
     total_words = HEADER_WORDS + (W + 1) + 4 * n_items + 3 * n_merge
-    header = [PLAN_MAGIC, PLAN_VERSION, B, H, variant, T, W, c, n_items, P, n_merge, 1, cpw,
+    header = [PLAN_MAGIC, PLAN_VERSION, B, H, variant, T, W, cap, n_items, P, n_merge, 1, cpw,
               total_words, num_sms, 0]
     words = header + indptr_w + words_items + merge
     assert len(words) == total_words

@@ -2,8 +2,10 @@
 
 The pages fix no chunking rule, only its job (cover every key once, balance
 long and short contexts across SMs), so these pins check that job: exact
-coverage, partial numbering, the merge list, and the longest-first placement
-bound makespan <= ceil(total/W) + largest item.
+coverage, partial numbering, the merge list, and the wrap-around fill's
+bounds: every worker's load within MIN_PIECE - 1 tiles of the budget cap, cap
+within MIN_PIECE tiles of the ideal ceil((total + items) / W), no cut piece
+shorter than MIN_PIECE tiles, and at most W - 1 cuts.
 """
 import numpy as np
 import pytest
@@ -33,12 +35,13 @@ def _check(indptr, H, sms):
     T, c = d["T"], d["c"]
     assert d["wptr"][0] == 0 and d["wptr"][-1] == d["n"]
     assert all(a <= b for a, b in zip(d["wptr"], d["wptr"][1:]))
+    items_max = c - PR.ITEM_OVERHEAD + PR.MIN_PIECE - 1 if c else 0
     # exact coverage of each request's keys
     cover = {b: [] for b in range(B)}
     parts = {}
     for (b, s, e, p) in d["items"]:
         assert indptr[b] <= s < e <= indptr[b + 1]
-        assert e - s <= c * T
+        assert e - s <= items_max * T
         cover[b].append((s, e))
         if p >= 0:
             assert p not in parts
@@ -65,14 +68,24 @@ def _check(indptr, H, sms):
             _, p0, p1 = mset[b]
             assert p1 - p0 == (nb if nb > 1 else 0)
             assert sorted(p for (bb, _, _, p) in d["items"] if bb == b) == list(range(p0, p1))
-    # LPT bound on the placement
+    # fill bounds
+    tiles = [-(-(indptr[b + 1] - indptr[b]) // T) for b in range(B)]
+    total, nonempty = sum(tiles), sum(1 for t in tiles if t > 0)
     loads = []
     for w in range(d["W"]):
         its = d["items"][d["wptr"][w]:d["wptr"][w + 1]]
         loads.append(sum(-(-(e - s) // T) + PR.ITEM_OVERHEAD for (_, s, e, _) in its))
-    if d["n"]:
-        biggest = max(-(-(e - s) // T) + PR.ITEM_OVERHEAD for (_, s, e, _) in d["items"])
-        assert max(loads) <= -(-sum(loads) // d["W"]) + biggest
+    if total:
+        ideal = -(-(total + (nonempty + d["W"] - 1) * PR.ITEM_OVERHEAD) // d["W"])
+        assert ideal <= c <= ideal + PR.MIN_PIECE
+        assert max(loads) <= c + PR.MIN_PIECE - 1
+        cuts = sum(len(cover[b]) - 1 for b in range(B) if tiles[b] > 0)
+        assert cuts <= d["W"] - 1 and d["P"] <= 2 * cuts
+        for b in range(B):
+            if len(cover[b]) > 1:
+                assert all(-(-(e - s) // T) >= PR.MIN_PIECE for (s, e) in cover[b])
+    else:
+        assert c == 0 and d["n"] == 0
     # workspace holds P partial states
     assert ws >= PR.WS_HEADER_BYTES + d["P"] * H * (512 + 1) * 4 and ws % 256 == 0
     return d
@@ -102,7 +115,7 @@ def test_edge_batches():
 
 def test_long_request_is_split_over_workers():
     d = _check([0, 65536, 196608], 128, 152)
-    assert d["P"] >= d["W"] - 1                     # both requests cut into many chunks
+    assert d["P"] >= d["W"] - 1                     # both requests cut into many pieces
     T, W = d["T"], d["W"]
     loads = []
     for w in range(W):
@@ -110,6 +123,14 @@ def test_long_request_is_split_over_workers():
         loads.append(sum(-(-(e - s) // T) + PR.ITEM_OVERHEAD for (_, s, e, _) in its))
     total_tiles = 196608 // T
     assert max(loads) <= -(-total_tiles // W) + PR.ITEM_OVERHEAD    # within one tile of perfect
+
+
+def test_uniform_batch_cuts_few_requests():
+    # 128 requests of 64 tiles on 76 workers: perfect balance needs cuts, but
+    # only at worker boundaries
+    d = _check([4096 * i for i in range(129)], 128, 152)
+    assert d["P"] <= 2 * (d["W"] - 1)
+    assert d["n"] <= 128 + d["W"] - 1
 
 
 def test_unsupported_heads():
