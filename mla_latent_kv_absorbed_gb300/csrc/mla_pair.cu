@@ -673,24 +673,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst_f = p.part_o + (static_cast<size_t>(part) * H + h) * kLatent + 256 * cta;
         }
 #pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
-          uint32_t o[16];
-          tmem_ld16(tmem + lane_off + kTmO + 16 * c, o);
-          tmem_wait_ld();
+        for (int cb = 0; cb < 8; ++cb) {          // 32 columns per TMEM round trip, 32-byte stores
+          uint32_t o[32];
+          {
+            uint32_t a[16], c[16];
+            tmem_ld16(tmem + lane_off + kTmO + 32 * cb, a);
+            tmem_ld16(tmem + lane_off + kTmO + 32 * cb + 16, c);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) { o[i] = a[i]; o[16 + i] = c[i]; }
+          }
           if (head_ok) {
             if (dst_f) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                reinterpret_cast<float4*>(dst_f + 16 * c)[i] =
-                    make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-            } else {
-              uint32_t hv[8];
+              for (int i = 0; i < 4; ++i) {
+                uint32_t v[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                hv[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-              reinterpret_cast<uint4*>(dst_h + 16 * c)[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-              reinterpret_cast<uint4*>(dst_h + 16 * c)[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                for (int k = 0; k < 8; ++k) v[k] = __float_as_uint(__uint_as_float(o[8 * i + k]) * inv);
+                st_global_v8(dst_f + 32 * cb + 8 * i, v);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                uint32_t v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  v[k] = pack_bf16x2(__uint_as_float(o[16 * i + 2 * k]) * inv, __uint_as_float(o[16 * i + 2 * k + 1]) * inv);
+                st_global_v8(dst_h + 32 * cb + 16 * i, v);
+              }
             }
           }
         }

@@ -22,15 +22,16 @@
 //
 // The shared-memory ring holds 2.5 (H=16) or 2 (H=32) tiles, so the gather of
 // the next tile runs while the current one is scored.  A single warp issuing
-// gather4 completes one op every ~70-110 cycles, so four producer warps
-// share every tile (a tile lands in about a quarter of the time).
+// gather4 completes one op every ~70-110 cycles, so the tile's nine 16-op
+// gather jobs are spread over several producer warps (nine with 16 heads,
+// five with 32, whose softmax needs more registers per thread).
 //
 // Warp roles (one CTA per SM, persistent over the plan's work items):
 //   warps 0-3   softmax / epilogue (TMEM lane quadrants 0-3)
-//   warp 4      MMA issuer (one thread)
-//   warp 5      TMEM allocator and query loader (TMA)
-//   warp 6      index stager: slot numbers to shared memory, rows prefetched into L2
-//   warps 7-10  gather producers
+//   warp 4      QK issuer and query loader (one thread, blocking waits)
+//   warp 5      TMEM allocator and PV issuer (one thread, blocking waits)
+//   warp 6      index stager: slot numbers to shared memory
+//   warps 7..   gather producers
 // With M = 64 the score tile S^T puts token rows 16q..16q+15 in TMEM lanes
 // 32q..32q+15 (q = lane quadrant); O^T (M = 128) puts latent dim r in lane r.
 //
@@ -44,13 +45,16 @@
 namespace mla {
 namespace swab {
 
-constexpr int kProducers = 4;
-constexpr int kIdxSlots = 4;              // tiles of slot indices staged ahead (also the L2 prefetch distance)
-constexpr int kProducerWarp0 = 7;
-constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
+constexpr int kIdxSlots = 4;              // tiles of slot indices staged ahead
+constexpr int kQkWarp = 4, kPvWarp = 5, kIdxWarp = 6, kProducerWarp0 = 7;
 
 template <int NH>
 struct Cfg {
+  // Nine gather jobs per tile (latent atoms 0-7, the rope atom), 16 gather4
+  // each; producer k takes jobs k, k + P, ...  With 16 heads every job has its
+  // own warp; with 32 the softmax needs the registers of a smaller CTA.
+  static constexpr int kProducers = (NH == 16) ? 9 : 5;
+  static constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
   static constexpr int T = 64;                           // tokens per tile
   static constexpr int kPairSlots = (NH == 16) ? 10 : 8;  // ring of latent atom pairs (16 KB each)
   static constexpr int kRopeSlots = 4;
@@ -79,7 +83,7 @@ struct Cfg {
   static constexpr int bPvDone = bPEmpty + 2;
   static constexpr int bOFull = bPvDone + 1;
   static constexpr int bOEmpty = bOFull + 1;
-  static constexpr int bDrain = bOEmpty + 1;
+  static constexpr int bDrain = bOEmpty + 1;             // both issuers' final commits
   static constexpr int bIdxFull = bDrain + 1;
   static constexpr int bIdxEmpty = bIdxFull + kIdxSlots;
   static constexpr int kNumBars = bIdxEmpty + kIdxSlots;
@@ -195,7 +199,7 @@ __device__ __forceinline__ UnitRef unit_ref(uint32_t base, uint32_t g, int u) {
 }
 
 template <int NH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     swab_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qn,
                 const __grid_constant__ CUtensorMap tm_qr, const DecodeParams p) {
   using C = Cfg<NH>;
@@ -224,13 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(C::bQFull), 1); mbar_init(bar(C::bQEmpty), 1);
     mbar_init(bar(C::bPvDone), 1); mbar_init(bar(C::bOFull), 1); mbar_init(bar(C::bOEmpty), 4);
-    mbar_init(bar(C::bDrain), 1);
-    for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(C::bIdxFull + i), 1); mbar_init(bar(C::bIdxEmpty + i), kProducers); }
+    mbar_init(bar(C::bDrain), 2);
+    for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(C::bIdxFull + i), 1); mbar_init(bar(C::bIdxEmpty + i), C::kProducers); }
     for (int i = 0; i < C::kPairSlots + C::kRopeSlots; ++i) last_armed[i] = -1;
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kPvWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -239,14 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 6) {
+  if (warp == kIdxWarp) {
     // ---------------------------------------------------------- index stager
     // Walks the tiles in plan order, loads each tile's 64 slot numbers
     // (coalesced), replaces out-of-range ones by slot 0 (flagged) and the
-    // ragged tail by the last valid slot, publishes them in a small ring, and
-    // prefetches every row's nine 128-byte lines into L2 together (through
-    // the load/store path, leaving the TMA unit to the gathers), so the nine
-    // gather pieces of a row later hit L2.
+    // ragged tail by the last valid slot, and publishes them in a small ring.
     int* idx_ring = reinterpret_cast<int*>(smem + C::kOffIdx);
     uint32_t g = 0;
     bool ok = true;
@@ -272,14 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
           idx_ring[slot * C::T + lane + 32 * k] = v[k];
         }
-        // the 9 lines of each of the tile's rows, 18 per lane
-        for (int q = lane; q < 9 * C::T; q += 32) {
-          const int r = q / 9, line = q - 9 * (q / 9);
-          const int lo = __shfl_sync(0xffffffffu, v[0], r & 31);   // row r's slot lives in lane r%32,
-          const int hi = __shfl_sync(0xffffffffu, v[1], r & 31);   // element r/32
-          const int vr = (r >> 5) ? hi : lo;
-          if (t0 + r < n) prefetch_l2_line(p.kv_cache + static_cast<size_t>(vr) * (kRow * 2) + line * 128);
-        }
         if (__any_sync(0xffffffffu, oob) && lane == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::bIdxFull + slot));
@@ -288,10 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
     // A warp completes one gather4 only every ~70-110 cycles, so a tile's
-    // landing time is set by how many gathers one warp issues for it.  All
-    // four producers share every tile: producer pw gathers latent atoms pw
-    // and pw+4 (16 gathers each) and rope gathers 4pw..4pw+3.  A pair unit
-    // is armed by the producer of its even atom; the rope by producer 0.
+    // landing time is set by how many gathers one warp issues for it.  The
+    // tile's nine jobs (latent atoms 0-7, the rope atom; 16 gather4 each) are
+    // dealt round-robin over the producers.  A pair unit is armed by the
+    // producer of its even atom.
     const int pw = warp - kProducerWarp0;
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
     const uint64_t pol = l2_policy_evict_first();
@@ -312,26 +305,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 v = *reinterpret_cast<const int4*>(idx_ring + islot * C::T + 4 * (lane & 15));
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::bIdxEmpty + islot));
-        if (lane == 0) MLA_TRACE_EVENT(pw == 0 ? 0 : 8 + pw, g);
-        const int src = 4 * pw + (lane & 3);
-        const int r0 = __shfl_sync(0xffffffffu, v.x, src), r1 = __shfl_sync(0xffffffffu, v.y, src);
-        const int r2 = __shfl_sync(0xffffffffu, v.z, src), r3 = __shfl_sync(0xffffffffu, v.w, src);
+        if (lane == 0) MLA_TRACE_EVENT(pw == 0 ? 0 : (pw < 4 ? 8 + pw : 15), g);
 #pragma unroll 1
-        for (int k = 0; k < 3 && ok; ++k) {
-          const int a = k == 0 ? pw : k == 1 ? pw + 4 : 8;     // latent atom, latent atom, rope slice
+        for (int a = pw; a < 9 && ok; a += C::kProducers) {
           const UnitRef r = unit_ref<NH>(base, g, a < 8 ? a >> 1 : 4);
           bool e_ok = true;
           if (lane == 0 && r.use > 0) e_ok = mbar_wait(r.empty, (r.use - 1) & 1, wc);
           e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
           if (!e_ok) { ok = false; break; }
-          const bool arms = r.rope ? pw == 0 : (a & 1) == 0;
+          const bool arms = r.rope || (a & 1) == 0;
           if (lane == 0 && arms) mbar_arrive_expect_tx(r.full, r.rope ? C::kAtom : C::kPair);
           __syncwarp();
-          if (r.rope) {
-            if (lane < 4) tma_gather4(r.addr + (4 * pw + lane) * 512, &tm_kv, 512, r0, r1, r2, r3, r.full, pol);
-          } else if (lane < 16) {
-            tma_gather4(r.addr + (a & 1) * C::kAtom + lane * 512, &tm_kv, 64 * a, v.x, v.y, v.z, v.w, r.full, pol);
-          }
+          if (lane < 16)
+            tma_gather4(r.addr + (r.rope ? 0 : (a & 1) * C::kAtom) + lane * 512, &tm_kv, 64 * a, v.x, v.y, v.z,
+                        v.w, r.full, pol);
           if (lane == 0) atomicMax(last_armed + (r.rope ? C::kPairSlots : 0) + r.slot, static_cast<int>(r.use));
         }
         if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
@@ -339,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // drain: every copy armed by any producer has landed before the CTA can
     // exit (slots are shared between producer warps, so use the latest use)
-    named_bar_sync(3, 32 * kProducers);
+    named_bar_sync(3, 32 * C::kProducers);
     if (pw == 0) {
       for (int i = lane; i < C::kPairSlots + C::kRopeSlots; i += 32) {
         const int u = last_armed[i];
@@ -348,153 +335,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 4) {
-    // ----------------------------------------------------------- MMA issuer
-    // An event loop over two cursors: the QK cursor walks (tile, unit) as
-    // ring units land; the PV cursor issues a tile's PV as soon as its P is
-    // ready (PV first: it frees ring slots for the gather).  The issue path is
-    // kept lean -- descriptors are advanced by constant offsets and ring
-    // positions by running counters -- because every instruction of this one
-    // thread sits between two tensor-core operations.
-    if (lane == 0) {
-      const uint64_t dq = sdesc(base + C::kOffQ, 16, 1024);        // Q atom 0 (B of QK)
-      const uint64_t dk = sdesc(base + C::kOffLat, 16, 1024);      // pair slot 0 (A of QK)
-      const uint64_t dr = sdesc(base + C::kOffRope, 16, 1024);     // rope slot 0 (A of QK)
-      const uint64_t dv = sdesc(base + C::kOffLat, C::kAtom, 1024);  // pair slot 0 (A of PV, MN-major)
-      const uint64_t dp = sdesc(base + C::kOffP, 16, 1024);        // P^T buffer 0 (B of PV)
-      const uint32_t bar0 = bar(0);
-      auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
-      auto bar_at = [&](int i) -> uint32_t { return bar0 + 8u * i; };
-      auto next_valid = [&](int it) {
-        while (it < it1 && !item_ok(p, items[4 * it], items[4 * it + 1], items[4 * it + 2])) ++it;
-        return it;
-      };
-      auto ntiles = [&](int it) { return it < it1 ? (items[4 * it + 2] - items[4 * it + 1] + C::T - 1) / C::T : 0; };
-      // QK cursor
-      int q_it = next_valid(it0), q_nt = ntiles(q_it), q_j = 0, q_u = 0;
-      uint32_t q_g = 0, q_nitem = 0, qs = 0, qph = 0, qr = 0, qrph = 0;
-      bool q_ready = false;
-      // PV cursor
-      int p_it = q_it, p_nt = q_nt, p_j = 0;
-      uint32_t p_g = 0, p_nitem = 0, ps = 0;
-      uint64_t t_last = globaltimer();
-      while (p_it < it1) {
-        bool prog = false;
-        if (p_g < q_g) {
-          const uint32_t buf = p_g & 1;
-          const bool first = p_j == 0;
-          if (mbar_test_wait(bar_at(C::bPFull + buf), (p_g >> 1) & 1) &&
-              (!first || p_nitem == 0 || mbar_test_wait(bar_at(C::bOEmpty), (p_nitem - 1) & 1))) {
-            tc_fence_after();
-            MLA_TRACE_EVENT(4, p_g);
-            const uint64_t bp = D(dp, buf * C::kPBytes);
-#pragma unroll
-            for (int mb = 0; mb < 4; ++mb) {
-              const uint64_t av = D(dv, ps * C::kPair);
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                umma_ss(tmem + C::kTmO + mb * NH, D(av, ks * 2048), D(bp, ks * 32), C::kIdescPV,
-                        (first && ks == 0) ? 0u : 1u);
-              umma_commit(bar_at(C::bLatEmpty + ps));
-              ps = (ps + 1 == C::kPairSlots) ? 0 : ps + 1;
-            }
-            umma_commit(bar_at(C::bPEmpty + buf));
-            umma_commit(bar_at(C::bPvDone));
-            MLA_TRACE_EVENT(5, p_g);
-            if (++p_j == p_nt) {
-              umma_commit(bar_at(C::bOFull));
-              ++p_nitem;
-              p_it = next_valid(p_it + 1);
-              p_nt = ntiles(p_it);
-              p_j = 0;
-            }
-            ++p_g;
-            prog = true;
-          }
-        }
-        if (!prog && q_it < it1) {
-          if (!q_ready) {
-            q_ready = (q_j != 0 || mbar_test_wait(bar_at(C::bQFull), q_nitem & 1)) &&
-                      (q_g < 2 || mbar_test_wait(bar_at(C::bSEmpty + (q_g & 1)), ((q_g >> 1) - 1) & 1));
-            if (q_ready) MLA_TRACE_EVENT(2, q_g);
-          }
-          if (q_ready) {
-            const uint32_t d_s = tmem + C::kTmS + (q_g & 1) * NH;
-            if (q_u < 4) {
-              if (mbar_test_wait(bar_at(C::bLatFull + qs), qph)) {
-                tc_fence_after();
-                const uint64_t ak = D(dk, qs * C::kPair);
-                const uint64_t bq = D(dq, 2 * q_u * C::kQAtom);
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    umma_ss(d_s, D(ak, h * C::kAtom + 32 * kk), D(bq, h * C::kQAtom + 32 * kk), C::kIdescQK,
-                            (q_u | h | kk) != 0 ? 1u : 0u);
-                if (++qs == static_cast<uint32_t>(C::kPairSlots)) { qs = 0; qph ^= 1; }
-                ++q_u;
-                prog = true;
-              }
-            } else if (mbar_test_wait(bar_at(C::bRopeFull + qr), qrph)) {
-              tc_fence_after();
-              const uint64_t ar = D(dr, qr * C::kAtom);
-              const uint64_t bq = D(dq, 8 * C::kQAtom);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) umma_ss(d_s, D(ar, 32 * kk), D(bq, 32 * kk), C::kIdescQK, 1u);
-              umma_commit(bar_at(C::bRopeEmpty + qr));
-              if (++qr == static_cast<uint32_t>(C::kRopeSlots)) { qr = 0; qrph ^= 1; }
-              umma_commit(bar_at(C::bSFull + (q_g & 1)));
-              MLA_TRACE_EVENT(3, q_g);
-              const bool last = q_j == q_nt - 1;
-              if (last) umma_commit(bar_at(C::bQEmpty));
-              q_u = 0;
-              q_ready = false;
-              ++q_g;
-              if (last) {
-                ++q_nitem;
-                q_it = next_valid(q_it + 1);
-                q_nt = ntiles(q_it);
-                q_j = 0;
-              } else {
-                ++q_j;
-              }
-              prog = true;
-            }
-          }
-        }
-        if (prog) {
-          t_last = globaltimer();
-        } else {
-          if (*abort_flag) break;
-          if (globaltimer() - t_last > MLA_WAIT_LIMIT_NS) {
-            *abort_flag = 1;
-            record_status(p.status, MLA_ERR_TIMEOUT);
-            break;
-          }
-        }
-      }
-      // every MMA issued by this thread has completed before TMEM is freed
-      umma_commit(bar_at(C::bDrain));
-      drain_wait(bar_at(C::bDrain), 0);
-    }
-    __syncwarp();
-  } else if (warp == 5) {
-    // --------------------------------------------------------- query loader
+  } else if (warp == kQkWarp) {
+    // ----------------------------------------------- QK issuer + query loader
+    // One thread that blocks on its barriers (no polling).  Per item it loads
+    // the query (latent atoms and rope) once the previous item's last QK has
+    // read the old one; per tile it scores each ring unit as it lands.
     if (lane == 0) {
       tma_prefetch_desc(&tm_qn);
       tma_prefetch_desc(&tm_qr);
-      uint32_t nitem = 0;
+      const uint64_t dq = sdesc(base + C::kOffQ, 16, 1024);        // Q atom 0 (B of QK)
+      const uint64_t dk = sdesc(base + C::kOffLat, 16, 1024);      // pair slot 0 (A of QK)
+      const uint64_t dr = sdesc(base + C::kOffRope, 16, 1024);     // rope slot 0 (A of QK)
+      auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
       const uint32_t qbase = base + C::kOffQ;
-      for (int it = it0; it < it1; ++it) {
+      uint32_t g = 0, nitem = 0, qs = 0, qph = 0, qr = 0, qrph = 0;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++it) {
         const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
         if (!item_ok(p, b, s, e)) continue;
+        const int nt = (e - s + C::T - 1) / C::T;
         if (nitem > 0 && !mbar_wait(bar(C::bQEmpty), (nitem - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(bar(C::bQFull), C::kQBytes);
         for (int a = 0; a < 8; ++a) tma_load_2d(qbase + a * C::kQAtom, &tm_qn, 64 * a, b * p.heads, bar(C::bQFull));
         tma_load_2d(qbase + 8 * C::kQAtom, &tm_qr, 0, b * p.heads, bar(C::bQFull));
+        if (!mbar_wait(bar(C::bQFull), nitem & 1, wc)) break;
+        for (int j = 0; j < nt; ++j, ++g) {
+          const uint32_t d_s = tmem + C::kTmS + (g & 1) * NH;
+          if (g >= 2 && !mbar_wait(bar(C::bSEmpty + (g & 1)), ((g >> 1) - 1) & 1, wc)) { ok = false; break; }
+          MLA_TRACE_EVENT(2, g);
+#pragma unroll 1
+          for (int u = 0; u < 4 && ok; ++u) {
+            if (!mbar_wait(bar(C::bLatFull + qs), qph, wc)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ak = D(dk, qs * C::kPair);
+            const uint64_t bq = D(dq, 2 * u * C::kQAtom);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ss(d_s, D(ak, h * C::kAtom + 32 * kk), D(bq, h * C::kQAtom + 32 * kk), C::kIdescQK,
+                        (u | h | kk) != 0 ? 1u : 0u);
+            if (++qs == static_cast<uint32_t>(C::kPairSlots)) { qs = 0; qph ^= 1; }
+          }
+          if (!ok || !mbar_wait(bar(C::bRopeFull + qr), qrph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ar = D(dr, qr * C::kAtom);
+          const uint64_t bq = D(dq, 8 * C::kQAtom);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) umma_ss(d_s, D(ar, 32 * kk), D(bq, 32 * kk), C::kIdescQK, 1u);
+          umma_commit(bar(C::bRopeEmpty + qr));
+          if (++qr == static_cast<uint32_t>(C::kRopeSlots)) { qr = 0; qrph ^= 1; }
+          umma_commit(bar(C::bSFull + (g & 1)));
+          if (j == nt - 1) umma_commit(bar(C::bQEmpty));
+          MLA_TRACE_EVENT(3, g);
+        }
         ++nitem;
       }
-      if (nitem > 0) drain_wait(bar(C::bQFull), (nitem - 1) & 1);
+      umma_commit(bar(C::bDrain));
+      drain_wait(bar(C::bDrain), 0);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    // Issues a tile's PV once its P^T is written and releases each pair unit
+    // as soon as its 128-dim block is done.
+    if (lane == 0) {
+      const uint64_t dv = sdesc(base + C::kOffLat, C::kAtom, 1024);  // pair slot 0 (A of PV, MN-major)
+      const uint64_t dp = sdesc(base + C::kOffP, 16, 1024);        // P^T buffer 0 (B of PV)
+      auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
+      uint32_t g = 0, nitem = 0, ps = 0;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++it) {
+        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+        if (!item_ok(p, b, s, e)) continue;
+        const int nt = (e - s + C::T - 1) / C::T;
+        for (int j = 0; j < nt; ++j, ++g) {
+          const uint32_t buf = g & 1;
+          if (!mbar_wait(bar(C::bPFull + buf), (g >> 1) & 1, wc)) { ok = false; break; }
+          if (j == 0 && nitem > 0 && !mbar_wait(bar(C::bOEmpty), (nitem - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          MLA_TRACE_EVENT(4, g);
+          const uint64_t bp = D(dp, buf * C::kPBytes);
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb) {
+            const uint64_t av = D(dv, ps * C::kPair);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(tmem + C::kTmO + mb * NH, D(av, ks * 2048), D(bp, ks * 32), C::kIdescPV,
+                      (j == 0 && ks == 0) ? 0u : 1u);
+            umma_commit(bar(C::bLatEmpty + ps));
+            ps = (ps + 1 == static_cast<uint32_t>(C::kPairSlots)) ? 0 : ps + 1;
+          }
+          umma_commit(bar(C::bPEmpty + buf));
+          umma_commit(bar(C::bPvDone));
+          if (j == nt - 1) umma_commit(bar(C::bOFull));
+          MLA_TRACE_EVENT(5, g);
+        }
+        ++nitem;
+      }
+      umma_commit(bar(C::bDrain));
+      drain_wait(bar(C::bDrain), 0);
     }
     __syncwarp();
   } else {
@@ -650,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == kPvWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 template <int NH>
@@ -664,7 +604,7 @@ int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap
       return MLA_ERR_CUDA;
     attr_done = true;
   }
-  swab_kernel<NH><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
+  swab_kernel<NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
