@@ -44,7 +44,7 @@
 //               the softmax and pushes it to the peer (st.async)
 //   warp 8      QK issuer and rope-query loader (one thread)
 //   warp 9      TMEM allocator and PV issuer (one thread)
-//   warp 10     index stager (slot numbers to shared memory, L2 row prefetch)
+//   warp 10     index stager (slot numbers to shared memory)
 //   warps 11-15 gather producers: latent atoms 0-3 of the CTA's half, rope
 //
 // Pushing a tile's rows stalls the issuing warps for as long as the link
@@ -249,14 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 2; ++k) {
           if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
           idx_ring[slot * T + lane + 32 * k] = v[k];
-        }
-        // this CTA prefetches the lines of every other row into L2
-        for (int q = lane; q < 9 * (T / 2); q += 32) {
-          const int rr = q / 9, line = q - 9 * rr, r = 2 * rr + static_cast<int>(cta);
-          const int lo = __shfl_sync(0xffffffffu, v[0], r & 31);
-          const int hi = __shfl_sync(0xffffffffu, v[1], r & 31);
-          const int vr = (r >> 5) ? hi : lo;
-          if (t0 + r < n) prefetch_l2_line(p.kv_cache + static_cast<size_t>(vr) * (kRow * 2) + line * 128);
         }
         if (__any_sync(0xffffffffu, oob) && lane == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
         __syncwarp();

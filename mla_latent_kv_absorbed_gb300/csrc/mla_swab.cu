@@ -20,7 +20,7 @@
 // online softmax, kv_c reused as the value; "Attention backends", paragraph
 // "MLA": 576 wide for k and 512 for v, one shared vector per token.)
 //
-// The shared-memory ring holds 2.5 (H=16) or 2 (H=32) tiles, so the gather of
+// The shared-memory ring holds 2.75 (H=16) or 2.25 (H=32) tiles, so the gather of
 // the next tile runs while the current one is scored.  A single warp issuing
 // gather4 completes one op every ~70-110 cycles, so the tile's nine 16-op
 // gather jobs are spread over several producer warps (nine with 16 heads,
@@ -56,8 +56,8 @@ struct Cfg {
   static constexpr int kProducers = (NH == 16) ? 9 : 5;
   static constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
   static constexpr int T = 64;                           // tokens per tile
-  static constexpr int kPairSlots = (NH == 16) ? 10 : 8;  // ring of latent atom pairs (16 KB each)
-  static constexpr int kRopeSlots = 4;
+  static constexpr int kPairSlots = (NH == 16) ? 11 : 9;  // ring of latent atom pairs (16 KB each)
+  static constexpr int kRopeSlots = 3;
   static constexpr int kAtom = T * 128;                  // 8 KB: 64 tokens x 64 dims
   static constexpr int kPair = 2 * kAtom;                // dims 128u .. 128u+127
   static constexpr int kQAtom = NH * 128;
