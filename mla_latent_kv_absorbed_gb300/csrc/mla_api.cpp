@@ -121,8 +121,7 @@ int check_run_args(const int32_t* plan_host, const int32_t* plan_dev, int32_t ou
                    size_t workspace_bytes) {
   if (!plan_header_ok(plan_host) || !plan_dev) return MLA_ERR_INVALID_ARG;
   if (out_dtype != 0 && out_dtype != 1) return MLA_ERR_UNSUPPORTED;
-  const size_t need = kWsHeaderBytes +
-                      static_cast<size_t>(plan_host[kHPartials]) * plan_host[kHHeads] * (kLatent + 1) * 4;
+  const size_t need = ws_needed_bytes(plan_host);
   if (!workspace || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
   return MLA_OK;

@@ -9,16 +9,26 @@
 // Partials with lse_i = -inf weigh nothing; no live partial gives out = 0,
 // lse = -inf (an empty request).
 //
-// One 128-thread block per (entry, head); each thread owns four latent dims
-// and reads them as one float4 per partial, so the partials stream through
-// in coalesced 2 KB rows.
+// One 128-thread block per (entry, head).  The partial LSEs are loaded in
+// parallel (thread i takes partial i) and their weights go through shared
+// memory; then each thread owns four latent dims and streams the partial rows
+// as float4, four partials in flight, so a merge costs two memory round trips.
+// The kernel is launched as a programmatic dependent of the decode kernel:
+// its blocks are scheduled while the decode kernel drains and wait
+// (griddepcontrol.wait) until its partial states are complete and visible.
 #include <cuda_bf16.h>
 
+#include "mla_device.cuh"
 #include "mla_launch.h"
 
 namespace mla {
 
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+constexpr int kMergeThreads = 128;
+constexpr int kMergeChunk = 1024;   // partials whose weights one pass keeps in shared memory
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+  __shared__ float s_w[kMergeChunk];
+  __shared__ float s_red[4];
   const int e = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   int b, p0, p1;
   if (p.list) {
@@ -30,23 +40,65 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
     p0 = p.indptr[e];
     p1 = p.indptr[e + 1];
   }
+  griddep_wait();
   const int H = p.heads;
-  float M = -INFINITY;
-  for (int i = p0; i < p1; ++i) M = fmaxf(M, __ldg(p.part_lse + static_cast<size_t>(i) * H + h));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (M > -INFINITY) {
-    for (int i = p0; i < p1; ++i) {
-      const float l = __ldg(p.part_lse + static_cast<size_t>(i) * H + h);
-      const float w = (l == -INFINITY) ? 0.f : expf(l - M);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(
-                                 p.part_o + (static_cast<size_t>(i) * H + h) * kLatent) + tid);
+  float wsum = 0.f, M = -INFINITY;
+  for (int c0 = p0; c0 < p1; c0 += kMergeChunk) {
+    // this chunk's partials: LSEs in parallel, then the chunk maximum
+    const int nc = min(kMergeChunk, p1 - c0);
+    float m = -INFINITY;
+    for (int i = tid; i < nc; i += kMergeThreads) {
+      const float l = __ldcg(p.part_lse + static_cast<size_t>(c0 + i) * H + h);
+      s_w[i] = l;
+      m = fmaxf(m, l);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((tid & 31) == 0) s_red[tid >> 5] = m;
+    __syncthreads();
+    const float mc = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+    // fold the chunk into the running state (one chunk unless a request has
+    // more than kMergeChunk partials)
+    const float mn = fmaxf(M, mc);
+    if (mn > -INFINITY && M > -INFINITY && mn != M) {
+      const float a = expf(M - mn);
+      wsum *= a;
+      acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+    }
+    M = mn;
+    for (int i = tid; i < nc; i += kMergeThreads) {
+      const float l = s_w[i];
+      s_w[i] = (l == -INFINITY || M == -INFINITY) ? 0.f : expf(l - M);
+    }
+    __syncthreads();
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(c0) * H + h) * kLatent) + tid;
+    const size_t stride = static_cast<size_t>(H) * kLatent / 4;   // float4 per partial
+    int i = 0;
+    for (; i + 4 <= nc; i += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = __ldcg(src + (i + q) * stride);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float w = s_w[i + q];
+        wsum += w;
+        acc.x = fmaf(w, v[q].x, acc.x);
+        acc.y = fmaf(w, v[q].y, acc.y);
+        acc.z = fmaf(w, v[q].z, acc.z);
+        acc.w = fmaf(w, v[q].w, acc.w);
+      }
+    }
+    for (; i < nc; ++i) {
+      const float4 v = __ldcg(src + i * stride);
+      const float w = s_w[i];
       wsum += w;
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
       acc.w = fmaf(w, v.w, acc.w);
     }
+    __syncthreads();   // s_w and s_red are reused by the next chunk
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + 4 * tid;
@@ -63,9 +115,21 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
 
 int launch_merge(const MergeParams& p, int entries, cudaStream_t stream) {
   if (entries <= 0) return MLA_OK;
-  dim3 grid(entries, p.heads);
-  merge_kernel<<<grid, 128, 0, stream>>>(p);
-  return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(entries, p.heads);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, merge_kernel, p) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
 }
 
 }  // namespace mla

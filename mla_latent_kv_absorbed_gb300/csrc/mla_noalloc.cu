@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "mla_internal.h"
+#include "mla_plan.h"
 
 namespace {
 
@@ -51,9 +52,8 @@ extern "C" int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* p
                                       void* out, int32_t out_dtype, float* lse, void* stream) {
   using namespace mla;
   if (!plan_host || plan_host[kHMagic] != kPlanMagic) return MLA_ERR_INVALID_ARG;
-  if (plan_host[kHPartials] < 0 || plan_host[kHHeads] < 1) return MLA_ERR_INVALID_ARG;
-  const size_t need = kWsHeaderBytes +
-                      static_cast<size_t>(plan_host[kHPartials]) * plan_host[kHHeads] * (kLatent + 1) * 4;
+  if (plan_host[kHPartials] < 0 || plan_host[kHHeads] < 1 || plan_host[kHBatch] < 0) return MLA_ERR_INVALID_ARG;
+  const size_t need = ws_needed_bytes(plan_host);
   if (need > kScratchBytes) return MLA_ERR_WORKSPACE;
   void* ws = scratch_on_current_device();
   if (!ws) return MLA_ERR_CUDA;

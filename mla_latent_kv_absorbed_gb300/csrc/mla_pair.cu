@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();                            // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the merge kernel may be launched now: it waits for this grid to finish
+  griddep_launch_dependents();
   bool aborted = false;                          // set by the softmax / sender warps only
 
   if (warp == kIdxWarp) {

@@ -172,5 +172,8 @@ size_t ws_part_o_offset() { return kWsHeaderBytes; }
 size_t ws_part_lse_offset(const int32_t* header) {
   return kWsHeaderBytes + static_cast<size_t>(header[kHPartials]) * header[kHHeads] * kLatent * 4;
 }
+size_t ws_needed_bytes(const int32_t* header) {
+  return ws_part_lse_offset(header) + static_cast<size_t>(header[kHPartials]) * header[kHHeads] * 4;
+}
 
 }  // namespace mla

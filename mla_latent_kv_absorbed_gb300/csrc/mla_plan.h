@@ -19,5 +19,8 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
 
 size_t ws_part_o_offset();
 size_t ws_part_lse_offset(const int32_t* header);
+// Workspace bytes mla_decode_run needs for a plan: status header, fp32
+// partial states [P,H,512] and their LSEs [P,H].
+size_t ws_needed_bytes(const int32_t* header);
 
 }  // namespace mla

@@ -2,109 +2,129 @@
 //
 // With only 16 or 32 query heads the tensor core's M side cannot be the
 // heads, so both products run "swapped": tokens (or latent dims) on M, heads
-// on N.
+// on N.  A tcgen05.mma costs about the same ~50 cycles whatever its M (64 or
+// 128) and its N (16..64), so the kernel is built to issue as few as possible:
 //
-//   QK:  S^T[64 tok x H]    = K_tile[64 tok x 576] . Q[H x 576]^T        (M = 64, K-major A and B)
-//   PV:  O^T[128 dim x H]  += V^T[128 dim x 64 tok] . P^T[64 tok x H]    (M = 128, A read MN-major
-//                                                                         from the same tile)
+//   QK, folded: the 576 score dims are split into two halves,
+//       h0 = latent atoms 0-3 + rope dims 0-31,  h1 = latent atoms 4-7 + rope dims 32-63,
+//     and the two halves of a 64-token tile are stacked on M:
+//       D[128 x 2H] = [K_h0; K_h1] (128 rows) . [Q_h0; Q_h1]^T (2H rows), K = 288
+//     Rows 0-63 x cols [0,H) hold the h0 partial score, rows 64-127 x cols
+//     [H,2H) the h1 partial (the two off-diagonal blocks are never read), so
+//     a tile takes 18 MMAs instead of 36.  S = partial_h0 + partial_h1.
+//   PV: O^T[128 dims x H] += V^T[128 dims x 64 tok] . P^T[64 tok x H]   (4 blocks of M = 128 dims,
+//                                                                          A read MN-major from the same atoms)
 //
 // The rows of a request are gathered from the page-size-1 cache with TMA
 // gather4 (four slots per instruction) into 128-byte-swizzled "atoms" of 64
-// tokens x 64 dims (8 KB): 8 latent atoms and 1 rope atom per 64-token tile.
-// Latent atoms travel in pairs (16 KB ring units, the 128 latent dims one PV
-// block consumes), one 32-lane gather4 instruction per unit.
-// Each latent atom is read twice by the tensor core -- as part of the key
-// (score over 576) and as the value (latent reused as V) -- and is released
-// after its PV, so every cache byte crosses HBM once.
+// tokens x 64 dims (8 KB).  A tile lands in three ring units: latent unit A
+// holds atoms {0, 4, 1, 5}, unit B atoms {2, 6, 3, 7} (so atom c+4 follows
+// atom c and one 128-row descriptor covers both halves), and the rope unit
+// holds the rope atom followed by the rope shifted by 32 dims (dims 544-607;
+// the 32 past the row end are the TMA's zero fill).  Each latent byte is read
+// by the tensor core twice -- in the key (score over 576) and as the value
+// (the latent reused as V) -- and its unit is released after its PVs, so
+// every cache byte crosses HBM once.
 // ("实现差距：MLA 与 DeepSeek V3", section 2.4: dual-path score, FA2-style
 // online softmax, kv_c reused as the value; "Attention backends", paragraph
 // "MLA": 576 wide for k and 512 for v, one shared vector per token.)
 //
-// The shared-memory ring holds 2.75 (H=16) or 2.25 (H=32) tiles, so the gather of
-// the next tile runs while the current one is scored.  A single warp issuing
-// gather4 completes one op every ~70-110 cycles, so the tile's nine 16-op
-// gather jobs are spread over several producer warps (nine with 16 heads,
-// five with 32, whose softmax needs more registers per thread).
-//
 // Warp roles (one CTA per SM, persistent over the plan's work items):
-//   warps 0-3   softmax / epilogue (TMEM lane quadrants 0-3)
+//   warps 0-3   softmax / epilogue / merge (TMEM lane quadrants 0-3)
 //   warp 4      QK issuer and query loader (one thread, blocking waits)
 //   warp 5      TMEM allocator and PV issuer (one thread, blocking waits)
-//   warp 6      index stager: slot numbers to shared memory
-//   warps 7..   gather producers
-// With M = 64 the score tile S^T puts token rows 16q..16q+15 in TMEM lanes
-// 32q..32q+15 (q = lane quadrant); O^T (M = 128) puts latent dim r in lane r.
+//   warps 6-15  gather producers, one gather job (16 gather4) of every tile
+//               each; a producer reads its tile's slot numbers itself
 //
-// Softmax: scores are scaled into log2 units; each head keeps a reference
-// maximum m_ref that only moves when a tile exceeds it by more than 8 (a
-// group vote per tile); then O and the running sums are rescaled once.  So
-// P = 2^(s - m_ref) <= 256 always fits bf16 and the fp32 sums.
+// Softmax: warps 0-1 read the h0 partials of tokens 0-63 (lanes 0-63), warps
+// 2-3 the h1 partials (lanes 64-127); each pair keeps half the heads and
+// hands the other half to its partner through shared memory, so each of the
+// 128 threads finishes one token for H/2 heads.  Scores are in log2 units;
+// each head keeps a reference maximum m_ref that only moves when a tile
+// exceeds it by more than 8 (a vote per tile); then O and the running sums
+// are rescaled once.  So P = 2^(s - m_ref) <= 256 always fits bf16.
+//
+// Epilogue: O^T is scaled by 1/l, staged in shared memory and written with
+// 16-byte stores (a warp writes 512 contiguous bytes), to out/lse for a
+// request the plan left whole, else as an fp32 partial state for the merge
+// kernel, which is launched as a programmatic dependent of this kernel.
 #include "mla_device.cuh"
 #include "mla_launch.h"
 
 namespace mla {
 namespace swab {
 
-constexpr int kIdxSlots = 4;              // tiles of slot indices staged ahead
-constexpr int kQkWarp = 4, kPvWarp = 5, kIdxWarp = 6, kProducerWarp0 = 7;
+constexpr int T = 64;                      // tokens per tile
+constexpr int kQkWarp = 4, kPvWarp = 5, kProducerWarp0 = 6;
+constexpr int kProducers = 10;             // latent atoms 0-7, rope, shifted rope
+constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
+constexpr int kAtom = T * 128;             // 8 KB: 64 tokens x 64 dims
+constexpr int kUnit = 4 * kAtom;           // latent unit: atoms {c, c+4, c+1, c+5}
+constexpr int kRopeUnit = 2 * kAtom;       // rope atom, then the rope shifted by 32 dims
+constexpr int kRopeUnits = 2;
+#ifndef MLA_SWAB_LEAD
+#define MLA_SWAB_LEAD 1
+#endif
+constexpr int kLeadTiles = MLA_SWAB_LEAD;   // tiles a producer may run ahead of the landed ones
+constexpr int kBarSm = 1, kBarVote = 2, kBarPair0 = 3, kBarProd = 5;   // named barriers
 
 template <int NH>
 struct Cfg {
-  // Nine gather jobs per tile (latent atoms 0-7, the rope atom), 16 gather4
-  // each; producer k takes jobs k, k + P, ...  With 16 heads every job has its
-  // own warp; with 32 the softmax needs the registers of a smaller CTA.
-  static constexpr int kProducers = (NH == 16) ? 9 : 5;
-  static constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
-  static constexpr int T = 64;                           // tokens per tile
-  static constexpr int kPairSlots = (NH == 16) ? 11 : 9;  // ring of latent atom pairs (16 KB each)
-  static constexpr int kRopeSlots = 3;
-  static constexpr int kAtom = T * 128;                  // 8 KB: 64 tokens x 64 dims
-  static constexpr int kPair = 2 * kAtom;                // dims 128u .. 128u+127
-  static constexpr int kQAtom = NH * 128;
-  static constexpr int kQBytes = 9 * kQAtom;
-  static constexpr int kPBytes = NH * 128;               // P^T: NH heads x 64 tokens
+  static constexpr int kHalf = NH / 2;
+  static constexpr int kLatUnits = (NH == 16) ? 5 : 4;   // 2.5 or 2 tiles of latent
+  static constexpr int kQPair = 2 * NH * 128;            // two Q atoms of NH rows
+  static constexpr int kQBytes = 5 * kQPair;             // 4 latent pairs + the rope pair
+  static constexpr int kPBuf = NH * 128;                 // P^T: NH heads x 64 tokens bf16
+  static constexpr int kXBytes = 2 * kHalf * T * 4;      // partial-score exchange, both directions
+  static constexpr int kStage = NH * 128 * 4;            // epilogue staging: 4 warps x [NH][32] fp32
   static constexpr int kOffLat = 0;
-  static constexpr int kOffRope = kOffLat + kPairSlots * kPair;
-  static constexpr int kOffQ = kOffRope + kRopeSlots * kAtom;
+  static constexpr int kOffRope = kOffLat + kLatUnits * kUnit;
+  static constexpr int kOffQ = kOffRope + kRopeUnits * kRopeUnit;
   static constexpr int kOffP = kOffQ + kQBytes;
-  static constexpr int kOffRed = kOffP + 2 * kPBytes;    // [2][4][NH] floats
-  static constexpr int kOffBar = kOffRed + 2 * 4 * NH * 4;
+  static constexpr int kOffX = kOffP + 2 * kPBuf;
+  static constexpr int kOffRed = kOffX + kStage;         // [2 bufs][2 pairs][2 warps][kHalf] floats
+  static constexpr int kOffBc = kOffRed + 8 * kHalf * 4; // [NH] floats: alpha, then 1/l
   // barrier indices
   static constexpr int bLatFull = 0;
-  static constexpr int bLatEmpty = kPairSlots;
-  static constexpr int bRopeFull = 2 * kPairSlots;
-  static constexpr int bRopeEmpty = bRopeFull + kRopeSlots;
-  static constexpr int bQFull = bRopeEmpty + kRopeSlots;
+  static constexpr int bLatEmpty = bLatFull + kLatUnits;
+  static constexpr int bRopeFull = bLatEmpty + kLatUnits;
+  static constexpr int bRopeEmpty = bRopeFull + kRopeUnits;
+  static constexpr int bQFull = bRopeEmpty + kRopeUnits;
   static constexpr int bQEmpty = bQFull + 1;
-  static constexpr int bSFull = bQEmpty + 1;
-  static constexpr int bSEmpty = bSFull + 2;
-  static constexpr int bPFull = bSEmpty + 2;
-  static constexpr int bPEmpty = bPFull + 2;
-  static constexpr int bPvDone = bPEmpty + 2;
-  static constexpr int bOFull = bPvDone + 1;
-  static constexpr int bOEmpty = bOFull + 1;
+  static constexpr int bSFull = bQEmpty + 1;             // [2] QK(g) is in S buffer g&1
+  static constexpr int bSEmpty = bSFull + 2;             // [2] the softmax has read it
+  static constexpr int bPFull = bSEmpty + 2;             // [2] P(g) is in P buffer g&1
+  static constexpr int bPDone = bPFull + 2;              // [2] PV(g) has completed
+  static constexpr int bOBlk = bPDone + 2;               // [4] an item's last PV of O^T block mb is done
+  static constexpr int bOEmpty = bOBlk + 4;
   static constexpr int bDrain = bOEmpty + 1;             // both issuers' final commits
-  static constexpr int bIdxFull = bDrain + 1;
-  static constexpr int bIdxEmpty = bIdxFull + kIdxSlots;
-  static constexpr int kNumBars = bIdxEmpty + kIdxSlots;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffLast = kOffMisc + 16;           // [kPairSlots + kRopeSlots] ints
-  static constexpr int kOffIdx = (kOffLast + 4 * (kPairSlots + kRopeSlots) + 15) / 16 * 16;   // [kIdxSlots][T] ints
-  static constexpr int kSmemBytes = kOffIdx + 4 * kIdxSlots * T + 1024;   // + alignment slack
-  static constexpr int kTmemCols = (6 * NH <= 128) ? 128 : 256;
-  static constexpr int kTmS = 0;       // S^T buffers: columns [0,NH) and [NH,2NH)
-  static constexpr int kTmO = 2 * NH;  // O^T blocks: columns 2NH + mb*NH
-  static constexpr uint32_t kIdescQK = idesc_bf16(64, NH, false, false);
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kOffBar = kOffBc + NH * 4;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem slot, abort flag, merge decision
+  static constexpr int kOffLast = kOffMisc + 32;            // [kLatUnits + kRopeUnits] last armed use
+  static constexpr int kSmemBytes = kOffLast + 4 * (kLatUnits + kRopeUnits) + 1024;   // + alignment slack
+  static constexpr int kTmemCols = 8 * NH;                  // S: 2 x 2NH, O^T: 4 x NH
+  static constexpr int kTmS = 0;
+  static constexpr int kTmO = 4 * NH;
+  static constexpr uint32_t kIdescQK = idesc_bf16(128, 2 * NH, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(128, NH, true, false);
+  static_assert(kStage >= kXBytes, "the exchange and the epilogue staging share a region");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "atoms must be 1024-byte aligned");
-  static_assert(kOffIdx % 16 == 0, "index ring alignment");
+  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBuf % 1024 == 0 && kQPair % 1024 == 0,
+                "atoms must be 1024-byte aligned");
+  static_assert(kOffBar % 8 == 0, "alignment");
 };
 
-__device__ __forceinline__ bool item_ok(const DecodeParams& p, int b, int s, int e) {
-  if (b < 0 || b >= p.batch) return false;
+// Items every role processes: a request in range and a token range inside
+// kv_indices (so no access can leave the arrays).  Whether the range also
+// lies inside its own request is checked off the critical path by one
+// producer (item_in_request), which only records MLA_ERR_PLAN_MISMATCH.
+__device__ __forceinline__ bool item_ok(const DecodeParams& p, int nnz, int b, int s, int e) {
+  return b >= 0 && b < p.batch && 0 <= s && s < e && e <= nnz;
+}
+__device__ __forceinline__ bool item_in_request(const DecodeParams& p, int b, int s, int e) {
   const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
-  return lo <= s && s < e && e <= hi;
+  return lo <= s && e <= hi;
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight copies).
@@ -115,94 +135,60 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Max (or sum) over the 128 softmax threads of v[h], for every h; all threads
-// get the result.  `red` is [2][4][NH]; `k` alternates the half in use.
-template <int NH, bool kSum>
-__device__ __forceinline__ void group_reduce(float (&v)[NH], float* red, int wq, int lane, int& k) {
+// Max (or sum) over the 64 threads of a warp pair -- the two warps that hold
+// the same heads -- of v[i] for every i; both warps get the result.  `red` is
+// [2 bufs][2 pairs][2 warps][K]; `k` alternates the buffer.
+template <int K, bool kSum>
+__device__ __forceinline__ void pair_reduce(float (&v)[K], float* red, int pair, int wip, int lane, int& k) {
 #pragma unroll
-  for (int h = 0; h < NH; ++h) {
+  for (int i = 0; i < K; ++i) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[h], off);
-      v[h] = kSum ? v[h] + o : fmaxf(v[h], o);
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], off);
+      v[i] = kSum ? v[i] + o : fmaxf(v[i], o);
     }
   }
-  float* r = red + (k & 1) * 4 * NH;
+  float* r = red + ((k & 1) * 2 + pair) * 2 * K;
   if (lane == 0) {
 #pragma unroll
-    for (int h = 0; h < NH; h += 4)
-      *reinterpret_cast<float4*>(r + wq * NH + h) = make_float4(v[h], v[h + 1], v[h + 2], v[h + 3]);
+    for (int i = 0; i < K; i += 4)
+      *reinterpret_cast<float4*>(r + wip * K + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
   }
-  named_bar_sync(1, 128);
+  named_bar_sync(kBarPair0 + pair, 64);
 #pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    const float a = r[h], b = r[NH + h], c = r[2 * NH + h], d = r[3 * NH + h];
-    v[h] = kSum ? (a + b) + (c + d) : fmaxf(fmaxf(a, b), fmaxf(c, d));
-  }
+  for (int i = 0; i < K; ++i) v[i] = kSum ? r[i] + r[K + i] : fmaxf(r[i], r[K + i]);
   ++k;
 }
 
-template <int NH>
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[NH]) {
-  if constexpr (NH == 16) {
-    tmem_ld16(taddr, r);
-  } else {
-    uint32_t a[16], b[16];
-    tmem_ld16(taddr, a);
-    tmem_ld16(taddr + 16, b);
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N % 16 == 0, "16-column loads");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) { r[i] = a[i]; r[16 + i] = b[i]; }
-  }
-}
-
-template <int NH>
-__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&r)[NH]) {
-  if constexpr (NH == 16) {
-    tmem_st16(taddr, r);
-  } else {
-    uint32_t a[16], b[16];
+  for (int c = 0; c < N / 16; ++c) {
+    uint32_t a[16];
+    tmem_ld16(taddr + 16 * c, a);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) { a[i] = r[i]; b[i] = r[16 + i]; }
-    tmem_st16(taddr, a);
-    tmem_st16(taddr + 16, b);
+    for (int i = 0; i < 16; ++i) r[16 * c + i] = a[i];
   }
 }
 
-// A tile is five ring units: latent atom pairs u = 0..3 (dims 128u..128u+127,
-// 16 KB) and the rope atom u = 4 (8 KB).  Returns the unit's ring position.
-struct UnitRef {
-  uint32_t addr, full, empty, use, slot;
-  bool rope;
-};
-
-template <int NH>
-__device__ __forceinline__ UnitRef unit_ref(uint32_t base, uint32_t g, int u) {
-  using C = Cfg<NH>;
-  UnitRef r;
-  if (u < 4) {
-    const uint32_t seq = g * 4 + u;
-    r.slot = seq % C::kPairSlots;
-    r.use = seq / C::kPairSlots;
-    r.addr = base + C::kOffLat + r.slot * C::kPair;
-    r.full = base + C::kOffBar + 8u * (C::bLatFull + r.slot);
-    r.empty = base + C::kOffBar + 8u * (C::bLatEmpty + r.slot);
-    r.rope = false;
-  } else {
-    r.slot = g % C::kRopeSlots;
-    r.use = g / C::kRopeSlots;
-    r.addr = base + C::kOffRope + r.slot * C::kAtom;
-    r.full = base + C::kOffBar + 8u * (C::bRopeFull + r.slot);
-    r.empty = base + C::kOffBar + 8u * (C::bRopeEmpty + r.slot);
-    r.rope = true;
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+#pragma unroll
+  for (int c = 0; c < N / 16; ++c) {
+    uint32_t a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = r[16 * c + i];
+    tmem_st16(taddr + 16 * c, a);
   }
-  return r;
 }
 
 template <int NH>
-__global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     swab_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qn,
                 const __grid_constant__ CUtensorMap tm_qr, const DecodeParams p) {
   using C = Cfg<NH>;
+  constexpr int kHalf = C::kHalf;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -213,24 +199,34 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   int* last_armed = reinterpret_cast<int*>(smem + C::kOffLast);   // per ring slot: last armed use
   const WaitCtx wc{abort_flag, p.status};
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    MLA_TRACE_RAW(15, 0, static_cast<long long>(globaltimer()));
+    MLA_TRACE_RAW(15, 2, static_cast<long long>(smid));
+    MLA_TRACE_RAW(15, 3, clock64());
+  }
+#endif
 
   const int w = blockIdx.x;
   const int32_t* wptr = p.plan + kHeaderWords;
   const int it0 = wptr[w], it1 = wptr[w + 1];
   const int32_t* items = p.plan + p.items_off;
+  const int nnz = __ldg(p.kv_indptr + p.batch);   // loaded alongside the plan words
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kPairSlots; ++i) { mbar_init(bar(C::bLatFull + i), 1); mbar_init(bar(C::bLatEmpty + i), 1); }
-    for (int i = 0; i < C::kRopeSlots; ++i) { mbar_init(bar(C::bRopeFull + i), 1); mbar_init(bar(C::bRopeEmpty + i), 1); }
+    for (int i = 0; i < C::kLatUnits; ++i) { mbar_init(bar(C::bLatFull + i), 1); mbar_init(bar(C::bLatEmpty + i), 1); }
+    for (int i = 0; i < kRopeUnits; ++i) { mbar_init(bar(C::bRopeFull + i), 1); mbar_init(bar(C::bRopeEmpty + i), 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::bSFull + i), 1); mbar_init(bar(C::bSEmpty + i), 4);
-      mbar_init(bar(C::bPFull + i), 4); mbar_init(bar(C::bPEmpty + i), 1);
+      mbar_init(bar(C::bPFull + i), 4); mbar_init(bar(C::bPDone + i), 1);
     }
     mbar_init(bar(C::bQFull), 1); mbar_init(bar(C::bQEmpty), 1);
-    mbar_init(bar(C::bPvDone), 1); mbar_init(bar(C::bOFull), 1); mbar_init(bar(C::bOEmpty), 4);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(C::bOBlk + i), 1);
+    mbar_init(bar(C::bOEmpty), 4);
     mbar_init(bar(C::bDrain), 2);
-    for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(C::bIdxFull + i), 1); mbar_init(bar(C::bIdxEmpty + i), C::kProducers); }
-    for (int i = 0; i < C::kPairSlots + C::kRopeSlots; ++i) last_armed[i] = -1;
+    for (int i = 0; i < C::kLatUnits + kRopeUnits; ++i) last_armed[i] = -1;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -242,149 +238,162 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) MLA_TRACE_RAW(15, 5, clock64());
+  // the merge kernel may be launched now: it waits for this grid to finish
+  griddep_launch_dependents();
 
-  if (warp == kIdxWarp) {
-    // ---------------------------------------------------------- index stager
-    // Walks the tiles in plan order, loads each tile's 64 slot numbers
-    // (coalesced), replaces out-of-range ones by slot 0 (flagged) and the
-    // ragged tail by the last valid slot, and publishes them in a small ring.
-    int* idx_ring = reinterpret_cast<int*>(smem + C::kOffIdx);
-    uint32_t g = 0;
-    bool ok = true;
-    for (int it = it0; it < it1 && ok; ++it) {
-      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      if (!item_ok(p, b, s, e)) {
-        if (lane == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
-        continue;
-      }
-      const int n = e - s;
-      for (int t0 = 0; t0 < n; t0 += C::T, ++g) {
-        const uint32_t slot = g % kIdxSlots, use = g / kIdxSlots;
-        int v[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) v[k] = __ldg(p.kv_indices + s + min(t0 + lane + 32 * k, n - 1));
-        bool w_ok = true;
-        if (lane == 0 && use > 0) w_ok = mbar_wait(bar(C::bIdxEmpty + slot), (use - 1) & 1, wc);
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) { ok = false; break; }
-        bool oob = false;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
-          idx_ring[slot * C::T + lane + 32 * k] = v[k];
-        }
-        if (__any_sync(0xffffffffu, oob) && lane == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::bIdxFull + slot));
-      }
-    }
-  } else if (warp >= kProducerWarp0) {
+  if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
     // A warp completes one gather4 only every ~70-110 cycles, so a tile's
-    // landing time is set by how many gathers one warp issues for it.  The
-    // tile's nine jobs (latent atoms 0-7, the rope atom; 16 gather4 each) are
-    // dealt round-robin over the producers.  A pair unit is armed by the
-    // producer of its even atom.
-    const int pw = warp - kProducerWarp0;
-    if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
+    // landing time is set by how many gathers one warp issues for it: each
+    // producer owns one of the tile's ten gather jobs (16 gather4 each).
+    // Job k < 8 is latent atom k (unit (k >> 1) & 1, position 2(k & 1) + (k >> 2));
+    // job 8 the rope atom (dims 512..575), job 9 the rope shifted by 32 dims.
+    // Jobs 0, 2 and 8 arm their unit's full barrier with the unit's bytes.
+    // Slot numbers come straight from kv_indices (lane l < 16 loads tokens
+    // 4l..4l+3, issued before the wait for ring space so the load overlaps
+    // it); an out-of-range slot reads row 0 and sets MLA_ERR_INDEX_OOB, and
+    // the ragged tail repeats the last valid slot (its scores are masked).
+    const int job = warp - kProducerWarp0;
+    if (lane == 0 && job == 0) tma_prefetch_desc(&tm_kv);
+    const bool rope = job >= 8;
+    const int u = (job >> 1) & 1;
+    const int x = rope ? (job == 8 ? kLatent : kLatent + 32) : 64 * job;
+    const uint32_t pos_off = rope ? (job - 8) * kAtom : ((job & 1) * 2 + (job >> 2)) * kAtom;
+    const bool arms = rope ? job == 8 : (job == 0 || job == 2);
+    const uint32_t arm_bytes = rope ? kRopeUnit : kUnit;
     const uint64_t pol = l2_policy_evict_first();
-    const int* idx_ring = reinterpret_cast<const int*>(smem + C::kOffIdx);
     uint32_t g = 0;
     bool ok = true;
     for (int it = it0; it < it1 && ok; ++it) {
       const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      if (!item_ok(p, b, s, e)) continue;
-      const int n = e - s;
-      for (int t0 = 0; t0 < n && ok; t0 += C::T, ++g) {
-        const uint32_t islot = g % kIdxSlots;
-        bool w_ok = true;
-        if (lane == 0) w_ok = mbar_wait(bar(C::bIdxFull + islot), (g / kIdxSlots) & 1, wc);
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) { ok = false; break; }
-        // lane l < 16 holds tokens 4l..4l+3 (gather op l of an atom)
-        const int4 v = *reinterpret_cast<const int4*>(idx_ring + islot * C::T + 4 * (lane & 15));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::bIdxEmpty + islot));
-        if (lane == 0) MLA_TRACE_EVENT(pw == 0 ? 0 : (pw < 4 ? 8 + pw : 15), g);
-#pragma unroll 1
-        for (int a = pw; a < 9 && ok; a += C::kProducers) {
-          const UnitRef r = unit_ref<NH>(base, g, a < 8 ? a >> 1 : 4);
-          bool e_ok = true;
-          if (lane == 0 && r.use > 0) e_ok = mbar_wait(r.empty, (r.use - 1) & 1, wc);
-          e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-          if (!e_ok) { ok = false; break; }
-          const bool arms = r.rope || (a & 1) == 0;
-          if (lane == 0 && arms) mbar_arrive_expect_tx(r.full, r.rope ? C::kAtom : C::kPair);
-          __syncwarp();
-          if (lane < 16)
-            tma_gather4(r.addr + (r.rope ? 0 : (a & 1) * C::kAtom) + lane * 512, &tm_kv, 64 * a, v.x, v.y, v.z,
-                        v.w, r.full, pol);
-          if (lane == 0) atomicMax(last_armed + (r.rope ? C::kPairSlots : 0) + r.slot, static_cast<int>(r.use));
-        }
-        if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
+      if (!item_ok(p, nnz, b, s, e)) {
+        if (lane == 0 && job == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+        continue;
       }
+      const bool in_req = job != 0 || item_in_request(p, b, s, e);
+      const int n = e - s;
+      for (int t0 = 0; t0 < n && ok; t0 += T, ++g) {
+        int v[4];
+        bool oob = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[q] = __ldg(p.kv_indices + s + min(t0 + 4 * (lane & 15) + q, n - 1));
+          if (v[q] < 0 || static_cast<long long>(v[q]) >= p.num_slots) { oob = true; v[q] = 0; }
+        }
+        if (oob && job == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
+        if (lane == 0 && job < 4) MLA_TRACE_EVENT(job == 0 ? 0 : 8 + job, g);
+        uint32_t slot, use, addr, full, empty;
+        int last_idx;
+        if (rope) {
+          slot = g % kRopeUnits;
+          use = g / kRopeUnits;
+          addr = base + C::kOffRope + slot * kRopeUnit;
+          full = bar(C::bRopeFull + slot);
+          empty = bar(C::bRopeEmpty + slot);
+          last_idx = C::kLatUnits + slot;
+        } else {
+          const uint32_t seq = 2 * g + u;
+          slot = seq % C::kLatUnits;
+          use = seq / C::kLatUnits;
+          addr = base + C::kOffLat + slot * kUnit;
+          full = bar(C::bLatFull + slot);
+          empty = bar(C::bLatEmpty + slot);
+          last_idx = slot;
+        }
+        bool e_ok = true;
+        if (lane == 0 && use > 0) e_ok = mbar_wait(empty, (use - 1) & 1, wc);
+        // pace: the same unit of tile g - kLeadTiles must have landed, so that
+        // about kLeadTiles tiles per SM are in flight (enough to cover the
+        // memory latency; more would only lengthen the memory queues)
+        if (lane == 0 && e_ok && g >= static_cast<uint32_t>(kLeadTiles)) {
+          const uint32_t gp = g - kLeadTiles;
+          if (rope) {
+            e_ok = mbar_wait(bar(C::bRopeFull + gp % kRopeUnits), (gp / kRopeUnits) & 1, wc);
+          } else {
+            const uint32_t sp = 2 * gp + u;
+            e_ok = mbar_wait(bar(C::bLatFull + sp % C::kLatUnits), (sp / C::kLatUnits) & 1, wc);
+          }
+        }
+        e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+        if (!e_ok) { ok = false; break; }
+        if (lane == 0 && arms) mbar_arrive_expect_tx(full, arm_bytes);
+        __syncwarp();
+        if (lane < 16) tma_gather4(addr + pos_off + lane * 512, &tm_kv, x, v[0], v[1], v[2], v[3], full, pol);
+        if (lane == 0 && arms) atomicMax(last_armed + last_idx, static_cast<int>(use));
+        if (lane == 0 && job == 0) MLA_TRACE_EVENT(1, g);
+      }
+      if (!in_req && lane == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
     }
     // drain: every copy armed by any producer has landed before the CTA can
     // exit (slots are shared between producer warps, so use the latest use)
-    named_bar_sync(3, 32 * C::kProducers);
-    if (pw == 0) {
-      for (int i = lane; i < C::kPairSlots + C::kRopeSlots; i += 32) {
-        const int u = last_armed[i];
-        const int bfull = i < C::kPairSlots ? C::bLatFull + i : C::bRopeFull + (i - C::kPairSlots);
-        if (u >= 0) drain_wait(bar(bfull), u & 1);
+    named_bar_sync(kBarProd, 32 * kProducers);
+    if (job == 0) {
+      for (int i = lane; i < C::kLatUnits + kRopeUnits; i += 32) {
+        const int uu = last_armed[i];
+        const int bfull = i < C::kLatUnits ? C::bLatFull + i : C::bRopeFull + (i - C::kLatUnits);
+        if (uu >= 0) drain_wait(bar(bfull), uu & 1);
       }
     }
     __syncwarp();
   } else if (warp == kQkWarp) {
     // ----------------------------------------------- QK issuer + query loader
-    // One thread that blocks on its barriers (no polling).  Per item it loads
-    // the query (latent atoms and rope) once the previous item's last QK has
-    // read the old one; per tile it scores each ring unit as it lands.
+    // One thread that blocks on its barriers.  Per item it loads the query
+    // (four latent atom pairs {c, c+4} and the rope pair) once the previous
+    // item's last QK has read the old one; per tile it scores units A, B and
+    // the rope unit as they land: 8 + 8 + 2 MMAs into S buffer g&1.
     if (lane == 0) {
       tma_prefetch_desc(&tm_qn);
       tma_prefetch_desc(&tm_qr);
-      const uint64_t dq = sdesc(base + C::kOffQ, 16, 1024);        // Q atom 0 (B of QK)
-      const uint64_t dk = sdesc(base + C::kOffLat, 16, 1024);      // pair slot 0 (A of QK)
-      const uint64_t dr = sdesc(base + C::kOffRope, 16, 1024);     // rope slot 0 (A of QK)
+      const uint64_t dq = sdesc(base + C::kOffQ, 16, 1024);      // Q pair 0 (B of QK)
+      const uint64_t dk = sdesc(base + C::kOffLat, 16, 1024);    // latent unit slot 0 (A of QK)
+      const uint64_t dr = sdesc(base + C::kOffRope, 16, 1024);   // rope unit slot 0 (A of QK)
       auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
       const uint32_t qbase = base + C::kOffQ;
-      uint32_t g = 0, nitem = 0, qs = 0, qph = 0, qr = 0, qrph = 0;
+      uint32_t g = 0, nitem = 0, ls = 0, lph = 0, rs = 0, rph = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
         const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-        if (!item_ok(p, b, s, e)) continue;
-        const int nt = (e - s + C::T - 1) / C::T;
+        if (!item_ok(p, nnz, b, s, e)) continue;
+        const int nt = (e - s + T - 1) / T;
         if (nitem > 0 && !mbar_wait(bar(C::bQEmpty), (nitem - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(bar(C::bQFull), C::kQBytes);
-        for (int a = 0; a < 8; ++a) tma_load_2d(qbase + a * C::kQAtom, &tm_qn, 64 * a, b * p.heads, bar(C::bQFull));
-        tma_load_2d(qbase + 8 * C::kQAtom, &tm_qr, 0, b * p.heads, bar(C::bQFull));
+        for (int c = 0; c < 4; ++c) {
+          tma_load_2d(qbase + c * C::kQPair, &tm_qn, 64 * c, b * p.heads, bar(C::bQFull));
+          tma_load_2d(qbase + c * C::kQPair + NH * 128, &tm_qn, 64 * (c + 4), b * p.heads, bar(C::bQFull));
+        }
+        tma_load_2d(qbase + 4 * C::kQPair, &tm_qr, 0, b * p.heads, bar(C::bQFull));
+        tma_load_2d(qbase + 4 * C::kQPair + NH * 128, &tm_qr, 32, b * p.heads, bar(C::bQFull));
+        if (nitem < 8) MLA_TRACE_RAW(14, 2 * nitem, clock64());
         if (!mbar_wait(bar(C::bQFull), nitem & 1, wc)) break;
+        if (nitem < 8) MLA_TRACE_RAW(14, 2 * nitem + 1, clock64());
         for (int j = 0; j < nt; ++j, ++g) {
-          const uint32_t d_s = tmem + C::kTmS + (g & 1) * NH;
+          const uint32_t d_s = tmem + C::kTmS + (g & 1) * 2 * NH;
           if (g >= 2 && !mbar_wait(bar(C::bSEmpty + (g & 1)), ((g >> 1) - 1) & 1, wc)) { ok = false; break; }
           MLA_TRACE_EVENT(2, g);
 #pragma unroll 1
-          for (int u = 0; u < 4 && ok; ++u) {
-            if (!mbar_wait(bar(C::bLatFull + qs), qph, wc)) { ok = false; break; }
+          for (int uu = 0; uu < 2 && ok; ++uu) {
+            if (!mbar_wait(bar(C::bLatFull + ls), lph, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t ak = D(dk, qs * C::kPair);
-            const uint64_t bq = D(dq, 2 * u * C::kQAtom);
+            const uint64_t ak = D(dk, ls * kUnit);
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int pr = 0; pr < 2; ++pr) {
+              const uint64_t bq = D(dq, (2 * uu + pr) * C::kQPair);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_ss(d_s, D(ak, h * C::kAtom + 32 * kk), D(bq, h * C::kQAtom + 32 * kk), C::kIdescQK,
-                        (u | h | kk) != 0 ? 1u : 0u);
-            if (++qs == static_cast<uint32_t>(C::kPairSlots)) { qs = 0; qph ^= 1; }
+                umma_ss(d_s, D(ak, pr * 2 * kAtom + 32 * kk), D(bq, 32 * kk), C::kIdescQK,
+                        (uu | pr | kk) != 0 ? 1u : 0u);
+            }
+            if (++ls == static_cast<uint32_t>(C::kLatUnits)) { ls = 0; lph ^= 1; }
           }
-          if (!ok || !mbar_wait(bar(C::bRopeFull + qr), qrph, wc)) { ok = false; break; }
+          if (!ok || !mbar_wait(bar(C::bRopeFull + rs), rph, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t ar = D(dr, qr * C::kAtom);
-          const uint64_t bq = D(dq, 8 * C::kQAtom);
+          const uint64_t ar = D(dr, rs * kRopeUnit);
+          const uint64_t bq = D(dq, 4 * C::kQPair);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) umma_ss(d_s, D(ar, 32 * kk), D(bq, 32 * kk), C::kIdescQK, 1u);
-          umma_commit(bar(C::bRopeEmpty + qr));
-          if (++qr == static_cast<uint32_t>(C::kRopeSlots)) { qr = 0; qrph ^= 1; }
+          for (int kk = 0; kk < 2; ++kk) umma_ss(d_s, D(ar, 32 * kk), D(bq, 32 * kk), C::kIdescQK, 1u);
+          umma_commit(bar(C::bRopeEmpty + rs));
+          if (++rs == static_cast<uint32_t>(kRopeUnits)) { rs = 0; rph ^= 1; }
           umma_commit(bar(C::bSFull + (g & 1)));
           if (j == nt - 1) umma_commit(bar(C::bQEmpty));
           MLA_TRACE_EVENT(3, g);
@@ -397,38 +406,45 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     __syncwarp();
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
-    // Issues a tile's PV once its P^T is written and releases each pair unit
-    // as soon as its 128-dim block is done.
+    // Issues a tile's PV once its P^T is written: the two 128-dim blocks of
+    // unit A (dims 0-127 = atoms 0,1 and dims 256-383 = atoms 4,5), then
+    // unit A is released; the same for unit B (dims 128-255, 384-511).
     if (lane == 0) {
-      const uint64_t dv = sdesc(base + C::kOffLat, C::kAtom, 1024);  // pair slot 0 (A of PV, MN-major)
-      const uint64_t dp = sdesc(base + C::kOffP, 16, 1024);        // P^T buffer 0 (B of PV)
+      const uint64_t dv = sdesc(base + C::kOffLat, 2 * kAtom, 1024);   // A of PV, MN-major: atoms 2 apart
+      const uint64_t dp = sdesc(base + C::kOffP, 16, 1024);            // P^T buffer 0 (B of PV)
       auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
-      uint32_t g = 0, nitem = 0, ps = 0;
+      uint32_t g = 0, nitem = 0, ls = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
         const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-        if (!item_ok(p, b, s, e)) continue;
-        const int nt = (e - s + C::T - 1) / C::T;
+        if (!item_ok(p, nnz, b, s, e)) continue;
+        const int nt = (e - s + T - 1) / T;
         for (int j = 0; j < nt; ++j, ++g) {
           const uint32_t buf = g & 1;
           if (!mbar_wait(bar(C::bPFull + buf), (g >> 1) & 1, wc)) { ok = false; break; }
+          if (j == nt - 1 && nitem < 8) MLA_TRACE_RAW(12, 8 * nitem + 4, clock64());
           if (j == 0 && nitem > 0 && !mbar_wait(bar(C::bOEmpty), (nitem - 1) & 1, wc)) { ok = false; break; }
           tc_fence_after();
           MLA_TRACE_EVENT(4, g);
-          const uint64_t bp = D(dp, buf * C::kPBytes);
+          const uint64_t bp = D(dp, buf * C::kPBuf);
 #pragma unroll
-          for (int mb = 0; mb < 4; ++mb) {
-            const uint64_t av = D(dv, ps * C::kPair);
+          for (int uu = 0; uu < 2; ++uu) {
+            const uint64_t au = D(dv, ls * kUnit);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_ss(tmem + C::kTmO + mb * NH, D(av, ks * 2048), D(bp, ks * 32), C::kIdescPV,
-                      (j == 0 && ks == 0) ? 0u : 1u);
-            umma_commit(bar(C::bLatEmpty + ps));
-            ps = (ps + 1 == static_cast<uint32_t>(C::kPairSlots)) ? 0 : ps + 1;
+            for (int hi = 0; hi < 2; ++hi) {
+              const int mb = uu + 2 * hi;            // 128-dim block
+              const uint64_t av = D(au, hi * kAtom);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ss(tmem + C::kTmO + mb * NH, D(av, ks * 2048), D(bp, ks * 32), C::kIdescPV,
+                        (j == 0 && ks == 0) ? 0u : 1u);
+              if (j == nt - 1) umma_commit(bar(C::bOBlk + mb));   // the epilogue streams blocks as they finish
+              if (j == nt - 1 && nitem < 8) MLA_TRACE_RAW(12, 8 * nitem + mb, clock64());
+            }
+            umma_commit(bar(C::bLatEmpty + ls));
+            ls = (ls + 1 == static_cast<uint32_t>(C::kLatUnits)) ? 0 : ls + 1;
           }
-          umma_commit(bar(C::bPEmpty + buf));
-          umma_commit(bar(C::bPvDone));
-          if (j == nt - 1) umma_commit(bar(C::bOFull));
+          umma_commit(bar(C::bPDone + buf));
           MLA_TRACE_EVENT(5, g);
         }
         ++nitem;
@@ -438,17 +454,18 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     }
     __syncwarp();
   } else {
-    // --------------------------------------------------- softmax + epilogue
-    const int wq = warp;                          // lane quadrant
-    const int t = 16 * wq + lane;                 // token row of S^T (lanes 0-15 only)
-    const bool row_lane = lane < 16;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const int dim_row = 32 * wq + lane;           // latent row of O^T (within a 128-dim block)
+    // ------------------------------------------------- softmax + epilogue
+    const int pair = warp >> 1, wip = warp & 1;
+    const int t = 32 * wip + lane;                        // token of the tile
+    const int tid = threadIdx.x;                          // 0..127
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float* X = reinterpret_cast<float*>(smem + C::kOffX);
     float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+    float* bc = reinterpret_cast<float*>(smem + C::kOffBc);
     int rk = 0;
     uint32_t g = 0, nitem = 0;
     bool aborted = false;
-    float m_ref[NH], l_part[NH];
+    float m_ref[kHalf], l_part[kHalf];
     auto wait = [&](uint32_t bb, uint32_t par) {
       if (aborted) return;
       bool r = true;
@@ -456,19 +473,20 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       r = __shfl_sync(0xffffffffu, r, 0);
       if (!r) aborted = true;
     };
+
     for (int it = it0; it < it1; ++it) {
       const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
       const int part = items[4 * it + 3];
-      if (!item_ok(p, b, s, e)) continue;
-      const int n = e - s, nt = (n + C::T - 1) / C::T;
+      if (!item_ok(p, nnz, b, s, e)) continue;
+      const int n = e - s, nt = (n + T - 1) / T;
       for (int j = 0; j < nt; ++j, ++g) {
         const uint32_t buf = g & 1;
         wait(bar(C::bSFull + buf), (g >> 1) & 1);
-        if (threadIdx.x == 0) MLA_TRACE_EVENT(6, g);
+        if (tid == 0) MLA_TRACE_EVENT(6, g);
         tc_fence_after();
         uint32_t r[NH];
         if (!aborted) {
-          tmem_ld_row<NH>(tmem + lane_off + C::kTmS + buf * NH, r);
+          tmem_ld_cols<NH>(tmem + lane_off + C::kTmS + buf * 2 * NH + pair * NH, r);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -477,112 +495,183 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(bar(C::bSEmpty + buf));
-        const bool valid = row_lane && t < n - j * C::T;
-        float sv[NH];
+        // hand the partner pair the partials of its heads, take ours
+        float own[kHalf];
 #pragma unroll
-        for (int h = 0; h < NH; ++h) sv[h] = valid ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
+        for (int k = 0; k < kHalf; ++k) {
+          own[k] = __uint_as_float(pair ? r[kHalf + k] : r[k]);
+          X[(pair * kHalf + k) * T + t] = __uint_as_float(pair ? r[k] : r[kHalf + k]);
+        }
+        named_bar_sync(kBarSm, 128);
+        const bool valid = t < n - j * T;
+        float sv[kHalf];
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k)
+          sv[k] = valid ? (own[k] + X[((1 - pair) * kHalf + k) * T + t]) * p.scale_log2 : -INFINITY;
         if (j == 0) {
 #pragma unroll
-          for (int h = 0; h < NH; ++h) { m_ref[h] = sv[h]; l_part[h] = 0.f; }
-          group_reduce<NH, false>(m_ref, red, wq, lane, rk);
+          for (int k = 0; k < kHalf; ++k) { m_ref[k] = sv[k]; l_part[k] = 0.f; }
+          pair_reduce<kHalf, false>(m_ref, red, pair, wip, lane, rk);
+          named_bar_sync(kBarVote, 128);   // keeps X reuse ordered like the vote below
         } else {
           bool need = false;
 #pragma unroll
-          for (int h = 0; h < NH; ++h) need |= sv[h] > m_ref[h] + 8.f;
-          need = named_bar_or(2, 128, need);
+          for (int k = 0; k < kHalf; ++k) need |= sv[k] > m_ref[k] + 8.f;
+          need = named_bar_or(kBarVote, 128, need);
           if (need) {
-            float mt[NH], alpha[NH];
+            float mt[kHalf], alpha[kHalf];
 #pragma unroll
-            for (int h = 0; h < NH; ++h) mt[h] = sv[h];
-            group_reduce<NH, false>(mt, red, wq, lane, rk);
+            for (int k = 0; k < kHalf; ++k) mt[k] = sv[k];
+            pair_reduce<kHalf, false>(mt, red, pair, wip, lane, rk);
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              const float mn = fmaxf(m_ref[h], mt[h]);
-              alpha[h] = ex2_approx(m_ref[h] - mn);
-              m_ref[h] = mn;
-              l_part[h] *= alpha[h];
+            for (int k = 0; k < kHalf; ++k) {
+              const float mn = fmaxf(m_ref[k], mt[k]);
+              alpha[k] = ex2_approx(m_ref[k] - mn);
+              m_ref[k] = mn;
+              l_part[k] *= alpha[k];
             }
-            // rescale O^T after the previous tile's PV has landed
-            wait(bar(C::bPvDone), (g - 1) & 1);
+            if (wip == 0 && lane == 0) {
+#pragma unroll
+              for (int k = 0; k < kHalf; ++k) bc[pair * kHalf + k] = alpha[k];
+            }
+            named_bar_sync(kBarSm, 128);
+            float alpha_all[NH];   // registers: the TMEM accesses below are compiler barriers
+#pragma unroll
+            for (int h = 0; h < NH; ++h) alpha_all[h] = bc[h];
+            // rescale O^T (every head's column) after the previous tile's PV has landed
+            wait(bar(C::bPDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1);
             tc_fence_after();
             if (!aborted) {
 #pragma unroll 1
               for (int mb = 0; mb < 4; ++mb) {
                 uint32_t o[NH];
                 const uint32_t ta = tmem + lane_off + C::kTmO + mb * NH;
-                tmem_ld_row<NH>(ta, o);
+                tmem_ld_cols<NH>(ta, o);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < NH; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-                tmem_st_row<NH>(ta, o);
+                for (int h = 0; h < NH; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha_all[h]);
+                tmem_st_cols<NH>(ta, o);
               }
               tmem_wait_st();
             }
           }
         }
-        float pv[NH];
+        float pv[kHalf];
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          pv[h] = ex2_approx(sv[h] - m_ref[h]);   // -inf rows give 0
-          l_part[h] += pv[h];
+        for (int k = 0; k < kHalf; ++k) {
+          pv[k] = ex2_approx(sv[k] - m_ref[k]);   // -inf rows give 0
+          l_part[k] += pv[k];
         }
-        if (g >= 2) wait(bar(C::bPEmpty + buf), ((g >> 1) - 1) & 1);
-        if (!aborted && row_lane) {
+        if (g >= 2) wait(bar(C::bPDone + buf), ((g >> 1) - 1) & 1);
+        if (!aborted) {
           // P^T[buf]: K-major, 128B swizzle; row = head, 64 tokens per 128-byte row
-          uint8_t* pb = smem + C::kOffP + buf * C::kPBytes;
+          uint8_t* pb = smem + C::kOffP + buf * C::kPBuf;
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
+          for (int k = 0; k < kHalf; ++k) {
+            const int h = pair * kHalf + k;
             const int off = (h >> 3) * 1024 + (h & 7) * 128 + ((((t >> 3) ^ (h & 7)) & 7) << 4) + (t & 7) * 2;
-            *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pv[h]);
+            *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pv[k]);
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(bar(C::bPFull + buf));
-        if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
+        if (tid == 0) MLA_TRACE_EVENT(7, g);
       }
       // ------------------------------------------------------------ epilogue
-      wait(bar(C::bOFull), nitem & 1);
-      tc_fence_after();
-      float l_tot[NH];
+      // The softmax sums and the LSE do not depend on O: they overlap the
+      // item's last PV.  Then each 128-dim block of O^T is read from TMEM as
+      // soon as its last MMA is done (PV order 0, 2, 1, 3), scaled by 1/l and
+      // written through the warp's own staging rows (no CTA barrier).
+      if (tid == 0 && nitem < 24) MLA_TRACE_RAW(15, 8 + 2 * nitem, clock64());
+      const bool to_out = part < 0;
+      float l_tot[kHalf];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) l_tot[h] = l_part[h];
-      group_reduce<NH, true>(l_tot, red, wq, lane, rk);
-      if (!aborted) {
+      for (int k = 0; k < kHalf; ++k) l_tot[k] = l_part[k];
+      pair_reduce<kHalf, true>(l_tot, red, pair, wip, lane, rk);
+      if (wip == 0 && lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kHalf; k += 4)
+          *reinterpret_cast<float4*>(bc + pair * kHalf + k) = make_float4(
+              __frcp_rn(l_tot[k]), __frcp_rn(l_tot[k + 1]), __frcp_rn(l_tot[k + 2]), __frcp_rn(l_tot[k + 3]));
+      }
+      {
+        // lane k of the pair's first warp writes head pair*kHalf + k
+        float my_lse = 0.f;
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k)
+          if (lane == k) my_lse = (m_ref[k] + __log2f(l_tot[k])) * 0.69314718055994531f;
+        if (!aborted && wip == 0 && lane < kHalf) {
+          const int h = pair * kHalf + lane;
+          if (to_out) { if (p.lse) p.lse[static_cast<size_t>(b) * p.heads + h] = my_lse; }
+          else p.part_lse[static_cast<size_t>(part) * p.heads + h] = my_lse;
+        }
+      }
+      named_bar_sync(kBarSm, 128);
+      float inv_l[NH];     // registers: the TMEM accesses below are compiler barriers
+#pragma unroll
+      for (int h = 0; h < NH; ++h) inv_l[h] = bc[h];
+      if (tid == 0 && nitem < 8) MLA_TRACE_RAW(13, 8 * nitem, clock64());
+      const bool st_bf16 = to_out && p.out_bf16;
+      const int esz = st_bf16 ? 2 : 4;
+      uint8_t* dst = to_out ? reinterpret_cast<uint8_t*>(p.out) + static_cast<size_t>(b) * p.heads * kLatent * esz
+                            : reinterpret_cast<uint8_t*>(p.part_o + static_cast<size_t>(part) * p.heads * kLatent);
+      uint8_t* wst = smem + C::kOffX + warp * NH * 32 * 4;   // this warp's [NH][32] staging rows
+      const int lg = st_bf16 ? 2 : 3;                          // 16-byte chunks per head row: 4 or 8
 #pragma unroll 1
-        for (int mb = 0; mb < 4; ++mb) {
-          uint32_t o[NH];
-          tmem_ld_row<NH>(tmem + lane_off + C::kTmO + mb * NH, o);
+      for (int r = 0; r < 2; ++r) {
+        // blocks r and r+2 come from one latent unit; the commit after the
+        // second also covers the first
+        if (tid == 0 && nitem < 4) MLA_TRACE_RAW(14, 16 + 8 * nitem + r, clock64());
+        wait(bar(C::bOBlk + r + 2), nitem & 1);
+        if (tid == 0 && nitem < 4) MLA_TRACE_RAW(14, 48 + 4 * nitem + r, clock64());
+        tc_fence_after();
+        uint32_t o[2][NH];
+        if (!aborted) {
+          tmem_ld_cols<NH>(tmem + lane_off + C::kTmO + r * NH, o[0]);
+          tmem_ld_cols<NH>(tmem + lane_off + C::kTmO + (r + 2) * NH, o[1]);
           tmem_wait_ld();
-          const int dim = 128 * mb + dim_row;
+        } else {
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            const float v = __uint_as_float(o[h]) / l_tot[h];
-            if (part < 0) {
-              const size_t idx = (static_cast<size_t>(b) * p.heads + h) * kLatent + dim;
-              if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
-              else reinterpret_cast<float*>(p.out)[idx] = v;
-            } else {
-              p.part_o[(static_cast<size_t>(part) * p.heads + h) * kLatent + dim] = v;
+          for (int h = 0; h < NH; ++h) o[0][h] = o[1][h] = 0;
+        }
+        if (r == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && !aborted) mbar_arrive(bar(C::bOEmpty));
+        }
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int mb = r + 2 * hb;
+          if (st_bf16) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              reinterpret_cast<__nv_bfloat16*>(wst)[h * 32 + lane] =
+                  __float2bfloat16_rn(__uint_as_float(o[hb][h]) * inv_l[h]);
+          } else {
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              reinterpret_cast<float*>(wst)[h * 32 + lane] = __uint_as_float(o[hb][h]) * inv_l[h];
+          }
+          __syncwarp();
+          // the warp's block: NH heads x 32 dims as 16-byte chunks, head-major
+#pragma unroll
+          for (int k = 0; k < NH * 8 / 32; ++k) {
+            const int c = lane + 32 * k;
+            if (c < (NH << lg) && !aborted) {
+              const int h = c >> lg, cc = c & ((1 << lg) - 1);
+              const uint4 v = *reinterpret_cast<const uint4*>(wst + (h * 32) * esz + 16 * cc);
+              *reinterpret_cast<uint4*>(dst + (static_cast<size_t>(h) * kLatent + 128 * mb + 32 * warp) * esz + 16 * cc) =
+                  v;
             }
           }
+          __syncwarp();
         }
+        if (tid == 0 && nitem < 8) MLA_TRACE_RAW(13, 8 * nitem + 1 + r, clock64());
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && !aborted) mbar_arrive(bar(C::bOEmpty));
-      if (!aborted) {
-        const int tid = threadIdx.x;
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          if (tid == h) {
-            const float l = (m_ref[h] + __log2f(l_tot[h])) * 0.69314718055994531f;
-            if (part < 0) { if (p.lse) p.lse[static_cast<size_t>(b) * p.heads + h] = l; }
-            else p.part_lse[static_cast<size_t>(part) * p.heads + h] = l;
-          }
-        }
-      }
+      named_bar_sync(kBarSm, 128);   // the staging rows double as the next tile's exchange buffer
+      if (tid == 0 && nitem < 24) MLA_TRACE_RAW(15, 9 + 2 * nitem, clock64());
       ++nitem;
     }
   }
@@ -591,6 +680,12 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kPvWarp) tmem_dealloc(tmem, C::kTmemCols);
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0) {
+    MLA_TRACE_RAW(15, 1, static_cast<long long>(globaltimer()));
+    MLA_TRACE_RAW(15, 4, clock64());
+  }
+#endif
 }
 
 template <int NH>
@@ -604,7 +699,7 @@ int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap
       return MLA_ERR_CUDA;
     attr_done = true;
   }
-  swab_kernel<NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
+  swab_kernel<NH><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
