@@ -18,14 +18,15 @@ constexpr int32_t kPlanMagic = 0x4D4C4131;
 constexpr int32_t kPlanVersion = 1;
 constexpr int kHeaderWords = 16;
 enum PlanHeader : int {
-  kHMagic = 0, kHVersion, kHBatch, kHHeads, kHVariant, kHTile, kHWorkers, kHChunkTiles /* load budget per worker */,
+  kHMagic = 0, kHVersion, kHBatch, kHHeads, kHVariant, kHTile, kHWorkers, kHCap /* load budget per worker, tokens */,
   kHItems, kHPartials, kHMerges, kHHeadGroups, kHCtasPerWorker, kHTotalWords, kHNumSms,
   kHReserved
 };
 constexpr int kVariantSwab = 1;  // H in {16, 32}: one CTA per worker, 128-token tiles
 constexpr int kVariantPair = 2;  // H in 48..128: a 2-CTA cluster per worker, 64-token tiles
-constexpr int kItemOverheadTiles = 1;
-constexpr int kMinPieceTiles = 1;
+constexpr int kItemOverheadTokens = 32;   // plan cost of one work item (its epilogue), in tokens
+constexpr int kMinPieceTokens = 64;       // no cut piece is shorter
+constexpr int kCapStepTokens = 8;         // the budget grows in these steps until the fill fits
 constexpr size_t kWsHeaderBytes = 256;
 
 // offsets of the plan arrays, from the header

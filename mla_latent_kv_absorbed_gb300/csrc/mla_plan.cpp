@@ -6,14 +6,18 @@
 //
 //   * variant by head count: H in {16, 32} -> one CTA per worker; H in
 //     48..128 (step 16) -> a 2-CTA cluster per worker; 64-token tiles for both;
-//   * W workers = SMs / CTAs-per-worker; an item of t tiles costs t + 1;
+//   * W workers = SMs / CTAs-per-worker; loads are counted in tokens, an item
+//     of n tokens costs its tiles, roundup(n, 64), plus kItemOverheadTokens
+//     (its epilogue): a worker's time follows its tiles, ragged or not;
 //   * wrap-around fill: requests, in order, are poured into workers 0, 1, ...
 //     each up to a load budget cap, so a request is cut only where a worker
-//     is full (at most W - 1 cuts, hence few partial states to merge);
-//   * no cut piece is shorter than kMinPieceTiles: with less space left the
+//     is full (at most W - 1 cuts, hence few partial states to merge), at a
+//     tile boundary of the request (only its last piece has a ragged tile);
+//   * no cut piece is shorter than kMinPieceTokens: with less space left the
 //     worker is closed, and a shorter tail stays with its head piece;
-//   * cap starts at ceil((total + (nonempty + W - 1)) / W) and grows by one
-//     tile until the fill fits on W workers.
+//   * cap starts at ceil((total + (nonempty + W - 1) * overhead) / W) tokens,
+//     total counting every request in whole tiles, and grows by
+//     kCapStepTokens until the fill fits on W workers.
 // The plan is deterministic: equal inputs give identical words.
 #include <algorithm>
 #include <cstdint>
@@ -27,36 +31,39 @@ namespace {
 
 struct Piece {
   int b;
-  long long k0;      // first tile of the piece inside its request
-  long long tiles;
+  long long k0;      // first token of the piece inside its request
+  long long n;       // tokens
 };
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+constexpr long long kTileTokens = 64;
+inline long long round_up_tile(long long n) { return ceil_div(n, kTileTokens) * kTileTokens; }
 
-// Wrap-around fill with load budget cap; false when W workers do not suffice.
-bool fill(const std::vector<long long>& tiles, int W, long long cap, std::vector<std::vector<Piece>>& lists) {
+// Wrap-around fill with load budget cap (tokens); false when W workers do not suffice.
+bool fill(const std::vector<long long>& len, int W, long long cap, std::vector<std::vector<Piece>>& lists) {
   lists.assign(W, {});
   int w = 0;
   long long used = 0;
-  for (size_t b = 0; b < tiles.size(); ++b) {
+  for (size_t b = 0; b < len.size(); ++b) {
     long long k0 = 0;
-    const long long t = tiles[b];
-    while (k0 < t) {
+    const long long L = len[b];
+    while (k0 < L) {
       if (w == W) return false;
-      const long long rem = t - k0;
-      const long long space = cap - used - kItemOverheadTiles;
+      const long long rem = L - k0;
+      const long long space = cap - used - kItemOverheadTokens;
+      const long long fit = space / kTileTokens * kTileTokens;   // whole tiles that fit
       long long take;
-      if (rem <= space || (space >= 1 && rem - space < kMinPieceTiles)) {
+      if (round_up_tile(rem) <= space || (fit >= kTileTokens && rem - fit < kMinPieceTokens)) {
         take = rem;
-      } else if (space >= kMinPieceTiles) {
-        take = space;
+      } else if (fit >= kMinPieceTokens) {
+        take = fit;
       } else {
         ++w;
         used = 0;
         continue;
       }
       lists[w].push_back({static_cast<int>(b), k0, take});
-      used += take + kItemOverheadTiles;
+      used += round_up_tile(take) + kItemOverheadTokens;
       k0 += take;
     }
   }
@@ -87,21 +94,18 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
   const int W = num_sms / cpw;
   if (W < 1) return MLA_ERR_INVALID_ARG;
 
-  std::vector<long long> tiles(B);
-  long long total = 0;
+  std::vector<long long> len(B);
+  long long total = 0, nonempty = 0;   // total in whole tiles
   for (int b = 0; b < B; ++b) {
-    const long long L = static_cast<long long>(indptr[b + 1]) - indptr[b];
-    tiles[b] = ceil_div(L, T);
-    total += tiles[b];
+    len[b] = static_cast<long long>(indptr[b + 1]) - indptr[b];
+    total += round_up_tile(len[b]);
+    nonempty += len[b] > 0 ? 1 : 0;
   }
-
-  long long nonempty = 0;
-  for (long long t : tiles) nonempty += t > 0 ? 1 : 0;
   long long cap = 0;
   std::vector<std::vector<Piece>> lists(W);
   if (total > 0) {
-    cap = ceil_div(total + (nonempty + W - 1) * kItemOverheadTiles, W);
-    while (!fill(tiles, W, cap, lists)) ++cap;
+    cap = ceil_div(total + (nonempty + W - 1) * kItemOverheadTokens, W);
+    while (!fill(len, W, cap, lists)) cap += kCapStepTokens;
   }
 
   std::vector<long long> npieces(B, 0), pstart(B), seen(B, 0);
@@ -116,8 +120,8 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
   std::vector<int32_t> wptr(1, 0), items;
   for (int w = 0; w < W; ++w) {
     for (const Piece& pc : lists[w]) {
-      const long long begin = static_cast<long long>(indptr[pc.b]) + pc.k0 * T;
-      const long long end = std::min<long long>(indptr[pc.b + 1], begin + pc.tiles * T);
+      const long long begin = static_cast<long long>(indptr[pc.b]) + pc.k0;
+      const long long end = begin + pc.n;
       const long long part = npieces[pc.b] > 1 ? pstart[pc.b] + seen[pc.b] : -1;
       ++seen[pc.b];
       items.push_back(pc.b);
@@ -148,7 +152,7 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
   words[kHVariant] = variant;
   words[kHTile] = T;
   words[kHWorkers] = W;
-  words[kHChunkTiles] = static_cast<int32_t>(cap);
+  words[kHCap] = static_cast<int32_t>(cap);
   words[kHItems] = static_cast<int32_t>(n_items);
   words[kHPartials] = static_cast<int32_t>(P);
   words[kHMerges] = static_cast<int32_t>(n_merge);

@@ -62,16 +62,22 @@ constexpr int kAtom = T * 128;             // 8 KB: 64 tokens x 64 dims
 constexpr int kUnit = 4 * kAtom;           // latent unit: atoms {c, c+4, c+1, c+5}
 constexpr int kRopeUnit = 2 * kAtom;       // rope atom, then the rope shifted by 32 dims
 constexpr int kRopeUnits = 2;
-#ifndef MLA_SWAB_LEAD
-#define MLA_SWAB_LEAD 1
+#ifndef MLA_SWAB_LEAD_UNITS
+#define MLA_SWAB_LEAD_UNITS 4
 #endif
-constexpr int kLeadTiles = MLA_SWAB_LEAD;   // tiles a producer may run ahead of the landed ones
+// Pacing: a producer issues latent unit s only once unit s - kLeadUnits has
+// landed (and rope unit g once rope unit g - kLeadRope has), which bounds the
+// bytes in flight per SM; more would only lengthen the memory queues.
+constexpr int kLeadUnits = MLA_SWAB_LEAD_UNITS;
+constexpr int kLeadRope = (kLeadUnits + 1) / 2;
+static_assert(kLeadRope <= kRopeUnits, "a rope slot's phase must not be lapped while it is waited on");
 constexpr int kBarSm = 1, kBarVote = 2, kBarPair0 = 3, kBarProd = 5;   // named barriers
 
 template <int NH>
 struct Cfg {
   static constexpr int kHalf = NH / 2;
   static constexpr int kLatUnits = (NH == 16) ? 5 : 4;   // 2.5 or 2 tiles of latent
+  static_assert(kLeadUnits <= kLatUnits, "a latent slot's phase must not be lapped while it is waited on");
   static constexpr int kQPair = 2 * NH * 128;            // two Q atoms of NH rows
   static constexpr int kQBytes = 5 * kQPair;             // 4 latent pairs + the rope pair
   static constexpr int kPBuf = NH * 128;                 // P^T: NH heads x 64 tokens bf16
@@ -303,15 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bool e_ok = true;
         if (lane == 0 && use > 0) e_ok = mbar_wait(empty, (use - 1) & 1, wc);
-        // pace: the same unit of tile g - kLeadTiles must have landed, so that
-        // about kLeadTiles tiles per SM are in flight (enough to cover the
-        // memory latency; more would only lengthen the memory queues)
-        if (lane == 0 && e_ok && g >= static_cast<uint32_t>(kLeadTiles)) {
-          const uint32_t gp = g - kLeadTiles;
+        if (lane == 0 && e_ok) {
           if (rope) {
-            e_ok = mbar_wait(bar(C::bRopeFull + gp % kRopeUnits), (gp / kRopeUnits) & 1, wc);
-          } else {
-            const uint32_t sp = 2 * gp + u;
+            if (g >= static_cast<uint32_t>(kLeadRope)) {
+              const uint32_t gp = g - kLeadRope;
+              e_ok = mbar_wait(bar(C::bRopeFull + gp % kRopeUnits), (gp / kRopeUnits) & 1, wc);
+            }
+          } else if (2 * g + u >= static_cast<uint32_t>(kLeadUnits)) {
+            const uint32_t sp = 2 * g + u - kLeadUnits;
             e_ok = mbar_wait(bar(C::bLatFull + sp % C::kLatUnits), (sp / C::kLatUnits) & 1, wc);
           }
         }

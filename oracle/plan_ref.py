@@ -13,16 +13,18 @@ contexts across SMs.  They give no rule, so this is the one the library uses:
     H in {48, 64, ..., 128} -> "pair" (a two-CTA cluster per worker); both
     work in 64-token tiles;
   * W workers = SMs (swab) or SMs // 2 (pair);
-  * tiles_b = ceil(L_b / T); total = sum tiles_b; a work item of t tiles
-    costs t + ITEM_OVERHEAD;
+  * loads are counted in tokens: a work item of n tokens costs its tiles,
+    ceil(n / T) * T, plus ITEM_OVERHEAD; total = sum over requests of
+    ceil(L_b / T) * T;
   * wrap-around fill: requests are walked in b order and poured into workers
     0, 1, ... in turn, each worker up to a load budget cap; a request is cut
-    only where a worker is full, so there are at most W - 1 cuts;
-  * no cut piece is shorter than MIN_PIECE tiles: with space < MIN_PIECE left
+    only where a worker is full, at a tile boundary of the request (so only
+    its last piece can be ragged), and there are at most W - 1 cuts;
+  * no cut piece is shorter than MIN_PIECE tokens: with space < MIN_PIECE left
     the worker is closed, and a tail shorter than MIN_PIECE stays with the
     head piece (the worker then overshoots cap by < MIN_PIECE);
   * cap starts at ceil((total + (nonempty + W - 1) * ITEM_OVERHEAD) / W) and
-    grows by one tile until the fill fits on the W workers;
+    grows by CAP_STEP tokens until the fill fits on the W workers;
   * partial slots are numbered over the cut requests in (b, piece) order; an
     uncut request's item writes out/lse directly (partial = -1);
   * the merge list holds every request that is cut or empty, in b order, with
@@ -37,8 +39,9 @@ from __future__ import annotations
 PLAN_MAGIC = 0x4D4C4131
 PLAN_VERSION = 1
 HEADER_WORDS = 16
-ITEM_OVERHEAD = 1
-MIN_PIECE = 1
+ITEM_OVERHEAD = 32    # tokens
+MIN_PIECE = 64        # tokens
+CAP_STEP = 8          # tokens
 WS_HEADER_BYTES = 256
 D_LATENT = 512
 
@@ -59,27 +62,35 @@ def _ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def _fill(tiles, W, cap):
+TILE = 64
+
+
+def _round_up(n: int) -> int:
+    return _ceil_div(n, TILE) * TILE
+
+
+def _fill(lengths, W, cap):
     """Wrap-around fill with load budget cap: per-worker lists of
-    (b, first tile, tiles), or None when W workers do not suffice."""
+    (b, first token, tokens), or None when W workers do not suffice."""
     lists = [[] for _ in range(W)]
     w, used = 0, 0
-    for b, t in enumerate(tiles):
+    for b, t in enumerate(lengths):
         k0 = 0
         while k0 < t:
             if w == W:
                 return None
             rem = t - k0
             space = cap - used - ITEM_OVERHEAD
-            if rem <= space or (space >= 1 and rem - space < MIN_PIECE):
+            fit = (space // TILE) * TILE if space > 0 else 0      # whole tiles that fit
+            if _round_up(rem) <= space or (fit >= TILE and rem - fit < MIN_PIECE):
                 take = rem
-            elif space >= MIN_PIECE:
-                take = space
+            elif fit >= MIN_PIECE:
+                take = fit
             else:
                 w, used = w + 1, 0
                 continue
             lists[w].append((b, k0, take))
-            used += take + ITEM_OVERHEAD
+            used += _round_up(take) + ITEM_OVERHEAD
             k0 += take
     return lists
 
@@ -95,17 +106,16 @@ def build_plan(kv_indptr, H: int, num_sms: int):
     W = num_sms // cpw
     if W < 1:
         raise ValueError("too few SMs")
-    tiles = [_ceil_div(L, T) for L in lengths]
-    total = sum(tiles)
-    nonempty = sum(1 for t in tiles if t > 0)
+    total = sum(_round_up(L) for L in lengths)
+    nonempty = sum(1 for L in lengths if L > 0)
 
     if total > 0:
         cap = _ceil_div(total + (nonempty + W - 1) * ITEM_OVERHEAD, W)
         while True:
-            lists = _fill(tiles, W, cap)
+            lists = _fill(lengths, W, cap)
             if lists is not None:
                 break
-            cap += 1
+            cap += CAP_STEP
     else:
         cap, lists = 0, [[] for _ in range(W)]
 
@@ -125,8 +135,8 @@ def build_plan(kv_indptr, H: int, num_sms: int):
     seen = [0] * B
     for w in range(W):
         for (b, k0, t) in lists[w]:
-            begin = int(kv_indptr[b]) + k0 * T
-            end = min(int(kv_indptr[b + 1]), begin + t * T)
+            begin = int(kv_indptr[b]) + k0
+            end = begin + t
             part = pstart[b] + seen[b] if npieces[b] > 1 else -1
             seen[b] += 1
             words_items += [b, begin, end, part]

@@ -3,9 +3,10 @@
 The pages fix no chunking rule, only its job (cover every key once, balance
 long and short contexts across SMs), so these pins check that job: exact
 coverage, partial numbering, the merge list, and the wrap-around fill's
-bounds: every worker's load within MIN_PIECE - 1 tiles of the budget cap, cap
-within MIN_PIECE tiles of the ideal ceil((total + items) / W), no cut piece
-shorter than MIN_PIECE tiles, and at most W - 1 cuts.
+bounds (in tokens, pieces costed in whole tiles): every worker's load within
+MIN_PIECE of the budget cap, cap within 2 MIN_PIECE + CAP_STEP of the ideal
+ceil((total + items) / W), cuts only at tile boundaries of the request, no
+cut piece shorter than MIN_PIECE, and at most W - 1 cuts.
 """
 import numpy as np
 import pytest
@@ -35,13 +36,13 @@ def _check(indptr, H, sms):
     T, c = d["T"], d["c"]
     assert d["wptr"][0] == 0 and d["wptr"][-1] == d["n"]
     assert all(a <= b for a, b in zip(d["wptr"], d["wptr"][1:]))
-    items_max = c - PR.ITEM_OVERHEAD + PR.MIN_PIECE - 1 if c else 0
+    items_max = c - PR.ITEM_OVERHEAD + PR.MIN_PIECE if c else 0   # tokens
     # exact coverage of each request's keys
     cover = {b: [] for b in range(B)}
     parts = {}
     for (b, s, e, p) in d["items"]:
         assert indptr[b] <= s < e <= indptr[b + 1]
-        assert e - s <= items_max * T
+        assert e - s <= items_max
         cover[b].append((s, e))
         if p >= 0:
             assert p not in parts
@@ -68,22 +69,26 @@ def _check(indptr, H, sms):
             _, p0, p1 = mset[b]
             assert p1 - p0 == (nb if nb > 1 else 0)
             assert sorted(p for (bb, _, _, p) in d["items"] if bb == b) == list(range(p0, p1))
-    # fill bounds
-    tiles = [-(-(indptr[b + 1] - indptr[b]) // T) for b in range(B)]
-    total, nonempty = sum(tiles), sum(1 for t in tiles if t > 0)
+    # fill bounds (tokens)
+    lengths = [int(indptr[b + 1] - indptr[b]) for b in range(B)]
+    rup = lambda n: -(-n // T) * T
+    total, nonempty = sum(rup(L) for L in lengths), sum(1 for L in lengths if L > 0)
     loads = []
     for w in range(d["W"]):
         its = d["items"][d["wptr"][w]:d["wptr"][w + 1]]
-        loads.append(sum(-(-(e - s) // T) + PR.ITEM_OVERHEAD for (_, s, e, _) in its))
+        loads.append(sum(rup(e - s) + PR.ITEM_OVERHEAD for (_, s, e, _) in its))
+    for b in range(B):
+        for (s, e) in sorted(cover[b])[:-1]:
+            assert (e - s) % T == 0                      # only a request's last piece is ragged
     if total:
         ideal = -(-(total + (nonempty + d["W"] - 1) * PR.ITEM_OVERHEAD) // d["W"])
-        assert ideal <= c <= ideal + PR.MIN_PIECE
-        assert max(loads) <= c + PR.MIN_PIECE - 1
-        cuts = sum(len(cover[b]) - 1 for b in range(B) if tiles[b] > 0)
+        assert ideal <= c <= ideal + 2 * PR.MIN_PIECE + PR.CAP_STEP
+        assert max(loads) <= c + PR.MIN_PIECE
+        cuts = sum(len(cover[b]) - 1 for b in range(B) if lengths[b] > 0)
         assert cuts <= d["W"] - 1 and d["P"] <= 2 * cuts
         for b in range(B):
             if len(cover[b]) > 1:
-                assert all(-(-(e - s) // T) >= PR.MIN_PIECE for (s, e) in cover[b])
+                assert all(e - s >= PR.MIN_PIECE for (s, e) in cover[b])
     else:
         assert c == 0 and d["n"] == 0
     # workspace holds P partial states
@@ -116,13 +121,10 @@ def test_edge_batches():
 def test_long_request_is_split_over_workers():
     d = _check([0, 65536, 196608], 128, 152)
     assert d["P"] >= d["W"] - 1                     # both requests cut into many pieces
-    T, W = d["T"], d["W"]
-    loads = []
-    for w in range(W):
-        its = d["items"][d["wptr"][w]:d["wptr"][w + 1]]
-        loads.append(sum(-(-(e - s) // T) + PR.ITEM_OVERHEAD for (_, s, e, _) in its))
-    total_tiles = 196608 // T
-    assert max(loads) <= -(-total_tiles // W) + PR.ITEM_OVERHEAD    # within one tile of perfect
+    W = d["W"]
+    tokens = [sum(e - s for (_, s, e, _) in d["items"][d["wptr"][w]:d["wptr"][w + 1]]) for w in range(W)]
+    perfect = -(-196608 // W)
+    assert max(tokens) <= perfect + 2 * PR.ITEM_OVERHEAD + PR.MIN_PIECE + PR.CAP_STEP   # within ~2 tiles of perfect
 
 
 def test_uniform_batch_cuts_few_requests():
