@@ -480,15 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx *= 1.000030517578125f;
           e_own = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127, -100);
           const float inv = pow2i(min(14 - e_own, 127)), st = pow2i(max(e_own - 14, -126));
-          const uint64_t inv2 = f2_pack(inv, inv), enc2 = f2_pack(kEncBias, kEncBias);
-          const uint64_t st2 = f2_pack(st, st), dec2 = f2_pack(-kEncBias * st, -kEncBias * st);
-          const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+          const float2 inv2 = f2_pack(inv, inv), enc2 = f2_pack(kEncBias, kEncBias);
+          const float2 st2 = f2_pack(st, st), dec2 = f2_pack(-kEncBias * st, -kEncBias * st);
+          const float2 sl2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t o16[16];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const uint64_t t = f2_fma(f2_pack(__uint_as_float(r[16 * c + 2 * i]), __uint_as_float(r[16 * c + 2 * i + 1])),
+              const float2 t = f2_fma(f2_pack(__uint_as_float(r[16 * c + 2 * i]), __uint_as_float(r[16 * c + 2 * i + 1])),
                                         inv2, enc2);
               float t0, t1;
               f2_unpack(t, t0, t1);
@@ -567,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e_peer =
             (head_ok && !aborted) ? *reinterpret_cast<const int*>(smem + kOffXE + xs * 512 + h * 4) : -100;
         const float st_p = pow2i(max(e_peer - 14, -126));
-        const uint64_t st2 = f2_pack(st_p, st_p), dec2 = f2_pack(-kDecBias * st_p, -kDecBias * st_p);
-        const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+        const float2 st2 = f2_pack(st_p, st_p), dec2 = f2_pack(-kDecBias * st_p, -kDecBias * st_p);
+        const float2 sl2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {            // 8 tokens per 16-byte chunk
           uint4 pv = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);   // code of 0
@@ -577,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int t = 8 * c + 2 * k;
-            const uint64_t f = f2_pack(__uint_as_float(__byte_perm(pq[k], 0x4B000000u, 0x7610)),
+            const float2 f = f2_pack(__uint_as_float(__byte_perm(pq[k], 0x4B000000u, 0x7610)),
                                        __uint_as_float(__byte_perm(pq[k], 0x4B000000u, 0x7632)));
-            const uint64_t sp = f2_mul(f2_fma(f, st2, dec2), sl2);
+            const float2 sp = f2_mul(f2_fma(f, st2, dec2), sl2);
             float s0, s1;
             f2_unpack(f2_add(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), sp), s0, s1);
             sv[t] = __float_as_uint(s0);
@@ -625,8 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // P = 2^(s - m_ref) as bf16, written over the peer's rows (K-major, 128-byte swizzle)
-        const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
-        uint64_t l2 = f2_pack(0.f, 0.f);
+        const float2 nm2 = f2_pack(-m_ref, -m_ref);
+        float2 l2 = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t pk[4];
