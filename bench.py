@@ -227,9 +227,13 @@ def run_reference(args, batch, rank, pg):
 
 def workload_config(batch, args, rotate=None):
     spec = batch.spec
-    l2 = ("inputs larger than L2: step k reads input set k mod %d (own KV pool, q, indices), "
-          "the other sets stream %.0f MB of cache in between (> 4x L2)" % rotate) if rotate else \
-        "flushed before every timed step (256 MiB write, outside the events)"
+    if rotate and rotate[0] > 1:
+        l2 = ("inputs larger than L2: step k reads input set k mod %d (own KV pool, q, indices), "
+              "the other sets stream %.0f MB of cache in between" % rotate)
+    elif rotate:
+        l2 = "one input set, steps back to back (profiling run; not a benchmark number)"
+    else:
+        l2 = "flushed before every timed step (256 MiB write, outside the events)"
     return {"workload": spec.name if spec else "custom", "batch": batch.batch, "heads": batch.heads,
             "kv_lora_rank": 512, "qk_rope_head_dim": 64, "nnz": batch.nnz, "pool_slots": batch.pool,
             "max_context": int(batch.lengths.max()), "page_size": 1, "out_dtype": "fp32",
@@ -266,7 +270,7 @@ def run_ours(args, batch, world, rank, local, pg):
     # that the other R-1 steps stream more than 4x L2 of cache rows
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     step_kv_bytes = batch.nnz * 1152
-    R = max(2, math.ceil(4 * l2_bytes / step_kv_bytes) + 1)
+    R = args.sets if args.sets > 0 else max(2, math.ceil(4 * l2_bytes / step_kv_bytes) + 1)
     sets = [(q_nope, q_rope, kv, indices_d)]
     for _ in range(R - 1):
         sets.append((q_nope.clone(), q_rope.clone(), kv.clone(), indices_d.clone()))
@@ -435,6 +439,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="input sets rotated over the back-to-back steps (0: enough to defeat L2; 1 for profiling)")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     args = ap.parse_args(argv)

@@ -188,3 +188,30 @@ def test_many_head_workloads_sampled(number):
     req = sorted(set([0, bt.batch - 1] + list(range(0, bt.batch, max(1, bt.batch // 6)))))
     ro, rl = oracle(bt, requests=req)
     assert_close(out, lse, ro, rl, requests=req)
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_plan_item_outside_its_request_is_reported_not_faulted(H):
+    # A plan item naming the wrong request (its tokens still inside kv_indices)
+    # and one reaching past kv_indices: the call returns, the device status
+    # reads MLA_ERR_PLAN_MISMATCH, and the next call with a good plan is clean.
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding
+    bt = _batch([300, 200, 500], H, seed=21)
+    dev = to_device(bt)
+    dec = binding.Decoder(bt.kv_indptr, H)
+    W = int(dec.plan_host[6])
+    items_off = 16 + W + 1
+    bad = dec.plan_host.copy()
+    bad[items_off] = (bad[items_off] + 1) % bt.batch          # first item now names another request
+    n_items = int(bad[8])
+    bad[items_off + 4 * (n_items - 1) + 2] = bt.nnz + 64      # last item reaches past kv_indices
+    out = torch.zeros((bt.batch, H, 512), device="cuda")
+    lse = torch.zeros((bt.batch, H), device="cuda")
+    binding.decode_run(bad, torch.from_numpy(bad).cuda(), dev["q_nope"], dev["q_rope"], dev["kv_cache"],
+                       dev["kv_indptr"], dev["kv_indices"], bt.sm_scale, out, lse, dec.workspace)
+    assert dec.check() == 7          # MLA_ERR_PLAN_MISMATCH
+    dec.workspace.zero_()
+    (o2, l2), _ = run_gpu(bt, dev=dev)
+    ro, rl = oracle(bt)
+    assert_close(o2, l2, ro, rl)
