@@ -20,43 +20,47 @@
 //
 // The exchange is the narrow path: an SM moves only about 9 bytes per cycle
 // to its cluster peer, so the partial rows travel as 16-bit fixed point with
-// one power-of-two scale per row (64 scores: 128 B + a 4-byte exponent, half
-// of fp32).  With s_max the largest |partial| of the row, the step is at most
-// 2^-14 s_max and the rounding error at most 2^-15 s_max per partial.  Both
-// CTAs add the two DEQUANTISED partials, so S, P, the running maximum and the
-// row sums are bit-identical in the pair.
+// a power-of-two scale per row and 32-token half (32 scores: 64 B + a 4-byte
+// exponent).  With s_max the largest |partial| of the half row, the step is
+// at most 2^-14 s_max and the rounding error at most 2^-15 s_max per partial.
+// Both CTAs add the two DEQUANTISED partials, so S, P, the running maximum
+// and the row sums are bit-identical in the pair.
 //
 // TMEM (512 columns per CTA): O_c [0,256) fp32; the query's latent half
 // [256,384) as packed bf16 (A operand of QK, read from TMEM); two score
 // buffers [384,448), [448,512) that hold this CTA's fp32 partial, then its
-// quantised row (32 packed columns and the row exponent).
+// dequantised row.
 //
 // Shared memory per CTA: a ring of 4 latent blocks (64 tokens x 256 dims,
 // 32 KB, gathered with TMA gather4), 3 rope atoms (8 KB), the rope query
 // (16 KB), 3 exchange slots (16 KB each: the peer's quantised partial rows,
 // later overwritten in place by P as bf16, the A operand of PV), the peer's
-// row exponents and a small ring of slot indices.
+// exponents and the softmax warps' reduction buffers.
 //
-// Warp roles per CTA (512 threads):
-//   warps 0-3   softmax / epilogue: thread h owns head h (TMEM lane h); adds
-//               the two quantised partials, writes P, keeps m and l
-//   warps 4-7   sender: quantises this CTA's partial, leaves it in TMEM for
-//               the softmax and pushes it to the peer (st.async)
-//   warp 8      QK issuer and rope-query loader (one thread)
-//   warp 9      TMEM allocator and PV issuer (one thread)
-//   warp 10     index stager (slot numbers to shared memory)
-//   warps 11-15 gather producers: latent atoms 0-3 of the CTA's half, rope
+// Warp roles per CTA (736 threads).  Warp w of the sixteen score warps owns
+// heads 32(w%4)..+31 (TMEM lane h = head h) and tokens 32((w/4)%2)..+31 of
+// every tile; the sender and the softmax warp of the same heads and tokens
+// hand the S buffer over in place:
+//   warps 8-15  senders: load this CTA's latent half of the query into TMEM;
+//               for tile g quantise their part of this CTA's partial, leave
+//               the dequantised values in TMEM and push the codes into the
+//               peer's exchange slot (st.async)
+//   warps 0-7   softmax: add the peer's codes to the dequantised row, take the
+//               softmax (the row maximum is combined with the partner warp of
+//               the other token half), write P over the peer's rows; after an
+//               item's last tile, the epilogue (1/l, O, lse)
+//   warp 16     QK issuer and rope-query loader (one thread)
+//   warp 17     TMEM allocator and PV issuer (one thread)
+//   warps 18-22 gather producers: latent atoms 0-3 of the CTA's half, rope;
+//               each loads its tile's slot numbers itself
+// Splitting senders from softmax lets tile g+1 be quantised and pushed while
+// tile g is still in its softmax, so the exchange latency is hidden.
 //
-// Pushing a tile's rows stalls the issuing warps for as long as the link
-// needs to carry them, so only the sender warps push; nothing on the
-// softmax -> PV -> QK chain waits behind a push.  Per tile g (S buffer
-// g mod 2, exchange slot g mod 3):
-//   QK(g) -> sender quantises, stores the int16 row over the partial in the
-//   S buffer and pushes it into the peer's slot -> softmax waits for the
-//   peer's rows, reads its own from TMEM (freeing the S buffer for
-//   QK(g+2)), adds them, writes P over the peer's rows -> PV(g) frees the
-//   latent block and, through a multicast commit, tells the PEER that its
-//   rows for tile g+3 may land in this slot.
+// Per tile g (S buffer g mod 2, exchange slot g mod 3): QK(g) -> the senders
+// quantise and push -> the softmax warps add the peer's rows and read the
+// buffer (freeing it for QK(g+2)), write P -> PV(g) frees the latent block
+// and, through a multicast commit, tells the PEER that its rows for tile g+3
+// may land in this slot.
 // The softmax moves its reference maximum lazily (threshold 8 in log2
 // units) as in the few-heads kernel.
 #include "mla_device.cuh"
@@ -66,24 +70,27 @@ namespace mla {
 namespace pair {
 
 constexpr int T = 64;                        // tokens per tile
+constexpr int TH = 32;                       // tokens of a tile per row warp
+constexpr int kRowWarps = 8;                 // softmax warps 0-7 and sender warps 8-15 alike
 constexpr int kProducers = 5;                // latent atoms 0-3 and the rope
-constexpr int kIdxSlots = 4;
-constexpr int kMmaWarp = 8, kLoaderWarp = 9, kIdxWarp = 10, kProducerWarp0 = 11;
+constexpr int kSendWarp0 = 8, kMmaWarp = 16, kLoaderWarp = 17, kProducerWarp0 = 18;
 constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
 constexpr int kLatBlocks = 4;                // ring of latent blocks (every latent producer fills every block)
 constexpr int kRopeSlots = 3;
 constexpr int kXSlots = 3;                   // exchange slots
+constexpr int kLead = 3;                     // a producer issues tile g once tile g - kLead has landed
 constexpr int kAtom = T * 128;               // 8 KB: 64 tokens x 64 dims
 constexpr int kLatBlock = 4 * kAtom;         // 32 KB: 64 tokens x 256 dims
 constexpr int kXSlot = 128 * 128;            // 128 rows x 128 B (64 int16 scores, then 64 bf16 P)
-constexpr int kXRowBytes = 128 + 4;          // bytes one head's row carries to the peer
+constexpr int kXeSlot = 2 * 128 * 4;         // [2 token halves][128 rows] int32 exponents
+constexpr int kXBytes = kXSlot + kXeSlot;    // bytes the peer sends per tile
 constexpr int kOffLat = 0;
 constexpr int kOffRope = kOffLat + kLatBlocks * kLatBlock;
 constexpr int kOffQR = kOffRope + kRopeSlots * kAtom;   // rope query: 128 rows x 128 B (K-major SW128)
 constexpr int kOffX = kOffQR + 128 * 128;
-constexpr int kOffXE = kOffX + kXSlots * kXSlot;        // [kXSlots][128] int32 row exponents from the peer
-constexpr int kOffIdx = kOffXE + kXSlots * 128 * 4;
-constexpr int kOffBar = kOffIdx + 4 * kIdxSlots * T;
+constexpr int kOffXE = kOffX + kXSlots * kXSlot;        // [kXSlots] exponent blocks from the peer
+constexpr int kOffRed = kOffXE + kXSlots * kXeSlot;     // [2 bufs][2 halves][128] row maxima, [2][128] row sums
+constexpr int kOffBar = kOffRed + (2 * 2 * 128 + 2 * 128) * 4;
 // barriers
 constexpr int bLatFull = 0;
 constexpr int bLatEmpty = bLatFull + kLatBlocks;
@@ -92,18 +99,16 @@ constexpr int bRopeEmpty = bRopeFull + kRopeSlots;
 constexpr int bQFull = bRopeEmpty + kRopeSlots;
 constexpr int bQEmpty = bQFull + 1;
 constexpr int bSFull = bQEmpty + 1;          // [2] this CTA's partial is in the S buffer
-constexpr int bSQuant = bSFull + 2;          // [2] the quantised row is in the S buffer
-constexpr int bSFree = bSQuant + 2;          // [2] the softmax has read the S buffer
+constexpr int bSQuant = bSFull + 2;          // [2] the senders left the dequantised row in the S buffer
+constexpr int bSFree = bSQuant + 2;          // [2] the softmax warps have read the S buffer
 constexpr int bPFull = bSFree + 2;           // [kXSlots] P is in the exchange slot
-constexpr int bPvDone = bPFull + kXSlots;
-constexpr int bOFull = bPvDone + 1;
+constexpr int bPvDone = bPFull + kXSlots;    // [2] PV(g) has completed (buffer g mod 2)
+constexpr int bOFull = bPvDone + 2;
 constexpr int bOEmpty = bOFull + 1;
 constexpr int bXFull = bOEmpty + 1;          // [kXSlots] the peer's rows have landed in this CTA's slot
 constexpr int bXFree = bXFull + kXSlots;     // [kXSlots] the PEER's slot may take this CTA's next rows
 constexpr int bDrain = bXFree + kXSlots;
-constexpr int bIdxFull = bDrain + 1;
-constexpr int bIdxEmpty = bIdxFull + kIdxSlots;
-constexpr int kNumBars = bIdxEmpty + kIdxSlots;
+constexpr int kNumBars = bDrain + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffLast = kOffMisc + 16;      // [kLatBlocks + kRopeSlots] last armed use
 constexpr int kSmemBytes = kOffLast + 4 * (kLatBlocks + kRopeSlots) + 1024;
@@ -111,32 +116,29 @@ constexpr int kTmO = 0, kTmQ = 256, kTmS = 384;
 constexpr uint32_t kIdescQK = idesc_bf16(128, T, false, false);     // M=128 heads, N=64 tokens
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // N=256 dims, B (V) MN-major
 static_assert(kProducers == 5, "producers 0-3 gather the latent atoms, producer 4 the rope");
-static_assert(kThreads == 512, "16 warps");
+static_assert(kThreads == 736, "23 warps");
+static_assert(kLead < kLatBlocks && kLead <= kRopeSlots, "a ring slot's phase must not be lapped while waited on");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 1024 == 0 && kXSlot % 1024 == 0 &&
-                  kOffIdx % 16 == 0,
+                  kOffXE % 16 == 0 && kOffBar % 8 == 0,
               "alignment");
 
-__device__ __forceinline__ bool item_ok(const DecodeParams& p, int b, int s, int e) {
-  if (b < 0 || b >= p.batch) return false;
+// Items every role processes: a request in range and a token range inside
+// kv_indices (so no access can leave the arrays).  Whether the range also
+// lies inside its own request is checked off the critical path by one
+// producer (item_in_request), which only records MLA_ERR_PLAN_MISMATCH.
+__device__ __forceinline__ bool item_ok(const DecodeParams& p, int nnz, int b, int s, int e) {
+  return b >= 0 && b < p.batch && 0 <= s && s < e && e <= nnz;
+}
+__device__ __forceinline__ bool item_in_request(const DecodeParams& p, int b, int s, int e) {
   const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
-  return lo <= s && s < e && e <= hi;
+  return lo <= s && e <= hi;
 }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > MLA_WAIT_LIMIT_NS) return;
-  }
-}
-
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  uint32_t a[16];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    tmem_ld16(taddr + 16 * c, a);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) r[16 * c + i] = a[i];
   }
 }
 
@@ -186,25 +188,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int it0 = wptr[w], it1 = wptr[w + 1];
   const int32_t* items = p.plan + p.items_off;
   const int H = p.heads;
+  const int nnz = __ldg(p.kv_indptr + p.batch);   // loaded alongside the plan words
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLatBlocks; ++i) { mbar_init(bar(bLatFull + i), 1); mbar_init(bar(bLatEmpty + i), 1); }
     for (int i = 0; i < kRopeSlots; ++i) { mbar_init(bar(bRopeFull + i), 1); mbar_init(bar(bRopeEmpty + i), 1); }
-    mbar_init(bar(bQFull), 5);                   // 4 sender warps (latent half) + the rope TMA
+    mbar_init(bar(bQFull), kRowWarps + 1);       // the row warps (latent half) + the rope TMA
     mbar_init(bar(bQEmpty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(bSFull + i), 1); mbar_init(bar(bSQuant + i), 4); mbar_init(bar(bSFree + i), 4);
+      mbar_init(bar(bSFull + i), 1); mbar_init(bar(bSQuant + i), kRowWarps); mbar_init(bar(bSFree + i), kRowWarps);
     }
     for (int i = 0; i < kXSlots; ++i) {
-      mbar_init(bar(bPFull + i), 4);
+      mbar_init(bar(bPFull + i), kRowWarps);
       mbar_init(bar(bXFull + i), 1);             // own expect_tx; the bytes come from the peer
       mbar_init(bar(bXFree + i), 1);             // the peer's PV commit
     }
     mbar_init(bar(bPvDone), 1);
+    mbar_init(bar(bPvDone + 1), 1);
     mbar_init(bar(bOFull), 1);
-    mbar_init(bar(bOEmpty), 4);
+    mbar_init(bar(bOEmpty), kRowWarps);
     mbar_init(bar(bDrain), 2);                   // both issuers' final commits
-    for (int i = 0; i < kIdxSlots; ++i) { mbar_init(bar(bIdxFull + i), 1); mbar_init(bar(bIdxEmpty + i), kProducers); }
     for (int i = 0; i < kLatBlocks + kRopeSlots; ++i) last_armed[i] = -1;
     *abort_flag = 0;
     fence_mbar_init();
@@ -225,96 +228,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   bool aborted = false;                          // set by the softmax / sender warps only
 
-  if (warp == kIdxWarp) {
-    // ---------------------------------------------------------- index stager
-    int* idx_ring = reinterpret_cast<int*>(smem + kOffIdx);
-    uint32_t g = 0;
-    bool ok = true;
-    for (int it = it0; it < it1 && ok; ++it) {
-      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      if (!item_ok(p, b, s, e)) {
-        if (lane == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
-        continue;
-      }
-      const int n = e - s;
-      for (int t0 = 0; t0 < n; t0 += T, ++g) {
-        const uint32_t slot = g % kIdxSlots, use = g / kIdxSlots;
-        int v[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) v[k] = __ldg(p.kv_indices + s + min(t0 + lane + 32 * k, n - 1));
-        bool w_ok = true;
-        if (lane == 0 && use > 0) w_ok = mbar_wait(bar(bIdxEmpty + slot), (use - 1) & 1, wc);
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) { ok = false; break; }
-        bool oob = false;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
-          idx_ring[slot * T + lane + 32 * k] = v[k];
-        }
-        if (__any_sync(0xffffffffu, oob) && lane == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bIdxFull + slot));
-      }
-    }
-  } else if (warp >= kProducerWarp0) {
+  if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
     // A warp completes one gather4 only every ~70-110 cycles, so a tile's
     // landing time is set by how many gathers one warp issues for it.  The
     // five producers split every tile evenly: producer pw < 4 gathers latent
     // atom pw of the CTA's half, producer 4 the rope atom; 16 gathers each.
+    // Each loads its tile's slot numbers (lane l < 16: tokens 4l..4l+3)
+    // before it waits for ring space; an out-of-range slot reads row 0 and
+    // sets MLA_ERR_INDEX_OOB, the ragged tail repeats the last valid slot.
     const int pw = warp - kProducerWarp0;
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
     const uint64_t pol = l2_policy_evict_first();
-    const int* idx_ring = reinterpret_cast<const int*>(smem + kOffIdx);
     uint32_t g = 0;
     bool ok = true;
     for (int it = it0; it < it1 && ok; ++it) {
       const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      if (!item_ok(p, b, s, e)) continue;
+      if (!item_ok(p, nnz, b, s, e)) {
+        if (lane == 0 && pw == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+        continue;
+      }
+      const bool in_req = pw != 0 || item_in_request(p, b, s, e);
       const int n = e - s;
       for (int t0 = 0; t0 < n && ok; t0 += T, ++g) {
-        const uint32_t islot = g % kIdxSlots;
-        bool w_ok = true;
-        if (lane == 0) w_ok = mbar_wait(bar(bIdxFull + islot), (g / kIdxSlots) & 1, wc);
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) { ok = false; break; }
-        // lane l < 16 holds tokens 4l..4l+3 (gather op l of an atom)
-        const int4 v = *reinterpret_cast<const int4*>(idx_ring + islot * T + 4 * (lane & 15));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(bIdxEmpty + islot));
+        int v[4];
+        bool oob = false;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[k] = __ldg(p.kv_indices + s + min(t0 + 4 * (lane & 15) + k, n - 1));
+          if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
+        }
+        if (oob && pw == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
         if (lane == 0 && pw == 0) MLA_TRACE_EVENT(0, g);
-        if (pw < 4) {
-          const uint32_t blk = g % kLatBlocks, use = g / kLatBlocks;
-          bool e_ok = true;
-          if (lane == 0 && use > 0) e_ok = mbar_wait(bar(bLatEmpty + blk), (use - 1) & 1, wc);
-          e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-          if (!e_ok) { ok = false; break; }
-          const uint32_t full = bar(bLatFull + blk);
-          if (lane == 0 && pw == 0) mbar_arrive_expect_tx(full, kLatBlock);
-          __syncwarp();
-          if (lane < 16)
-            tma_gather4(base + kOffLat + blk * kLatBlock + pw * kAtom + lane * 512, &tm_kv,
-                        64 * (4 * static_cast<int>(cta) + pw), v.x, v.y, v.z, v.w, full, pol);
-          if (lane == 0) atomicMax(last_armed + blk, static_cast<int>(use));
-          if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
-        } else {
-          const uint32_t rs = g % kRopeSlots, use = g / kRopeSlots;
-          bool e_ok = true;
-          if (lane == 0 && use > 0) e_ok = mbar_wait(bar(bRopeEmpty + rs), (use - 1) & 1, wc);
-          e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-          if (!e_ok) { ok = false; break; }
-          const uint32_t full = bar(bRopeFull + rs);
+        const bool rope = pw == 4;
+        const uint32_t nslots = rope ? kRopeSlots : kLatBlocks;
+        const uint32_t slot = g % nslots, use = g / nslots;
+        const uint32_t full = bar((rope ? bRopeFull : bLatFull) + slot);
+        bool e_ok = true;
+        if (lane == 0 && use > 0) e_ok = mbar_wait(bar((rope ? bRopeEmpty : bLatEmpty) + slot), (use - 1) & 1, wc);
+        if (lane == 0 && e_ok && g >= static_cast<uint32_t>(kLead)) {   // pace: tile g - kLead has landed
+          const uint32_t gp = g - kLead;
+          e_ok = mbar_wait(bar((rope ? bRopeFull : bLatFull) + gp % nslots), (gp / nslots) & 1, wc);
+        }
+        e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+        if (!e_ok) { ok = false; break; }
+        if (rope) {
           if (lane == 0) mbar_arrive_expect_tx(full, kAtom);
           if (lane == 0) MLA_TRACE_EVENT(11, g);
           __syncwarp();
           if (lane < 16)
-            tma_gather4(base + kOffRope + rs * kAtom + lane * 512, &tm_kv, 512, v.x, v.y, v.z, v.w, full, pol);
-          if (lane == 0) atomicMax(last_armed + kLatBlocks + rs, static_cast<int>(use));
+            tma_gather4(base + kOffRope + slot * kAtom + lane * 512, &tm_kv, 512, v[0], v[1], v[2], v[3], full, pol);
+          if (lane == 0) atomicMax(last_armed + kLatBlocks + slot, static_cast<int>(use));
+        } else {
+          if (lane == 0 && pw == 0) mbar_arrive_expect_tx(full, kLatBlock);
+          __syncwarp();
+          if (lane < 16)
+            tma_gather4(base + kOffLat + slot * kLatBlock + pw * kAtom + lane * 512, &tm_kv,
+                        64 * (4 * static_cast<int>(cta) + pw), v[0], v[1], v[2], v[3], full, pol);
+          if (lane == 0 && pw == 0) atomicMax(last_armed + slot, static_cast<int>(use));
+          if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
         }
       }
+      if (!in_req && lane == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
     }
-    named_bar_sync(3, 32 * kProducers);
+    named_bar_sync(9, 32 * kProducers);
     if (pw == 0 && lane < kLatBlocks + kRopeSlots) {
       const int u = last_armed[lane];
       const int bfull = lane < kLatBlocks ? bLatFull + lane : bRopeFull + (lane - kLatBlocks);
@@ -335,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
         const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-        if (!item_ok(p, b, s, e)) continue;
+        if (!item_ok(p, nnz, b, s, e)) continue;
         const int nt = (e - s + T - 1) / T;
         // the rope query of this item replaces the previous one once its last QK is done
         if (nitem > 0 && !mbar_wait(bar(bQEmpty), (nitem - 1) & 1, wc)) break;
@@ -385,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
         const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-        if (!item_ok(p, b, s, e)) continue;
+        if (!item_ok(p, nnz, b, s, e)) continue;
         const int nt = (e - s + T - 1) / T;
         for (int j = 0; j < nt; ++j, ++g) {
           const uint32_t xs = g % kXSlots, blk = g % kLatBlocks;
@@ -400,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_ss(tmem + kTmO, D(ap, ks * 32), D(bv, ks * 2048), kIdescPV, (j == 0 && ks == 0) ? 0u : 1u);
           umma_commit(bar(bLatEmpty + blk));
           umma_commit_mc(bar(bXFree + xs), peer_mask);         // the peer may send into this slot again
-          umma_commit(bar(bPvDone));
+          umma_commit(bar(bPvDone + (g & 1)));
           if (j == nt - 1) umma_commit(bar(bOFull));
           MLA_TRACE_EVENT(5, g);
         }
@@ -410,125 +387,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(bar(bDrain), 0);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // --------------------------------------------------------------- sender
-    const int qd = warp - 4;                     // TMEM lane quadrant of this warp
-    const int h = 32 * qd + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+  } else {
+    // ----------------------------------------------- sender and softmax warps
+    const bool is_sender = warp >= kSendWarp0;
+    const int q = warp & 3, th = (warp >> 2) & 1;   // TMEM lane quadrant, token half of every tile
+    const int h = 32 * q + lane;                 // head == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const bool head_ok = h < H;
     const uint32_t sw = static_cast<uint32_t>(h & 7);      // 16-byte chunk c of row h sits at c ^ (h mod 8)
     const uint32_t xrow_peer = mapa_shared(base + kOffX + h * 128, peer);
-    const uint32_t xe_peer = mapa_shared(base + kOffXE + h * 4, peer);
+    const uint32_t xe_peer = mapa_shared(base + kOffXE + (th * 128 + h) * 4, peer);
     const uint32_t xfull_peer = mapa_shared(bar(bXFull), peer);
-    auto wait = [&](uint32_t bb, uint32_t par, bool cluster_scope) {
-      if (aborted) return;
-      bool r = true;
-      if (lane == 0) r = cluster_scope ? mbar_wait<true>(bb, par, wc) : mbar_wait(bb, par, wc);
-      r = __shfl_sync(0xffffffffu, r, 0);
-      if (!r) aborted = true;
-    };
-    uint32_t g = 0, nitem = 0;
-    for (int it = it0; it < it1; ++it) {
-      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      if (!item_ok(p, b, s, e)) continue;
-      const int nt = (e - s + T - 1) / T;
-      // -- query latent half into TMEM (after the previous item's last QK)
-      if (nitem > 0) wait(bar(bQEmpty), (nitem - 1) & 1, false);
-      tc_fence_after();
-      if (!aborted) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(b) * H + h) * kLatent +
-                                                          256 * cta);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {            // 8 x 16 columns = 256 bf16
-          uint32_t r[16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 v = head_ok ? __ldg(src + 4 * c + k) : make_uint4(0, 0, 0, 0);
-            r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
-          }
-          tmem_st16(tmem + lane_off + kTmQ + 16 * c, r);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && !aborted) mbar_arrive(bar(bQFull));
-
-      for (int j = 0; j < nt; ++j, ++g) {
-        const uint32_t sb = g & 1, xs = g % kXSlots;
-        const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64;
-        wait(bar(bSFull + sb), (g >> 1) & 1, false);
-        if (threadIdx.x == 128) MLA_TRACE_EVENT(6, g);
-        tc_fence_after();
-        // quantise the partial row: 64 codes on the step 2^(e-14), where e is the
-        // exponent of max|s| nudged up by 2^-15 so that no code rounds to 32768;
-        // the scaled dequantised row goes back into the S buffer for the softmax
-        uint32_t qw[32];
-        int e_own;
-        {
-          uint32_t r[64];
-          if (!aborted) {
-            tmem_ld64(tm_s, r);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) r[i] = 0;
-          }
-          float mx = 0.f;
-#pragma unroll
-          for (int i = 0; i < 64; i += 2) mx = max3(mx, fabsf(__uint_as_float(r[i])), fabsf(__uint_as_float(r[i + 1])));
-          mx *= 1.000030517578125f;
-          e_own = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127, -100);
-          const float inv = pow2i(min(14 - e_own, 127)), st = pow2i(max(e_own - 14, -126));
-          const float2 inv2 = f2_pack(inv, inv), enc2 = f2_pack(kEncBias, kEncBias);
-          const float2 st2 = f2_pack(st, st), dec2 = f2_pack(-kEncBias * st, -kEncBias * st);
-          const float2 sl2 = f2_pack(p.scale_log2, p.scale_log2);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o16[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float2 t = f2_fma(f2_pack(__uint_as_float(r[16 * c + 2 * i]), __uint_as_float(r[16 * c + 2 * i + 1])),
-                                        inv2, enc2);
-              float t0, t1;
-              f2_unpack(t, t0, t1);
-              qw[8 * c + i] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x5410);
-              float d0, d1;
-              f2_unpack(f2_mul(f2_fma(t, st2, dec2), sl2), d0, d1);
-              o16[2 * i] = __float_as_uint(d0);
-              o16[2 * i + 1] = __float_as_uint(d1);
-            }
-            if (!aborted) tmem_st16(tm_s + 16 * c, o16);
-          }
-          if (!aborted) tmem_wait_st();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && !aborted) mbar_arrive(bar(bSQuant + sb));
-        if (threadIdx.x == 128) MLA_TRACE_EVENT(13, g);
-        // push it into the peer's slot xs once the peer's PV(g - kXSlots) has read that slot
-        if (g >= kXSlots) wait(bar(bXFree + xs), ((g / kXSlots) - 1) & 1, true);
-        if (threadIdx.x == 128) MLA_TRACE_EVENT(14, g);
-        if (!aborted && head_ok) {
-          const uint32_t fb = xfull_peer + 8u * xs;
-          const uint32_t dst = xrow_peer + xs * kXSlot;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_async_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), qw[4 * c], qw[4 * c + 1], qw[4 * c + 2],
-                        qw[4 * c + 3], fb);
-          st_async_b32(xe_peer + xs * 512, static_cast<uint32_t>(e_own), fb);
-        }
-        if (threadIdx.x == 128) MLA_TRACE_EVENT(8, g);
-      }
-      ++nitem;
-    }
-  } else {
-    // --------------------------------------------------- softmax + epilogue
-    const int h = 32 * warp + lane;              // head == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const bool head_ok = h < H;
-    const uint32_t sw = static_cast<uint32_t>(h & 7);
-    uint32_t g = 0, nitem = 0;
+    float* red_max = reinterpret_cast<float*>(smem + kOffRed);            // [2][2][128]
+    float* red_l = red_max + 2 * 2 * 128;                                 // [2 halves][128]
     float m_ref = 0.f, l_sum = 0.f;
     auto wait = [&](uint32_t bb, uint32_t par, bool cluster_scope) {
       if (aborted) return;
@@ -537,142 +408,219 @@ __global__ void __launch_bounds__(kThreads, 1)
       r = __shfl_sync(0xffffffffu, r, 0);
       if (!r) aborted = true;
     };
-    for (int it = it0; it < it1; ++it) {
-      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      const int part = items[4 * it + 3];
-      if (!item_ok(p, b, s, e)) continue;
-      const int n = e - s, nt = (n + T - 1) / T;
-      for (int j = 0; j < nt; ++j, ++g) {
-        const uint32_t sb = g & 1, xs = g % kXSlots;
-        const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64;
-        if (warp == 0 && lane == 0 && !aborted) mbar_arrive_expect_tx(bar(bXFull + xs), H * kXRowBytes);
-        wait(bar(bSQuant + sb), (g >> 1) & 1, false);
-        // this CTA's scaled dequantised row; then the S buffer is free for QK(g+2)
-        uint32_t sv[64];
+
+    // -- tile g of this CTA: quantise this warp's 32 partial scores of row h,
+    //    keep the dequantised (scaled) values in TMEM, push the codes to the peer
+    auto send = [&](uint32_t g) {
+      const uint32_t sb = g & 1, xs = g % kXSlots;
+      const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64 + th * TH;
+      wait(bar(bSFull + sb), (g >> 1) & 1, false);
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(6, g);
+      tc_fence_after();
+      uint32_t qw[16];
+      int e_own;
+      {
+        uint32_t r[32];
         if (!aborted) {
-          tc_fence_after();
-          tmem_ld64(tm_s, sv);
+          tmem_ld16(tm_s, *reinterpret_cast<uint32_t(*)[16]>(r));
+          tmem_ld16(tm_s + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) sv[i] = 0;
+          for (int i = 0; i < 32; ++i) r[i] = 0;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && !aborted) mbar_arrive(bar(bSFree + sb));
-        wait(bar(bXFull + xs), (g / kXSlots) & 1, true);
-        if (threadIdx.x == 0) MLA_TRACE_EVENT(9, g);
-        // s = own + peer (log2 units), the same in both CTAs; -inf past the item end
-        uint8_t* xrow = smem + kOffX + xs * kXSlot + h * 128;
-        const int e_peer =
-            (head_ok && !aborted) ? *reinterpret_cast<const int*>(smem + kOffXE + xs * 512 + h * 4) : -100;
-        const float st_p = pow2i(max(e_peer - 14, -126));
-        const float2 st2 = f2_pack(st_p, st_p), dec2 = f2_pack(-kDecBias * st_p, -kDecBias * st_p);
+        // the step is 2^(e-14), e the exponent of max|s| nudged up by 2^-15 so
+        // that no code rounds to 32768
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) mx = max3(mx, fabsf(__uint_as_float(r[i])), fabsf(__uint_as_float(r[i + 1])));
+        mx *= 1.000030517578125f;
+        e_own = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127, -100);
+        const float inv = pow2i(min(14 - e_own, 127)), st = pow2i(max(e_own - 14, -126));
+        const float2 inv2 = f2_pack(inv, inv), enc2 = f2_pack(kEncBias, kEncBias);
+        const float2 st2 = f2_pack(st, st), dec2 = f2_pack(-kEncBias * st, -kEncBias * st);
         const float2 sl2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {            // 8 tokens per 16-byte chunk
-          uint4 pv = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);   // code of 0
-          if (head_ok && !aborted) pv = *reinterpret_cast<const uint4*>(xrow + ((static_cast<uint32_t>(c) ^ sw) << 4));
-          const uint32_t pq[4] = {pv.x, pv.y, pv.z, pv.w};
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o16[16];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int t = 8 * c + 2 * k;
-            const float2 f = f2_pack(__uint_as_float(__byte_perm(pq[k], 0x4B000000u, 0x7610)),
-                                       __uint_as_float(__byte_perm(pq[k], 0x4B000000u, 0x7632)));
-            const float2 sp = f2_mul(f2_fma(f, st2, dec2), sl2);
-            float s0, s1;
-            f2_unpack(f2_add(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), sp), s0, s1);
-            sv[t] = __float_as_uint(s0);
-            sv[t + 1] = __float_as_uint(s1);
+          for (int i = 0; i < 8; ++i) {
+            const float2 t = f2_fma(f2_pack(__uint_as_float(r[16 * c + 2 * i]), __uint_as_float(r[16 * c + 2 * i + 1])),
+                                    inv2, enc2);
+            qw[8 * c + i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x5410);
+            const float2 d = f2_mul(f2_fma(t, st2, dec2), sl2);
+            o16[2 * i] = __float_as_uint(d.x);
+            o16[2 * i + 1] = __float_as_uint(d.y);
           }
+          if (!aborted) tmem_st16(tm_s + 16 * c, o16);
         }
-        const int nvalid = n - j * T;
-        if (nvalid < T) {
-#pragma unroll
-          for (int t = 0; t < T; ++t)
-            if (t >= nvalid) sv[t] = __float_as_uint(-INFINITY);
-        }
-        float mt = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < T; t += 2) mt = max3(mt, __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
-        if (j == 0) {
-          m_ref = mt;
-          l_sum = 0.f;
-        } else {
-          const bool need = mt > m_ref + 8.f;
-          if (__any_sync(0xffffffffu, need)) {
-            // rescale O (this CTA's 256 dims) after the previous PV has landed
-            wait(bar(bPvDone), (g - 1) & 1, false);
-            tc_fence_after();
-            const float alpha = need ? ex2_approx(m_ref - mt) : 1.f;
-            if (need) {
-              m_ref = mt;
-              l_sum *= alpha;
-            }
-            if (!aborted) {
-#pragma unroll 1
-              for (int c = 0; c < 16; ++c) {
-                uint32_t o[16];
-                tmem_ld16(tmem + lane_off + kTmO + 16 * c, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st16(tmem + lane_off + kTmO + 16 * c, o);
-              }
-              tmem_wait_st();
-            }
-            tc_fence_before();
-          }
-        }
-        // P = 2^(s - m_ref) as bf16, written over the peer's rows (K-major, 128-byte swizzle)
-        const float2 nm2 = f2_pack(-m_ref, -m_ref);
-        float2 l2 = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float d0, d1;
-            f2_unpack(f2_add(f2_pack(__uint_as_float(sv[8 * c + 2 * i]), __uint_as_float(sv[8 * c + 2 * i + 1])), nm2),
-                      d0, d1);
-            const float a = ex2_approx(d0), d = ex2_approx(d1);
-            l2 = f2_add(l2, f2_pack(a, d));
-            pk[i] = pack_bf16x2(a, d);
-          }
-          if (!aborted)
-            *reinterpret_cast<uint4*>(xrow + ((static_cast<uint32_t>(c) ^ sw) << 4)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        float l0, l1;
-        f2_unpack(l2, l0, l1);
-        l_sum += l0 + l1;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && !aborted) mbar_arrive(bar(bPFull + xs));
-        if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
+        if (!aborted) tmem_wait_st();
       }
-      // ------------------------------------------------------------ epilogue
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(bar(bSQuant + sb));
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(13, g);
+      // push into the peer's slot xs once the peer's PV(g - kXSlots) has read it
+      if (g >= kXSlots) wait(bar(bXFree + xs), ((g / kXSlots) - 1) & 1, true);
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(14, g);
+      if (!aborted) {
+        const uint32_t fb = xfull_peer + 8u * xs;
+        const uint32_t dst = xrow_peer + xs * kXSlot;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t c = static_cast<uint32_t>(4 * th + k);
+          st_async_v4(dst + ((c ^ sw) << 4), qw[4 * k], qw[4 * k + 1], qw[4 * k + 2], qw[4 * k + 3], fb);
+        }
+        st_async_b32(xe_peer + xs * kXeSlot, static_cast<uint32_t>(e_own), fb);
+      }
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(8, g);
+    };
+
+    // -- tile g (j-th of an item of n tokens): add the peer's rows, softmax, P
+    auto softmax = [&](uint32_t g, int j, int n) {
+      const uint32_t sb = g & 1, xs = g % kXSlots;
+      const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64 + th * TH;
+      // arm slot xs for the peer's rows of tile g: done here, by the warp that
+      // also waits on it, so the arm for tile g + kXSlots cannot come before
+      // this tile's phase has completed (the peer's bytes may land either side)
+      if (warp == 0 && lane == 0 && !aborted) mbar_arrive_expect_tx(bar(bXFull + xs), kXBytes);
+      wait(bar(bSQuant + sb), (g >> 1) & 1, false);
+      uint32_t sv[32];
+      if (!aborted) {
+        tc_fence_after();
+        tmem_ld16(tm_s, *reinterpret_cast<uint32_t(*)[16]>(sv));
+        tmem_ld16(tm_s + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[i] = 0;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(bar(bSFree + sb));
+      wait(bar(bXFull + xs), (g / kXSlots) & 1, true);
+      if (threadIdx.x == 0) MLA_TRACE_EVENT(9, g);
+      // s = own + peer (log2 units), the same in both CTAs; -inf past the item end
+      uint8_t* xrow = smem + kOffX + xs * kXSlot + h * 128;
+      const int e_peer = !aborted ? *reinterpret_cast<const int*>(smem + kOffXE + xs * kXeSlot + (th * 128 + h) * 4)
+                                  : -100;
+      const float st_p = pow2i(max(e_peer - 14, -126));
+      const float2 st2 = f2_pack(st_p, st_p), dec2 = f2_pack(-kDecBias * st_p, -kDecBias * st_p);
+      const float2 sl2 = f2_pack(p.scale_log2, p.scale_log2);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {            // 8 tokens per 16-byte chunk
+        const uint32_t c = static_cast<uint32_t>(4 * th + k);
+        uint4 pv = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);   // code of 0
+        if (!aborted) pv = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) << 4));
+        const uint32_t pq[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = 8 * k + 2 * i;
+          const float2 f = f2_pack(__uint_as_float(__byte_perm(pq[i], 0x4B000000u, 0x7610)),
+                                   __uint_as_float(__byte_perm(pq[i], 0x4B000000u, 0x7632)));
+          const float2 sp = f2_mul(f2_fma(f, st2, dec2), sl2);
+          const float2 s2 = f2_add(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), sp);
+          sv[t] = __float_as_uint(s2.x);
+          sv[t + 1] = __float_as_uint(s2.y);
+        }
+      }
+      const int nvalid = n - j * T - th * TH;
+      if (nvalid < TH) {
+#pragma unroll
+        for (int t = 0; t < TH; ++t)
+          if (t >= nvalid) sv[t] = __float_as_uint(-INFINITY);
+      }
+      float mh = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < TH; t += 2) mh = max3(mh, __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
+      // row maximum over the tile: combine with the partner warp (other token half)
+      float* rm = red_max + (g & 1) * 256;
+      rm[th * 128 + h] = mh;
+      named_bar_sync(1 + q, 64);
+      const float mt = fmaxf(rm[h], rm[128 + h]);
+      if (j == 0) {
+        m_ref = mt;
+        l_sum = 0.f;
+      } else {
+        const bool need = mt > m_ref + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale this warp's half of O (128 columns) after the previous PV has
+          // landed.  PV(g-3) is complete here (the peer sent tile g only after it
+          // had freed slot g mod 3), so the buffer of tile g-1 cannot be a lap behind.
+          wait(bar(bPvDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, false);
+          tc_fence_after();
+          const float alpha = need ? ex2_approx(m_ref - mt) : 1.f;
+          if (need) {
+            m_ref = mt;
+            l_sum *= alpha;
+          }
+          if (!aborted) {
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t o[16];
+              const uint32_t ta = tmem + lane_off + kTmO + 128 * th + 16 * c;
+              tmem_ld16(ta, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(ta, o);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+        }
+      }
+      // P = 2^(s - m_ref) as bf16, written over the peer's rows (K-major, 128-byte swizzle)
+      const float2 nm2 = f2_pack(-m_ref, -m_ref);
+      float2 l2 = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 d = f2_add(f2_pack(__uint_as_float(sv[8 * k + 2 * i]), __uint_as_float(sv[8 * k + 2 * i + 1])), nm2);
+          const float a = ex2_approx(d.x), e2 = ex2_approx(d.y);
+          l2 = f2_add(l2, f2_pack(a, e2));
+          pk[i] = pack_bf16x2(a, e2);
+        }
+        const uint32_t c = static_cast<uint32_t>(4 * th + k);
+        if (!aborted) *reinterpret_cast<uint4*>(xrow + ((c ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      l_sum += l2.x + l2.y;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(bar(bPFull + xs));
+      if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
+    };
+
+    // -- after an item's last tile: 1/l, O (this warp's 128 columns) and lse
+    auto epilogue = [&](int b, int part, uint32_t nitem) {
       if (threadIdx.x == 0 && nitem < 24) MLA_TRACE_RAW(15, 8 + 2 * nitem, clock64());
+      // the row sum over the tile halves, added in the same order by both warps
+      red_l[th * 128 + h] = l_sum;
+      named_bar_sync(1 + q, 64);
+      const float lsum = red_l[h] + red_l[128 + h];
       wait(bar(bOFull), nitem & 1, false);
       tc_fence_after();
       if (!aborted) {
-        const float inv = 1.f / l_sum;
+        const float inv = 1.f / lsum;
         float* dst_f = nullptr;
         __nv_bfloat16* dst_h = nullptr;
+        const size_t col0 = 256 * static_cast<size_t>(cta) + 128 * th;
         if (part < 0) {
-          const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + 256 * cta;
+          const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + col0;
           if (p.out_bf16) dst_h = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
           else dst_f = reinterpret_cast<float*>(p.out) + o;
         } else {
-          dst_f = p.part_o + (static_cast<size_t>(part) * H + h) * kLatent + 256 * cta;
+          dst_f = p.part_o + (static_cast<size_t>(part) * H + h) * kLatent + col0;
         }
 #pragma unroll 1
-        for (int cb = 0; cb < 8; ++cb) {          // 32 columns per TMEM round trip, 32-byte stores
+        for (int cb = 0; cb < 4; ++cb) {          // 32 columns per TMEM round trip, 32-byte stores
           uint32_t o[32];
           {
             uint32_t a[16], c[16];
-            tmem_ld16(tmem + lane_off + kTmO + 32 * cb, a);
-            tmem_ld16(tmem + lane_off + kTmO + 32 * cb + 16, c);
+            tmem_ld16(tmem + lane_off + kTmO + 128 * th + 32 * cb, a);
+            tmem_ld16(tmem + lane_off + kTmO + 128 * th + 32 * cb + 16, c);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) { o[i] = a[i]; o[16 + i] = c[i]; }
@@ -698,8 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (cta == 0 && head_ok) {
-          const float l = (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+        if (cta == 0 && th == 0 && head_ok) {
+          const float l = (m_ref + __log2f(lsum)) * 0.69314718055994531f;
           if (part < 0) { if (p.lse) p.lse[static_cast<size_t>(b) * H + h] = l; }
           else p.part_lse[static_cast<size_t>(part) * H + h] = l;
         }
@@ -708,6 +656,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0 && !aborted) mbar_arrive(bar(bOEmpty));
       if (threadIdx.x == 0 && nitem < 24) MLA_TRACE_RAW(15, 9 + 2 * nitem, clock64());
+    };
+
+    uint32_t g = 0, nitem = 0;
+    for (int it = it0; it < it1; ++it) {
+      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+      const int part = items[4 * it + 3];
+      if (!item_ok(p, nnz, b, s, e)) continue;
+      const int n = e - s, nt = (n + T - 1) / T;
+      if (is_sender) {
+        // -- query latent half of this item into TMEM (after the previous item's last QK)
+        if (nitem > 0) wait(bar(bQEmpty), (nitem - 1) & 1, false);
+        tc_fence_after();
+        if (!aborted) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(b) * H + h) * kLatent +
+                                                            256 * cta);
+#pragma unroll
+          for (int c = 4 * th; c < 4 * th + 4; ++c) {   // this warp's 4 x 16 columns = 128 bf16
+            uint32_t r[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 v = head_ok ? __ldg(src + 4 * c + k) : make_uint4(0, 0, 0, 0);
+              r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
+            }
+            tmem_st16(tmem + lane_off + kTmQ + 16 * c, r);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !aborted) mbar_arrive(bar(bQFull));
+        for (int j = 0; j < nt; ++j, ++g) send(g);
+      } else {
+        for (int j = 0; j < nt; ++j, ++g) softmax(g, j, n);
+        epilogue(b, part, nitem);
+      }
       ++nitem;
     }
   }
