@@ -240,26 +240,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pw = warp - kProducerWarp0;
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
     const uint64_t pol = l2_policy_evict_first();
+    // The slot numbers of the next tile are loaded while this tile waits for
+    // ring space and issues its gathers, so their latency is hidden.
+    int it = it0, s = 0, n = 0;
+    auto next_item = [&]() {                     // first usable item from `it` on
+      for (; it < it1; ++it) {
+        const int b = items[4 * it], s0 = items[4 * it + 1], e = items[4 * it + 2];
+        if (item_ok(p, nnz, b, s0, e)) {
+          if (pw == 0 && lane == 0 && !item_in_request(p, b, s0, e)) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+          s = s0;
+          n = e - s0;
+          return;
+        }
+        if (lane == 0 && pw == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+      }
+    };
+    auto load_slots = [&](int t0, int (&v)[4]) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = __ldg(p.kv_indices + s + min(t0 + 4 * (lane & 15) + k, n - 1));
+    };
+    next_item();
+    int t0 = 0;
+    int vn[4] = {0, 0, 0, 0};
+    if (it < it1) load_slots(0, vn);
     uint32_t g = 0;
     bool ok = true;
-    for (int it = it0; it < it1 && ok; ++it) {
-      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      if (!item_ok(p, nnz, b, s, e)) {
-        if (lane == 0 && pw == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
-        continue;
-      }
-      const bool in_req = pw != 0 || item_in_request(p, b, s, e);
-      const int n = e - s;
-      for (int t0 = 0; t0 < n && ok; t0 += T, ++g) {
-        int v[4];
-        bool oob = false;
+    while (it < it1 && ok) {
+      int v[4];
+      bool oob = false;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[k] = __ldg(p.kv_indices + s + min(t0 + 4 * (lane & 15) + k, n - 1));
-          if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
-        }
-        if (oob && pw == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
-        if (lane == 0 && pw == 0) MLA_TRACE_EVENT(0, g);
+      for (int k = 0; k < 4; ++k) {
+        v[k] = vn[k];
+        if (v[k] < 0 || static_cast<long long>(v[k]) >= p.num_slots) { oob = true; v[k] = 0; }
+      }
+      if (oob && pw == 0) record_status(p.status, MLA_ERR_INDEX_OOB);
+      // advance the cursor and prefetch the next tile's slot numbers
+      t0 += T;
+      if (t0 >= n) {
+        ++it;
+        next_item();
+        t0 = 0;
+      }
+      if (it < it1) load_slots(t0, vn);
+      if (lane == 0 && pw == 0) MLA_TRACE_EVENT(0, g);
+      {
         const bool rope = pw == 4;
         const uint32_t nslots = rope ? kRopeSlots : kLatBlocks;
         const uint32_t slot = g % nslots, use = g / nslots;
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
         }
       }
-      if (!in_req && lane == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+      ++g;
     }
     named_bar_sync(9, 32 * kProducers);
     if (pw == 0 && lane < kLatBlocks + kRopeSlots) {
