@@ -37,9 +37,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] array, box {box_cols, box_rows},
-// 128-byte swizzle.
+// 128-byte swizzle (64-byte for boxes 64 bytes wide).
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              uint32_t box_rows) {
+              uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -47,7 +47,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -168,15 +168,19 @@ int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev, const v
 
   CUtensorMap tm_kv, tm_qn, tm_qr;
   const uint64_t qrows = static_cast<uint64_t>(B) * H;
-  if (!make_map(&tm_kv, kv_cache, kRow, static_cast<uint64_t>(num_slots), 64, 1) ||
-      !make_map(&tm_qr, q_rope, kRope, qrows, 64, static_cast<uint32_t>(H)))
-    return MLA_ERR_CUDA;
+  if (!make_map(&tm_kv, kv_cache, kRow, static_cast<uint64_t>(num_slots), 64, 1)) return MLA_ERR_CUDA;
   if (plan_host[kHVariant] == kVariantSwab) {
-    if (!make_map(&tm_qn, q_nope, kLatent, qrows, 64, static_cast<uint32_t>(H))) return MLA_ERR_CUDA;
+    if (!make_map(&tm_qr, q_rope, kRope, qrows, 64, static_cast<uint32_t>(H)) ||
+        !make_map(&tm_qn, q_nope, kLatent, qrows, 64, static_cast<uint32_t>(H)))
+      return MLA_ERR_CUDA;
     return launch_swab(H, tm_kv, tm_qn, tm_qr, p, plan_host[kHWorkers], st);
   }
-  if (!make_map(&tm_qn, q_nope, kLatent, qrows, 64, 1)) return MLA_ERR_CUDA;
-  return launch_pair(H, tm_kv, tm_qn, tm_qr, p, plan_host[kHWorkers], st);
+  // the pair kernel's CTAs each take half of the rope dims: 64-byte rows
+  CUtensorMap tm_kr;
+  if (!make_map(&tm_kr, kv_cache, kRow, static_cast<uint64_t>(num_slots), 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&tm_qr, q_rope, kRope, qrows, 32, static_cast<uint32_t>(H), CU_TENSOR_MAP_SWIZZLE_64B))
+    return MLA_ERR_CUDA;
+  return launch_pair(H, tm_kv, tm_kr, tm_qr, p, plan_host[kHWorkers], st);
 }
 
 int mla_decode_merge(const int32_t* plan_host, const int32_t* plan_dev, void* out, int32_t out_dtype,

@@ -329,14 +329,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading-
 // and stride-dimension byte offsets (all >> 4), version 1 at bits 46-47,
-// layout type at bits 61-63 (2 = 128-byte swizzle).
+// layout type at bits 61-63 (2 = 128-byte swizzle, 4 = 64-byte swizzle).
 //   K-major, 128B swizzle: rows of 128 B (64 bf16 along K), 8-row atoms of
 //     1024 B; SBO = byte distance between consecutive 8-row groups; LBO unused.
 //     The K offset inside a 128-B row is added to the start address.
 //   MN-major, 128B swizzle: rows of 128 B (64 bf16 along M or N), one row per
 //     K index, 8-row atoms; LBO = byte distance between consecutive 64-wide
 //     M/N chunks; SBO = byte distance between consecutive 8-row K groups.
+//   K-major, 64B swizzle: the same with rows of 64 B (32 bf16 along K) and
+//     8-row atoms of 512 B.
 constexpr uint32_t kLayoutSw128 = 2;
+constexpr uint32_t kLayoutSw64 = 4;
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
                                           uint32_t layout = kLayoutSw128) {

@@ -75,19 +75,23 @@ constexpr int kRowWarps = 8;                 // softmax warps 0-7 and sender war
 constexpr int kProducers = 5;                // latent atoms 0-3 and the rope
 constexpr int kSendWarp0 = 8, kMmaWarp = 16, kLoaderWarp = 17, kProducerWarp0 = 18;
 constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
-constexpr int kLatBlocks = 4;                // ring of latent blocks (every latent producer fills every block)
-constexpr int kRopeSlots = 3;
-constexpr int kXSlots = 3;                   // exchange slots
-constexpr int kLead = 3;                     // a producer issues tile g once tile g - kLead has landed
+// A latent block is held from its gathers until its PV, the whole life of a
+// tile in the pipeline, so the ring is as deep as shared memory allows.
+constexpr int kLatBlocks = 5;                // ring of latent blocks (every latent producer fills every block)
+constexpr int kRopeSlots = 4;
+constexpr int kXSlots = 2;                   // exchange slots
+constexpr int kLead = 4;                     // a producer issues tile g once tile g - kLead has landed
 constexpr int kAtom = T * 128;               // 8 KB: 64 tokens x 64 dims
 constexpr int kLatBlock = 4 * kAtom;         // 32 KB: 64 tokens x 256 dims
+constexpr int kRopeAtom = T * 64;            // 4 KB: 64 tokens x this CTA's 32 rope dims (64-byte swizzle)
+constexpr int kQRBytes = 128 * 64;           // rope query: 128 rows x this CTA's 32 rope dims
 constexpr int kXSlot = 128 * 128;            // 128 rows x 128 B (64 int16 scores, then 64 bf16 P)
 constexpr int kXeSlot = 2 * 128 * 4;         // [2 token halves][128 rows] int32 exponents
 constexpr int kXBytes = kXSlot + kXeSlot;    // bytes the peer sends per tile
 constexpr int kOffLat = 0;
 constexpr int kOffRope = kOffLat + kLatBlocks * kLatBlock;
-constexpr int kOffQR = kOffRope + kRopeSlots * kAtom;   // rope query: 128 rows x 128 B (K-major SW128)
-constexpr int kOffX = kOffQR + 128 * 128;
+constexpr int kOffQR = kOffRope + kRopeSlots * kRopeAtom;   // rope query (K-major SW64)
+constexpr int kOffX = kOffQR + kQRBytes;
 constexpr int kOffXE = kOffX + kXSlots * kXSlot;        // [kXSlots] exponent blocks from the peer
 constexpr int kOffRed = kOffXE + kXSlots * kXeSlot;     // [2 bufs][2 halves][128] row maxima, [2][128] row sums
 constexpr int kOffBar = kOffRed + (2 * 2 * 128 + 2 * 128) * 4;
@@ -159,7 +163,8 @@ constexpr float kEncBias = 12615680.0f;      // 1.5 * 2^23 + 32768
 constexpr float kDecBias = 8421376.0f;       // 2^23 + 32768
 
 __global__ void __launch_bounds__(kThreads, 1)
-    pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qr,
+    pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kr,
+                const __grid_constant__ CUtensorMap tm_qr,
                 const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   // rope-query rows >= H stay zero (the TMA box has H rows)
-  for (int i = threadIdx.x; i < (128 * 128) / 16; i += blockDim.x)
+  for (int i = threadIdx.x; i < kQRBytes / 16; i += blockDim.x)
     *reinterpret_cast<uint4*>(smem + kOffQR + 16 * i) = make_uint4(0, 0, 0, 0);
   if (warp == kLoaderWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -239,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sets MLA_ERR_INDEX_OOB, the ragged tail repeats the last valid slot.
     const int pw = warp - kProducerWarp0;
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
+    if (lane == 0 && pw == 4) tma_prefetch_desc(&tm_kr);
     const uint64_t pol = l2_policy_evict_first();
     // The slot numbers of the next tile are loaded while this tile waits for
     // ring space and issues its gathers, so their latency is hidden.
@@ -297,11 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
         if (!e_ok) { ok = false; break; }
         if (rope) {
-          if (lane == 0) mbar_arrive_expect_tx(full, kAtom);
+          if (lane == 0) mbar_arrive_expect_tx(full, kRopeAtom);
           if (lane == 0) MLA_TRACE_EVENT(11, g);
           __syncwarp();
           if (lane < 16)
-            tma_gather4(base + kOffRope + slot * kAtom + lane * 512, &tm_kv, 512, v[0], v[1], v[2], v[3], full, pol);
+            tma_gather4(base + kOffRope + slot * kRopeAtom + lane * 256, &tm_kr, 512 + 32 * static_cast<int>(cta),
+                        v[0], v[1], v[2], v[3], full, pol);
           if (lane == 0) atomicMax(last_armed + kLatBlocks + slot, static_cast<int>(use));
         } else {
           if (lane == 0 && pw == 0) mbar_arrive_expect_tx(full, kLatBlock);
@@ -329,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_qr);
       const uint64_t dk = sdesc(base + kOffLat, 16, 1024);         // latent block 0, K-major (B of QK)
-      const uint64_t dr = sdesc(base + kOffRope, 16, 1024);        // rope slot 0 (B of QK)
-      const uint64_t dqr = sdesc(base + kOffQR, 16, 1024);         // rope query (A of QK)
+      const uint64_t dr = sdesc(base + kOffRope, 16, 512, kLayoutSw64);   // rope slot 0 (B of QK)
+      const uint64_t dqr = sdesc(base + kOffQR, 16, 512, kLayoutSw64);    // rope query (A of QK)
       auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
       uint32_t g = 0, nitem = 0;
       bool ok = true;
@@ -340,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = (e - s + T - 1) / T;
         // the rope query of this item replaces the previous one once its last QK is done
         if (nitem > 0 && !mbar_wait(bar(bQEmpty), (nitem - 1) & 1, wc)) break;
-        mbar_arrive_expect_tx(bar(bQFull), H * 128);
-        tma_load_2d(base + kOffQR, &tm_qr, 0, b * H, bar(bQFull));
+        mbar_arrive_expect_tx(bar(bQFull), H * 64);
+        tma_load_2d(base + kOffQR, &tm_qr, 32 * static_cast<int>(cta), b * H, bar(bQFull));
         if (!mbar_wait(bar(bQFull), nitem & 1, wc)) break;     // + the latent half in TMEM
         for (int j = 0; j < nt; ++j, ++g) {
           const uint32_t d_s = tmem + kTmS + (g & 1) * 64;
@@ -358,12 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(bRopeFull + rs), (g / kRopeSlots) & 1, wc)) { ok = false; break; }
           tc_fence_after();
           MLA_TRACE_EVENT(12, g);
-          const uint64_t br = D(dr, rs * kAtom);
+          const uint64_t br = D(dr, rs * kRopeAtom);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {        // this CTA's half of the rope dims
-            const uint32_t off = (2 * cta + kk) * 32;
-            umma_ss(d_s, D(dqr, off), D(br, off), kIdescQK, 1u);
-          }
+          for (int kk = 0; kk < 2; ++kk)          // this CTA's half of the rope dims: 2 K-steps of 16
+            umma_ss(d_s, D(dqr, kk * 32), D(br, kk * 32), kIdescQK, 1u);
           umma_commit(bar(bRopeEmpty + rs));
           umma_commit(bar(bSFull + (g & 1)));
           if (j == nt - 1) umma_commit(bar(bQEmpty));
@@ -739,9 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace pair
 
-int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap& tm_qr,
+int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kv_rope, const CUtensorMap& tm_qr,
                 const DecodeParams& p, int workers, cudaStream_t stream) {
-  (void)tm_qn;
   if (heads < 48 || heads > 128 || heads % 16 != 0) return MLA_ERR_UNSUPPORTED;
   static bool attr_done = false;
   if (!attr_done) {
@@ -762,7 +766,7 @@ int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, c
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pair::pair_kernel, tm_kv, tm_qr, p) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, pair::pair_kernel, tm_kv, tm_kv_rope, tm_qr, p) != cudaSuccess) return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
