@@ -1,6 +1,7 @@
 // The C ABI of libmla_decode.so (declared in include/mla_decode.h): argument
 // checks, the host plan, TMA descriptor encoding and kernel dispatch.  Nothing
 // here allocates device memory or synchronises except mla_check_errors.
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -200,7 +201,10 @@ int mla_decode_merge(const int32_t* plan_host, const int32_t* plan_dev, void* ou
   m.out = out;
   m.out_bf16 = out_dtype;
   m.lse = lse;
-  return launch_merge(m, m.n_entries, reinterpret_cast<cudaStream_t>(stream));
+  const int32_t* ml = plan_host + plan_merge_off(plan_host);
+  int max_pieces = 0;
+  for (int i = 0; i < m.n_entries; ++i) max_pieces = std::max(max_pieces, ml[3 * i + 2] - ml[3 * i + 1]);
+  return launch_merge(m, m.n_entries, max_pieces, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_decode_run(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope,
@@ -233,7 +237,7 @@ int mla_merge_states(const float* v_partial, const float* s_partial, const int32
   m.out = out;
   m.out_bf16 = out_dtype;
   m.lse = lse;
-  return launch_merge(m, batch, reinterpret_cast<cudaStream_t>(stream));
+  return launch_merge(m, batch, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_check_errors(void* workspace, void* stream) {

@@ -16,7 +16,8 @@ int launch_swab(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_qn,
 int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kv_rope,
                 const CUtensorMap& tm_qr, const DecodeParams& p, int workers, cudaStream_t stream);
 
-// LSE merge of partial states; one block per (entry, head).
-int launch_merge(const MergeParams& p, int entries, cudaStream_t stream);
+// LSE merge of partial states; one block per (entry, head).  max_pieces: the
+// most partials an entry has (sizes the block), or 0 when unknown.
+int launch_merge(const MergeParams& p, int entries, int max_pieces, cudaStream_t stream);
 
 }  // namespace mla

@@ -9,10 +9,13 @@
 // Partials with lse_i = -inf weigh nothing; no live partial gives out = 0,
 // lse = -inf (an empty request).
 //
-// One 128-thread block per (entry, head).  The partial LSEs are loaded in
-// parallel (thread i takes partial i) and their weights go through shared
-// memory; then each thread owns four latent dims and streams the partial rows
-// as float4, four partials in flight, so a merge costs two memory round trips.
+// One block per (entry, head) of G groups of 128 threads (G = 1, 2 or 4, from
+// the most pieces an entry has).  The partial LSEs are loaded in parallel and
+// their weights go through shared memory; then thread t of group k owns latent
+// dims 4t..4t+3 and streams the partials k, k+G, k+2G, ... as float4, four at a
+// time, so 4G partial rows per dim are in flight and a request cut into tens of
+// pieces costs a few memory round trips.  The groups' sums are added in a
+// fixed order.
 // The kernel is launched as a programmatic dependent of the decode kernel:
 // its blocks are scheduled while the decode kernel drains and wait
 // (griddepcontrol.wait) until its partial states are complete and visible.
@@ -23,13 +26,18 @@
 
 namespace mla {
 
-constexpr int kMergeThreads = 128;
+constexpr int kMergeGroups = 4;                      // at most
+constexpr int kMergeThreads = 128 * kMergeGroups;
 constexpr int kMergeChunk = 1024;   // partials whose weights one pass keeps in shared memory
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
   __shared__ float s_w[kMergeChunk];
-  __shared__ float s_red[4];
+  __shared__ float s_red[kMergeThreads / 32];
+  __shared__ float4 s_acc[kMergeGroups - 1][128];
+  __shared__ float s_wsum[kMergeGroups - 1];
   const int e = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int G = static_cast<int>(blockDim.x >> 7), grp = tid >> 7, t = tid & 127;
+  const int nthreads = static_cast<int>(blockDim.x);
   int b, p0, p1;
   if (p.list) {
     b = p.list[3 * e];
@@ -48,7 +56,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     // this chunk's partials: LSEs in parallel, then the chunk maximum
     const int nc = min(kMergeChunk, p1 - c0);
     float m = -INFINITY;
-    for (int i = tid; i < nc; i += kMergeThreads) {
+    for (int i = tid; i < nc; i += nthreads) {
       const float l = __ldcg(p.part_lse + static_cast<size_t>(c0 + i) * H + h);
       s_w[i] = l;
       m = fmaxf(m, l);
@@ -57,7 +65,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     if ((tid & 31) == 0) s_red[tid >> 5] = m;
     __syncthreads();
-    const float mc = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+    float mc = s_red[0];
+    for (int w = 1; w < nthreads / 32; ++w) mc = fmaxf(mc, s_red[w]);
     // fold the chunk into the running state (one chunk unless a request has
     // more than kMergeChunk partials)
     const float mn = fmaxf(M, mc);
@@ -67,21 +76,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
       acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
     }
     M = mn;
-    for (int i = tid; i < nc; i += kMergeThreads) {
+    for (int i = tid; i < nc; i += nthreads) {
       const float l = s_w[i];
       s_w[i] = (l == -INFINITY || M == -INFINITY) ? 0.f : expf(l - M);
     }
     __syncthreads();
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(c0) * H + h) * kLatent) + tid;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(c0) * H + h) * kLatent) + t;
     const size_t stride = static_cast<size_t>(H) * kLatent / 4;   // float4 per partial
-    int i = 0;
-    for (; i + 4 <= nc; i += 4) {
+    int i = grp;
+    for (; i + 3 * G < nc; i += 4 * G) {
       float4 v[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = __ldcg(src + (i + q) * stride);
+      for (int q = 0; q < 4; ++q) v[q] = __ldcg(src + (i + q * G) * stride);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float w = s_w[i + q];
+        const float w = s_w[i + q * G];
         wsum += w;
         acc.x = fmaf(w, v[q].x, acc.x);
         acc.y = fmaf(w, v[q].y, acc.y);
@@ -89,7 +98,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
         acc.w = fmaf(w, v[q].w, acc.w);
       }
     }
-    for (; i < nc; ++i) {
+    for (; i < nc; i += G) {
       const float4 v = __ldcg(src + i * stride);
       const float w = s_w[i];
       wsum += w;
@@ -100,8 +109,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     }
     __syncthreads();   // s_w and s_red are reused by the next chunk
   }
+  // add the groups' sums in a fixed order
+  if (grp > 0) {
+    s_acc[grp - 1][t] = acc;
+    if (t == 0) s_wsum[grp - 1] = wsum;
+  }
+  __syncthreads();
+  if (grp != 0) return;
+  for (int k = 0; k < G - 1; ++k) {
+    const float4 a = s_acc[k][t];
+    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+    wsum += s_wsum[k];
+  }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + 4 * tid;
+  const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + 4 * t;
   if (p.out_bf16) {
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
     dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
@@ -110,14 +131,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
-  if (tid == 0 && p.lse) p.lse[static_cast<size_t>(b) * H + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  if (t == 0 && p.lse) p.lse[static_cast<size_t>(b) * H + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
-int launch_merge(const MergeParams& p, int entries, cudaStream_t stream) {
+int launch_merge(const MergeParams& p, int entries, int max_pieces, cudaStream_t stream) {
   if (entries <= 0) return MLA_OK;
+  const int groups = max_pieces >= 16 ? 4 : max_pieces >= 8 ? 2 : 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(entries, p.heads);
-  cfg.blockDim = dim3(kMergeThreads);
+  cfg.blockDim = dim3(128 * groups);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
