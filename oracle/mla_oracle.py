@@ -31,7 +31,8 @@ Sources, by page and section:
   * "MLA and torch.compile: v0.3's two sources", section "MLA: starting from a
     439-line commit": kv_b_proj split into w_kc and w_vc; decode multiplies
     q_nope by w_kc before attention and the latent output by w_vc after it --
-    ``absorb_weights``, ``absorbed_attention``, ``decompressed_attention``.
+    ``absorb_weights``, ``absorb_query``, ``project_output``,
+    ``absorbed_attention``, ``decompressed_attention``.
   * same page, "Exercises", exercise 1: multiply-accumulate counts of the
     absorbing and decompressing paths -- ``mac_counts``.
 
@@ -174,10 +175,29 @@ def absorbed_attention(q_nope_heads, q_rope_heads, latents, k_rope, kv_b_proj, s
     output is moved to the value space by w_vc.  Returns [H, v].
     """
     w_kc, w_vc = absorb_weights(kv_b_proj, qk_nope_head_dim, v_head_dim)
-    q_lat = np.einsum("hn,hnr->hr", q_nope_heads, w_kc)              # bmm(q_nope, w_kc)
+    q_lat = absorb_query(q_nope_heads[None], w_kc)[0]                # bmm(q_nope, w_kc)
     rows = np.concatenate([latents, k_rope], axis=1)
     o_lat, _ = partial_state(q_lat, q_rope_heads, rows, sm_scale)
-    return np.einsum("hr,hrv->hv", o_lat, w_vc)                      # bmm(attn, w_vc)
+    return project_output(o_lat[None], w_vc)[0]                      # bmm(attn, w_vc)
+
+
+def absorb_query(q_nope: np.ndarray, w_kc: np.ndarray) -> np.ndarray:
+    """q_nope [B, H, nope] times each head's w_kc [H, nope, 512] -> [B, H, 512].
+
+    The query-side bmm of the absorbing path ("MLA and torch.compile", section
+    "MLA: starting from a 439-line commit": q_nope is multiplied by w_kc before
+    attention).  Inputs as float64 (or bf16 bits widened by the caller).
+    """
+    return np.einsum("bhn,hnr->bhr", np.asarray(q_nope, np.float64), np.asarray(w_kc, np.float64))
+
+
+def project_output(o_lat: np.ndarray, w_vc: np.ndarray) -> np.ndarray:
+    """o_lat [B, H, 512] times each head's w_vc [H, 512, v] -> [B, H, v].
+
+    The output-side bmm of the absorbing path (same section: the latent output
+    of the attention is multiplied by w_vc).
+    """
+    return np.einsum("bhr,hrv->bhv", np.asarray(o_lat, np.float64), np.asarray(w_vc, np.float64))
 
 
 def decompressed_attention(q_nope_heads, q_rope_heads, latents, k_rope, kv_b_proj, sm_scale,

@@ -50,6 +50,29 @@ def test_absorption_identity_matches_decompressed_mha(H, L):
     np.testing.assert_allclose(a, d, rtol=1e-11, atol=1e-12)
 
 
+def test_absorb_query_and_project_output_are_per_head_products():
+    # each head's rows are multiplied by that head's own matrix only: a head
+    # or operand mix-up changes a brute-force dot product here
+    rng = np.random.default_rng(11)
+    B, H, n, r = 2, 3, 4, 5
+    q = rng.standard_normal((B, H, n))
+    w = rng.standard_normal((H, n, r))
+    a = O.absorb_query(q, w)
+    assert a.shape == (B, H, r)
+    for b in range(B):
+        for h in range(H):
+            for j in range(r):
+                assert abs(a[b, h, j] - sum(q[b, h, i] * w[h, i, j] for i in range(n))) < 1e-12
+    o = rng.standard_normal((B, H, r))
+    wv = rng.standard_normal((H, r, n))
+    pr = O.project_output(o, wv)
+    assert pr.shape == (B, H, n)
+    for b in range(B):
+        for h in range(H):
+            for j in range(n):
+                assert abs(pr[b, h, j] - sum(o[b, h, i] * wv[h, i, j] for i in range(r))) < 1e-12
+
+
 def test_absorb_weights_layout():
     # kv_b_proj rows are [head][nope + v]; w_kc must pick the first nope rows
     # of each head's block, w_vc the remaining v rows, transposed.
