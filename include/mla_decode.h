@@ -191,6 +191,41 @@ int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* plan_dev,
                            float sm_scale, void* out, int32_t out_dtype, float* lse,
                            void* stream);
 
+/* mla_absorb_query -- asynchronous on `stream`.
+ *
+ * The query side of the absorbing path ("MLA and torch.compile: v0.3's two
+ * sources", section "MLA: starting from a 439-line commit": q_nope is
+ * multiplied by w_kc before attention): for every request b and head h,
+ *   q_nope[b, h, :] = q_pre[b, h, 0:128] . w_kc[h]        (fp32 sums, bf16 result)
+ * which is the q_nope that mla_decode_run takes.
+ *
+ *   q_pre     device bf16 [batch, num_heads, nope_dim], nope_dim = 128.
+ *   w_kc      device bf16 [num_heads, nope_dim, 512], row-major per head.
+ *   q_nope    device bf16 [batch, num_heads, 512] (written).
+ *   workspace NULL, or a decode workspace whose status word records a timeout
+ *             (read with mla_check_errors).
+ * Errors: MLA_ERR_UNSUPPORTED for nope_dim != 128; MLA_ERR_INVALID_ARG for
+ * null or non-16-byte-aligned pointers, batch < 0 or num_heads < 1; nothing
+ * is launched then.  batch == 0 launches nothing. */
+int mla_absorb_query(const void* q_pre, const void* w_kc, void* q_nope, int32_t batch, int32_t num_heads,
+                     int32_t nope_dim, void* workspace, void* stream);
+
+/* mla_project_output -- asynchronous on `stream`.
+ *
+ * The output side of the absorbing path (same section: the attention's
+ * latent output is multiplied by w_vc): for every request b and head h,
+ *   out[b, h, :] = o_lat[b, h, 0:512] . w_vc[h]            (fp32 sums)
+ *
+ *   o_lat     device bf16 [batch, num_heads, 512] (mla_decode_run with
+ *             out_dtype 1).
+ *   w_vc      device bf16 [num_heads, 512, v_dim], row-major per head, v_dim = 128.
+ *   out       device [batch, num_heads, v_dim], fp32 (out_dtype 0) or bf16 (1).
+ *   workspace as for mla_absorb_query.
+ * Errors as for mla_absorb_query (v_dim != 128 or a bad out_dtype give
+ * MLA_ERR_UNSUPPORTED). */
+int mla_project_output(const void* o_lat, const void* w_vc, void* out, int32_t out_dtype, int32_t batch,
+                       int32_t num_heads, int32_t v_dim, void* workspace, void* stream);
+
 /* mla_check_errors -- synchronises `stream`, reads the workspace status word,
  * clears it, and returns it (MLA_OK when the kernels found nothing wrong), or
  * MLA_ERR_CUDA if the stream reports a CUDA error. */

@@ -23,7 +23,7 @@ STATUS_NAMES = {
 }
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
-           "mla_decode_run_noalloc")
+           "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -55,6 +55,11 @@ _lib.mla_decode_run_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64,
                                         ctypes.c_int32, _vp, _vp]
 _lib.mla_check_errors.restype = ctypes.c_int
 _lib.mla_check_errors.argtypes = [_vp, _vp]
+_lib.mla_absorb_query.restype = ctypes.c_int
+_lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]
+_lib.mla_project_output.restype = ctypes.c_int
+_lib.mla_project_output.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    _vp, _vp]
 
 
 class MLAError(RuntimeError):
@@ -171,6 +176,25 @@ def merge_states(v_partial, s_partial, merge_indptr, out, lse, stream=None) -> N
                                out_dtype, _ptr(lse), _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_merge_states")
+
+
+def absorb_query(q_pre, w_kc, q_nope, workspace=None, stream=None) -> None:
+    """q_nope[b,h,:] = q_pre[b,h,:] . w_kc[h]: bf16 [B,H,128] x [H,128,512] -> bf16 [B,H,512]."""
+    B, H, n = (int(x) for x in q_pre.shape)
+    st = _lib.mla_absorb_query(_ptr(q_pre), _ptr(w_kc), _ptr(q_nope), B, H, n, _ptr(workspace),
+                               _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_absorb_query")
+
+
+def project_output(o_lat, w_vc, out, workspace=None, stream=None) -> None:
+    """out[b,h,:] = o_lat[b,h,:] . w_vc[h]: bf16 [B,H,512] x [H,512,128] -> fp32 or bf16 [B,H,128]."""
+    out_dtype = _out_dtype(out, "mla_project_output")
+    B, H = int(o_lat.shape[0]), int(o_lat.shape[1])
+    st = _lib.mla_project_output(_ptr(o_lat), _ptr(w_vc), _ptr(out), out_dtype, B, H, int(w_vc.shape[2]),
+                                 _ptr(workspace), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_project_output")
 
 
 def check_errors(workspace, stream=None) -> int:

@@ -240,6 +240,48 @@ int mla_merge_states(const float* v_partial, const float* s_partial, const int32
   return launch_merge(m, batch, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int mla_absorb_query(const void* q_pre, const void* w_kc, void* q_nope, int32_t batch, int32_t num_heads,
+                     int32_t nope_dim, void* workspace, void* stream) {
+  if (nope_dim != 128) return MLA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads < 1 || num_heads > 65535) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!q_pre || !w_kc || !q_nope || !aligned16(q_pre) || !aligned16(w_kc) || !aligned16(q_nope) ||
+      (workspace && !aligned16(workspace)))
+    return MLA_ERR_INVALID_ARG;
+  const uint64_t H = static_cast<uint64_t>(num_heads);
+  CUtensorMap tm_a, tm_w;
+  if (!make_map(&tm_a, q_pre, H * 128, static_cast<uint64_t>(batch), 64, 128) ||
+      !make_map(&tm_w, w_kc, kLatent, H * 128, 64, 64))
+    return MLA_ERR_CUDA;
+  HeadGemmParams p{};
+  p.out = q_nope;
+  p.status = static_cast<int*>(workspace);
+  p.rows = batch;
+  p.heads = num_heads;
+  return launch_absorb(tm_a, tm_w, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_project_output(const void* o_lat, const void* w_vc, void* out, int32_t out_dtype, int32_t batch,
+                       int32_t num_heads, int32_t v_dim, void* workspace, void* stream) {
+  if (v_dim != 128 || (out_dtype != 0 && out_dtype != 1)) return MLA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads < 1 || num_heads > 65535) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!o_lat || !w_vc || !out || !aligned16(o_lat) || !aligned16(w_vc) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return MLA_ERR_INVALID_ARG;
+  const uint64_t H = static_cast<uint64_t>(num_heads);
+  CUtensorMap tm_a, tm_w;
+  if (!make_map(&tm_a, o_lat, H * kLatent, static_cast<uint64_t>(batch), 64, 128) ||
+      !make_map(&tm_w, w_vc, 128, H * kLatent, 64, 64))
+    return MLA_ERR_CUDA;
+  HeadGemmParams p{};
+  p.out = out;
+  p.status = static_cast<int*>(workspace);
+  p.rows = batch;
+  p.heads = num_heads;
+  return launch_project(tm_a, tm_w, p, out_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mla_check_errors(void* workspace, void* stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

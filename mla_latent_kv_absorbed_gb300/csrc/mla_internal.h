@@ -67,4 +67,13 @@ struct MergeParams {
   float* lse;
 };
 
+// Per-head product C[b, h, :] = A[b, h, 0:K] . W[h] (the query absorption and
+// the output projection); A and W are read through tensor maps.
+struct HeadGemmParams {
+  void* out;                  // [rows, heads, N] bf16 or fp32
+  int* status;                // status word (MLA_ERR_TIMEOUT), or null
+  int rows;                   // B
+  int heads;                  // H
+};
+
 }  // namespace mla

@@ -20,4 +20,13 @@ int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kv_ro
 // most partials an entry has (sizes the block), or 0 when unknown.
 int launch_merge(const MergeParams& p, int entries, int max_pieces, cudaStream_t stream);
 
+// Query absorption q_nope[b,h,:] = q_pre[b,h,0:128] . w_kc[h] (128 x 512), bf16 out.
+// tm_a over q_pre as [B, H*128] (box 64 x 128), tm_w over w_kc as [H*128, 512] (box 64 x 64).
+int launch_absorb(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGemmParams& p, cudaStream_t stream);
+
+// Output projection out[b,h,:] = o_lat[b,h,0:512] . w_vc[h] (512 x 128), bf16 or fp32 out.
+// tm_a over o_lat as [B, H*512] (box 64 x 128), tm_w over w_vc as [H*512, 128] (box 64 x 64).
+int launch_project(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGemmParams& p, int out_bf16,
+                   cudaStream_t stream);
+
 }  // namespace mla

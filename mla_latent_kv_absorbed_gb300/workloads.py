@@ -163,3 +163,24 @@ def workload_stats(spec_number: int) -> dict:
     lengths = draw_lengths(spec, rng)
     return {"batch": spec.batch, "heads": spec.heads, "pool": spec.pool,
             "nnz": int(lengths.sum()), "max_len": int(lengths.max()), "min_len": int(lengths.min())}
+
+
+@dataclasses.dataclass
+class HeadProductInputs:
+    """Synthetic inputs of the two per-head products around the decode
+    (uint16 bf16 bits): the query before absorption and the w_kc / w_vc
+    weights split from a kv_b_proj of DeepSeek's shape (128 nope and 128 value
+    dims per head, rank 512)."""
+    q_pre: np.ndarray   # [B, H, 128]
+    w_kc: np.ndarray    # [H, 128, 512]
+    w_vc: np.ndarray    # [H, 512, 128]
+
+
+def make_head_product_inputs(batch: int, heads: int, seed: int) -> HeadProductInputs:
+    """N(0,1) queries; weights N(0, 1/fan_in) so the products stay O(1); all
+    rounded to bf16.  Draw order: q_pre, w_kc, w_vc."""
+    rng = np.random.default_rng(seed)
+    q_pre = _normal_bf16(rng, batch * heads, 128).reshape(batch, heads, 128)
+    w_kc = f32_to_bf16_bits(rng.standard_normal((heads, 128, 512), dtype=np.float32) / np.float32(math.sqrt(128)))
+    w_vc = f32_to_bf16_bits(rng.standard_normal((heads, 512, 128), dtype=np.float32) / np.float32(math.sqrt(512)))
+    return HeadProductInputs(q_pre=q_pre, w_kc=w_kc, w_vc=w_vc)

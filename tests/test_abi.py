@@ -141,3 +141,22 @@ def test_merge_rejects_bad_arguments(B):
     assert lib.mla_merge_states(None, None, None, 2, 16, None, 0, None, None) == 1
     assert lib.mla_merge_states(None, None, None, 0, 16, None, 0, None, None) == 0
     assert lib.mla_check_errors(None, None) == 1
+
+
+def test_head_products_reject_bad_arguments(B):
+    lib = B.library()
+    fake = 1 << 20
+    # unsupported head dims, then bad sizes and pointers; all before any launch
+    assert lib.mla_absorb_query(fake, fake, fake, 4, 16, 64, None, None) == 2
+    assert lib.mla_absorb_query(fake, fake, fake, -1, 16, 128, None, None) == 1
+    assert lib.mla_absorb_query(fake, fake, fake, 4, 0, 128, None, None) == 1
+    assert lib.mla_absorb_query(None, fake, fake, 4, 16, 128, None, None) == 1
+    assert lib.mla_absorb_query(fake + 2, fake, fake, 4, 16, 128, None, None) == 1
+    assert lib.mla_absorb_query(fake, fake, fake, 4, 16, 128, fake + 4, None) == 1
+    assert lib.mla_absorb_query(None, None, None, 0, 16, 128, None, None) == 0
+    assert lib.mla_project_output(fake, fake, fake, 0, 4, 16, 96, None, None) == 2
+    assert lib.mla_project_output(fake, fake, fake, 3, 4, 16, 128, None, None) == 2
+    assert lib.mla_project_output(fake, fake, fake, 0, -2, 16, 128, None, None) == 1
+    assert lib.mla_project_output(fake, None, fake, 1, 4, 16, 128, None, None) == 1
+    assert lib.mla_project_output(fake, fake, fake + 8, 0, 4, 16, 128, None, None) == 1
+    assert lib.mla_project_output(None, None, None, 0, 0, 16, 128, None, None) == 0
