@@ -240,6 +240,74 @@ def workload_config(batch, args, rotate=None):
             "l2": l2, "parallelism": f"replicas x{args.gpus}"}
 
 
+def time_head_products(batch, dev, peaks):
+    """The two per-head products around the decode at this workload's B and H
+    (query absorption q.w_kc, output projection o_lat.w_vc), each timed over
+    back-to-back launches that rotate through input sets totalling more than
+    4x L2, against its own roofline.  Not part of the decode step."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding, workloads
+    Bn, H = batch.batch, batch.heads
+    x = workloads.make_head_product_inputs(Bn, H, seed=workloads.SEED_BASE + 900)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    q_pre, w_kc, w_vc = bf(x.q_pre), bf(x.w_kc), bf(x.w_vc)
+    o_lat = torch.randn((Bn, H, 512), device=dev).to(torch.bfloat16)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    for name in ("absorb", "project"):
+        if name == "absorb":
+            a, w = q_pre, w_kc
+            out_shape, out_dt, out_size = (Bn, H, 512), torch.bfloat16, 2
+            K, N = 128, 512
+        else:
+            a, w = o_lat, w_vc
+            out_shape, out_dt, out_size = (Bn, H, 128), torch.float32, 4
+            K, N = 512, 128
+        bytes_alg = H * K * N * 2 + Bn * H * K * 2 + Bn * H * N * out_size
+        flops = 2 * Bn * H * K * N
+        R = max(20, math.ceil(4 * l2 / bytes_alg) + 1)
+        sets = [(a.clone(), w.clone(), torch.empty(out_shape, dtype=out_dt, device=dev)) for _ in range(R)]
+        fn = binding.absorb_query if name == "absorb" else binding.project_output
+        for k in range(3):
+            fn(*sets[k % R])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(R):
+            fn(*sets[k])
+        e1.record()
+        torch.cuda.synchronize()
+        us_eager = e0.elapsed_time(e1) * 1e3 / R
+        # the same launches captured in a CUDA graph: the device time without
+        # the host's per-call work (argument checks, tensor-map encoding)
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for k in range(R):
+                    fn(*sets[k], stream=cap)
+        torch.cuda.current_stream().wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / R
+        t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9) * 1e6
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+        res[name] = {"us": us, "us_eager": us_eager, "roofline_us": max(t_hbm, t_tc), "frac": max(t_hbm, t_tc) / us,
+                     "bound": "hbm" if t_hbm >= t_tc else "tensor", "algorithmic_bytes": bytes_alg,
+                     "algorithmic_flops": flops, "launches": R}
+        del sets
+    res["note"] = ("q_pre [B,H,128] . w_kc [H,128,512] -> bf16, o_lat [B,H,512] . w_vc [H,512,128] -> fp32; "
+                   "synthetic weights N(0,1/fan_in); launches rotating input sets > 4x L2, timed as one CUDA-graph replay "
+                   "(us) and as eager back-to-back calls (us_eager)")
+    return res
+
+
 def run_ours(args, batch, world, rank, local, pg):
     import numpy as np
     import torch
@@ -405,6 +473,8 @@ def run_ours(args, batch, world, rank, local, pg):
     roof["roofline_us"] = max(t_hbm, t_tc) * 1e6
     roof["step_frac_of_roofline"] = max(t_hbm, t_tc) * 1e3 / ms
 
+    head_products = time_head_products(batch, dev, peaks)
+
     cpu = None
     if not args.no_cpu_baseline:
         us, nreq, tok = cpu_oracle_sample(batch, args.cpu_budget_s)
@@ -419,6 +489,7 @@ def run_ours(args, batch, world, rank, local, pg):
         "latent_kv_gbs": batch.nnz * 1152 / (ms * 1e-3) / 1e9 * world,
         "step_us_l2_flushed": flushed_ms * 1e3,
         "roofline": roof,
+        "head_products": head_products,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "includes": "host plan + pinned H2D (q, indptr, indices, plan) + kernels + D2H (out, lse)"},
