@@ -226,6 +226,19 @@ def decompressed_attention(q_nope_heads, q_rope_heads, latents, k_rope, kv_b_pro
     return out
 
 
+def append_rows(kv_cache_bits: np.ndarray, slots: np.ndarray, rows_bits: np.ndarray) -> np.ndarray:
+    """The cache after a decode step's append: row b (576 wide, latent then
+    rope key) goes to slot slots[b]; every other row is unchanged.  Returns a
+    new array ("实现差距：MLA 与 DeepSeek V3", section 2.4: the Pallas V2 kernel
+    writes the new token's kv_c and k_pe into the cache pages before attending).
+    Slots must be distinct and inside the pool."""
+    out = np.array(kv_cache_bits, copy=True)
+    idx = np.asarray(slots, dtype=np.int64)
+    assert len(set(idx.tolist())) == idx.shape[0], "slots must be distinct"
+    out[idx] = np.asarray(rows_bits)
+    return out
+
+
 def mac_counts(num_heads: int, qk_nope_head_dim: int, kv_lora_rank: int, history: int):
     """Multiply-accumulates to bring one decode query against the history.
 

@@ -73,6 +73,26 @@ def test_absorb_query_and_project_output_are_per_head_products():
                 assert abs(pr[b, h, j] - sum(o[b, h, i] * wv[h, i, j] for i in range(r))) < 1e-12
 
 
+def test_append_then_decode_equals_decode_over_the_extended_rows():
+    # appending a request's new row to a free slot and adding that slot to its
+    # index list is the same as attending over its old rows plus the new row
+    rng = np.random.default_rng(21)
+    pool, H, L = 40, 3, 6
+    bits = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kv = bits(rng.standard_normal((pool, 576)))
+    new = bits(rng.standard_normal((1, 576)))
+    idx = rng.permutation(pool - 1)[:L].astype(np.int32)
+    kv2 = O.append_rows(kv, np.array([pool - 1]), new)
+    assert np.array_equal(kv2[:pool - 1], kv[:pool - 1]) and np.array_equal(kv2[pool - 1], new[0])
+    qn, qr = bits(rng.standard_normal((1, H, 512))), bits(rng.standard_normal((1, H, 64)))
+    ind2 = np.concatenate([idx, [pool - 1]]).astype(np.int32)
+    o, l = O.decode_attention(qn, qr, kv2, np.array([0, L + 1]), ind2, SM)
+    rows = np.concatenate([O.bf16_bits_to_f64(kv[idx]), O.bf16_bits_to_f64(new)], axis=0)
+    ro, rl = O.partial_state(O.bf16_bits_to_f64(qn[0]), O.bf16_bits_to_f64(qr[0]), rows, SM)
+    np.testing.assert_allclose(o[0], ro, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(l[0], rl, rtol=1e-13, atol=1e-13)
+
+
 def test_absorb_weights_layout():
     # kv_b_proj rows are [head][nope + v]; w_kc must pick the first nope rows
     # of each head's block, w_vc the remaining v rows, transposed.
