@@ -226,6 +226,24 @@ int mla_absorb_query(const void* q_pre, const void* w_kc, void* q_nope, int32_t 
 int mla_project_output(const void* o_lat, const void* w_vc, void* out, int32_t out_dtype, int32_t batch,
                        int32_t num_heads, int32_t v_dim, void* workspace, void* stream);
 
+/* mla_append_kv -- asynchronous on `stream`.
+ *
+ * Writes a decode step's new cache rows: rows[b] (576 bf16: the 512-wide
+ * latent, then the 64-wide rope key) goes to kv_cache[slots[b]]
+ * ("实现差距：MLA 与 DeepSeek V3", section 2.4: the new token's kv_c and k_pe
+ * are written to the cache before attention).  Run it before mla_decode_run
+ * on the same stream when the new tokens' slots are in kv_indices.
+ *
+ *   kv_cache   device bf16 [num_slots, 576], written in place.
+ *   slots      device int32 [batch], distinct (two rows to one slot: either may win).
+ *   rows       device bf16 [batch, 576].
+ *   workspace  NULL, or a decode workspace: a slot outside [0, num_slots) is
+ *              skipped and recorded there as MLA_ERR_INDEX_OOB (mla_check_errors).
+ * Errors: MLA_ERR_INVALID_ARG for null or non-16-byte-aligned pointers,
+ * batch < 0 or num_slots < 1; nothing is launched then. */
+int mla_append_kv(void* kv_cache, int64_t num_slots, const int32_t* slots, const void* rows, int32_t batch,
+                  void* workspace, void* stream);
+
 /* mla_check_errors -- synchronises `stream`, reads the workspace status word,
  * clears it, and returns it (MLA_OK when the kernels found nothing wrong), or
  * MLA_ERR_CUDA if the stream reports a CUDA error. */

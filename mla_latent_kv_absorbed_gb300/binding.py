@@ -23,7 +23,8 @@ STATUS_NAMES = {
 }
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
-           "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output")
+           "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
+           "mla_append_kv")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -57,6 +58,8 @@ _lib.mla_check_errors.restype = ctypes.c_int
 _lib.mla_check_errors.argtypes = [_vp, _vp]
 _lib.mla_absorb_query.restype = ctypes.c_int
 _lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]
+_lib.mla_append_kv.restype = ctypes.c_int
+_lib.mla_append_kv.argtypes = [_vp, ctypes.c_int64, _vp, _vp, ctypes.c_int32, _vp, _vp]
 _lib.mla_project_output.restype = ctypes.c_int
 _lib.mla_project_output.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     _vp, _vp]
@@ -195,6 +198,14 @@ def project_output(o_lat, w_vc, out, workspace=None, stream=None) -> None:
                                  _ptr(workspace), _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_project_output")
+
+
+def append_kv(kv_cache, slots, rows, workspace=None, stream=None) -> None:
+    """kv_cache[slots[b]] = rows[b]: bf16 [num_slots, 576] <- bf16 [B, 576] at int32 slots [B]."""
+    st = _lib.mla_append_kv(_ptr(kv_cache), int(kv_cache.shape[0]), _ptr(slots), _ptr(rows), int(rows.shape[0]),
+                            _ptr(workspace), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_append_kv")
 
 
 def check_errors(workspace, stream=None) -> int:

@@ -282,6 +282,22 @@ int mla_project_output(const void* o_lat, const void* w_vc, void* out, int32_t o
   return launch_project(tm_a, tm_w, p, out_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int mla_append_kv(void* kv_cache, int64_t num_slots, const int32_t* slots, const void* rows, int32_t batch,
+                  void* workspace, void* stream) {
+  if (batch < 0 || num_slots < 1) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!kv_cache || !slots || !rows || !aligned16(kv_cache) || !aligned16(rows) || (workspace && !aligned16(workspace)))
+    return MLA_ERR_INVALID_ARG;
+  AppendParams p{};
+  p.kv_cache = kv_cache;
+  p.src = rows;
+  p.slots = slots;
+  p.status = static_cast<int*>(workspace);
+  p.num_slots = num_slots;
+  p.rows = batch;
+  return launch_append(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mla_check_errors(void* workspace, void* stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -76,4 +76,14 @@ struct HeadGemmParams {
   int heads;                  // H
 };
 
+// Cache append: rows [rows, 576] bf16 to kv_cache[slots[r]].
+struct AppendParams {
+  void* kv_cache;             // [num_slots, 576] bf16
+  const void* src;            // [rows, 576] bf16
+  const int32_t* slots;       // [rows]
+  int* status;                // status word, or null
+  long long num_slots;
+  int rows;
+};
+
 }  // namespace mla

@@ -29,4 +29,7 @@ int launch_absorb(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGe
 int launch_project(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGemmParams& p, int out_bf16,
                    cudaStream_t stream);
 
+// Cache append of a step's new rows.
+int launch_append(const AppendParams& p, cudaStream_t stream);
+
 }  // namespace mla

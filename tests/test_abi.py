@@ -160,3 +160,13 @@ def test_head_products_reject_bad_arguments(B):
     assert lib.mla_project_output(fake, None, fake, 1, 4, 16, 128, None, None) == 1
     assert lib.mla_project_output(fake, fake, fake + 8, 0, 4, 16, 128, None, None) == 1
     assert lib.mla_project_output(None, None, None, 0, 0, 16, 128, None, None) == 0
+
+
+def test_append_rejects_bad_arguments(B):
+    lib = B.library()
+    fake = 1 << 20
+    assert lib.mla_append_kv(fake, 100, fake, fake, -1, None, None) == 1
+    assert lib.mla_append_kv(fake, 0, fake, fake, 2, None, None) == 1
+    assert lib.mla_append_kv(None, 100, fake, fake, 2, None, None) == 1
+    assert lib.mla_append_kv(fake, 100, fake, fake + 8, 2, None, None) == 1
+    assert lib.mla_append_kv(None, 100, None, None, 0, None, None) == 0
