@@ -191,6 +191,40 @@ int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* plan_dev,
                            float sm_scale, void* out, int32_t out_dtype, float* lse,
                            void* stream);
 
+/* mla_decode_step_host -- one decode step from HOST buffers, asynchronous on `stream`.
+ *
+ * Plans the batch on the host (mla_decode_plan with the current device's SM
+ * count) into `plan`, copies the plan words, q_nope, q_rope, kv_indptr and
+ * kv_indices into the caller's device `staging` buffer, runs mla_decode_run
+ * there, and copies out and lse back into host memory -- seven
+ * cudaMemcpyAsync and the decode's launches.  The kernels go on `stream`,
+ * the copies in on `copy_in_stream` and the copies out on `copy_out_stream`
+ * when those are not NULL (ordered with the kernels through events), else on
+ * `stream`.  With page-locked host buffers every copy is asynchronous: keep
+ * the host buffers (and `plan`) unchanged until the copies have passed this
+ * step.  A serving loop alternates two staging buffers over consecutive
+ * steps with one copy-in and one copy-out stream, so one step's copies
+ * overlap its neighbours' kernels.
+ *
+ *   q_nope, q_rope, kv_indptr, kv_indices, out, lse
+ *               HOST buffers, same shapes and dtypes as for mla_decode_run.
+ *   kv_cache    device, as for mla_decode_run.
+ *   plan        host int32 buffer of plan_words (query the size with
+ *               mla_decode_plan(..., plan = NULL, ...)).
+ *   staging     device buffer of at least mla_step_staging_bytes(batch,
+ *               num_heads, nnz, plan words, out_dtype) bytes.
+ *   workspace   device, at least the plan's workspace bytes.
+ * Errors: those of mla_decode_plan and mla_decode_run; MLA_ERR_WORKSPACE when
+ * staging or workspace is too small; MLA_ERR_INVALID_ARG for null pointers or
+ * batch < 1.  Nothing is copied or launched on an error found before the
+ * first copy. */
+size_t mla_step_staging_bytes(int32_t batch, int32_t num_heads, int64_t nnz, size_t plan_words, int32_t out_dtype);
+int mla_decode_step_host(const void* q_nope, const void* q_rope, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, int32_t batch, int32_t num_heads, const void* kv_cache,
+                         int64_t num_slots, float sm_scale, void* out, int32_t out_dtype, float* lse,
+                         int32_t* plan, size_t plan_words, void* staging, size_t staging_bytes, void* workspace,
+                         size_t workspace_bytes, void* stream, void* copy_in_stream, void* copy_out_stream);
+
 /* mla_absorb_query -- asynchronous on `stream`.
  *
  * The query side of the absorbing path ("MLA and torch.compile: v0.3's two

@@ -24,7 +24,7 @@ STATUS_NAMES = {
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
-           "mla_append_kv")
+           "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -58,6 +58,12 @@ _lib.mla_check_errors.restype = ctypes.c_int
 _lib.mla_check_errors.argtypes = [_vp, _vp]
 _lib.mla_absorb_query.restype = ctypes.c_int
 _lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]
+_lib.mla_step_staging_bytes.restype = ctypes.c_size_t
+_lib.mla_step_staging_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int32]
+_lib.mla_decode_step_host.restype = ctypes.c_int
+_lib.mla_decode_step_host.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, _vp, ctypes.c_int64,
+                                      ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp,
+                                      ctypes.c_size_t, _vp, ctypes.c_size_t, _vp, _vp, _vp]
 _lib.mla_append_kv.restype = ctypes.c_int
 _lib.mla_append_kv.argtypes = [_vp, ctypes.c_int64, _vp, _vp, ctypes.c_int32, _vp, _vp]
 _lib.mla_project_output.restype = ctypes.c_int
@@ -206,6 +212,26 @@ def append_kv(kv_cache, slots, rows, workspace=None, stream=None) -> None:
                             _ptr(workspace), _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_append_kv")
+
+
+def step_staging_bytes(batch: int, num_heads: int, nnz: int, plan_words: int, out_dtype: int) -> int:
+    return int(_lib.mla_step_staging_bytes(batch, num_heads, nnz, plan_words, out_dtype))
+
+
+def decode_step_host(q_nope, q_rope, kv_indptr, kv_indices, kv_cache, sm_scale, out, lse, plan, staging, workspace,
+                     stream=None, copy_in_stream=None, copy_out_stream=None) -> None:
+    """One step from host tensors (pinned for asynchronous copies): plan, copy in, run, copy out on `stream`.
+    `plan` is a host int32 tensor with room for the plan words."""
+    out_dtype = _out_dtype(out, "mla_decode_step_host")
+    B, H = int(q_nope.shape[0]), int(q_nope.shape[1])
+    st = _lib.mla_decode_step_host(_ptr(q_nope), _ptr(q_rope), _ptr(kv_indptr), _ptr(kv_indices), B, H,
+                                   _ptr(kv_cache), int(kv_cache.shape[0]), float(sm_scale), _ptr(out), out_dtype,
+                                   _ptr(lse), _ptr(plan), int(plan.numel()), _ptr(staging), int(staging.numel()),
+                                   _ptr(workspace), int(workspace.numel()), _stream_handle(stream),
+                                   None if copy_in_stream is None else _stream_handle(copy_in_stream),
+                                   None if copy_out_stream is None else _stream_handle(copy_out_stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_step_host")
 
 
 def check_errors(workspace, stream=None) -> int:

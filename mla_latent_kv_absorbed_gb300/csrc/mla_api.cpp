@@ -219,6 +219,101 @@ int mla_decode_run(const int32_t* plan_host, const int32_t* plan_dev, const void
   return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
 }
 
+namespace {
+// Device staging of one host-buffer step: plan words, q_nope, q_rope,
+// kv_indptr, kv_indices, out, lse; each region 256-byte aligned.
+struct StepLayout {
+  size_t plan, qn, qr, ptr, idx, out, lse, total;
+};
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+StepLayout step_layout(int32_t B, int32_t H, int64_t nnz, size_t plan_words, int32_t out_dtype) {
+  StepLayout l{};
+  size_t o = 0;
+  l.plan = o; o = align256(o + plan_words * 4);
+  l.qn = o;   o = align256(o + static_cast<size_t>(B) * H * kLatent * 2);
+  l.qr = o;   o = align256(o + static_cast<size_t>(B) * H * kRope * 2);
+  l.ptr = o;  o = align256(o + static_cast<size_t>(B + 1) * 4);
+  l.idx = o;  o = align256(o + static_cast<size_t>(nnz) * 4);
+  l.out = o;  o = align256(o + static_cast<size_t>(B) * H * kLatent * (out_dtype ? 2 : 4));
+  l.lse = o;  o = align256(o + static_cast<size_t>(B) * H * 4);
+  l.total = o;
+  return l;
+}
+}  // namespace
+
+size_t mla_step_staging_bytes(int32_t batch, int32_t num_heads, int64_t nnz, size_t plan_words, int32_t out_dtype) {
+  if (batch < 0 || num_heads < 1 || nnz < 0) return 0;
+  return step_layout(batch, num_heads, nnz, plan_words, out_dtype).total;
+}
+
+int mla_decode_step_host(const void* q_nope, const void* q_rope, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, int32_t batch, int32_t num_heads, const void* kv_cache,
+                         int64_t num_slots, float sm_scale, void* out, int32_t out_dtype, float* lse,
+                         int32_t* plan, size_t plan_words, void* staging, size_t staging_bytes, void* workspace,
+                         size_t workspace_bytes, void* stream, void* copy_in_stream, void* copy_out_stream) {
+  if (!q_nope || !q_rope || !kv_indptr || !out || !lse || !plan || !staging || batch < 1 || out_dtype < 0 ||
+      out_dtype > 1)
+    return MLA_ERR_INVALID_ARG;
+  size_t need = 0, ws_need = 0;
+  const int rc = mla_decode_plan(kv_indptr, batch, num_heads, 0, plan, plan_words, &need, &ws_need);
+  if (rc != MLA_OK) return rc;
+  const int64_t nnz = kv_indptr[batch];
+  if (nnz > 0 && !kv_indices) return MLA_ERR_INVALID_ARG;
+  const StepLayout l = step_layout(batch, num_heads, nnz, need, out_dtype);
+  if (staging_bytes < l.total || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE;
+  if (!aligned16(staging)) return MLA_ERR_INVALID_ARG;
+  cudaStream_t run_st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t st = copy_in_stream ? reinterpret_cast<cudaStream_t>(copy_in_stream) : run_st;
+  cudaStream_t st_out = copy_out_stream ? reinterpret_cast<cudaStream_t>(copy_out_stream) : run_st;
+  // with separate copy streams: the run waits for the copies in, the copies
+  // out wait for the run (events from a small per-thread ring, reused round
+  // robin; a wait takes the event's state at the time it is issued)
+  thread_local cudaEvent_t ring[8] = {};
+  thread_local int ring_next = 0;
+  cudaEvent_t ev_in = nullptr, ev_run = nullptr;
+  for (int i = 0; i < 2; ++i) {
+    cudaEvent_t& e = ring[(ring_next + i) % 8];
+    if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  if (st != run_st) ev_in = ring[ring_next];
+  if (st_out != run_st) ev_run = ring[(ring_next + 1) % 8];
+  ring_next = (ring_next + 2) % 8;
+  uint8_t* d = static_cast<uint8_t*>(staging);
+  const size_t qn_bytes = static_cast<size_t>(batch) * num_heads * kLatent * 2;
+  const size_t qr_bytes = static_cast<size_t>(batch) * num_heads * kRope * 2;
+  if (cudaMemcpyAsync(d + l.plan, plan, need * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d + l.qn, q_nope, qn_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d + l.qr, q_rope, qr_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d + l.ptr, kv_indptr, static_cast<size_t>(batch + 1) * 4, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      (nnz > 0 && cudaMemcpyAsync(d + l.idx, kv_indices, static_cast<size_t>(nnz) * 4, cudaMemcpyHostToDevice, st) !=
+                      cudaSuccess)) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (ev_in && (cudaEventRecord(ev_in, st) != cudaSuccess || cudaStreamWaitEvent(run_st, ev_in, 0) != cudaSuccess)) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  const int rr = mla_decode_run(plan, reinterpret_cast<const int32_t*>(d + l.plan), d + l.qn, d + l.qr, kv_cache,
+                                num_slots, reinterpret_cast<const int32_t*>(d + l.ptr),
+                                reinterpret_cast<const int32_t*>(d + l.idx), sm_scale, d + l.out, out_dtype,
+                                reinterpret_cast<float*>(d + l.lse), workspace, workspace_bytes, stream);
+  if (rr != MLA_OK) return rr;
+  if (ev_run && (cudaEventRecord(ev_run, run_st) != cudaSuccess || cudaStreamWaitEvent(st_out, ev_run, 0) != cudaSuccess)) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  const size_t out_bytes = static_cast<size_t>(batch) * num_heads * kLatent * (out_dtype ? 2 : 4);
+  if (cudaMemcpyAsync(out, d + l.out, out_bytes, cudaMemcpyDeviceToHost, st_out) != cudaSuccess ||
+      cudaMemcpyAsync(lse, d + l.lse, static_cast<size_t>(batch) * num_heads * 4, cudaMemcpyDeviceToHost, st_out) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
 int mla_merge_states(const float* v_partial, const float* s_partial, const int32_t* merge_indptr,
                      int32_t batch, int32_t num_heads, void* out, int32_t out_dtype, float* lse,
                      void* stream) {

@@ -132,3 +132,33 @@ def test_absorbing_step_eager_and_in_a_cuda_graph(H):
     torch.cuda.synchronize()
     assert dec.check() == 0
     check(*inp2)
+
+
+@pytest.mark.parametrize("H,out_dtype", [(16, "f32"), (128, "bf16")])
+def test_host_buffer_step_equals_device_run(H, out_dtype):
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding, workloads as W
+    from tests._helpers import to_device
+    bt = W.make_batch([5, 300, 1, 2100], heads=H, pool=4096, seed=71 + H)
+    dev = to_device(bt)
+    dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    dec = binding.Decoder(bt.kv_indptr, H)
+    ref_out = torch.empty((bt.batch, H, 512), dtype=dt, device="cuda")
+    ref_lse = torch.empty((bt.batch, H), dtype=torch.float32, device="cuda")
+    dec.run(dev["q_nope"], dev["q_rope"], dev["kv_cache"], dev["kv_indptr"], dev["kv_indices"], bt.sm_scale,
+            ref_out, ref_lse)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hq = pin(bt.q_nope.view(np.int16)).view(torch.bfloat16)
+    hr = pin(bt.q_rope.view(np.int16)).view(torch.bfloat16)
+    hp, hi = pin(bt.kv_indptr.astype(np.int32)), pin(bt.kv_indices.astype(np.int32))
+    out = torch.empty((bt.batch, H, 512), dtype=dt).pin_memory()
+    lse = torch.empty((bt.batch, H), dtype=torch.float32).pin_memory()
+    plan = torch.empty(dec.plan_host.shape[0], dtype=torch.int32).pin_memory()
+    staging = torch.empty(binding.step_staging_bytes(bt.batch, H, bt.nnz, plan.numel(), 0 if dt == torch.float32 else 1),
+                          dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(dec.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+    binding.decode_step_host(hq, hr, hp, hi, dev["kv_cache"], bt.sm_scale, out, lse, plan, staging, ws)
+    torch.cuda.synchronize()
+    assert binding.check_errors(ws) == 0
+    assert np.array_equal(plan.numpy(), dec.plan_host)
+    assert torch.equal(out, ref_out.cpu()) and torch.equal(lse, ref_lse.cpu())
