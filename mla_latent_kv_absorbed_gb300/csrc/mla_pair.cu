@@ -559,9 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < TH; ++t)
           if (t >= nvalid) sv[t] = __float_as_uint(-INFINITY);
       }
-      float mh = -INFINITY;
+      // the half row's maximum as a tree (short dependency chains)
+      float mx8[8];
 #pragma unroll
-      for (int t = 0; t < TH; t += 2) mh = max3(mh, __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
+      for (int i = 0; i < 8; ++i)
+        mx8[i] = max3(__uint_as_float(sv[4 * i]), __uint_as_float(sv[4 * i + 1]),
+                      fmaxf(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])));
+      const float mh = fmaxf(max3(mx8[0], mx8[1], mx8[2]), max3(max3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       // row maximum over the tile: combine with the partner warp (other token half)
       float* rm = red_max + (g & 1) * 256;
       rm[th * 128 + h] = mh;
@@ -601,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P = 2^(s - m_ref) as bf16, written over the peer's rows (K-major, 128-byte swizzle)
       const float2 nm2 = f2_pack(-m_ref, -m_ref);
-      float2 l2 = f2_pack(0.f, 0.f);
+      float2 l4[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t pk[4];
@@ -609,12 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 4; ++i) {
           const float2 d = f2_add(f2_pack(__uint_as_float(sv[8 * k + 2 * i]), __uint_as_float(sv[8 * k + 2 * i + 1])), nm2);
           const float a = ex2_approx(d.x), e2 = ex2_approx(d.y);
-          l2 = f2_add(l2, f2_pack(a, e2));
+          l4[i] = f2_add(l4[i], f2_pack(a, e2));   // four independent sums
           pk[i] = pack_bf16x2(a, e2);
         }
         const uint32_t c = static_cast<uint32_t>(4 * th + k);
         if (!aborted) *reinterpret_cast<uint4*>(xrow + ((c ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      const float2 l2 = f2_add(f2_add(l4[0], l4[1]), f2_add(l4[2], l4[3]));
       l_sum += l2.x + l2.y;
       fence_proxy_async_smem();
       __syncwarp();
