@@ -35,6 +35,9 @@ Sources, by page and section:
     ``absorbed_attention``, ``decompressed_attention``.
   * same page, "Exercises", exercise 1: multiply-accumulate counts of the
     absorbing and decompressing paths -- ``mac_counts``.
+  * "[sglang] EAGLE 트리 검증 어텐션 최적화", section "들어가며": draft tokens
+    verified in one pass, each attending to the shared prefix and its
+    ancestors -- ``decode_attention_multi_query`` (chain-shaped drafts).
 
 Pins (tests/test_oracle_pins.py, CPU only): the absorption identity against a
 decompressed multi-head attention evaluated with scipy's softmax; brute-force
@@ -112,6 +115,33 @@ def decode_attention(q_nope_bits, q_rope_bits, kv_cache_bits, kv_indptr, kv_indi
         rows = gather_rows(kv_cache_bits, kv_indices, int(kv_indptr[b]), int(kv_indptr[b + 1]))
         o, l = partial_state(bf16_bits_to_f64(qn[b]), bf16_bits_to_f64(qr[b]), rows, sm_scale)
         out[b], lse[b] = o, l
+    return out, lse
+
+
+def decode_attention_multi_query(q_nope_bits, q_rope_bits, kv_cache_bits, kv_indptr, kv_indices, sm_scale, q_len):
+    """Decode of q_len new tokens per request (speculative verification).
+
+    q_nope [B, q_len, H, 512], q_rope [B, q_len, H, 64] (bf16 bits); request b's
+    context of L_b rows ends with its q_len draft tokens, and query i
+    (0 <= i < q_len) attends to the shared context and to its own ancestors,
+    i.e. to the first L_b - q_len + i + 1 rows ("[sglang] EAGLE 트리 검증 어텐션
+    최적화", section "들어가며": every query attends to the shared prefix and
+    to its ancestor draft tokens; a chain of drafts is the causal case).
+    Returns (out [B, q_len, H, 512], lse [B, q_len, H]).
+    """
+    qn = np.asarray(q_nope_bits)
+    qr = np.asarray(q_rope_bits)
+    B, Q, H = qn.shape[0], qn.shape[1], qn.shape[2]
+    assert Q == q_len
+    out = np.empty((B, Q, H, KV_LORA_RANK))
+    lse = np.empty((B, Q, H))
+    for b in range(B):
+        lo, hi = int(kv_indptr[b]), int(kv_indptr[b + 1])
+        assert hi - lo >= q_len, "a context holds at least its new tokens"
+        for i in range(Q):
+            rows = gather_rows(kv_cache_bits, kv_indices, lo, hi - q_len + i + 1)
+            o, l = partial_state(bf16_bits_to_f64(qn[b, i]), bf16_bits_to_f64(qr[b, i]), rows, sm_scale)
+            out[b, i], lse[b, i] = o, l
     return out, lse
 
 

@@ -93,6 +93,39 @@ def test_append_then_decode_equals_decode_over_the_extended_rows():
     np.testing.assert_allclose(l[0], rl, rtol=1e-13, atol=1e-13)
 
 
+def test_multi_query_causal_decode_pins():
+    # (a) q_len = 1 is the ordinary decode; (b) query i of a request equals an
+    # ordinary decode of that request truncated to its causal length; (c) with
+    # a single-row context extension, the last query's lse is the brute-force
+    # log-sum-exp over every row
+    rng = np.random.default_rng(33)
+    bits = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    pool, H, Q = 50, 2, 3
+    kv = bits(rng.standard_normal((pool, 576)))
+    lens = [3, 7]
+    ind = rng.permutation(pool)[:sum(lens)].astype(np.int32)
+    ptr = np.array([0, 3, 10])
+    qn1, qr1 = bits(rng.standard_normal((2, H, 512))), bits(rng.standard_normal((2, H, 64)))
+    o1, l1 = O.decode_attention_multi_query(qn1[:, None], qr1[:, None], kv, ptr, ind, SM, 1)
+    r1, rl1 = O.decode_attention(qn1, qr1, kv, ptr, ind, SM)
+    np.testing.assert_array_equal(o1[:, 0], r1)
+    np.testing.assert_array_equal(l1[:, 0], rl1)
+    qn, qr = bits(rng.standard_normal((2, Q, H, 512))), bits(rng.standard_normal((2, Q, H, 64)))
+    o, l = O.decode_attention_multi_query(qn, qr, kv, ptr, ind, SM, Q)
+    for b in range(2):
+        for i in range(Q):
+            n = lens[b] - Q + i + 1
+            tr_ptr = np.array([0, n])
+            tr_ind = ind[ptr[b]:ptr[b] + n]
+            ro, rl = O.decode_attention(qn[b, i][None], qr[b, i][None], kv, tr_ptr, tr_ind, SM)
+            np.testing.assert_allclose(o[b, i], ro[0], rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(l[b, i], rl[0], rtol=1e-13, atol=1e-13)
+    b, i, h = 1, Q - 1, 1
+    q = np.concatenate([O.bf16_bits_to_f64(qn[b, i, h]), O.bf16_bits_to_f64(qr[b, i, h])])
+    s_all = [SM * _dot(q, O.bf16_bits_to_f64(kv[ind[ptr[b] + t]])) for t in range(lens[b])]
+    assert abs(l[b, i, h] - math.log(sum(math.exp(x) for x in s_all))) < 1e-12
+
+
 def test_absorb_weights_layout():
     # kv_b_proj rows are [head][nope + v]; w_kc must pick the first nope rows
     # of each head's block, w_vc the remaining v rows, transposed.
