@@ -191,6 +191,29 @@ int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* plan_dev,
                            float sm_scale, void* out, int32_t out_dtype, float* lse,
                            void* stream);
 
+/* mla_decode_run_multi_query -- asynchronous on `stream`.
+ *
+ * Verification of q_len draft tokens per request in one pass ("[sglang]
+ * EAGLE 트리 검증 어텐션 최적화", section "들어가며": every query attends to
+ * the shared context and to its ancestor drafts; this is the chain case).
+ * Request b's context of L_b rows (kv_indptr / kv_indices) ends with its
+ * q_len drafts; query i (0-based) attends to its first L_b - q_len + 1 + i
+ * rows.  The q_len x H query rows are read as the heads of one request, so
+ * each cache row is gathered once for all of them:
+ *   plan        mla_decode_plan(kv_indptr, B, q_len * H, ...).
+ *   q_nope      bf16 [B, q_len, H, 512];  q_rope  bf16 [B, q_len, H, 64].
+ *   out, lse    [B, q_len, H, 512] (out_dtype as for mla_decode_run), [B, q_len, H].
+ * A query row with no row to attend to (L_b < q_len) gets out = 0, lse = -inf.
+ * Errors: MLA_ERR_INVALID_ARG when q_len < 1 or the plan's head count is not a
+ * multiple of q_len; MLA_ERR_UNSUPPORTED when q_len > 1 and q_len * H is 16
+ * or 32 (the few-heads kernel has no per-row limit); otherwise as for
+ * mla_decode_run (q_len = 1 is mla_decode_run). */
+int mla_decode_run_multi_query(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len,
+                               const void* q_nope, const void* q_rope, const void* kv_cache, int64_t num_slots,
+                               const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale, void* out,
+                               int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 /* mla_decode_step_host -- one decode step from HOST buffers, asynchronous on `stream`.
  *
  * Plans the batch on the host (mla_decode_plan with the current device's SM

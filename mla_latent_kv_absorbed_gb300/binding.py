@@ -24,7 +24,7 @@ STATUS_NAMES = {
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
-           "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host")
+           "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -58,6 +58,9 @@ _lib.mla_check_errors.restype = ctypes.c_int
 _lib.mla_check_errors.argtypes = [_vp, _vp]
 _lib.mla_absorb_query.restype = ctypes.c_int
 _lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]
+_lib.mla_decode_run_multi_query.restype = ctypes.c_int
+_lib.mla_decode_run_multi_query.argtypes = [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp,
+                                            ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
 _lib.mla_step_staging_bytes.restype = ctypes.c_size_t
 _lib.mla_step_staging_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int32]
 _lib.mla_decode_step_host.restype = ctypes.c_int
@@ -212,6 +215,20 @@ def append_kv(kv_cache, slots, rows, workspace=None, stream=None) -> None:
                             _ptr(workspace), _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_append_kv")
+
+
+def decode_run_multi_query(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale,
+                           out, lse, workspace, stream=None) -> None:
+    """q_len draft tokens per request in one pass: q [B, q_len, H, 576 split], out [B, q_len, H, 512]."""
+    out_dtype = _out_dtype(out, "mla_decode_run_multi_query")
+    plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    st = _lib.mla_decode_run_multi_query(plan_host.ctypes.data, _ptr(plan_dev), int(q_len), _ptr(q_nope),
+                                         _ptr(q_rope), _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(kv_indptr),
+                                         _ptr(kv_indices), float(sm_scale), _ptr(out), out_dtype, _ptr(lse),
+                                         _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                         _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_run_multi_query")
 
 
 def step_staging_bytes(batch: int, num_heads: int, nnz: int, plan_words: int, out_dtype: int) -> int:

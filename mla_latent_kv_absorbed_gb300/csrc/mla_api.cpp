@@ -130,11 +130,38 @@ int check_run_args(const int32_t* plan_host, const int32_t* plan_dev, int32_t ou
 
 }  // namespace
 
+namespace {
+int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len, const void* q_nope,
+                const void* q_rope, const void* kv_cache, int64_t num_slots, const int32_t* kv_indptr,
+                const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
+                void* workspace, size_t workspace_bytes, void* stream);
+}  // namespace
+
 int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope,
                       const void* q_rope, const void* kv_cache, int64_t num_slots,
                       const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale, void* out,
                       int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
                       void* stream) {
+  return attend_impl(plan_host, plan_dev, 1, q_nope, q_rope, kv_cache, num_slots, kv_indptr, kv_indices, sm_scale,
+                     out, out_dtype, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_run_multi_query(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len,
+                               const void* q_nope, const void* q_rope, const void* kv_cache, int64_t num_slots,
+                               const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale, void* out,
+                               int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  const int rc = attend_impl(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache, num_slots, kv_indptr,
+                             kv_indices, sm_scale, out, out_dtype, lse, workspace, workspace_bytes, stream);
+  if (rc != MLA_OK) return rc;
+  return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
+}
+
+namespace {
+int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len, const void* q_nope,
+                const void* q_rope, const void* kv_cache, int64_t num_slots, const int32_t* kv_indptr,
+                const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
+                void* workspace, size_t workspace_bytes, void* stream) {
   const int rc0 = check_run_args(plan_host, plan_dev, out_dtype, workspace, workspace_bytes);
   if (rc0 != MLA_OK) return rc0;
   if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
@@ -166,6 +193,11 @@ int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev, const v
   p.items_off = plan_items_off(plan_host);
   p.num_workers = plan_host[kHWorkers];
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  // multi-query: the plan's head count is q_len x the heads of one query, and
+  // only the two-CTA kernel applies the per-row causal limit
+  if (q_len < 1 || H % q_len != 0) return MLA_ERR_INVALID_ARG;
+  if (q_len > 1 && plan_host[kHVariant] == kVariantSwab) return MLA_ERR_UNSUPPORTED;
+  p.q_len = q_len;
 
   CUtensorMap tm_kv, tm_qn, tm_qr;
   const uint64_t qrows = static_cast<uint64_t>(B) * H;
@@ -183,6 +215,7 @@ int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev, const v
     return MLA_ERR_CUDA;
   return launch_pair(H, tm_kv, tm_kr, tm_qr, p, plan_host[kHWorkers], st);
 }
+}  // namespace
 
 int mla_decode_merge(const int32_t* plan_host, const int32_t* plan_dev, void* out, int32_t out_dtype,
                      float* lse, void* workspace, size_t workspace_bytes, void* stream) {

@@ -53,6 +53,7 @@ struct DecodeParams {
   int items_off;
   int num_workers;
   float scale_log2;           // sm_scale * log2(e)
+  int q_len;                  // queries per request (rows = q_len x heads per query); <= 1: one
 };
 
 struct MergeParams {

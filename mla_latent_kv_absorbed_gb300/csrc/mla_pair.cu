@@ -571,9 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       rm[th * 128 + h] = mh;
       named_bar_sync(1 + q, 64);
       const float mt = fmaxf(rm[h], rm[128 + h]);
-      if (j == 0) {
+      if (j == 0 || m_ref == -INFINITY) {
+        // an item's first tile sets the reference; so does the first tile
+        // with a valid score when a causal query row had none before (O and
+        // the row sum are still zero then)
         m_ref = mt;
-        l_sum = 0.f;
+        if (j == 0) l_sum = 0.f;
       } else {
         const bool need = mt > m_ref + 8.f;
         if (__any_sync(0xffffffffu, need)) {
@@ -604,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P = 2^(s - m_ref) as bf16, written over the peer's rows (K-major, 128-byte swizzle)
-      const float2 nm2 = f2_pack(-m_ref, -m_ref);
+      const float m_eff = m_ref == -INFINITY ? 0.f : m_ref;   // a row with no valid score yet: P = 0
+      const float2 nm2 = f2_pack(-m_eff, -m_eff);
       float2 l4[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -637,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait(bar(bOFull), nitem & 1, false);
       tc_fence_after();
       if (!aborted) {
-        const float inv = 1.f / lsum;
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;     // no valid score: out = 0
         float* dst_f = nullptr;
         __nv_bfloat16* dst_h = nullptr;
         const size_t col0 = 256 * static_cast<size_t>(cta) + 128 * th;
@@ -681,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (cta == 0 && th == 0 && head_ok) {
-          const float l = (m_ref + __log2f(lsum)) * 0.69314718055994531f;
+          const float l = lsum > 0.f ? (m_ref + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
           if (part < 0) { if (p.lse) p.lse[static_cast<size_t>(b) * H + h] = l; }
           else p.part_lse[static_cast<size_t>(part) * H + h] = l;
         }
@@ -722,7 +726,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !aborted) mbar_arrive(bar(bQFull));
         for (int j = 0; j < nt; ++j, ++g) send(g);
       } else {
-        for (int j = 0; j < nt; ++j, ++g) softmax(g, j, n);
+        // multi-query: row h is query h / (H / q_len) of its request, which
+        // sees the first L - q_len + 1 + i rows of the request's context
+        int n_row = n;
+        if (p.q_len > 1) {
+          const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+          const int i = h / (H / p.q_len);
+          n_row = max(0, min(n, (hi - lo) - p.q_len + 1 + i - (s - lo)));
+        }
+        for (int j = 0; j < nt; ++j, ++g) softmax(g, j, n_row);
         epilogue(b, part, nitem);
       }
       ++nitem;
