@@ -191,6 +191,25 @@ int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* plan_dev,
                            float sm_scale, void* out, int32_t out_dtype, float* lse,
                            void* stream);
 
+/* mla_merge_two_states -- asynchronous on `stream`.
+ *
+ * Row-wise merge of two attention states over disjoint key sets, for every
+ * row r of `rows` (a row is a request-head pair, 512 wide):
+ *   m = max(lse_a, lse_b);  w = exp(lse - m);
+ *   out = (w_a o_a + w_b o_b) / (w_a + w_b);  lse = m + ln(w_a + w_b)
+ * with -inf states weighing nothing (both -inf: out = 0, lse = -inf).  This
+ * is the last step of a shared-prefix cascade ("[sglang] EAGLE 트리 검증
+ * 어텐션 최적화", section "들어가며": prefix attention shared by every query,
+ * suffix attention per query, the two merged by LSE): the prefix pass runs
+ * mla_decode_run once over the prefix rows with the G x H query rows of G
+ * requests as the heads of one request (each prefix row gathered once), the
+ * suffix pass is an ordinary mla_decode_run, both with fp32 out.
+ *   o_a, o_b    device fp32 [rows, 512];  lse_a, lse_b  device fp32 [rows].
+ *   out         device [rows, 512], fp32 (0) or bf16 (1); may be o_a.
+ *   lse         device fp32 [rows] or NULL; may be lse_a. */
+int mla_merge_two_states(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b, int64_t rows,
+                         void* out, int32_t out_dtype, float* lse, void* stream);
+
 /* mla_decode_run_multi_query -- asynchronous on `stream`.
  *
  * Verification of q_len draft tokens per request in one pass ("[sglang]

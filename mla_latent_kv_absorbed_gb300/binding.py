@@ -24,7 +24,8 @@ STATUS_NAMES = {
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
-           "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query")
+           "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query",
+           "mla_merge_two_states")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -61,6 +62,8 @@ _lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
 _lib.mla_decode_run_multi_query.restype = ctypes.c_int
 _lib.mla_decode_run_multi_query.argtypes = [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp,
                                             ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.mla_merge_two_states.restype = ctypes.c_int
+_lib.mla_merge_two_states.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_int32, _vp, _vp]
 _lib.mla_step_staging_bytes.restype = ctypes.c_size_t
 _lib.mla_step_staging_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int32]
 _lib.mla_decode_step_host.restype = ctypes.c_int
@@ -229,6 +232,16 @@ def decode_run_multi_query(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache,
                                          _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_decode_run_multi_query")
+
+
+def merge_two_states(o_a, lse_a, o_b, lse_b, out, lse, stream=None) -> None:
+    """Row-wise LSE merge of two fp32 states [..., 512] / [...] into out (fp32 or bf16) and lse."""
+    out_dtype = _out_dtype(out, "mla_merge_two_states")
+    rows = int(lse_a.numel())
+    st = _lib.mla_merge_two_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, _ptr(out), out_dtype,
+                                   _ptr(lse), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_merge_two_states")
 
 
 def step_staging_bytes(batch: int, num_heads: int, nnz: int, plan_words: int, out_dtype: int) -> int:

@@ -410,6 +410,16 @@ int mla_project_output(const void* o_lat, const void* w_vc, void* out, int32_t o
   return launch_project(tm_a, tm_w, p, out_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int mla_merge_two_states(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b, int64_t rows,
+                         void* out, int32_t out_dtype, float* lse, void* stream) {
+  if (out_dtype != 0 && out_dtype != 1) return MLA_ERR_UNSUPPORTED;
+  if (rows < 0 || rows > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  if (rows == 0) return MLA_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !out || !aligned16(o_a) || !aligned16(o_b) || !aligned16(out))
+    return MLA_ERR_INVALID_ARG;
+  return launch_merge_two(o_a, lse_a, o_b, lse_b, out, out_dtype, lse, rows, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mla_append_kv(void* kv_cache, int64_t num_slots, const int32_t* slots, const void* rows, int32_t batch,
                   void* workspace, void* stream) {
   if (batch < 0 || num_slots < 1) return MLA_ERR_INVALID_ARG;

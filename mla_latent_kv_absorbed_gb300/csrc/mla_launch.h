@@ -29,6 +29,10 @@ int launch_absorb(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGe
 int launch_project(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGemmParams& p, int out_bf16,
                    cudaStream_t stream);
 
+// Merge of two states per row ([rows, 512] fp32 + [rows] lse each).
+int launch_merge_two(const float* o_a, const float* l_a, const float* o_b, const float* l_b, void* out, int out_bf16,
+                     float* lse, long long rows, cudaStream_t stream);
+
 // Cache append of a step's new rows.
 int launch_append(const AppendParams& p, cudaStream_t stream);
 

@@ -134,6 +134,41 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   if (t == 0 && p.lse) p.lse[static_cast<size_t>(b) * H + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
+// Two states per row, same layout ([rows, 512] and [rows]): the merge of a
+// shared-prefix pass with a per-request suffix pass (the EAGLE tree-verify
+// page's prefix / suffix attention merged by LSE).  One 128-thread block per
+// row, four dims per thread; out may be the first state's array.
+__global__ void __launch_bounds__(128) merge_two_kernel(const float* __restrict__ o_a, const float* __restrict__ l_a,
+                                                        const float* __restrict__ o_b, const float* __restrict__ l_b,
+                                                        void* out, int out_bf16, float* lse, long long rows) {
+  const long long r = blockIdx.x;
+  if (r >= rows) return;
+  const float la = __ldg(l_a + r), lb = __ldg(l_b + r);
+  const float m = fmaxf(la, lb);
+  const float wa = la == -INFINITY ? 0.f : expf(la - m), wb = lb == -INFINITY ? 0.f : expf(lb - m);
+  const float ws = wa + wb, inv = ws > 0.f ? 1.f / ws : 0.f;
+  const float4 a = reinterpret_cast<const float4*>(o_a + r * kLatent)[threadIdx.x];
+  const float4 b = reinterpret_cast<const float4*>(o_b + r * kLatent)[threadIdx.x];
+  const float4 v = make_float4((wa * a.x + wb * b.x) * inv, (wa * a.y + wb * b.y) * inv, (wa * a.z + wb * b.z) * inv,
+                               (wa * a.w + wb * b.w) * inv);
+  if (out_bf16) {
+    __nv_bfloat162* d = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + r * kLatent) +
+                        2 * threadIdx.x;
+    d[0] = __floats2bfloat162_rn(v.x, v.y);
+    d[1] = __floats2bfloat162_rn(v.z, v.w);
+  } else {
+    reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * kLatent)[threadIdx.x] = v;
+  }
+  if (threadIdx.x == 0 && lse) lse[r] = ws > 0.f ? m + logf(ws) : -INFINITY;
+}
+
+int launch_merge_two(const float* o_a, const float* l_a, const float* o_b, const float* l_b, void* out, int out_bf16,
+                     float* lse, long long rows, cudaStream_t stream) {
+  if (rows <= 0) return MLA_OK;
+  merge_two_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(o_a, l_a, o_b, l_b, out, out_bf16, lse, rows);
+  return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int launch_merge(const MergeParams& p, int entries, int max_pieces, cudaStream_t stream) {
   if (entries <= 0) return MLA_OK;
   const int groups = max_pieces >= 16 ? 4 : max_pieces >= 8 ? 2 : 1;

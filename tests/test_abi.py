@@ -170,3 +170,13 @@ def test_append_rejects_bad_arguments(B):
     assert lib.mla_append_kv(None, 100, fake, fake, 2, None, None) == 1
     assert lib.mla_append_kv(fake, 100, fake, fake + 8, 2, None, None) == 1
     assert lib.mla_append_kv(None, 100, None, None, 0, None, None) == 0
+
+
+def test_merge_two_rejects_bad_arguments(B):
+    lib = B.library()
+    fake = 1 << 20
+    assert lib.mla_merge_two_states(fake, fake, fake, fake, 4, fake, 2, None, None) == 2
+    assert lib.mla_merge_two_states(fake, fake, fake, fake, -1, fake, 0, None, None) == 1
+    assert lib.mla_merge_two_states(None, fake, fake, fake, 4, fake, 0, None, None) == 1
+    assert lib.mla_merge_two_states(fake + 4, fake, fake, fake, 4, fake, 0, None, None) == 1
+    assert lib.mla_merge_two_states(None, None, None, None, 0, None, 0, None, None) == 0
