@@ -356,6 +356,98 @@ def time_multi_query(batch, dev, peaks, kv, indptr_d, indices_d):
                     "synthetic queries, this workload's contexts; back-to-back launches over KV copies > 4x L2"}
 
 
+def time_cascade(batch, dev, peaks):
+    """Shared-prefix cascade at this workload's shape: every request gets a
+    shared 4096-row prefix in front of its own context (the workload's rows
+    as suffix).  Cascade = prefix pass (the query rows of 128 // H requests as
+    the heads of one pseudo-request, so the prefix is read once per group),
+    suffix pass, two-state merge; flat = one decode over prefix + suffix rows
+    per request.  Each captured in a CUDA graph and replayed back to back.
+    Only for H <= 32."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding
+    Bn, H = batch.batch, batch.heads
+    if H > 32:
+        return None
+    Lp, group = 4096, 128 // H
+    G = (Bn + group - 1) // group
+    rng = np.random.default_rng(11)
+    pool = batch.pool
+    prefix = rng.permutation(pool)[:Lp].astype(np.int32)
+    ti = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    kv = torch.from_numpy(np.ascontiguousarray(batch.kv_cache).view(np.int16)).view(torch.bfloat16).to(dev)
+    Bp = G * group                                   # padded to whole groups
+    qn = torch.randn((Bp, H, 512), device=dev).to(torch.bfloat16)
+    qr = torch.randn((Bp, H, 64), device=dev).to(torch.bfloat16)
+    sc = batch.sm_scale
+    # prefix pass: G pseudo-requests of group x H rows over the same prefix rows
+    p_ptr = np.arange(G + 1, dtype=np.int32) * Lp
+    dec_p = binding.Decoder(p_ptr, group * H, device=dev)
+    p_ind = ti(np.tile(prefix, G))
+    o_p = torch.empty((Bp, H, 512), dtype=torch.float32, device=dev)
+    l_p = torch.empty((Bp, H), dtype=torch.float32, device=dev)
+    # suffix pass: the workload's contexts (padding requests empty)
+    s_ptr = np.concatenate([batch.kv_indptr, np.full(Bp - Bn, batch.kv_indptr[-1])]).astype(np.int32)
+    dec_s = binding.Decoder(s_ptr, H, device=dev)
+    s_ind = ti(batch.kv_indices)
+    o_s, l_s = torch.empty_like(o_p), torch.empty_like(l_p)
+    out, lse = torch.empty_like(o_p), torch.empty_like(l_p)
+    # flat: each request over prefix + suffix
+    f_ptr = (s_ptr + np.arange(Bp + 1, dtype=np.int32) * Lp).astype(np.int32)
+    f_ind = np.concatenate([np.concatenate([prefix, batch.kv_indices[s_ptr[b]:s_ptr[b + 1]]]) for b in range(Bp)])
+    dec_f = binding.Decoder(f_ptr, H, device=dev)
+    f_ind_d = ti(f_ind)
+    o_f, l_f = torch.empty_like(o_p), torch.empty_like(l_p)
+    p_ptr_d, s_ptr_d, f_ptr_d = ti(p_ptr), ti(s_ptr), ti(f_ptr)
+
+    def cascade(stream=None):
+        dec_p.run(qn.view(G, group * H, 512), qr.view(G, group * H, 64), kv, p_ptr_d, p_ind, sc, o_p, l_p,
+                  stream=stream)
+        dec_s.run(qn, qr, kv, s_ptr_d, s_ind, sc, o_s, l_s, stream=stream)
+        binding.merge_two_states(o_p, l_p, o_s, l_s, out, lse, stream=stream)
+
+    def flat(stream=None):
+        dec_f.run(qn, qr, kv, f_ptr_d, f_ind_d, sc, o_f, l_f, stream=stream)
+
+    # each variant captured once in a CUDA graph (no host work between its
+    # launches), replayed back to back
+    res = {}
+    cap = torch.cuda.Stream(device=dev)
+    for name, fn in (("cascade", cascade), ("flat", flat)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                fn(stream=cap)
+        torch.cuda.current_stream().wait_stream(cap)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        n = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name + "_us"] = e0.elapsed_time(e1) * 1e3 / n
+        del g
+    for d in (dec_p, dec_s, dec_f):
+        if d.check() != 0:
+            raise RuntimeError("device status after cascade")
+    diff = (out - o_f).abs().max().item()
+    res.update({"prefix_rows": Lp, "requests": Bn, "requests_per_prefix_pass": group,
+                "max_abs_diff_cascade_vs_flat": diff,
+                "note": "shared prefix of 4096 rows in front of each context; cascade = prefix pass with the query "
+                        "rows of 128 // H requests as one pseudo-request's heads + suffix pass + mla_merge_two_states; "
+                        "CUDA-graph replays; L2 not flushed (the prefix rows are reused by design)"})
+    return res
+
+
 def run_ours(args, batch, world, rank, local, pg):
     import numpy as np
     import torch
@@ -551,6 +643,7 @@ def run_ours(args, batch, world, rank, local, pg):
 
     head_products = time_head_products(batch, dev, peaks)
     multi_query = time_multi_query(batch, dev, peaks, kv, indptr_d, indices_d)
+    cascade = time_cascade(batch, dev, peaks)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -568,6 +661,7 @@ def run_ours(args, batch, world, rank, local, pg):
         "roofline": roof,
         "head_products": head_products,
         "multi_query": multi_query,
+        "cascade": cascade,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "includes": "mla_decode_step_host: host plan + pinned H2D (q, indptr, indices, plan) + kernels + D2H "
