@@ -38,18 +38,26 @@ Sources, by page and section:
   * "[sglang] EAGLE 트리 검증 어텐션 최적화", section "들어가며": draft tokens
     verified in one pass, each attending to the shared prefix and its
     ancestors -- ``decode_attention_multi_query`` (chain-shaped drafts).
+  * "MLA and torch.compile", section "MLA: starting from a 439-line commit"
+    (FP8 KV cache; FP8 tensors are float8_e4m3fn) and "实现差距", section 2.4
+    (FP8 packing of new rows) -- ``e4m3_to_f64``, ``f32_to_e4m3``,
+    ``quantize_rows_e4m3``, ``decode_attention_fp8``, ``append_rows_fp8``.
 
 Pins (tests/test_oracle_pins.py, CPU only): the absorption identity against a
 decompressed multi-head attention evaluated with scipy's softmax; brute-force
 closed forms for 1-3 tokens; split-and-merge equals the unsplit result;
 invariance under relabelling cache slots; all-equal rows and q = 0 closed
-forms; the MAC counts printed in exercise 1 (tests/golden/).  Every function
-here is pinned by at least one of them.
+forms; the MAC counts printed in exercise 1 (tests/golden/); the E4M3 code
+table and rounding against torch's float8_e4m3fn conversions plus closed-form
+codes, ties and saturation; FP8 decode against the bf16 decode of the same
+(exactly representable) values.  Every function here is pinned by at least
+one of them.
 
 Readings taken where the pages are silent: the rope key sits at columns
 [512, 576) of a row; the LSE is natural-log and of the scaled scores; an empty
 request gives out = 0 and lse = -inf; merging skips partials whose lse is -inf;
-a slot named twice in one request counts twice.
+a slot named twice in one request counts twice; an FP8 cache holds E4M3
+codes with one float32 scale for the whole cache.
 """
 from __future__ import annotations
 
@@ -266,6 +274,88 @@ def append_rows(kv_cache_bits: np.ndarray, slots: np.ndarray, rows_bits: np.ndar
     idx = np.asarray(slots, dtype=np.int64)
     assert len(set(idx.tolist())) == idx.shape[0], "slots must be distinct"
     out[idx] = np.asarray(rows_bits)
+    return out
+
+
+# ------------------------------------------------------------ FP8 latent cache
+# "MLA and torch.compile: v0.3's two sources", section "MLA: starting from a
+# 439-line commit": an FP8 KV cache is one of the four parts of the 3-7x, and
+# the same section's FP8 weights are torch.float8_e4m3fn; "实现差距：MLA 与
+# DeepSeek V3", section 2.4: the V2 kernel packs new rows into an FP8 cache.
+# Reading taken (the pages give no format or scale): the cache holds E4M3
+# codes (the "fn" variant -- no infinities, largest finite 448), one byte per
+# value, 576 per row; a row value is code value x kv_scale, one float32 scale
+# for the whole cache.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact value of E4M3 codes (uint8): sign bit 7, exponent bits 3-6 with
+    bias 7, mantissa bits 0-2; exponent field 0 is subnormal (m/8 x 2^-6);
+    0x7F and 0xFF are NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    return np.where((c & 0x7F) == 0x7F, np.nan, sign * mag)
+
+
+def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to E4M3 codes: to the nearest finite value, a tie
+    to the code with an even last bit, magnitudes from 448 up (infinity too)
+    to 448, NaN to 0x7F; the sign is kept (a value that rounds to zero gives
+    +0 or -0).  Found by search over the 127 non-negative finite values."""
+    xf = np.asarray(x, dtype=np.float32)
+    a = np.abs(xf.astype(np.float64))
+    grid = e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))          # codes 0..0x7E: 0 .. 448, increasing
+    i = np.clip(np.searchsorted(grid, a, side="right") - 1, 0, 0x7E)
+    j = np.minimum(i + 1, 0x7E)
+    d_lo, d_hi = a - grid[i], grid[j] - a
+    up = (j > i) & ((d_hi < d_lo) | ((d_hi == d_lo) & (i % 2 == 1)))
+    code = np.where(up, j, i)
+    code = np.where(a >= E4M3_MAX, 0x7E, code)
+    code = code | np.where(np.signbit(xf), 0x80, 0)
+    return np.where(np.isnan(xf), 0x7F, code).astype(np.uint8)
+
+
+def quantize_rows_e4m3(rows_bits: np.ndarray, kv_scale: float) -> np.ndarray:
+    """FP8 codes of bf16 cache rows: each value divided by the cache scale in
+    float32 (one IEEE division, correctly rounded), then rounded to E4M3."""
+    x = bf16_bits_to_f64(rows_bits).astype(np.float32)             # exact
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        y = x / np.float32(kv_scale)
+    return f32_to_e4m3(y)
+
+
+def decode_attention_fp8(q_nope_bits, q_rope_bits, kv_codes, kv_scale, kv_indptr, kv_indices, sm_scale,
+                         requests=None):
+    """Absorbed MLA decode over an FP8 cache: every row value is its E4M3 code
+    value times kv_scale (the float32 scale widened exactly); otherwise the
+    same definition as ``decode_attention`` (the bf16 query is used as is)."""
+    qn = np.asarray(q_nope_bits)
+    qr = np.asarray(q_rope_bits)
+    B, H = qn.shape[0], qn.shape[1]
+    scale = float(np.float32(kv_scale))
+    out = np.full((B, H, KV_LORA_RANK), np.nan)
+    lse = np.full((B, H), np.nan)
+    todo = range(B) if requests is None else requests
+    for b in todo:
+        idx = np.asarray(kv_indices[int(kv_indptr[b]):int(kv_indptr[b + 1])], dtype=np.int64)
+        rows = e4m3_to_f64(np.asarray(kv_codes)[idx]) * scale
+        o, l = partial_state(bf16_bits_to_f64(qn[b]), bf16_bits_to_f64(qr[b]), rows, sm_scale)
+        out[b], lse[b] = o, l
+    return out, lse
+
+
+def append_rows_fp8(kv_codes: np.ndarray, slots: np.ndarray, rows_bits: np.ndarray, kv_scale: float) -> np.ndarray:
+    """The FP8 cache after a decode step's append: slot slots[b] receives the
+    codes of bf16 row b (``quantize_rows_e4m3``); every other row is unchanged."""
+    out = np.array(kv_codes, copy=True)
+    idx = np.asarray(slots, dtype=np.int64)
+    assert len(set(idx.tolist())) == idx.shape[0], "slots must be distinct"
+    out[idx] = quantize_rows_e4m3(rows_bits, kv_scale)
     return out
 
 

@@ -366,3 +366,102 @@ def test_planted_merge_mistake_is_caught(monkeypatch):
         with pytest.raises(AssertionError):
             test_split_merge_equals_unsplit(seed)
     monkeypatch.setattr(O, "merge_states", real)
+
+
+# ------------------------------------------------------------ FP8 latent cache
+
+def _torch_e4m3_values(codes):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def test_e4m3_code_table_matches_torch_and_closed_forms():
+    pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    v, t = O.e4m3_to_f64(codes), _torch_e4m3_values(codes)
+    assert np.array_equal(np.isnan(v), np.isnan(t)) and np.isnan(v).sum() == 2
+    assert np.array_equal(v[~np.isnan(v)], t[~np.isnan(t)])
+    # closed forms of the format: smallest subnormal, largest subnormal, smallest normal, one, largest finite
+    for code, val in ((0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9), (0x08, 2.0 ** -6), (0x38, 1.0), (0x7E, 448.0),
+                      (0xFE, -448.0), (0x80, 0.0)):
+        assert O.e4m3_to_f64(np.array([code], np.uint8))[0] == val
+
+
+def test_e4m3_rounding_matches_torch_in_range():
+    pytest.importorskip("torch")
+    import torch
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal(100000) * np.exp2(rng.uniform(-14, 9, 100000))).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.f32_to_e4m3(x), want)
+
+
+def test_e4m3_ties_go_to_the_even_code_and_large_values_saturate():
+    grid = O.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)       # every midpoint is exact in float32
+    assert np.array_equal(mids.astype(np.float64), (grid[:-1] + grid[1:]) / 2)
+    lo = np.arange(0x7E)
+    want = np.where(lo % 2 == 0, lo, lo + 1)
+    assert np.array_equal(O.f32_to_e4m3(mids), want.astype(np.uint8))
+    assert np.array_equal(O.f32_to_e4m3(-mids), (want | 0x80).astype(np.uint8))
+    big = np.array([448.0, 449.0, 463.9, 464.0, 1e6, np.inf, -1e30, -np.inf], np.float32)
+    assert np.array_equal(O.f32_to_e4m3(big), np.array([0x7E] * 6 + [0xFE] * 2, np.uint8))
+    assert O.f32_to_e4m3(np.array([np.nan], np.float32))[0] == 0x7F
+    # below half the smallest subnormal: signed zero; just above: the smallest subnormal
+    tiny = np.array([2.0 ** -11, -2.0 ** -11, 2.0 ** -10, 2.0 ** -10 * 1.0001], np.float32)
+    assert np.array_equal(O.f32_to_e4m3(tiny), np.array([0x00, 0x80, 0x00, 0x01], np.uint8))
+    # every finite code survives a round trip
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    assert np.array_equal(O.f32_to_e4m3(O.e4m3_to_f64(codes).astype(np.float32)), codes)
+
+
+def test_quantize_rows_divides_by_the_scale_then_rounds():
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    rng = np.random.default_rng(9)
+    codes = rng.integers(0, 256, size=(6, 576)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x42
+    for scale in (1.0, 2.0 ** -5, 8.0):
+        vals = O.e4m3_to_f64(codes) * scale                       # exact in bf16 for these scales
+        bits = W.f32_to_bf16_bits(vals.astype(np.float32))
+        assert np.array_equal(O.bf16_bits_to_f64(bits), vals)
+        assert np.array_equal(O.quantize_rows_e4m3(bits, scale), codes)
+    # the rounding sees the quotient: 1.0625 / 0.5 = 2.125 and 1.1875 / 0.5 = 2.375 are ties between codes
+    # 0x40 = 2.0 / 0x41 = 2.25 and 0x41 / 0x42 = 2.5, so both go to the even code; 1.125 / 0.5 = 2.25 is exact
+    one = W.f32_to_bf16_bits(np.array([1.0625, 1.1875, 1.125], np.float32))
+    assert np.array_equal(O.quantize_rows_e4m3(one, 0.5), np.array([0x40, 0x42, 0x41], np.uint8))
+
+
+def test_fp8_decode_equals_bf16_decode_of_the_same_values():
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    rng = np.random.default_rng(10)
+    pool, H = 300, 4
+    codes = O.f32_to_e4m3((rng.standard_normal((pool, 576)) * 16).astype(np.float32))
+    lengths = [0, 1, 7, 120]
+    indptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    indices = rng.permutation(pool)[:indptr[-1]].astype(np.int32)
+    qn = W.f32_to_bf16_bits(rng.standard_normal((4, H, 512)).astype(np.float32))
+    qr = W.f32_to_bf16_bits(rng.standard_normal((4, H, 64)).astype(np.float32))
+    for scale in (1.0, 2.0 ** -5):
+        bits = W.f32_to_bf16_bits((O.e4m3_to_f64(codes) * scale).astype(np.float32))
+        ro, rl = O.decode_attention(qn, qr, bits, indptr, indices, SM)
+        fo, fl = O.decode_attention_fp8(qn, qr, codes, scale, indptr, indices, SM)
+        assert np.array_equal(ro, fo) and np.array_equal(rl, fl)
+    # a scale is not a no-op: doubling it changes the scores
+    fo2, _ = O.decode_attention_fp8(qn, qr, codes, 2.0 ** -4, indptr, indices, SM)
+    assert not np.allclose(fo2[3], fo[3])
+
+
+def test_fp8_append_touches_only_its_slots():
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    rng = np.random.default_rng(11)
+    cache = rng.integers(0, 0x7E, size=(50, 576)).astype(np.uint8)
+    rows = W.f32_to_bf16_bits(rng.standard_normal((3, 576)).astype(np.float32))
+    slots = np.array([4, 17, 0], np.int32)
+    after = O.append_rows_fp8(cache, slots, rows, 2.0 ** -5)
+    keep = np.setdiff1d(np.arange(50), slots)
+    assert np.array_equal(after[keep], cache[keep])
+    assert np.array_equal(after[slots], O.quantize_rows_e4m3(rows, 2.0 ** -5))
+    back = O.e4m3_to_f64(after[slots]) * 2.0 ** -5
+    assert np.all(np.abs(back - O.bf16_bits_to_f64(rows)) <= np.abs(O.bf16_bits_to_f64(rows)) / 16 + 2.0 ** -15)
