@@ -448,6 +448,69 @@ def time_cascade(batch, dev, peaks):
     return res
 
 
+def time_fp8(batch, dev, peaks, step_us_bf16, indptr_d, indices_d):
+    """The same decode over an FP8 (E4M3) copy of the cache (mla_decode_run_fp8:
+    query prep, decode, merge), H <= 32 only.  Synthetic codes with kv_scale
+    2^-5; R pool copies whose touched bytes exceed 4x L2 are rotated inside one
+    captured CUDA graph, replayed after warm-up."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding, workloads as W
+    Bn, H = batch.batch, batch.heads
+    if H > 32:
+        return None
+    spec_seed = 20261200 + 80 + (batch.spec.number if batch.spec else 0)
+    codes = torch.from_numpy(W.make_fp8_cache(batch.pool, spec_seed)).to(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(4 * l2 / (batch.nnz * 576)) + 1)
+    kvs = [codes] + [codes.clone() for _ in range(R - 1)]
+    plan, _ = binding.decode_plan(batch.kv_indptr, H)
+    plan_d = torch.from_numpy(plan).to(dev)
+    ws = torch.zeros(binding.decode_fp8_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    qn = torch.from_numpy(np.ascontiguousarray(batch.q_nope).view(np.int16)).view(torch.bfloat16).to(dev)
+    qr = torch.from_numpy(np.ascontiguousarray(batch.q_rope).view(np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty((Bn, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((Bn, H), dtype=torch.float32, device=dev)
+    run = lambda k, stream=None: binding.decode_run_fp8(plan, plan_d, qn, qr, kvs[k % R], W.FP8_KV_SCALE, indptr_d,
+                                                         indices_d, batch.sm_scale, out, lse, ws, stream=stream)
+    for k in range(3):
+        run(k)
+    torch.cuda.synchronize()
+    st = binding.check_errors(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after the FP8 decode: {binding.status_string(st)}")
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for k in range(R):
+                run(k, stream=cap)
+    torch.cuda.current_stream().wait_stream(cap)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(3, math.ceil(60 / R))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    st = binding.check_errors(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after the FP8 decode: {binding.status_string(st)}")
+    us = e0.elapsed_time(e1) * 1e3 / (reps * R)
+    bytes_alg = batch.nnz * 576 + batch.nnz * 4 + Bn * H * (576 * 2 + 512 * 4 + 4) + (Bn + 1) * 4
+    t = bytes_alg / (peaks["hbm_gbs"] * 1e9) * 1e6
+    del kvs, g
+    return {"us": us, "roofline_us": t, "frac": t / us, "bound": "hbm", "algorithmic_bytes": bytes_alg,
+            "latent_kv_gbs": batch.nnz * 576 / (us * 1e-6) / 1e9, "speedup_vs_bf16_step": step_us_bf16 / us,
+            "kv_scale": W.FP8_KV_SCALE,
+            "note": "FP8 (E4M3) cache, one byte per value; query prep + decode (tcgen05 kind::f8f6f4) + merge per "
+                    "step; synthetic codes; R KV copies > 4x L2 rotated inside one CUDA graph"}
+
+
 def run_ours(args, batch, world, rank, local, pg):
     import numpy as np
     import torch
@@ -644,6 +707,7 @@ def run_ours(args, batch, world, rank, local, pg):
     head_products = time_head_products(batch, dev, peaks)
     multi_query = time_multi_query(batch, dev, peaks, kv, indptr_d, indices_d)
     cascade = time_cascade(batch, dev, peaks)
+    fp8 = time_fp8(batch, dev, peaks, ms * 1e3, indptr_d, indices_d)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -662,6 +726,7 @@ def run_ours(args, batch, world, rank, local, pg):
         "head_products": head_products,
         "multi_query": multi_query,
         "cascade": cascade,
+        "fp8_cache": fp8,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "includes": "mla_decode_step_host: host plan + pinned H2D (q, indptr, indices, plan) + kernels + D2H "

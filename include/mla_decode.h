@@ -320,6 +320,59 @@ int mla_project_output(const void* o_lat, const void* w_vc, void* out, int32_t o
 int mla_append_kv(void* kv_cache, int64_t num_slots, const int32_t* slots, const void* rows, int32_t batch,
                   void* workspace, void* stream);
 
+/* ---- FP8 latent cache ----------------------------------------------------
+ * "MLA and torch.compile: v0.3's two sources", section "MLA: starting from a
+ * 439-line commit": an FP8 KV cache is one of the four parts of the 3-7x
+ * (the page's FP8 tensors are float8_e4m3fn); "实现差距：MLA 与 DeepSeek V3",
+ * section 2.4: new rows are packed into the FP8 cache.  Format taken here:
+ * one E4M3 code (OCP "fn" variant: no infinities, largest finite 448) per
+ * value, 576 bytes per row (latent 0-511, rope key 512-575), and one float32
+ * kv_scale for the whole cache: value = code value x kv_scale. */
+
+/* mla_decode_fp8_workspace_bytes -- host.  Workspace mla_decode_run_fp8 needs
+ * for `plan`: the plan's own workspace plus the per-request query images
+ * (4 x H x 288 bytes) and per-head factors (H floats).
+ * Errors: MLA_ERR_INVALID_ARG for a bad plan or null result pointer;
+ * MLA_ERR_UNSUPPORTED unless the plan's H is 16 or 32. */
+int mla_decode_fp8_workspace_bytes(const int32_t* plan_host, size_t* workspace_bytes);
+
+/* mla_decode_run_fp8 -- asynchronous on `stream`.
+ *
+ * mla_decode_run over an FP8 cache: the same out / lse as the bf16 decode of
+ * the cache values (code value x kv_scale), with the bf16 query used as is.
+ * H must be 16 or 32 (the plan's H); other H give MLA_ERR_UNSUPPORTED.
+ *
+ *   kv_cache   device uint8 [num_slots, 576] E4M3 codes.
+ *   kv_scale   finite, > 0.
+ *   workspace  at least mla_decode_fp8_workspace_bytes(plan) bytes, 16-byte
+ *              aligned, zero-filled before first use (status word as for
+ *              mla_decode_run; the query images are rewritten every call, so
+ *              calls sharing a workspace must not overlap on the GPU).
+ *   all other arguments as for mla_decode_run.
+ * Launches a query-prep kernel (each request's query split into two E4M3
+ * parts hi + lo/32 after a per-head power-of-two scaling), the decode kernel
+ * as its programmatic dependent, and the plan's merge.
+ * Errors as for mla_decode_run; nothing is launched on an argument error. */
+int mla_decode_run_fp8(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope, const void* q_rope,
+                       const void* kv_cache, int64_t num_slots, float kv_scale, const int32_t* kv_indptr,
+                       const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* mla_append_kv_fp8 -- asynchronous on `stream`.
+ *
+ * mla_append_kv into an FP8 cache: the codes of rows[b] go to slot slots[b],
+ * each value divided by kv_scale in float32 (IEEE division) and rounded to
+ * the nearest E4M3 value (ties to the even code, magnitudes past 448 to 448).
+ *
+ *   kv_cache   device uint8 [num_slots, 576], written in place.
+ *   rows       device bf16 [batch, 576].
+ *   kv_scale   finite, > 0.
+ *   slots, workspace as for mla_append_kv.
+ * Errors: MLA_ERR_INVALID_ARG for null or non-16-byte-aligned pointers,
+ * batch < 0, num_slots < 1 or a bad kv_scale; nothing is launched then. */
+int mla_append_kv_fp8(void* kv_cache, int64_t num_slots, const int32_t* slots, const void* rows, int32_t batch,
+                      float kv_scale, void* workspace, void* stream);
+
 /* mla_check_errors -- synchronises `stream`, reads the workspace status word,
  * clears it, and returns it (MLA_OK when the kernels found nothing wrong), or
  * MLA_ERR_CUDA if the stream reports a CUDA error. */

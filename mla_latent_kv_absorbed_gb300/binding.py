@@ -25,7 +25,7 @@ EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decod
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
            "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query",
-           "mla_merge_two_states")
+           "mla_merge_two_states", "mla_decode_fp8_workspace_bytes", "mla_decode_run_fp8", "mla_append_kv_fp8")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -72,6 +72,13 @@ _lib.mla_decode_step_host.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int32, ctypes
                                       ctypes.c_size_t, _vp, ctypes.c_size_t, _vp, _vp, _vp]
 _lib.mla_append_kv.restype = ctypes.c_int
 _lib.mla_append_kv.argtypes = [_vp, ctypes.c_int64, _vp, _vp, ctypes.c_int32, _vp, _vp]
+_lib.mla_decode_fp8_workspace_bytes.restype = ctypes.c_int
+_lib.mla_decode_fp8_workspace_bytes.argtypes = [_vp, _c_szp]
+_lib.mla_decode_run_fp8.restype = ctypes.c_int
+_lib.mla_decode_run_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_float, _vp, _vp,
+                                    ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.mla_append_kv_fp8.restype = ctypes.c_int
+_lib.mla_append_kv_fp8.argtypes = [_vp, ctypes.c_int64, _vp, _vp, ctypes.c_int32, ctypes.c_float, _vp, _vp]
 _lib.mla_project_output.restype = ctypes.c_int
 _lib.mla_project_output.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     _vp, _vp]
@@ -218,6 +225,38 @@ def append_kv(kv_cache, slots, rows, workspace=None, stream=None) -> None:
                             _ptr(workspace), _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_append_kv")
+
+
+def decode_fp8_workspace_bytes(plan_host) -> int:
+    """Workspace bytes mla_decode_run_fp8 needs for a plan (H 16 or 32)."""
+    plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    n = ctypes.c_size_t(0)
+    st = _lib.mla_decode_fp8_workspace_bytes(plan_host.ctypes.data, ctypes.byref(n))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_fp8_workspace_bytes")
+    return int(n.value)
+
+
+def decode_run_fp8(plan_host, plan_dev, q_nope, q_rope, kv_cache, kv_scale, kv_indptr, kv_indices, sm_scale,
+                   out, lse, workspace, stream=None) -> None:
+    """Decode over an FP8 cache: kv_cache uint8 [num_slots, 576] E4M3 codes (value = code x kv_scale);
+    other tensors as for decode_run; workspace of decode_fp8_workspace_bytes(plan) bytes, zero-filled once."""
+    out_dtype = _out_dtype(out, "mla_decode_run_fp8")
+    plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    st = _lib.mla_decode_run_fp8(plan_host.ctypes.data, _ptr(plan_dev), _ptr(q_nope), _ptr(q_rope), _ptr(kv_cache),
+                                 int(kv_cache.shape[0]), float(kv_scale), _ptr(kv_indptr), _ptr(kv_indices),
+                                 float(sm_scale), _ptr(out), out_dtype, _ptr(lse), _ptr(workspace),
+                                 int(workspace.numel() * workspace.element_size()), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_run_fp8")
+
+
+def append_kv_fp8(kv_cache, slots, rows, kv_scale, workspace=None, stream=None) -> None:
+    """kv_cache[slots[b]] = E4M3(rows[b] / kv_scale): uint8 [num_slots, 576] <- bf16 [B, 576]."""
+    st = _lib.mla_append_kv_fp8(_ptr(kv_cache), int(kv_cache.shape[0]), _ptr(slots), _ptr(rows), int(rows.shape[0]),
+                                float(kv_scale), _ptr(workspace), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_append_kv_fp8")
 
 
 def decode_run_multi_query(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale,

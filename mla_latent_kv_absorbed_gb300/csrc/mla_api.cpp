@@ -436,6 +436,116 @@ int mla_append_kv(void* kv_cache, int64_t num_slots, const int32_t* slots, const
   return launch_append(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// FP8 decode workspace: the plan's workspace, then the query images [B] and
+// the per-head factors [B, H], each 256-byte aligned.
+struct Fp8WsLayout {
+  size_t img, fac, total;
+};
+Fp8WsLayout fp8_ws_layout(const int32_t* plan_host) {
+  Fp8WsLayout l{};
+  const size_t B = static_cast<size_t>(plan_host[kHBatch]), H = static_cast<size_t>(plan_host[kHHeads]);
+  l.img = (ws_needed_bytes(plan_host) + 255) & ~size_t(255);
+  l.fac = (l.img + B * fp8_image_bytes(static_cast<int>(H)) + 255) & ~size_t(255);
+  l.total = l.fac + B * H * 4;
+  return l;
+}
+}  // namespace
+
+int mla_decode_fp8_workspace_bytes(const int32_t* plan_host, size_t* workspace_bytes) {
+  if (!plan_header_ok(plan_host) || !workspace_bytes) return MLA_ERR_INVALID_ARG;
+  if (plan_host[kHVariant] != kVariantSwab) return MLA_ERR_UNSUPPORTED;
+  *workspace_bytes = fp8_ws_layout(plan_host).total;
+  return MLA_OK;
+}
+
+int mla_decode_run_fp8(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope, const void* q_rope,
+                       const void* kv_cache, int64_t num_slots, float kv_scale, const int32_t* kv_indptr,
+                       const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan_header_ok(plan_host) || !plan_dev) return MLA_ERR_INVALID_ARG;
+  if (plan_host[kHVariant] != kVariantSwab) return MLA_ERR_UNSUPPORTED;
+  if (out_dtype != 0 && out_dtype != 1) return MLA_ERR_UNSUPPORTED;
+  if (!std::isfinite(sm_scale) || !std::isfinite(kv_scale) || !(kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  const Fp8WsLayout wl = fp8_ws_layout(plan_host);
+  if (!workspace || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < wl.total) return MLA_ERR_WORKSPACE;
+  const int B = plan_host[kHBatch], H = plan_host[kHHeads];
+  if (B == 0 || plan_host[kHItems] == 0)
+    return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
+  if (!q_nope || !q_rope || !kv_cache || !kv_indptr || !kv_indices || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(kv_cache) || !aligned16(out) ||
+      !aligned16(kv_indices) || (lse && !aligned16(lse)))
+    return MLA_ERR_INVALID_ARG;
+  if (num_slots < 1 || num_slots > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p{};
+  p.plan = plan_dev;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.kv_cache = static_cast<const uint8_t*>(kv_cache);
+  p.out = out;
+  p.lse = lse;
+  p.part_o = reinterpret_cast<float*>(ws + ws_part_o_offset());
+  p.part_lse = reinterpret_cast<float*>(ws + ws_part_lse_offset(plan_host));
+  p.status = reinterpret_cast<int*>(ws);
+  p.num_slots = num_slots;
+  p.batch = B;
+  p.heads = H;
+  p.out_bf16 = out_dtype;
+  p.items_off = plan_items_off(plan_host);
+  p.num_workers = plan_host[kHWorkers];
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.q_len = 1;
+  Fp8Params p8{};
+  p8.img = ws + wl.img;
+  p8.fac = reinterpret_cast<const float*>(ws + wl.fac);
+  p8.kv_scale = kv_scale;
+  Fp8PrepParams pp{};
+  pp.q_nope = static_cast<const uint16_t*>(q_nope);
+  pp.q_rope = static_cast<const uint16_t*>(q_rope);
+  pp.img = ws + wl.img;
+  pp.fac = reinterpret_cast<float*>(ws + wl.fac);
+  pp.rows = B * H;
+  // 8-bit maps over the cache: 128-byte latent boxes and 32-byte rope boxes
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  CUtensorMap tm_lat, tm_rope;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(num_slots)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRow)};
+  cuuint32_t box_lat[2] = {128, 1}, box_rope[2] = {32, 1}, estr[2] = {1, 1};
+  if (fn(&tm_lat, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv_cache), dims, strides, box_lat, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      fn(&tm_rope, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv_cache), dims, strides, box_rope, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLA_ERR_CUDA;
+  const int rc = launch_swab8(H, tm_lat, tm_rope, p, p8, pp, plan_host[kHWorkers], st);
+  if (rc != MLA_OK) return rc;
+  return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_append_kv_fp8(void* kv_cache, int64_t num_slots, const int32_t* slots, const void* rows, int32_t batch,
+                      float kv_scale, void* workspace, void* stream) {
+  if (batch < 0 || num_slots < 1 || !std::isfinite(kv_scale) || !(kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!kv_cache || !slots || !rows || !aligned16(kv_cache) || !aligned16(rows) || (workspace && !aligned16(workspace)))
+    return MLA_ERR_INVALID_ARG;
+  AppendFp8Params p{};
+  p.kv_cache = static_cast<uint8_t*>(kv_cache);
+  p.src = static_cast<const uint16_t*>(rows);
+  p.slots = slots;
+  p.status = static_cast<int*>(workspace);
+  p.num_slots = num_slots;
+  p.rows = batch;
+  p.kv_scale = kv_scale;
+  return launch_append_fp8(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mla_check_errors(void* workspace, void* stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

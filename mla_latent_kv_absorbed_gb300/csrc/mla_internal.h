@@ -87,4 +87,31 @@ struct AppendParams {
   int rows;
 };
 
+// FP8 cache decode: the prep kernel's outputs, read by the decode kernel.
+struct Fp8Params {
+  const uint8_t* img;         // [B] query images (4H x 288 bytes each)
+  const float* fac;           // [B, H] per-head factors 2^-a
+  float kv_scale;             // cache value = E4M3 code value x kv_scale
+};
+
+// FP8 query prep: bf16 q_nope / q_rope -> query images and factors.
+struct Fp8PrepParams {
+  const uint16_t* q_nope;     // [B, H, 512] bf16
+  const uint16_t* q_rope;     // [B, H, 64] bf16
+  uint8_t* img;               // [B] images
+  float* fac;                 // [B, H]
+  int rows;                   // B * H
+};
+
+// FP8 cache append: rows [rows, 576] bf16 -> E4M3 codes of value / kv_scale.
+struct AppendFp8Params {
+  uint8_t* kv_cache;          // [num_slots, 576] E4M3
+  const uint16_t* src;        // [rows, 576] bf16
+  const int32_t* slots;       // [rows]
+  int* status;                // status word, or null
+  long long num_slots;
+  int rows;
+  float kv_scale;
+};
+
 }  // namespace mla

@@ -36,4 +36,16 @@ int launch_merge_two(const float* o_a, const float* l_a, const float* o_b, const
 // Cache append of a step's new rows.
 int launch_append(const AppendParams& p, cudaStream_t stream);
 
+// FP8-cache decode for H in {16, 32}: the query prep kernel, then the decode
+// kernel as its programmatic dependent; grid = plan workers.  tm_lat: uint8
+// [num_slots, 576], box {128, 1}, 128-B swizzle; tm_rope: box {32, 1}, 32-B swizzle.
+int launch_swab8(int heads, const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const DecodeParams& p,
+                 const Fp8Params& p8, const Fp8PrepParams& pp, int grid, cudaStream_t stream);
+
+// Bytes of one request's query image for the FP8 decode.
+size_t fp8_image_bytes(int heads);
+
+// FP8 cache append (quantises bf16 rows).
+int launch_append_fp8(const AppendFp8Params& p, cudaStream_t stream);
+
 }  // namespace mla

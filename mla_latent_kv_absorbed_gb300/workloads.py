@@ -184,3 +184,26 @@ def make_head_product_inputs(batch: int, heads: int, seed: int) -> HeadProductIn
     w_kc = f32_to_bf16_bits(rng.standard_normal((heads, 128, 512), dtype=np.float32) / np.float32(math.sqrt(128)))
     w_vc = f32_to_bf16_bits(rng.standard_normal((heads, 512, 128), dtype=np.float32) / np.float32(math.sqrt(512)))
     return HeadProductInputs(q_pre=q_pre, w_kc=w_kc, w_vc=w_vc)
+
+
+FP8_KV_SCALE = 2.0 ** -5   # cache scale of the synthetic FP8 caches: values about N(0, 1)
+
+
+def make_fp8_cache(pool: int, seed: int) -> np.ndarray:
+    """Synthetic FP8 (E4M3) cache [pool, 576] uint8, built from its bit fields:
+    a draw x ~ N(0, 1) * 32 gives the sign and the exponent field
+    clip(floor(log2 |x|) + 7, 0, 15); the mantissa field is uniform.  With
+    FP8_KV_SCALE the values are then roughly N(0, 1).  The NaN code is
+    replaced by the largest finite one."""
+    rng = np.random.default_rng(seed)
+    out = np.empty((pool, 576), dtype=np.uint8)
+    for r0 in range(0, pool, _GEN_ROWS):
+        r1 = min(pool, r0 + _GEN_ROWS)
+        x = rng.standard_normal((r1 - r0, 576), dtype=np.float32) * 32.0
+        m = rng.integers(0, 8, size=x.shape, dtype=np.uint8)
+        with np.errstate(divide="ignore"):
+            e = np.clip(np.floor(np.log2(np.abs(x))) + 7, 0, 15).astype(np.uint8)
+        code = (e << 3) | m
+        code = np.where(code == 0x7F, 0x7E, code).astype(np.uint8)
+        out[r0:r1] = code | np.where(x < 0, 0x80, 0).astype(np.uint8)
+    return out

@@ -180,3 +180,34 @@ def test_merge_two_rejects_bad_arguments(B):
     assert lib.mla_merge_two_states(None, fake, fake, fake, 4, fake, 0, None, None) == 1
     assert lib.mla_merge_two_states(fake + 4, fake, fake, fake, 4, fake, 0, None, None) == 1
     assert lib.mla_merge_two_states(None, None, None, None, 0, None, 0, None, None) == 0
+
+
+def test_fp8_entry_points_reject_bad_arguments(B):
+    lib = B.library()
+    fake = 1 << 20
+    plan, ws_bytes = B.decode_plan(np.array([0, 100, 300], dtype=np.int32), 16, num_sms=152)
+    need = B.decode_fp8_workspace_bytes(plan)
+    # plan workspace + two 18 KB query images + 2 x 16 factors, 256-byte aligned regions
+    assert need >= ws_bytes + 2 * 4 * 16 * 288 + 2 * 16 * 4
+    plan128, _ = B.decode_plan(np.array([0, 100], dtype=np.int32), 128, num_sms=152)
+    n = ctypes.c_size_t(0)
+    assert lib.mla_decode_fp8_workspace_bytes(np.ascontiguousarray(plan128).ctypes.data, ctypes.byref(n)) == 2
+    assert lib.mla_decode_fp8_workspace_bytes(None, ctypes.byref(n)) == 1
+
+    def run(plan_host=plan, kv_scale=0.03125, ws=fake, wsb=need, out_dtype=0, q=fake, slots=1000, scale=0.1):
+        ph = np.ascontiguousarray(plan_host, dtype=np.int32)
+        return lib.mla_decode_run_fp8(ph.ctypes.data, fake, q, fake, fake, slots, ctypes.c_float(kv_scale), fake,
+                                      fake, ctypes.c_float(scale), fake, out_dtype, fake, ws, wsb, None)
+
+    assert run(plan_host=plan128) == 2                   # only H = 16 or 32
+    assert run(kv_scale=0.0) == 1 and run(kv_scale=-1.0) == 1 and run(kv_scale=float("inf")) == 1
+    assert run(scale=float("nan")) == 1
+    assert run(out_dtype=2) == 2
+    assert run(wsb=need - 1) == 3                        # the plan's workspace alone is not enough
+    assert run(ws=fake + 8) == 1
+    assert run(q=fake + 2) == 1
+    assert run(slots=0) == 1
+    assert lib.mla_append_kv_fp8(fake, 100, fake, fake, 2, ctypes.c_float(0.0), None, None) == 1
+    assert lib.mla_append_kv_fp8(fake, 100, fake, fake, -1, ctypes.c_float(1.0), None, None) == 1
+    assert lib.mla_append_kv_fp8(fake + 4, 100, fake, fake, 2, ctypes.c_float(1.0), None, None) == 1
+    assert lib.mla_append_kv_fp8(None, 100, None, None, 0, ctypes.c_float(1.0), None, None) == 0
