@@ -76,12 +76,14 @@ int mla_abi_version(void);
  *   workspace_bytes    out: device workspace bytes mla_decode_run needs for this
  *                      plan (fp32 partial states plus a 256-byte status header).
  *
- * Rule: tiles of T = 64 tokens; W workers =
- * SMs (H <= 32) or SMs/2; candidate chunk sizes ceil(ceil(total_tiles/W)/k)
- * for k = 1..8; requests cut into chunks; chunks placed longest-first on the
- * least-loaded worker; the candidate with the smallest makespan (plus a fixed
- * merge cost if any request is cut) wins.  Requests left whole are written
- * straight to out/lse; cut or empty requests go through the LSE merge.
+ * Rule: tiles of T = 64 tokens; W workers = SMs (H <= 32) or SMs/2; a piece
+ * of n tokens costs its whole tiles plus 32 tokens (its epilogue); requests,
+ * in order, are poured into workers 0, 1, ... each up to a load budget, so a
+ * request is cut only where a worker is full and only at a tile boundary of
+ * the request (no cut piece shorter than 64 tokens); the budget starts at the
+ * balanced share and grows in steps of 8 tokens until W workers suffice.
+ * Requests left whole are written straight to out/lse; cut or empty requests
+ * go through the LSE merge.
  *
  * Returns MLA_OK, MLA_ERR_INVALID_ARG (malformed kv_indptr, negative batch),
  * MLA_ERR_UNSUPPORTED (head count), MLA_ERR_WORKSPACE (plan too small; sizes
@@ -319,6 +321,52 @@ int mla_project_output(const void* o_lat, const void* w_vc, void* out, int32_t o
  * batch < 0 or num_slots < 1; nothing is launched then. */
 int mla_append_kv(void* kv_cache, int64_t num_slots, const int32_t* slots, const void* rows, int32_t batch,
                   void* workspace, void* stream);
+
+/* ---- decode with a device-only plan (CUDA-graph replays) -------------------
+ * "Attention backends", paragraphs "Paged, ragged batches" and "The
+ * interface": for decode the CSR arrays live in buffers sized for the largest
+ * captured batch, so a captured graph replays kernels whose inputs change
+ * every step; before each replay the runner writes the new plan into those
+ * buffers.  mla_decode_run bakes the host plan's merge count and partial
+ * layout into its launches; this variant reads everything that changes from
+ * the device plan, so one capture serves every plan built for the same
+ * (max_batch, num_heads, num_sms). */
+
+/* mla_decode_graph_sizes -- host.  Capacities for plans of up to max_batch
+ * requests: *plan_words (int32 words of the device plan buffer) and
+ * *workspace_bytes (status header, then room for max_batch + W - 1 partial
+ * states, W = the plan's workers).  Any plan mla_decode_plan builds for
+ * batch <= max_batch with the same num_heads and num_sms fits.
+ * Errors: MLA_ERR_INVALID_ARG for max_batch < 1 or num_sms < 1;
+ * MLA_ERR_UNSUPPORTED for an unsupported num_heads. */
+int mla_decode_graph_sizes(int32_t max_batch, int32_t num_heads, int32_t num_sms, size_t* plan_words,
+                           size_t* workspace_bytes);
+
+/* mla_decode_run_graph -- asynchronous on `stream`; capturable in a CUDA
+ * graph and replayable after the buffers' contents change.
+ *
+ *   plan_dev   device int32 [plan_words]: a plan from mla_decode_plan (same
+ *              num_heads and num_sms, batch <= max_batch), copied in before
+ *              each launch or replay.  Read only on the device: the kernels
+ *              check its header (magic, version, heads, workers, batch, item
+ *              count against plan_words) and clamp its ranges; a bad plan
+ *              computes nothing and records MLA_ERR_PLAN_MISMATCH.
+ *   kv_indptr  device int32 [max_batch + 1]; entries past the plan's batch
+ *              repeat its last value.
+ *   q_nope, q_rope, out, lse: [max_batch, ...] as for mla_decode_run;
+ *              rows of requests past the plan's batch are not written.
+ *   workspace  >= the workspace_bytes of mla_decode_graph_sizes, 16-byte
+ *              aligned, zero-filled before first use.
+ *   other arguments as for mla_decode_run.
+ * Launches the decode kernel on the plan's workers and the merge kernel over
+ * max_batch possible entries (each block reads the plan's merge count).
+ * Errors: MLA_ERR_WORKSPACE when plan_words or workspace_bytes are below the
+ * capacities; otherwise as for mla_decode_run, with nothing launched. */
+int mla_decode_run_graph(const int32_t* plan_dev, size_t plan_words, int32_t max_batch, int32_t num_heads,
+                         int32_t num_sms, const void* q_nope, const void* q_rope, const void* kv_cache,
+                         int64_t num_slots, const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale,
+                         void* out, int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                         void* stream);
 
 /* ---- FP8 latent cache ----------------------------------------------------
  * "MLA and torch.compile: v0.3's two sources", section "MLA: starting from a

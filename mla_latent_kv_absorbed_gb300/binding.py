@@ -25,7 +25,8 @@ EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decod
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
            "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query",
-           "mla_merge_two_states", "mla_decode_fp8_workspace_bytes", "mla_decode_run_fp8", "mla_append_kv_fp8")
+           "mla_merge_two_states", "mla_decode_fp8_workspace_bytes", "mla_decode_run_fp8", "mla_append_kv_fp8",
+           "mla_decode_graph_sizes", "mla_decode_run_graph")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -79,6 +80,12 @@ _lib.mla_decode_run_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, cty
                                     ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
 _lib.mla_append_kv_fp8.restype = ctypes.c_int
 _lib.mla_append_kv_fp8.argtypes = [_vp, ctypes.c_int64, _vp, _vp, ctypes.c_int32, ctypes.c_float, _vp, _vp]
+_lib.mla_decode_graph_sizes.restype = ctypes.c_int
+_lib.mla_decode_graph_sizes.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _c_szp, _c_szp]
+_lib.mla_decode_run_graph.restype = ctypes.c_int
+_lib.mla_decode_run_graph.argtypes = [_vp, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp,
+                                      _vp, ctypes.c_int64, _vp, _vp, ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp,
+                                      ctypes.c_size_t, _vp]
 _lib.mla_project_output.restype = ctypes.c_int
 _lib.mla_project_output.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     _vp, _vp]
@@ -225,6 +232,29 @@ def append_kv(kv_cache, slots, rows, workspace=None, stream=None) -> None:
                             _ptr(workspace), _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_append_kv")
+
+
+def decode_graph_sizes(max_batch: int, num_heads: int, num_sms: int):
+    """(plan_words, workspace_bytes) capacities of mla_decode_run_graph."""
+    w, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = _lib.mla_decode_graph_sizes(int(max_batch), int(num_heads), int(num_sms), ctypes.byref(w), ctypes.byref(b))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_graph_sizes")
+    return int(w.value), int(b.value)
+
+
+def decode_run_graph(plan_dev, max_batch, num_heads, num_sms, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
+                     sm_scale, out, lse, workspace, stream=None) -> None:
+    """Decode reading its plan only from the device buffer plan_dev (int32, capacity words), so a captured
+    graph can be replayed after a new plan (and new CSR arrays) are copied into the same buffers."""
+    out_dtype = _out_dtype(out, "mla_decode_run_graph")
+    st = _lib.mla_decode_run_graph(_ptr(plan_dev), int(plan_dev.numel()), int(max_batch), int(num_heads),
+                                   int(num_sms), _ptr(q_nope), _ptr(q_rope), _ptr(kv_cache), int(kv_cache.shape[0]),
+                                   _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out), out_dtype,
+                                   _ptr(lse), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                   _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_run_graph")
 
 
 def decode_fp8_workspace_bytes(plan_host) -> int:

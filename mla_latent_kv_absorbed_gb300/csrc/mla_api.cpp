@@ -158,6 +158,28 @@ int mla_decode_run_multi_query(const int32_t* plan_host, const int32_t* plan_dev
 }
 
 namespace {
+// Tensor maps for the decode kernel of `variant` and its launch (grid = the
+// plan's workers); p is complete but for the maps.
+int launch_decode(const DecodeParams& p, int variant, const void* q_nope, const void* q_rope, const void* kv_cache,
+                  cudaStream_t st) {
+  const int H = p.heads;
+  CUtensorMap tm_kv, tm_qn, tm_qr;
+  const uint64_t qrows = static_cast<uint64_t>(p.batch) * H;
+  if (!make_map(&tm_kv, kv_cache, kRow, static_cast<uint64_t>(p.num_slots), 64, 1)) return MLA_ERR_CUDA;
+  if (variant == kVariantSwab) {
+    if (!make_map(&tm_qr, q_rope, kRope, qrows, 64, static_cast<uint32_t>(H)) ||
+        !make_map(&tm_qn, q_nope, kLatent, qrows, 64, static_cast<uint32_t>(H)))
+      return MLA_ERR_CUDA;
+    return launch_swab(H, tm_kv, tm_qn, tm_qr, p, p.num_workers, st);
+  }
+  // the pair kernel's CTAs each take half of the rope dims: 64-byte rows
+  CUtensorMap tm_kr;
+  if (!make_map(&tm_kr, kv_cache, kRow, static_cast<uint64_t>(p.num_slots), 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&tm_qr, q_rope, kRope, qrows, 32, static_cast<uint32_t>(H), CU_TENSOR_MAP_SWIZZLE_64B))
+    return MLA_ERR_CUDA;
+  return launch_pair(H, tm_kv, tm_kr, tm_qr, p, p.num_workers, st);
+}
+
 int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len, const void* q_nope,
                 const void* q_rope, const void* kv_cache, int64_t num_slots, const int32_t* kv_indptr,
                 const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
@@ -192,28 +214,14 @@ int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len
   p.out_bf16 = out_dtype;
   p.items_off = plan_items_off(plan_host);
   p.num_workers = plan_host[kHWorkers];
+  p.max_partials = plan_host[kHPartials];
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   // multi-query: the plan's head count is q_len x the heads of one query, and
   // only the two-CTA kernel applies the per-row causal limit
   if (q_len < 1 || H % q_len != 0) return MLA_ERR_INVALID_ARG;
   if (q_len > 1 && plan_host[kHVariant] == kVariantSwab) return MLA_ERR_UNSUPPORTED;
   p.q_len = q_len;
-
-  CUtensorMap tm_kv, tm_qn, tm_qr;
-  const uint64_t qrows = static_cast<uint64_t>(B) * H;
-  if (!make_map(&tm_kv, kv_cache, kRow, static_cast<uint64_t>(num_slots), 64, 1)) return MLA_ERR_CUDA;
-  if (plan_host[kHVariant] == kVariantSwab) {
-    if (!make_map(&tm_qr, q_rope, kRope, qrows, 64, static_cast<uint32_t>(H)) ||
-        !make_map(&tm_qn, q_nope, kLatent, qrows, 64, static_cast<uint32_t>(H)))
-      return MLA_ERR_CUDA;
-    return launch_swab(H, tm_kv, tm_qn, tm_qr, p, plan_host[kHWorkers], st);
-  }
-  // the pair kernel's CTAs each take half of the rope dims: 64-byte rows
-  CUtensorMap tm_kr;
-  if (!make_map(&tm_kr, kv_cache, kRow, static_cast<uint64_t>(num_slots), 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&tm_qr, q_rope, kRope, qrows, 32, static_cast<uint32_t>(H), CU_TENSOR_MAP_SWIZZLE_64B))
-    return MLA_ERR_CUDA;
-  return launch_pair(H, tm_kv, tm_kr, tm_qr, p, plan_host[kHWorkers], st);
+  return launch_decode(p, plan_host[kHVariant], q_nope, q_rope, kv_cache, st);
 }
 }  // namespace
 
@@ -437,6 +445,103 @@ int mla_append_kv(void* kv_cache, int64_t num_slots, const int32_t* slots, const
 }
 
 namespace {
+// Capacities of a decode whose plan is written into device buffers before
+// each CUDA-graph replay: at most max_batch requests on W workers give at
+// most max_batch + W - 1 pieces (a request is cut only where a worker is
+// full), so at most that many partial states and items and max_batch merge
+// entries.
+struct GraphSizes {
+  int variant, W;
+  long long P, words;
+  size_t ws, lse_off;
+};
+int graph_sizes(int32_t max_batch, int32_t H, int32_t num_sms, GraphSizes* g) {
+  int T = 0, cpw = 0;
+  if (max_batch < 1 || num_sms < 1) return MLA_ERR_INVALID_ARG;
+  g->variant = variant_for_heads(H, &T, &cpw);
+  if (!g->variant) return MLA_ERR_UNSUPPORTED;
+  g->W = num_sms / cpw;
+  if (g->W < 1) return MLA_ERR_INVALID_ARG;
+  g->P = static_cast<long long>(max_batch) + g->W - 1;
+  g->words = kHeaderWords + (g->W + 1ll) + 4ll * g->P + 3ll * max_batch;
+  g->lse_off = kWsHeaderBytes + static_cast<size_t>(g->P) * H * kLatent * 4;
+  g->ws = (g->lse_off + static_cast<size_t>(g->P) * H * 4 + 255) / 256 * 256;
+  if (g->words > (1ll << 31) - 1) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+}  // namespace
+
+int mla_decode_graph_sizes(int32_t max_batch, int32_t num_heads, int32_t num_sms, size_t* plan_words,
+                           size_t* workspace_bytes) {
+  GraphSizes g{};
+  const int rc = graph_sizes(max_batch, num_heads, num_sms, &g);
+  if (rc != MLA_OK) return rc;
+  if (plan_words) *plan_words = static_cast<size_t>(g.words);
+  if (workspace_bytes) *workspace_bytes = g.ws;
+  return MLA_OK;
+}
+
+int mla_decode_run_graph(const int32_t* plan_dev, size_t plan_words, int32_t max_batch, int32_t num_heads,
+                         int32_t num_sms, const void* q_nope, const void* q_rope, const void* kv_cache,
+                         int64_t num_slots, const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale,
+                         void* out, int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  GraphSizes g{};
+  const int rc0 = graph_sizes(max_batch, num_heads, num_sms, &g);
+  if (rc0 != MLA_OK) return rc0;
+  if (out_dtype != 0 && out_dtype != 1) return MLA_ERR_UNSUPPORTED;
+  if (!plan_dev || !q_nope || !q_rope || !kv_cache || !kv_indptr || !kv_indices || !out || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(kv_indices) ||
+      !aligned16(workspace) || (lse && !aligned16(lse)))
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale) || num_slots < 1 || num_slots > 0x7FFFFFFFll) return MLA_ERR_INVALID_ARG;
+  if (plan_words < static_cast<size_t>(g.words) || workspace_bytes < g.ws) return MLA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p{};
+  p.plan = plan_dev;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.kv_cache = static_cast<const uint8_t*>(kv_cache);
+  p.out = out;
+  p.lse = lse;
+  p.part_o = reinterpret_cast<float*>(ws + kWsHeaderBytes);
+  p.part_lse = reinterpret_cast<float*>(ws + g.lse_off);
+  p.status = reinterpret_cast<int*>(ws);
+  p.num_slots = num_slots;
+  p.batch = max_batch;
+  p.heads = num_heads;
+  p.out_bf16 = out_dtype;
+  p.items_off = kHeaderWords + g.W + 1;
+  p.num_workers = g.W;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.q_len = 1;
+  p.plan_cap_words = static_cast<int>(g.words);
+  p.max_partials = static_cast<int>(g.P);
+  const int rc = launch_decode(p, g.variant, q_nope, q_rope, kv_cache, st);
+  if (rc != MLA_OK) return rc;
+  MergeParams m{};
+  m.part_o = p.part_o;
+  m.part_lse = p.part_lse;
+  m.list = nullptr;
+  m.indptr = nullptr;
+  m.n_entries = max_batch;
+  m.heads = num_heads;
+  m.out = out;
+  m.out_bf16 = out_dtype;
+  m.lse = lse;
+  m.plan = plan_dev;
+  m.plan_cap_words = static_cast<int>(g.words);
+  m.batch = max_batch;
+  m.max_partials = static_cast<int>(g.P);
+  m.workers = g.W;
+  m.status = p.status;
+  return launch_merge(m, max_batch, 16, st);
+}
+
+namespace {
 // FP8 decode workspace: the plan's workspace, then the query images [B] and
 // the per-head factors [B, H], each 256-byte aligned.
 struct Fp8WsLayout {
@@ -498,6 +603,7 @@ int mla_decode_run_fp8(const int32_t* plan_host, const int32_t* plan_dev, const 
   p.out_bf16 = out_dtype;
   p.items_off = plan_items_off(plan_host);
   p.num_workers = plan_host[kHWorkers];
+  p.max_partials = plan_host[kHPartials];
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.q_len = 1;
   Fp8Params p8{};

@@ -56,6 +56,32 @@ __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// The item range [it0, it1) of worker w.  A device-only plan (graph replays:
+// the host wrote it into a fixed-capacity buffer without this call seeing
+// it) is checked here: magic, version, heads and workers must match the
+// launch, its batch must fit the buffers and its items the capacity; a bad
+// header gives no work and MLA_ERR_PLAN_MISMATCH, and the worker's range is
+// clamped to the plan's items.
+__device__ __forceinline__ void plan_items(const DecodeParams& p, int w, int& it0, int& it1) {
+  const int32_t* h = p.plan;
+  if (p.plan_cap_words <= 0) {
+    it0 = h[kHeaderWords + w];
+    it1 = h[kHeaderWords + w + 1];
+    return;
+  }
+  const int n = h[kHItems];
+  const bool good = h[kHMagic] == kPlanMagic && h[kHVersion] == kPlanVersion && h[kHHeads] == p.heads &&
+                    h[kHWorkers] == p.num_workers && h[kHBatch] >= 0 && h[kHBatch] <= p.batch && n >= 0 &&
+                    static_cast<long long>(p.items_off) + 4ll * n <= p.plan_cap_words;
+  if (!good) {
+    it0 = it1 = 0;
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+    return;
+  }
+  it0 = min(max(h[kHeaderWords + w], 0), n);
+  it1 = min(max(h[kHeaderWords + w + 1], it0), n);
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

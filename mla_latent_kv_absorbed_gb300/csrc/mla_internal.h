@@ -54,6 +54,9 @@ struct DecodeParams {
   int num_workers;
   float scale_log2;           // sm_scale * log2(e)
   int q_len;                  // queries per request (rows = q_len x heads per query); <= 1: one
+  int plan_cap_words;         // > 0: a device-only plan (graph replays) of at most this many words, checked
+                              // and clamped by the kernels; 0: a plan the host has checked
+  int max_partials;           // partial states the workspace holds; an item naming another writes nothing
 };
 
 struct MergeParams {
@@ -66,6 +69,12 @@ struct MergeParams {
   void* out;
   int out_bf16;
   float* lse;
+  const int32_t* plan;        // device-only plan: entries, list and bounds are read from it (list is null)
+  int plan_cap_words;
+  int batch;                  // requests the buffers hold
+  int max_partials;
+  int workers;                // the decode launch's workers (a device-only plan must match)
+  int* status;                // workspace status word (device-only plan), or null
 };
 
 // Per-head product C[b, h, :] = A[b, h, 0:K] . W[h] (the query absorption and

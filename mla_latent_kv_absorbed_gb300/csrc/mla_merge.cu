@@ -39,7 +39,24 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const int G = static_cast<int>(blockDim.x >> 7), grp = tid >> 7, t = tid & 127;
   const int nthreads = static_cast<int>(blockDim.x);
   int b, p0, p1;
-  if (p.list) {
+  if (p.plan) {
+    // device-only plan (graph replays): the entry count, the list and its
+    // bounds come from the plan words; the grid covers every possible entry
+    const int32_t* h = p.plan;
+    const int W = h[kHWorkers], n_items = h[kHItems], n_merges = h[kHMerges];
+    const long long off = kHeaderWords + static_cast<long long>(W) + 1 + 4ll * n_items;
+    const bool good = h[kHMagic] == kPlanMagic && h[kHVersion] == kPlanVersion && h[kHHeads] == p.heads &&
+                      W == p.workers &&
+                      n_items >= 0 && n_merges >= 0 && off + 3ll * n_merges <= p.plan_cap_words;
+    if (!good || e >= n_merges) return;
+    b = h[off + 3 * e];
+    p0 = h[off + 3 * e + 1];
+    p1 = h[off + 3 * e + 2];
+    if (b < 0 || b >= p.batch || p0 < 0 || p1 < p0 || p1 > p.max_partials) {
+      if (tid == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+      return;
+    }
+  } else if (p.list) {
     b = p.list[3 * e];
     p0 = p.list[3 * e + 1];
     p1 = p.list[3 * e + 2];

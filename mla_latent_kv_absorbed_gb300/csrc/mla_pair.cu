@@ -189,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 
   const int w = blockIdx.x >> 1;
-  const int32_t* wptr = p.plan + kHeaderWords;
-  const int it0 = wptr[w], it1 = wptr[w + 1];
+  int it0, it1;
+  plan_items(p, w, it0, it1);
   const int32_t* items = p.plan + p.items_off;
   const int H = p.heads;
   const int nnz = __ldg(p.kv_indptr + p.batch);   // loaded alongside the plan words
@@ -640,7 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lsum = red_l[h] + red_l[128 + h];
       wait(bar(bOFull), nitem & 1, false);
       tc_fence_after();
-      if (!aborted) {
+      const bool part_ok = part < p.max_partials;   // a device-only plan naming a partial past the workspace
+      if (!part_ok && threadIdx.x == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+      if (!aborted && part_ok) {
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;     // no valid score: out = 0
         float* dst_f = nullptr;
         __nv_bfloat16* dst_h = nullptr;

@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 
   const int w = blockIdx.x;
-  const int32_t* wptr = p.plan + kHeaderWords;
-  const int it0 = wptr[w], it1 = wptr[w + 1];
+  int it0, it1;
+  plan_items(p, w, it0, it1);
   const int32_t* items = p.plan + p.items_off;
   const int nnz = __ldg(p.kv_indptr + p.batch);   // loaded alongside the plan words
 
@@ -590,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // soon as its last MMA is done (PV order 0, 2, 1, 3), scaled by 1/l and
       // written through the warp's own staging rows (no CTA barrier).
       if (tid == 0 && nitem < 24) MLA_TRACE_RAW(15, 8 + 2 * nitem, clock64());
+      const bool tid0 = tid == 0;
       const bool to_out = part < 0;
+      const bool part_ok = part < p.max_partials;   // a device-only plan naming a partial past the workspace
+      if (!part_ok && tid0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
       float l_tot[kHalf];
 #pragma unroll
       for (int k = 0; k < kHalf; ++k) l_tot[k] = l_part[k];
@@ -607,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kHalf; ++k)
           if (lane == k) my_lse = (m_ref[k] + __log2f(l_tot[k])) * 0.69314718055994531f;
-        if (!aborted && wip == 0 && lane < kHalf) {
+        if (!aborted && part_ok && wip == 0 && lane < kHalf) {
           const int h = pair * kHalf + lane;
           if (to_out) { if (p.lse) p.lse[static_cast<size_t>(b) * p.heads + h] = my_lse; }
           else p.part_lse[static_cast<size_t>(part) * p.heads + h] = my_lse;
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < NH * 8 / 32; ++k) {
             const int c = lane + 32 * k;
-            if (c < (NH << lg) && !aborted) {
+            if (c < (NH << lg) && !aborted && part_ok) {
               const int h = c >> lg, cc = c & ((1 << lg) - 1);
               const uint4 v = *reinterpret_cast<const uint4*>(wst + (h * 32) * esz + 16 * cc);
               *reinterpret_cast<uint4*>(dst + (static_cast<size_t>(h) * kLatent + 128 * mb + 32 * warp) * esz + 16 * cc) =

@@ -311,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{abort_flag, p.status};
 
   const int w = blockIdx.x;
-  const int32_t* wptr = p.plan + kHeaderWords;
-  const int it0 = wptr[w], it1 = wptr[w + 1];
+  int it0, it1;
+  plan_items(p, w, it0, it1);
   const int32_t* items = p.plan + p.items_off;
   const int nnz = __ldg(p.kv_indptr + p.batch);
 
@@ -631,7 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !aborted) mbar_arrive(bar(C::bPFull + buf));
       }
       // ------------------------------------------------------------ epilogue
+      const bool tid0 = threadIdx.x == 0;
       const bool to_out = part < 0;
+      const bool part_ok = part < p.max_partials;   // a device-only plan naming a partial past the workspace
+      if (!part_ok && tid0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
       float l_tot[kHalf];
 #pragma unroll
       for (int k = 0; k < kHalf; ++k) l_tot[k] = l_part[k];
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kHalf; ++k)
           if (lane == k) my_lse = (m_ref[k] + __log2f(l_tot[k])) * 0.69314718055994531f;
-        if (!aborted && wip == 0 && lane < kHalf) {
+        if (!aborted && part_ok && wip == 0 && lane < kHalf) {
           const int h = pair * kHalf + lane;
           if (to_out) { if (p.lse) p.lse[static_cast<size_t>(b) * p.heads + h] = my_lse; }
           else p.part_lse[static_cast<size_t>(part) * p.heads + h] = my_lse;
@@ -701,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < NH * 8 / 32; ++k) {
           const int c = lane + 32 * k;
-          if (c < (NH << lg) && !aborted) {
+          if (c < (NH << lg) && !aborted && part_ok) {
             const int h = c >> lg, cc = c & ((1 << lg) - 1);
             const uint4 val = *reinterpret_cast<const uint4*>(wst + (h * 32) * esz + 16 * cc);
             *reinterpret_cast<uint4*>(dst + (static_cast<size_t>(h) * kLatent + 128 * mb + 32 * warp) * esz + 16 * cc) =

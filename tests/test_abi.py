@@ -211,3 +211,41 @@ def test_fp8_entry_points_reject_bad_arguments(B):
     assert lib.mla_append_kv_fp8(fake, 100, fake, fake, -1, ctypes.c_float(1.0), None, None) == 1
     assert lib.mla_append_kv_fp8(fake + 4, 100, fake, fake, 2, ctypes.c_float(1.0), None, None) == 1
     assert lib.mla_append_kv_fp8(None, 100, None, None, 0, ctypes.c_float(1.0), None, None) == 0
+
+
+def test_graph_capacities_hold_every_plan_they_promise(B):
+    # any plan for batch <= max_batch (same heads and SMs) fits the capacities of mla_decode_graph_sizes
+    rng = np.random.default_rng(12)
+    for H, sms, max_batch in ((16, 152, 40), (128, 152, 24), (32, 20, 9), (64, 7, 5)):
+        words, ws = B.decode_graph_sizes(max_batch, H, sms)
+        for _ in range(60):
+            b = int(rng.integers(0, max_batch + 1))
+            kind = rng.integers(0, 3)
+            if kind == 0:
+                lens = rng.integers(0, 5000, size=b)
+            elif kind == 1:
+                lens = np.full(b, int(rng.integers(1, 70000)))
+            else:
+                lens = np.where(rng.random(b) < 0.5, 0, rng.integers(1, 300, size=b))
+            indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+            plan, need_ws = B.decode_plan(indptr, H, num_sms=sms)
+            assert plan.size <= words and need_ws <= ws, (H, sms, b)
+    lib = B.library()
+    n = ctypes.c_size_t(0)
+    assert lib.mla_decode_graph_sizes(0, 16, 152, ctypes.byref(n), None) == 1
+    assert lib.mla_decode_graph_sizes(4, 16, 0, ctypes.byref(n), None) == 1
+    assert lib.mla_decode_graph_sizes(4, 24, 152, ctypes.byref(n), None) == 2
+
+
+def test_graph_run_rejects_bad_arguments(B):
+    lib = B.library()
+    fake = 1 << 20
+    words, ws = B.decode_graph_sizes(8, 16, 152)
+
+    def run(pw=words, wsb=ws, q=fake, heads=16, out_dtype=0, plan=fake):
+        return lib.mla_decode_run_graph(plan, pw, 8, heads, 152, q, fake, fake, 1000, fake, fake, ctypes.c_float(0.1),
+                                        fake, out_dtype, fake, fake, wsb, None)
+
+    assert run(pw=words - 1) == 3 and run(wsb=ws - 1) == 3
+    assert run(q=fake + 2) == 1 and run(plan=None) == 1
+    assert run(heads=24) == 2 and run(out_dtype=5) == 2
