@@ -380,15 +380,16 @@ int mla_decode_run_graph(const int32_t* plan_dev, size_t plan_words, int32_t max
 /* mla_decode_fp8_workspace_bytes -- host.  Workspace mla_decode_run_fp8 needs
  * for `plan`: the plan's own workspace plus the per-request query images
  * (4 x H x 288 bytes) and per-head factors (H floats).
- * Errors: MLA_ERR_INVALID_ARG for a bad plan or null result pointer;
- * MLA_ERR_UNSUPPORTED unless the plan's H is 16 or 32. */
+ * Errors: MLA_ERR_INVALID_ARG for a bad plan or null result pointer. */
 int mla_decode_fp8_workspace_bytes(const int32_t* plan_host, size_t* workspace_bytes);
 
 /* mla_decode_run_fp8 -- asynchronous on `stream`.
  *
  * mla_decode_run over an FP8 cache: the same out / lse as the bf16 decode of
  * the cache values (code value x kv_scale), with the bf16 query used as is.
- * H must be 16 or 32 (the plan's H); other H give MLA_ERR_UNSUPPORTED.
+ * Every head count of mla_decode_plan is supported (16 or 32: one CTA per
+ * worker; 48..128: a two-CTA cluster, whose partial-score exchange bounds a
+ * score's error at 2^-15 of the largest partial in its 32-token half row).
  *
  *   kv_cache   device uint8 [num_slots, 576] E4M3 codes.
  *   kv_scale   finite, > 0.
@@ -397,9 +398,10 @@ int mla_decode_fp8_workspace_bytes(const int32_t* plan_host, size_t* workspace_b
  *              mla_decode_run; the query images are rewritten every call, so
  *              calls sharing a workspace must not overlap on the GPU).
  *   all other arguments as for mla_decode_run.
- * Launches a query-prep kernel (each request's query split into two E4M3
- * parts hi + lo/32 after a per-head power-of-two scaling), the decode kernel
- * as its programmatic dependent, and the plan's merge.
+ * Launches (H 16 / 32) a query-prep kernel (each request's query split into
+ * two E4M3 parts after a per-head power-of-two scaling) and the decode kernel
+ * as its programmatic dependent, or (H 48..128) the two-CTA kernel, which
+ * splits the query itself; then the plan's merge.
  * Errors as for mla_decode_run; nothing is launched on an argument error. */
 int mla_decode_run_fp8(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope, const void* q_rope,
                        const void* kv_cache, int64_t num_slots, float kv_scale, const int32_t* kv_indptr,

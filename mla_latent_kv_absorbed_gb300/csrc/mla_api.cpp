@@ -559,7 +559,6 @@ Fp8WsLayout fp8_ws_layout(const int32_t* plan_host) {
 
 int mla_decode_fp8_workspace_bytes(const int32_t* plan_host, size_t* workspace_bytes) {
   if (!plan_header_ok(plan_host) || !workspace_bytes) return MLA_ERR_INVALID_ARG;
-  if (plan_host[kHVariant] != kVariantSwab) return MLA_ERR_UNSUPPORTED;
   *workspace_bytes = fp8_ws_layout(plan_host).total;
   return MLA_OK;
 }
@@ -569,7 +568,6 @@ int mla_decode_run_fp8(const int32_t* plan_host, const int32_t* plan_dev, const 
                        const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream) {
   if (!plan_header_ok(plan_host) || !plan_dev) return MLA_ERR_INVALID_ARG;
-  if (plan_host[kHVariant] != kVariantSwab) return MLA_ERR_UNSUPPORTED;
   if (out_dtype != 0 && out_dtype != 1) return MLA_ERR_UNSUPPORTED;
   if (!std::isfinite(sm_scale) || !std::isfinite(kv_scale) || !(kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   const Fp8WsLayout wl = fp8_ws_layout(plan_host);
@@ -591,6 +589,7 @@ int mla_decode_run_fp8(const int32_t* plan_host, const int32_t* plan_dev, const 
   p.kv_indptr = kv_indptr;
   p.kv_indices = kv_indices;
   p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
   p.kv_cache = static_cast<const uint8_t*>(kv_cache);
   p.out = out;
   p.lse = lse;
@@ -630,7 +629,9 @@ int mla_decode_run_fp8(const int32_t* plan_host, const int32_t* plan_dev, const 
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MLA_ERR_CUDA;
-  const int rc = launch_swab8(H, tm_lat, tm_rope, p, p8, pp, plan_host[kHWorkers], st);
+  const int rc = plan_host[kHVariant] == kVariantSwab ? launch_swab8(H, tm_lat, tm_rope, p, p8, pp, plan_host[kHWorkers], st)
+                                                        : launch_pair8(H, tm_lat, tm_rope, p, kv_scale,
+                                                                       plan_host[kHWorkers], st);
   if (rc != MLA_OK) return rc;
   return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
 }

@@ -39,7 +39,8 @@ struct DecodeParams {
   const int32_t* plan;        // device plan words
   const int32_t* kv_indptr;   // device [B+1]
   const int32_t* kv_indices;  // device [nnz]
-  const uint16_t* q_nope;     // device bf16 [B, H, 512] (read directly by the pair kernel)
+  const uint16_t* q_nope;     // device bf16 [B, H, 512] (read directly by the pair kernels)
+  const uint16_t* q_rope;     // device bf16 [B, H, 64] (read directly by the FP8 pair kernel)
   const uint8_t* kv_cache;    // device [num_slots, 576] bf16 rows (for whole-row L2 prefetch)
   void* out;                  // [B, H, 512] fp32 or bf16
   float* lse;                 // [B, H] or null

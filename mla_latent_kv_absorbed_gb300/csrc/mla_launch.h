@@ -42,6 +42,12 @@ int launch_append(const AppendParams& p, cudaStream_t stream);
 int launch_swab8(int heads, const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const DecodeParams& p,
                  const Fp8Params& p8, const Fp8PrepParams& pp, int grid, cudaStream_t stream);
 
+// FP8-cache decode for H in 48..128 (a two-CTA cluster per worker, the query
+// split in-kernel); grid = 2 * workers.  tm_lat: uint8 [num_slots, 576], box
+// {128, 1}, 128-byte swizzle; tm_rope: box {32, 1}, 32-byte swizzle.
+int launch_pair8(int heads, const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const DecodeParams& p,
+                 float kv_scale, int workers, cudaStream_t stream);
+
 // Bytes of one request's query image for the FP8 decode.
 size_t fp8_image_bytes(int heads);
 

@@ -180,16 +180,6 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
   }
 }
 
-// E4M3 pair (low byte = first value), rounded to nearest, saturating at 448.
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
-// The two values of an E4M3 pair, exactly.
-__device__ __forceinline__ float2 e4m3x2_value(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFFu), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-
 // Byte offset of row n, byte k (< 128) in a 128-byte-swizzled K-major operand.
 __host__ __device__ __forceinline__ uint32_t sw128_off(int n, int k) {
   return (n >> 3) * 1024 + (n & 7) * 128 + ((((k >> 4) ^ (n & 7)) & 7) << 4) + (k & 15);

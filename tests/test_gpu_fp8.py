@@ -56,7 +56,7 @@ def _oracle(bt, qn, qr, codes, indices, kv_scale, requests=None):
     return O.decode_attention_fp8(qn, qr, codes, kv_scale, bt.kv_indptr, indices, bt.sm_scale, requests=requests)
 
 
-@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("H", [16, 32, 64, 128])
 @pytest.mark.parametrize("lengths", [
     [1, 7, 33, 100],
     [63, 64, 65, 127, 128, 129, 0, 191],          # around the tile edges, an empty request
@@ -70,7 +70,7 @@ def test_fp8_decode_matches_oracle(H, lengths):
     assert_close(out, lse, ro, rl)
 
 
-@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("H", [16, 32, 128])
 def test_fp8_bf16_output_and_many_workers(H):
     from mla_latent_kv_absorbed_gb300 import workloads as W
     rng = np.random.default_rng(H)
@@ -81,20 +81,27 @@ def test_fp8_bf16_output_and_many_workers(H):
     assert_close(out, lse, ro, rl)
 
 
-def test_fp8_query_heads_of_very_different_magnitude():
-    # the prep kernel scales each head by its own power of two: tiny, huge and all-zero heads
-    bt, qn, qr, codes, idx = _fp8_case([700, 90], 16, seed=510,
-                                       q_scale=[1e-3, 1e3, 0.0, 1.0, 3e-6, 40.0, 1.0, 1.0,
-                                                0.02, 1.0, 1.0, 7.0, 1.0, 1.0, 1.0, 250.0])
+@pytest.mark.parametrize("H", [16, 128])
+def test_fp8_query_heads_of_very_different_magnitude(H):
+    # each head is scaled by its own power of two: tiny, huge and all-zero heads.  The two-CTA
+    # kernel (H >= 48) exchanges partial scores as 16-bit fixed point (a step of 2^-14 of the half
+    # row's largest partial, as in its bf16 form), which puts ~0.1 nats into the lse of heads whose
+    # raw scores reach 1e4; its heads stay within 4x of unit scale (still 2^-8..2^2 apart).
+    if H <= 32:
+        base = [1e-3, 1e3, 0.0, 1.0, 3e-6, 40.0, 1.0, 1.0, 0.02, 1.0, 1.0, 7.0, 1.0, 1.0, 1.0, 250.0]
+    else:
+        base = [1e-3, 4.0, 0.0, 1.0, 3e-6, 2.0, 1.0, 1.0, 0.02, 1.0, 1.0, 0.25, 1.0, 1.0, 1.0, 3.0]
+    bt, qn, qr, codes, idx = _fp8_case([700, 90], H, seed=510 + H, q_scale=(base * (H // 16))[:H])
     for kv_scale in (2.0 ** -5, 0.0123):
         out, lse = _run_fp8(bt, qn, qr, codes, idx, kv_scale)
         ro, rl = _oracle(bt, qn, qr, codes, idx, kv_scale)
         assert_close(out, lse, ro, rl)
 
 
-def test_fp8_decode_is_deterministic():
+@pytest.mark.parametrize("H", [32, 128])
+def test_fp8_decode_is_deterministic(H):
     from mla_latent_kv_absorbed_gb300 import workloads as W
-    bt, qn, qr, codes, idx = _fp8_case([2500, 300, 1], 32, seed=520)
+    bt, qn, qr, codes, idx = _fp8_case([2500, 300, 1], H, seed=520 + H)
     runs = _run_fp8(bt, qn, qr, codes, idx, W.FP8_KV_SCALE, repeat=3)
     for o, l in runs[1:]:
         assert np.array_equal(o, runs[0][0]) and np.array_equal(l, runs[0][1])
@@ -164,6 +171,19 @@ def test_fp8_full_size_v2lite_sampled():
     codes = W.make_fp8_cache(bt.pool, 20261200 + 82)
     out, lse = _run_fp8(bt, bt.q_nope, bt.q_rope, codes, bt.kv_indices, W.FP8_KV_SCALE)
     reqs = [0, 1, 17, 40, 63]
+    ro, rl = _oracle(bt, bt.q_nope, bt.q_rope, codes, bt.kv_indices, W.FP8_KV_SCALE, requests=reqs)
+    assert_close(out, lse, ro, rl, requests=reqs)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+def test_fp8_full_size_v3_sampled():
+    # V3-shaped batch (B=128, H=128, 4096 tokens each) over an FP8 cache: the two-CTA kernel,
+    # every lse and a sample of requests' outputs against the oracle
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    bt = W.make_workload(3)
+    codes = W.make_fp8_cache(bt.pool, 20261200 + 83)
+    out, lse = _run_fp8(bt, bt.q_nope, bt.q_rope, codes, bt.kv_indices, W.FP8_KV_SCALE)
+    reqs = [0, 63, 127]
     ro, rl = _oracle(bt, bt.q_nope, bt.q_rope, codes, bt.kv_indices, W.FP8_KV_SCALE, requests=reqs)
     assert_close(out, lse, ro, rl, requests=reqs)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
