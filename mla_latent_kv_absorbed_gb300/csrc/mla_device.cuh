@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -319,6 +320,18 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
 __device__ __forceinline__ float2 e4m3x2_value(uint32_t v) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFFu), __NV_E4M3);
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Two values as E4M3 hi + lo parts (low byte = a): hi = e4m3(x), lo =
+// e4m3(f16(x) - hi), the difference taken exactly in f16 (x rounded to f16
+// has 11 significant bits, hi 4); for 0 <= x <= 256 the pair keeps x to
+// about 8 significant bits.  Five instructions per pair.
+__device__ __forceinline__ void e4m3x2_split(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = e4m3x2(a, b);
+  const __half2_raw hv = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(hi), __NV_E4M3);
+  const __half2 r = __hsub2(__floats2half2_rn(a, b), *reinterpret_cast<const __half2*>(&hv));
+  lo = static_cast<uint32_t>(
+      __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3));
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T.

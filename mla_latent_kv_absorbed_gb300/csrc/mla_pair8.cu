@@ -18,11 +18,11 @@
 //     latent K-step of 32 dims takes 2 MMAs (the bf16 kernel takes 2 of 16);
 //     the senders multiply their partial by 2^-a before quantising it, so the
 //     two CTAs' partials are in the same units;
-//   - P' = 2^(s - m_ref + 7) likewise (a reference that lags the maximum by at
-//     most 1, so P' <= 256 and the maximum's weight is >= 128): hi = e4m3(P'), lo = e4m3(P' - hi),
+//   - P' = 2^(s - m_ref + 5) likewise (a reference that lags the maximum by at
+//     most 3, so P' <= 256 and the maximum's weight is >= 32): hi = e4m3(P'), lo = e4m3(P' - hi),
 //     written side by side in the exchange slot's 128-byte rows (bytes 0-63
-//     hi, 64-127 lo, one byte per token): 2 MMAs per 32-token K-step; the
-//     running sums add hi + lo, the weights the MMA used.
+//     hi, 64-127 lo, one byte per token): 2 MMAs per 32-token K-step (the
+//     split takes the difference in f16: five instructions per pair).
 // hi + lo holds q' and P to about 8 significant bits (bf16 has 8), within
 // 2^-10 absolute for the small elements.  The epilogue multiplies O by
 // kv_scale / l; the score decode multiplies by sm_scale * log2(e) * kv_scale.
@@ -444,8 +444,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) r[i] = 0;
         }
         // this CTA's partial in the units both CTAs share: times 2^-a (exact)
+        {
+          const float2 qf2 = f2_pack(q_fac, q_fac);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * q_fac);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 v = f2_mul(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), qf2);
+            r[i] = __float_as_uint(v.x);
+            r[i + 1] = __float_as_uint(v.y);
+          }
+        }
         // the step is 2^(e-14), e the exponent of max|s| nudged up by 2^-15 so
         // that no code rounds to 32768
         float mx = 0.f;
@@ -566,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = mt;
         if (j == 0) l_sum = 0.f;
       } else {
-        const bool need = mt > m_ref + 1.f;   // P' <= 2^8 (see below)
+        const bool need = mt > m_ref + 3.f;   // P' <= 2^8 (see below)
         if (__any_sync(0xffffffffu, need)) {
           // rescale this warp's half of O (128 columns) after the previous PV has
           // landed.  PV(g-3) is complete here (the peer sent tile g only after it
@@ -598,12 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (K-major, 128-byte swizzle): token t of the tile is byte t (hi) and
       // byte 64 + t (lo) of row h; this warp's 32 tokens are two 16-byte
       // chunks of each part
-      // P' = 2^(s - m_ref + 7): the reference moves once a tile's maximum is
-      // more than 1 above it, so P' <= 256, the row maximum's weight is at
-      // least 128 and lo (unscaled, it shares the accumulator with hi) stays
-      // in E4M3's normal range down to weights 2^-9 of it; lse takes the 2^7 out
+      // P' = 2^(s - m_ref + 5): the reference moves once a tile's maximum is
+      // more than 3 above it, so P' <= 256 and the row maximum's weight is at
+      // least 32; lo (unscaled: it shares the accumulator with hi) is exact
+      // to E4M3's precision down to weights 2^-7 of that and within 2^-10
+      // below, which stays under 2^-9 of the output even over thousands of
+      // such tokens; lse takes the 2^5 out
       const float m_eff = m_ref == -INFINITY ? 0.f : m_ref;   // a row with no valid score yet: P = 0
-      const float2 nm2 = f2_pack(7.f - m_eff, 7.f - m_eff);
+      const float2 nm2 = f2_pack(5.f - m_eff, 5.f - m_eff);
       float2 l4[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int k = 0; k < 2; ++k) {              // 16 tokens per chunk
@@ -613,11 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = 16 * k + 2 * i;
           const float2 d = f2_add(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), nm2);
           const float a = ex2_approx(d.x), e2 = ex2_approx(d.y);
-          const uint32_t h2 = e4m3x2(a, e2);
-          const float2 hv = e4m3x2_value(h2);
-          const uint32_t l2 = e4m3x2(a - hv.x, e2 - hv.y);
-          const float2 lv = e4m3x2_value(l2);
-          l4[i & 3] = f2_add(l4[i & 3], f2_add(hv, lv));   // four independent sums of hi + lo
+          uint32_t h2, l2;
+          e4m3x2_split(a, e2, h2, l2);
+          l4[i & 3] = f2_add(l4[i & 3], f2_pack(a, e2));   // four independent sums (fp32 P, as the bf16 kernel)
           if (i & 1) {
             ph[i >> 1] |= h2 << 16;
             pl[i >> 1] |= l2 << 16;
@@ -696,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (cta == 0 && th == 0 && head_ok) {
-          const float l = lsum > 0.f ? (m_ref + __log2f(lsum) - 7.f) * 0.69314718055994531f : -INFINITY;
+          const float l = lsum > 0.f ? (m_ref + __log2f(lsum) - 5.f) * 0.69314718055994531f : -INFINITY;
           if (part < 0) { if (p.lse) p.lse[static_cast<size_t>(b) * H + h] = l; }
           else p.part_lse[static_cast<size_t>(part) * H + h] = l;
         }
