@@ -97,11 +97,21 @@ int mla_decode_plan(const int32_t* kv_indptr, int32_t batch, int32_t num_heads, 
   if (!variant_for_heads(num_heads, &T, &cpw)) return MLA_ERR_UNSUPPORTED;
   if (num_sms < 0) return MLA_ERR_INVALID_ARG;
   if (num_sms == 0) {
+    // the SM count of the current device, queried once per device
+    static int sms_of[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    if (cudaGetDevice(&dev) != cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_CUDA;
+    }
+    if (dev >= 0 && dev < 64 && sms_of[dev] > 0) {
+      num_sms = sms_of[dev];
+    } else {
+      if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+      }
+      if (dev >= 0 && dev < 64) sms_of[dev] = num_sms;
     }
   }
   std::vector<int32_t> words;

@@ -30,6 +30,7 @@ namespace mla {
 namespace {
 
 struct Piece {
+  int w;             // worker
   int b;
   long long k0;      // first token of the piece inside its request
   long long n;       // tokens
@@ -39,9 +40,11 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 constexpr long long kTileTokens = 64;
 inline long long round_up_tile(long long n) { return ceil_div(n, kTileTokens) * kTileTokens; }
 
-// Wrap-around fill with load budget cap (tokens); false when W workers do not suffice.
-bool fill(const std::vector<long long>& len, int W, long long cap, std::vector<std::vector<Piece>>& lists) {
-  lists.assign(W, {});
+// Wrap-around fill with load budget cap (tokens); false when W workers do not
+// suffice.  Pieces come out in worker order (the fill only moves forward), so
+// one flat list holds them all: no allocation per attempt once it has grown.
+bool fill(const std::vector<long long>& len, int W, long long cap, std::vector<Piece>& pieces) {
+  pieces.clear();
   int w = 0;
   long long used = 0;
   for (size_t b = 0; b < len.size(); ++b) {
@@ -62,7 +65,7 @@ bool fill(const std::vector<long long>& len, int W, long long cap, std::vector<s
         used = 0;
         continue;
       }
-      lists[w].push_back({static_cast<int>(b), k0, take});
+      pieces.push_back({w, static_cast<int>(b), k0, take});
       used += round_up_tile(take) + kItemOverheadTokens;
       k0 += take;
     }
@@ -102,68 +105,76 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
     nonempty += len[b] > 0 ? 1 : 0;
   }
   long long cap = 0;
-  std::vector<std::vector<Piece>> lists(W);
+  std::vector<Piece> pieces;
+  pieces.reserve(static_cast<size_t>(B) + W);
   if (total > 0) {
     cap = ceil_div(total + (nonempty + W - 1) * kItemOverheadTokens, W);
-    while (!fill(len, W, cap, lists)) cap += kCapStepTokens;
+    while (!fill(len, W, cap, pieces)) cap += kCapStepTokens;
   }
 
-  std::vector<long long> npieces(B, 0), pstart(B), seen(B, 0);
-  for (const auto& lst : lists)
-    for (const Piece& pc : lst) ++npieces[pc.b];
-  long long P = 0;
+  // per request: pieces, first partial index, pieces numbered so far (one allocation)
+  std::vector<long long> acc(3 * static_cast<size_t>(B), 0);
+  long long* npieces = acc.data();
+  long long* pstart = npieces + B;
+  long long* seen = pstart + B;
+  for (const Piece& pc : pieces) ++npieces[pc.b];
+  long long P = 0, n_merge = 0;
   for (int b = 0; b < B; ++b) {
     pstart[b] = P;
     if (npieces[b] > 1) P += npieces[b];
+    if (npieces[b] != 1) ++n_merge;
   }
+  const long long n_items = static_cast<long long>(pieces.size());
+  const long long total_words = kHeaderWords + (W + 1) + 4 * n_items + 3 * n_merge;
+  if (total_words > (1ll << 31) - 1 || P > (1ll << 31) - 1) return MLA_ERR_INVALID_ARG;
 
-  std::vector<int32_t> wptr(1, 0), items;
+  // the words are written in place: header, worker_indptr, items, merge entries
+  words.assign(static_cast<size_t>(total_words), 0);
+  int32_t* hw = words.data();
+  hw[kHMagic] = kPlanMagic;
+  hw[kHVersion] = kPlanVersion;
+  hw[kHBatch] = B;
+  hw[kHHeads] = H;
+  hw[kHVariant] = variant;
+  hw[kHTile] = T;
+  hw[kHWorkers] = W;
+  hw[kHCap] = static_cast<int32_t>(cap);
+  hw[kHItems] = static_cast<int32_t>(n_items);
+  hw[kHPartials] = static_cast<int32_t>(P);
+  hw[kHMerges] = static_cast<int32_t>(n_merge);
+  hw[kHHeadGroups] = 1;
+  hw[kHCtasPerWorker] = cpw;
+  hw[kHTotalWords] = static_cast<int32_t>(total_words);
+  hw[kHNumSms] = num_sms;
+  hw[kHReserved] = 0;
+  int32_t* wptr = hw + kHeaderWords;
+  int32_t* items = wptr + W + 1;
+  int32_t* merge = items + 4 * n_items;
+  wptr[0] = 0;
+  size_t pi = 0;
   for (int w = 0; w < W; ++w) {
-    for (const Piece& pc : lists[w]) {
+    for (; pi < pieces.size() && pieces[pi].w == w; ++pi) {
+      const Piece& pc = pieces[pi];
       const long long begin = static_cast<long long>(indptr[pc.b]) + pc.k0;
       const long long end = begin + pc.n;
       const long long part = npieces[pc.b] > 1 ? pstart[pc.b] + seen[pc.b] : -1;
       ++seen[pc.b];
-      items.push_back(pc.b);
-      items.push_back(static_cast<int32_t>(begin));
-      items.push_back(static_cast<int32_t>(end));
-      items.push_back(static_cast<int32_t>(part));
+      int32_t* itw = items + 4 * pi;
+      itw[0] = pc.b;
+      itw[1] = static_cast<int32_t>(begin);
+      itw[2] = static_cast<int32_t>(end);
+      itw[3] = static_cast<int32_t>(part);
     }
-    wptr.push_back(static_cast<int32_t>(items.size() / 4));
+    wptr[w + 1] = static_cast<int32_t>(pi);
   }
-  std::vector<int32_t> merge;
   for (int b = 0; b < B; ++b) {
     if (npieces[b] != 1) {
-      merge.push_back(b);
-      merge.push_back(static_cast<int32_t>(pstart[b]));
-      merge.push_back(static_cast<int32_t>(pstart[b] + (npieces[b] > 1 ? npieces[b] : 0)));
+      merge[0] = b;
+      merge[1] = static_cast<int32_t>(pstart[b]);
+      merge[2] = static_cast<int32_t>(pstart[b] + (npieces[b] > 1 ? npieces[b] : 0));
+      merge += 3;
     }
   }
-  const long long n_items = static_cast<long long>(items.size() / 4);
-  const long long n_merge = static_cast<long long>(merge.size() / 3);
-  const long long total_words = kHeaderWords + (W + 1) + 4 * n_items + 3 * n_merge;
-  if (total_words > (1ll << 31) - 1 || P > (1ll << 31) - 1) return MLA_ERR_INVALID_ARG;
-
-  words.assign(kHeaderWords, 0);
-  words[kHMagic] = kPlanMagic;
-  words[kHVersion] = kPlanVersion;
-  words[kHBatch] = B;
-  words[kHHeads] = H;
-  words[kHVariant] = variant;
-  words[kHTile] = T;
-  words[kHWorkers] = W;
-  words[kHCap] = static_cast<int32_t>(cap);
-  words[kHItems] = static_cast<int32_t>(n_items);
-  words[kHPartials] = static_cast<int32_t>(P);
-  words[kHMerges] = static_cast<int32_t>(n_merge);
-  words[kHHeadGroups] = 1;
-  words[kHCtasPerWorker] = cpw;
-  words[kHTotalWords] = static_cast<int32_t>(total_words);
-  words[kHNumSms] = num_sms;
-  words[kHReserved] = 0;
-  words.insert(words.end(), wptr.begin(), wptr.end());
-  words.insert(words.end(), items.begin(), items.end());
-  words.insert(words.end(), merge.begin(), merge.end());
 
   size_t ws = kWsHeaderBytes + static_cast<size_t>(P) * H * kLatent * 4 + static_cast<size_t>(P) * H * 4;
   ws = (ws + 255) / 256 * 256;
