@@ -226,10 +226,9 @@ int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len
   p.num_workers = plan_host[kHWorkers];
   p.max_partials = plan_host[kHPartials];
   p.scale_log2 = sm_scale * 1.4426950408889634f;
-  // multi-query: the plan's head count is q_len x the heads of one query, and
-  // only the two-CTA kernel applies the per-row causal limit
+  // multi-query: the plan's head count is q_len x the heads of one query;
+  // both decode kernels apply the per-row causal limit
   if (q_len < 1 || H % q_len != 0) return MLA_ERR_INVALID_ARG;
-  if (q_len > 1 && plan_host[kHVariant] == kVariantSwab) return MLA_ERR_UNSUPPORTED;
   p.q_len = q_len;
   return launch_decode(p, plan_host[kHVariant], q_nope, q_rope, kv_cache, st);
 }

@@ -189,7 +189,9 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
   }
 }
 
-template <int NH>
+// kMQ: several query tokens per request (q_len > 1), each row with its own
+// causal limit; the single-query instantiation carries none of it.
+template <int NH, bool kMQ>
 __global__ void __launch_bounds__(kThreads, 1)
     swab_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qn,
                 const __grid_constant__ CUtensorMap tm_qr, const DecodeParams p) {
@@ -484,6 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int part = items[4 * it + 3];
       if (!item_ok(p, nnz, b, s, e)) continue;
       const int n = e - s, nt = (n + T - 1) / T;
+      // multi-query: head row h is query i = h / (NH / q_len) of its request,
+      // which sees the first L - q_len + 1 + i rows of the request's context,
+      // i.e. the item's first mq_base + i tokens
+      constexpr bool mq = kMQ;
+      int mq_base = n, mq_heads = NH;
+      if (mq) {
+        const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+        mq_base = (hi - lo) - p.q_len + 1 - (s - lo);
+        mq_heads = NH / p.q_len;
+      }
       for (int j = 0; j < nt; ++j, ++g) {
         const uint32_t buf = g & 1;
         wait(bar(C::bSFull + buf), (g >> 1) & 1);
@@ -508,11 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           X[(pair * kHalf + k) * T + t] = __uint_as_float(pair ? r[k] : r[kHalf + k]);
         }
         named_bar_sync(kBarSm, 128);
-        const bool valid = t < n - j * T;
         float sv[kHalf];
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k)
-          sv[k] = valid ? (own[k] + X[((1 - pair) * kHalf + k) * T + t]) * p.scale_log2 : -INFINITY;
+        for (int k = 0; k < kHalf; ++k) {
+          const int lim = mq ? max(0, min(n, mq_base + (pair * kHalf + k) / mq_heads)) : n;
+          sv[k] = t < lim - j * T ? (own[k] + X[((1 - pair) * kHalf + k) * T + t]) * p.scale_log2 : -INFINITY;
+        }
         if (j == 0) {
 #pragma unroll
           for (int k = 0; k < kHalf; ++k) { m_ref[k] = sv[k]; l_part[k] = 0.f; }
@@ -531,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kHalf; ++k) {
               const float mn = fmaxf(m_ref[k], mt[k]);
-              alpha[k] = ex2_approx(m_ref[k] - mn);
+              alpha[k] = (kMQ && mn == -INFINITY) ? 1.f : ex2_approx(m_ref[k] - mn);   // a row with no score yet
               m_ref[k] = mn;
               l_part[k] *= alpha[k];
             }
@@ -564,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float pv[kHalf];
 #pragma unroll
         for (int k = 0; k < kHalf; ++k) {
-          pv[k] = ex2_approx(sv[k] - m_ref[k]);   // -inf rows give 0
+          // -inf scores give 0; so does a row with no score yet (m_ref -inf, multi-query)
+          pv[k] = ex2_approx(sv[k] - ((kMQ && m_ref[k] == -INFINITY) ? 0.f : m_ref[k]));
           l_part[k] += pv[k];
         }
         if (g >= 2) wait(bar(C::bPDone + buf), ((g >> 1) - 1) & 1);
@@ -601,8 +615,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (wip == 0 && lane == 0) {
 #pragma unroll
         for (int k = 0; k < kHalf; k += 4)
-          *reinterpret_cast<float4*>(bc + pair * kHalf + k) = make_float4(
-              __frcp_rn(l_tot[k]), __frcp_rn(l_tot[k + 1]), __frcp_rn(l_tot[k + 2]), __frcp_rn(l_tot[k + 3]));
+          if (kMQ)   // a row with nothing to attend: out 0
+            *reinterpret_cast<float4*>(bc + pair * kHalf + k) = make_float4(
+                l_tot[k] > 0.f ? __frcp_rn(l_tot[k]) : 0.f, l_tot[k + 1] > 0.f ? __frcp_rn(l_tot[k + 1]) : 0.f,
+                l_tot[k + 2] > 0.f ? __frcp_rn(l_tot[k + 2]) : 0.f, l_tot[k + 3] > 0.f ? __frcp_rn(l_tot[k + 3]) : 0.f);
+          else
+            *reinterpret_cast<float4*>(bc + pair * kHalf + k) = make_float4(
+                __frcp_rn(l_tot[k]), __frcp_rn(l_tot[k + 1]), __frcp_rn(l_tot[k + 2]), __frcp_rn(l_tot[k + 3]));
       }
       {
         // lane k of the pair's first warp writes head pair*kHalf + k
@@ -696,18 +715,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 }
 
-template <int NH>
+template <int NH, bool kMQ>
 int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap& tm_qr,
            const DecodeParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<NH>;
   static bool attr_done = false;   // the attribute is per function, set once per process
   if (!attr_done) {
-    if (cudaFuncSetAttribute(swab_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(swab_kernel<NH, kMQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return MLA_ERR_CUDA;
     attr_done = true;
   }
-  swab_kernel<NH><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
+  swab_kernel<NH, kMQ><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -715,8 +734,11 @@ int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap
 
 int launch_swab(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_qn,
                 const CUtensorMap& tm_qr, const DecodeParams& p, int grid, cudaStream_t stream) {
-  if (heads == 16) return swab::launch<16>(tm_kv, tm_qn, tm_qr, p, grid, stream);
-  if (heads == 32) return swab::launch<32>(tm_kv, tm_qn, tm_qr, p, grid, stream);
+  const bool mq = p.q_len > 1;
+  if (heads == 16) return mq ? swab::launch<16, true>(tm_kv, tm_qn, tm_qr, p, grid, stream)
+                             : swab::launch<16, false>(tm_kv, tm_qn, tm_qr, p, grid, stream);
+  if (heads == 32) return mq ? swab::launch<32, true>(tm_kv, tm_qn, tm_qr, p, grid, stream)
+                             : swab::launch<32, false>(tm_kv, tm_qn, tm_qr, p, grid, stream);
   return MLA_ERR_UNSUPPORTED;
 }
 

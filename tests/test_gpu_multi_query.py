@@ -43,7 +43,8 @@ def _check(out, lse, ro, rl):
         assert np.abs(lse[fin] - rl[fin]).max() <= ATOL_LSE
 
 
-@pytest.mark.parametrize("q_len,H", [(4, 16), (2, 32), (3, 32), (2, 64), (8, 16), (1, 64)])
+@pytest.mark.parametrize("q_len,H", [(4, 16), (2, 32), (3, 32), (2, 64), (8, 16), (1, 64),
+                                     (2, 8), (4, 4), (2, 16), (4, 8), (16, 2)])   # 16 / 32 rows: few-heads kernel
 def test_multi_query_matches_oracle(q_len, H):
     from oracle import mla_oracle as O
     lengths = [q_len, 70, 300, 1500]
@@ -70,7 +71,7 @@ def test_multi_query_across_cut_requests_and_bf16_output():
     _check(out, lse, ro, rl)
 
 
-def test_multi_query_short_context_rows_and_unsupported_variant():
+def test_multi_query_short_context_rows_on_both_kernels():
     import torch
     from mla_latent_kv_absorbed_gb300 import binding
     q_len, H = 4, 16
@@ -78,7 +79,16 @@ def test_multi_query_short_context_rows_and_unsupported_variant():
     out, lse, _ = _run(bt, q_len, H)
     assert np.all(out[0, :2] == 0) and np.all(np.isneginf(lse[0, :2]))
     assert np.isfinite(lse[0, 2:]).all() and np.isfinite(lse[1]).all()
-    # q_len x H = 32 runs on the few-heads kernel, which has no per-row limit
-    bt2 = _batch([10, 20], 2, 16, seed=6)
+    # the same on the few-heads kernel (q_len x H = 16 rows)
+    from oracle import mla_oracle as O
+    bt2 = _batch([2, 9, 130], 4, 4, seed=6)
+    out2, lse2, _ = _run(bt2, 4, 4)
+    assert np.all(out2[0, :2] == 0) and np.all(np.isneginf(lse2[0, :2]))
+    # requests 1 and 2 (at least q_len rows: the oracle's domain) against the oracle
+    B = bt2.batch
+    ro, rl = O.decode_attention_multi_query(bt2.q_nope.reshape(B, 4, 4, 512)[1:], bt2.q_rope.reshape(B, 4, 4, 64)[1:],
+                                            bt2.kv_cache, bt2.kv_indptr[1:], bt2.kv_indices, bt2.sm_scale, 4)
+    _check(out2[1:], lse2[1:], ro, rl)
+    # a q_len that does not divide the plan's rows is refused
     with pytest.raises(binding.MLAError):
-        _run(bt2, 2, 16)
+        _run(bt2, 3, 4)
