@@ -309,51 +309,62 @@ def time_head_products(batch, dev, peaks):
 
 
 def time_multi_query(batch, dev, peaks, kv, indptr_d, indices_d):
-    """Draft verification at this workload's lengths: q_len = 64 / H draft tokens
-    per request (the q_len x H query rows fill the two-CTA kernel's 64 rows),
-    timed over back-to-back launches that rotate KV copies larger than 4x L2.
-    Only for H <= 32 (at H = 128 the rows would exceed 128)."""
+    """Draft verification at this workload's lengths, at two draft counts:
+    q_len = 64 / H (the q_len x H = 64 rows run on the two-CTA kernel) and
+    q_len = 32 / H (32 rows: the few-heads kernel), each timed over
+    back-to-back launches that rotate KV copies larger than 4x L2.  Only for
+    H <= 32 (at H = 128 the rows would exceed 128)."""
     import numpy as np
     import torch
     from mla_latent_kv_absorbed_gb300 import binding
     Bn, H = batch.batch, batch.heads
     if H > 32:
         return None
-    q_len = 64 // H
-    qn = torch.randn((Bn, q_len, H, 512), device=dev).to(torch.bfloat16)
-    qr = torch.randn((Bn, q_len, H, 64), device=dev).to(torch.bfloat16)
-    plan, ws_bytes = binding.decode_plan(batch.kv_indptr, q_len * H)
-    plan_d = torch.from_numpy(plan).to(dev)
-    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    out = torch.empty((Bn, q_len, H, 512), dtype=torch.float32, device=dev)
-    lse = torch.empty((Bn, q_len, H), dtype=torch.float32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     R = max(2, math.ceil(4 * l2 / (batch.nnz * 1152)) + 1)
     kvs = [kv] + [kv.clone() for _ in range(R - 1)]
-    run = lambda k: binding.decode_run_multi_query(plan, plan_d, q_len, qn, qr, kvs[k % R], indptr_d, indices_d,
-                                                   batch.sm_scale, out, lse, ws)
-    for k in range(3):
-        run(k)
-    torch.cuda.synchronize()
-    n = max(20, R)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for k in range(n):
-        run(k)
-    e1.record()
-    torch.cuda.synchronize()
-    st = binding.check_errors(ws)
-    if st != 0:
-        raise RuntimeError(f"device status after multi-query: {binding.status_string(st)}")
-    us = e0.elapsed_time(e1) * 1e3 / n
-    rows = Bn * q_len * H
-    bytes_alg = batch.nnz * 1152 + batch.nnz * 4 + rows * (576 * 2 + 512 * 4 + 4) + (Bn + 1) * 4
-    flops = 2176 * H * sum(max(0, int(L) - q_len + 1 + i) for L in batch.lengths for i in range(q_len))
-    t = max(bytes_alg / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+
+    def one(q_len):
+        qn = torch.randn((Bn, q_len, H, 512), device=dev).to(torch.bfloat16)
+        qr = torch.randn((Bn, q_len, H, 64), device=dev).to(torch.bfloat16)
+        plan, ws_bytes = binding.decode_plan(batch.kv_indptr, q_len * H)
+        plan_d = torch.from_numpy(plan).to(dev)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        out = torch.empty((Bn, q_len, H, 512), dtype=torch.float32, device=dev)
+        lse = torch.empty((Bn, q_len, H), dtype=torch.float32, device=dev)
+        run = lambda k: binding.decode_run_multi_query(plan, plan_d, q_len, qn, qr, kvs[k % R], indptr_d, indices_d,
+                                                       batch.sm_scale, out, lse, ws)
+        for k in range(3):
+            run(k)
+        torch.cuda.synchronize()
+        n = max(20, R)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(n):
+            run(k)
+        e1.record()
+        torch.cuda.synchronize()
+        st = binding.check_errors(ws)
+        if st != 0:
+            raise RuntimeError(f"device status after multi-query: {binding.status_string(st)}")
+        us = e0.elapsed_time(e1) * 1e3 / n
+        rows = Bn * q_len * H
+        bytes_alg = batch.nnz * 1152 + batch.nnz * 4 + rows * (576 * 2 + 512 * 4 + 4) + (Bn + 1) * 4
+        flops = 2176 * H * sum(max(0, int(L) - q_len + 1 + i) for L in batch.lengths for i in range(q_len))
+        t = max(bytes_alg / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+        return q_len, us, t
+
+    q_len, us, t = one(64 // H)
+    res = {"q_len": q_len, "heads_per_query": H, "us": us, "roofline_us": t, "frac": t / us}
+    if 32 // H >= 2:
+        q2, us2, t2 = one(32 // H)
+        res["q_len_32_rows"] = {"q_len": q2, "us": us2, "roofline_us": t2, "frac": t2 / us2,
+                                "kernel": "few-heads (32 rows)"}
+    res["note"] = ("q_len draft tokens per request verified in one pass (mla_decode_run_multi_query); the main "
+                   "figure is 64 rows (two-CTA kernel), q_len_32_rows the few-heads kernel; synthetic queries, this "
+                   "workload's contexts; back-to-back launches over KV copies > 4x L2")
     del kvs
-    return {"q_len": q_len, "heads_per_query": H, "us": us, "roofline_us": t, "frac": t / us,
-            "note": "q_len draft tokens per request verified in one pass (mla_decode_run_multi_query); "
-                    "synthetic queries, this workload's contexts; back-to-back launches over KV copies > 4x L2"}
+    return res
 
 
 def time_cascade(batch, dev, peaks):
