@@ -225,10 +225,11 @@ int mla_merge_two_states(const float* o_a, const float* lse_a, const float* o_b,
  *   q_nope      bf16 [B, q_len, H, 512];  q_rope  bf16 [B, q_len, H, 64].
  *   out, lse    [B, q_len, H, 512] (out_dtype as for mla_decode_run), [B, q_len, H].
  * A query row with no row to attend to (L_b < q_len) gets out = 0, lse = -inf.
+ * Both decode kernels apply the per-row limit (q_len * H of 16 or 32: one CTA
+ * per worker; 48..128: a two-CTA cluster).
  * Errors: MLA_ERR_INVALID_ARG when q_len < 1 or the plan's head count is not a
- * multiple of q_len; MLA_ERR_UNSUPPORTED when q_len > 1 and q_len * H is 16
- * or 32 (the few-heads kernel has no per-row limit); otherwise as for
- * mla_decode_run (q_len = 1 is mla_decode_run). */
+ * multiple of q_len; otherwise as for mla_decode_run (q_len = 1 is
+ * mla_decode_run). */
 int mla_decode_run_multi_query(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len,
                                const void* q_nope, const void* q_rope, const void* kv_cache, int64_t num_slots,
                                const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale, void* out,
