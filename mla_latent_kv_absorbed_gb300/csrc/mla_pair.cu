@@ -31,11 +31,12 @@
 // buffers [384,448), [448,512) that hold this CTA's fp32 partial, then its
 // dequantised row.
 //
-// Shared memory per CTA: a ring of 4 latent blocks (64 tokens x 256 dims,
-// 32 KB, gathered with TMA gather4), 3 rope atoms (8 KB), the rope query
-// (16 KB), 3 exchange slots (16 KB each: the peer's quantised partial rows,
-// later overwritten in place by P as bf16, the A operand of PV), the peer's
-// exponents and the softmax warps' reduction buffers.
+// Shared memory per CTA: a ring of 5 latent blocks (64 tokens x 256 dims,
+// 32 KB, gathered with TMA gather4), 4 rope atoms (4 KB: this CTA's 32 rope
+// dims, 64-byte swizzle), the rope query (8 KB), 2 exchange slots (16 KB
+// each: the peer's quantised partial rows, later overwritten in place by P as
+// bf16, the A operand of PV), the peer's exponents and the softmax warps'
+// reduction buffers.
 //
 // Warp roles per CTA (736 threads).  Warp w of the sixteen score warps owns
 // heads 32(w%4)..+31 (TMEM lane h = head h) and tokens 32((w/4)%2)..+31 of
@@ -56,10 +57,10 @@
 // Splitting senders from softmax lets tile g+1 be quantised and pushed while
 // tile g is still in its softmax, so the exchange latency is hidden.
 //
-// Per tile g (S buffer g mod 2, exchange slot g mod 3): QK(g) -> the senders
-// quantise and push -> the softmax warps add the peer's rows and read the
-// buffer (freeing it for QK(g+2)), write P -> PV(g) frees the latent block
-// and, through a multicast commit, tells the PEER that its rows for tile g+3
+// Per tile g (S buffer g mod 2, exchange slot g mod 2): QK(g) -> the senders
+// quantise and push -> the softmax warps read the buffer (freeing it for
+// QK(g+2)) and add the peer's rows, write P -> PV(g) frees the latent block
+// and, through a multicast commit, tells the PEER that its rows for tile g+2
 // may land in this slot.
 // The softmax moves its reference maximum lazily (threshold 8 in log2
 // units) as in the few-heads kernel.
@@ -581,8 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = mt > m_ref + 8.f;
         if (__any_sync(0xffffffffu, need)) {
           // rescale this warp's half of O (128 columns) after the previous PV has
-          // landed.  PV(g-3) is complete here (the peer sent tile g only after it
-          // had freed slot g mod 3), so the buffer of tile g-1 cannot be a lap behind.
+          // landed.  PV(g-2) is complete here (the peer sent tile g only after
+          // this CTA's PV(g-2) had freed slot g mod 2), so the barrier of tile
+          // g-1 cannot be a lap behind.
           wait(bar(bPvDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, false);
           tc_fence_after();
           const float alpha = need ? ex2_approx(m_ref - mt) : 1.f;

@@ -71,7 +71,7 @@ constexpr int kLatBlock = 2 * kAtom;         // 16 KB: 64 tokens x 256 dims
 constexpr int kRopeAtom = T * 32;            // 2 KB: 64 tokens x this CTA's 32 rope dims (32-byte swizzle)
 constexpr int kQRPlane = 128 * 32;           // rope query part: 128 rows x 32 E4M3 (32-byte swizzle)
 constexpr int kQRBytes = 2 * kQRPlane;       // hi, then lo
-constexpr int kXSlot = 128 * 128;            // 128 rows x 128 B (64 int16 scores, then 64 bf16 P)
+constexpr int kXSlot = 128 * 128;            // 128 rows x 128 B (64 int16 scores, then P: 64 hi and 64 lo E4M3)
 constexpr int kXeSlot = 2 * 128 * 4;         // [2 token halves][128 rows] int32 exponents
 constexpr int kXBytes = kXSlot + kXeSlot;    // bytes the peer sends per tile
 constexpr int kOffLat = 0;
@@ -576,8 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = mt > m_ref + 3.f;   // P' <= 2^8 (see below)
         if (__any_sync(0xffffffffu, need)) {
           // rescale this warp's half of O (128 columns) after the previous PV has
-          // landed.  PV(g-3) is complete here (the peer sent tile g only after it
-          // had freed slot g mod 3), so the buffer of tile g-1 cannot be a lap behind.
+          // landed.  PV(g-2) is complete here (the peer sent tile g only after
+          // this CTA's PV(g-2) had freed slot g mod 2), so the barrier of tile
+          // g-1 cannot be a lap behind.
           wait(bar(bPvDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, false);
           tc_fence_after();
           const float alpha = need ? ex2_approx(m_ref - mt) : 1.f;
