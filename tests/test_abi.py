@@ -248,3 +248,15 @@ def test_graph_run_rejects_bad_arguments(B):
     assert run(pw=words - 1) == 3 and run(wsb=ws - 1) == 3
     assert run(q=fake + 2) == 1 and run(plan=None) == 1
     assert run(heads=24) == 2 and run(out_dtype=5) == 2
+
+
+def test_binding_refuses_to_load_without_the_library(tmp_path):
+    # the binding has no fallback: beside no built library, importing it raises
+    import importlib.util
+    import shutil
+    src = os.path.join(ROOT, "mla_latent_kv_absorbed_gb300", "binding.py")
+    shutil.copy(src, tmp_path / "binding.py")
+    spec = importlib.util.spec_from_file_location("mla_binding_without_library", tmp_path / "binding.py")
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError, match="libmla_decode.so is missing"):
+        spec.loader.exec_module(mod)

@@ -178,6 +178,25 @@ def test_pair_kernel_variant_and_empty_requests():
     assert np.all(out[[0, 2, 4]] == 0)
 
 
+@pytest.mark.parametrize("H", [16, 128])
+def test_every_request_empty(H):
+    # a plan without items: nothing is gathered, and the plan's merge alone
+    # writes a zero output and lse = -inf for every request
+    import torch
+    bt = _batch([0, 0, 0], H, seed=5)
+    for dt in (torch.float32, torch.bfloat16):
+        (out, lse), dec = run_gpu(bt, out_dtype=dt)
+        assert dec.header[8] == 0 and dec.header[10] == 3
+        assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_empty_batch_is_a_no_op(H):
+    bt = _batch([], H, seed=6)
+    (out, lse), dec = run_gpu(bt)
+    assert dec.header[2] == 0 and out.shape == (0, H, 512) and lse.shape == (0, H)
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("number", [3, 4, 5])
 def test_many_head_workloads_sampled(number):

@@ -56,6 +56,14 @@ def _oracle(bt, qn, qr, codes, indices, kv_scale, requests=None):
     return O.decode_attention_fp8(qn, qr, codes, kv_scale, bt.kv_indptr, indices, bt.sm_scale, requests=requests)
 
 
+@pytest.mark.parametrize("H", [16, 128])
+def test_fp8_every_request_empty(H):
+    # no plan items: the plan's merge alone writes zeros and lse = -inf
+    bt, qn, qr, codes, indices = _fp8_case([0, 0, 0, 0], H, seed=41)
+    out, lse = _run_fp8(bt, qn, qr, codes, indices, 2.0 ** -5)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
 @pytest.mark.parametrize("H", [16, 32, 64, 128])
 @pytest.mark.parametrize("lengths", [
     [1, 7, 33, 100],
