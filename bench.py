@@ -25,6 +25,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -66,14 +67,25 @@ KERNEL_SOURCES = {
 }
 
 
+_C_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(text):
+    """C/CUDA source with its comments removed (string literals kept),
+    trailing blanks and empty lines dropped."""
+    text = _C_TOKENS.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_sha(kernel):
-    """Digest of the sources that make up one decode kernel."""
+    """Digest of the code (not the comments) of the sources that make up one
+    decode kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_absorbed_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -111,7 +111,12 @@ int mla_decode_plan(const int32_t* kv_indptr, int32_t batch, int32_t num_heads, 
  *                 sticky device status read by mla_check_errors).
  *
  * Launches the decode kernel and, when the plan cut or left empty any request,
- * the merge kernel.  Device-side faults are not possible from bad indices: an
+ * the merge kernel.  An empty request (kv_indptr[b+1] == kv_indptr[b]) gets
+ * out = 0 and lse = -inf.  When no request has a token the decode kernel is
+ * not launched (q_nope, q_rope, kv_cache, kv_indptr and kv_indices may then be
+ * NULL) and the merge alone writes out and lse; with batch == 0 nothing is
+ * launched and only plan_dev and workspace are checked (the other device
+ * pointers may be NULL).  Device-side faults are not possible from bad indices: an
  * index outside [0, num_slots) reads row 0 and sets MLA_ERR_INDEX_OOB in the
  * workspace status.  The call does not synchronise; read device-side status
  * with mla_check_errors.  Safe to capture in a CUDA graph (no host sync, no

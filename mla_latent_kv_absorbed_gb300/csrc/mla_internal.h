@@ -22,7 +22,7 @@ enum PlanHeader : int {
   kHItems, kHPartials, kHMerges, kHHeadGroups, kHCtasPerWorker, kHTotalWords, kHNumSms,
   kHReserved
 };
-constexpr int kVariantSwab = 1;  // H in {16, 32}: one CTA per worker, 128-token tiles
+constexpr int kVariantSwab = 1;  // H in {16, 32}: one CTA per worker, 64-token tiles
 constexpr int kVariantPair = 2;  // H in 48..128: a 2-CTA cluster per worker, 64-token tiles
 constexpr int kItemOverheadTokens = 32;   // plan cost of one work item (its epilogue), in tokens
 constexpr int kMinPieceTokens = 64;       // no cut piece is shorter

@@ -260,3 +260,21 @@ def test_binding_refuses_to_load_without_the_library(tmp_path):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError, match="libmla_decode.so is missing"):
         spec.loader.exec_module(mod)
+
+
+def test_empty_batch_run_checks_arguments_and_launches_nothing(B):
+    # batch == 0: the host checks still apply to the plan, plan_dev and the
+    # workspace; the data pointers may be NULL and no CUDA call is made
+    lib = B.library()
+    plan, ws_bytes = B.decode_plan(np.array([0], dtype=np.int32), 16, num_sms=152)
+    assert plan[2] == 0
+    fake = 1 << 20   # never dereferenced
+    ph = np.ascontiguousarray(plan, dtype=np.int32)
+
+    def run(plan_dev=fake, ws=fake):
+        return lib.mla_decode_run(ph.ctypes.data, plan_dev, None, None, None, 1, None, None, ctypes.c_float(0.1),
+                                  None, 0, None, ws, ws_bytes, None)
+
+    assert run() == 0
+    assert run(plan_dev=None) == 1
+    assert run(ws=None) == 1
