@@ -414,7 +414,7 @@ def time_cascade(batch, dev, peaks):
     Bn, H = batch.batch, batch.heads
     if H > 32:
         return None
-    Lp, group = 4096, 128 // H
+    Lp, group = min(4096, batch.pool), 128 // H            # distinct prefix slots: at most the pool
     G = (Bn + group - 1) // group
     rng = np.random.default_rng(11)
     pool = batch.pool
@@ -440,6 +440,10 @@ def time_cascade(batch, dev, peaks):
     # flat: each request over prefix + suffix
     f_ptr = (s_ptr + np.arange(Bp + 1, dtype=np.int32) * Lp).astype(np.int32)
     f_ind = np.concatenate([np.concatenate([prefix, batch.kv_indices[s_ptr[b]:s_ptr[b + 1]]]) for b in range(Bp)])
+    # every index array holds exactly the slots its kv_indptr names
+    if not (len(prefix) == Lp and G * Lp == p_ptr[-1] and len(batch.kv_indices) == s_ptr[-1] == batch.nnz
+            and len(f_ind) == f_ptr[-1]):
+        raise RuntimeError("cascade index arrays do not match their kv_indptr")
     dec_f = binding.Decoder(f_ptr, H, device=dev)
     f_ind_d = ti(f_ind)
     o_f, l_f = torch.empty_like(o_p), torch.empty_like(l_p)

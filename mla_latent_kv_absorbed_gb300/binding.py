@@ -347,16 +347,29 @@ class Decoder:
         self.plan_dev = torch.from_numpy(self.plan_host).to(device)
         self.workspace = torch.zeros(max(self.workspace_bytes, 256), dtype=torch.uint8, device=device)
         self.num_heads = num_heads
+        self.batch = int(np.asarray(kv_indptr_host).shape[0]) - 1
+        self.nnz = int(np.asarray(kv_indptr_host)[-1])
+
+    def _check_csr(self, kv_indptr, kv_indices):
+        # the kernels trust kv_indices to hold kv_indptr[batch] slots; the
+        # plan's host copy of kv_indptr lets this be checked before a launch
+        if kv_indptr.numel() != self.batch + 1:
+            raise ValueError(f"kv_indptr has {kv_indptr.numel()} entries, the plan was built for {self.batch + 1}")
+        if self.nnz > 0 and (kv_indices is None or kv_indices.numel() < self.nnz):
+            n = 0 if kv_indices is None else kv_indices.numel()
+            raise ValueError(f"kv_indices has {n} entries, the plan's kv_indptr ends at {self.nnz}")
 
     @property
     def header(self):
         return self.plan_host[:16]
 
     def run(self, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse, stream=None):
+        self._check_csr(kv_indptr, kv_indices)
         decode_run(self.plan_host, self.plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
                    sm_scale, out, lse, self.workspace, stream)
 
     def attend(self, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse, stream=None):
+        self._check_csr(kv_indptr, kv_indices)
         decode_attend(self.plan_host, self.plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
                       sm_scale, out, lse, self.workspace, stream)
 

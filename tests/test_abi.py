@@ -278,3 +278,16 @@ def test_empty_batch_run_checks_arguments_and_launches_nothing(B):
     assert run() == 0
     assert run(plan_dev=None) == 1
     assert run(ws=None) == 1
+
+
+def test_decoder_refuses_index_arrays_shorter_than_its_plan(B):
+    # the kernels trust kv_indices to hold kv_indptr[batch] slots: the
+    # convenience holder checks that on the host before any launch
+    import torch
+    dec = B.Decoder(np.array([0, 100, 300], dtype=np.int32), 16, device="cpu", num_sms=152)
+    ok_ptr, ok_idx = torch.zeros(3, dtype=torch.int32), torch.zeros(300, dtype=torch.int32)
+    dec._check_csr(ok_ptr, ok_idx)
+    with pytest.raises(ValueError, match="kv_indices has 299 entries"):
+        dec._check_csr(ok_ptr, torch.zeros(299, dtype=torch.int32))
+    with pytest.raises(ValueError, match="kv_indptr has 4 entries"):
+        dec._check_csr(torch.zeros(4, dtype=torch.int32), ok_idx)
