@@ -400,9 +400,34 @@ def time_multi_query(batch, dev, peaks, kv, indptr_d, indices_d):
     return res
 
 
+def cascade_csr(batch):
+    """Host CSR arrays of the shared-prefix leg (H <= 32): a prefix of
+    min(4096, pool) distinct slots; G pseudo-requests of 128 // H requests'
+    rows over it (p_ptr, p_ind); the workload's contexts as suffixes, padded
+    with empty requests to whole groups (s_ptr); and each request over prefix
+    + suffix (f_ptr, f_ind).  Raises unless every index array holds exactly
+    the slots its kv_indptr names."""
+    import numpy as np
+    Bn, H = batch.batch, batch.heads
+    Lp, group = min(4096, batch.pool), 128 // H            # distinct prefix slots: at most the pool
+    G = (Bn + group - 1) // group
+    Bp = G * group                                           # padded to whole groups
+    prefix = np.random.default_rng(11).permutation(batch.pool)[:Lp].astype(np.int32)
+    p_ptr = np.arange(G + 1, dtype=np.int32) * Lp
+    p_ind = np.tile(prefix, G)
+    s_ptr = np.concatenate([batch.kv_indptr, np.full(Bp - Bn, batch.kv_indptr[-1])]).astype(np.int32)
+    f_ptr = (s_ptr + np.arange(Bp + 1, dtype=np.int32) * Lp).astype(np.int32)
+    f_ind = np.concatenate([np.concatenate([prefix, batch.kv_indices[s_ptr[b]:s_ptr[b + 1]]]) for b in range(Bp)])
+    if not (len(prefix) == Lp and len(p_ind) == p_ptr[-1] and len(batch.kv_indices) == s_ptr[-1] == batch.nnz
+            and len(f_ind) == f_ptr[-1]):
+        raise RuntimeError("cascade index arrays do not match their kv_indptr")
+    return {"prefix_rows": Lp, "group": group, "groups": G, "padded_batch": Bp, "p_ptr": p_ptr, "p_ind": p_ind,
+            "s_ptr": s_ptr, "f_ptr": f_ptr, "f_ind": f_ind}
+
+
 def time_cascade(batch, dev, peaks):
     """Shared-prefix cascade at this workload's shape: every request gets a
-    shared 4096-row prefix in front of its own context (the workload's rows
+    shared prefix of min(4096, pool) rows in front of its own context (the workload's rows
     as suffix).  Cascade = prefix pass (the query rows of 128 // H requests as
     the heads of one pseudo-request, so the prefix is read once per group),
     suffix pass, two-state merge; flat = one decode over prefix + suffix rows
@@ -414,36 +439,25 @@ def time_cascade(batch, dev, peaks):
     Bn, H = batch.batch, batch.heads
     if H > 32:
         return None
-    Lp, group = min(4096, batch.pool), 128 // H            # distinct prefix slots: at most the pool
-    G = (Bn + group - 1) // group
-    rng = np.random.default_rng(11)
-    pool = batch.pool
-    prefix = rng.permutation(pool)[:Lp].astype(np.int32)
+    c = cascade_csr(batch)
+    Lp, group, G, Bp = c["prefix_rows"], c["group"], c["groups"], c["padded_batch"]
+    p_ptr, s_ptr, f_ptr, f_ind = c["p_ptr"], c["s_ptr"], c["f_ptr"], c["f_ind"]
     ti = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
     kv = torch.from_numpy(np.ascontiguousarray(batch.kv_cache).view(np.int16)).view(torch.bfloat16).to(dev)
-    Bp = G * group                                   # padded to whole groups
     qn = torch.randn((Bp, H, 512), device=dev).to(torch.bfloat16)
     qr = torch.randn((Bp, H, 64), device=dev).to(torch.bfloat16)
     sc = batch.sm_scale
     # prefix pass: G pseudo-requests of group x H rows over the same prefix rows
-    p_ptr = np.arange(G + 1, dtype=np.int32) * Lp
     dec_p = binding.Decoder(p_ptr, group * H, device=dev)
-    p_ind = ti(np.tile(prefix, G))
+    p_ind = ti(c["p_ind"])
     o_p = torch.empty((Bp, H, 512), dtype=torch.float32, device=dev)
     l_p = torch.empty((Bp, H), dtype=torch.float32, device=dev)
     # suffix pass: the workload's contexts (padding requests empty)
-    s_ptr = np.concatenate([batch.kv_indptr, np.full(Bp - Bn, batch.kv_indptr[-1])]).astype(np.int32)
     dec_s = binding.Decoder(s_ptr, H, device=dev)
     s_ind = ti(batch.kv_indices)
     o_s, l_s = torch.empty_like(o_p), torch.empty_like(l_p)
     out, lse = torch.empty_like(o_p), torch.empty_like(l_p)
     # flat: each request over prefix + suffix
-    f_ptr = (s_ptr + np.arange(Bp + 1, dtype=np.int32) * Lp).astype(np.int32)
-    f_ind = np.concatenate([np.concatenate([prefix, batch.kv_indices[s_ptr[b]:s_ptr[b + 1]]]) for b in range(Bp)])
-    # every index array holds exactly the slots its kv_indptr names
-    if not (len(prefix) == Lp and G * Lp == p_ptr[-1] and len(batch.kv_indices) == s_ptr[-1] == batch.nnz
-            and len(f_ind) == f_ptr[-1]):
-        raise RuntimeError("cascade index arrays do not match their kv_indptr")
     dec_f = binding.Decoder(f_ptr, H, device=dev)
     f_ind_d = ti(f_ind)
     o_f, l_f = torch.empty_like(o_p), torch.empty_like(l_p)

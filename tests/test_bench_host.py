@@ -33,3 +33,30 @@ def test_traffic_file_entries_are_well_formed():
         assert float(nbytes) > 0
         assert re.fullmatch(r"[0-9a-f]{16}", digest)
         assert len(bench.kernel_source_sha(kernel)) == 16
+
+
+def test_cascade_leg_index_arrays_match_their_kv_indptr():
+    # the shared-prefix leg's CSR arrays for every few-heads workload: each
+    # index array holds exactly the slots its kv_indptr names, all in the pool
+    from types import SimpleNamespace
+
+    import numpy as np
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    for number, spec in W.WORKLOADS.items():
+        if spec.heads > 32:
+            continue
+        rng = np.random.default_rng(spec.seed)
+        lengths = W.draw_lengths(spec, rng)
+        indptr = np.zeros(len(lengths) + 1, dtype=np.int32)
+        indptr[1:] = np.cumsum(lengths)
+        nnz = int(indptr[-1])
+        batch = SimpleNamespace(batch=len(lengths), heads=spec.heads, pool=spec.pool, kv_indptr=indptr,
+                                kv_indices=rng.permutation(spec.pool)[:nnz].astype(np.int32), nnz=nnz)
+        c = bench.cascade_csr(batch)
+        assert c["prefix_rows"] == min(4096, spec.pool)
+        assert len(np.unique(c["p_ind"][:c["prefix_rows"]])) == c["prefix_rows"]
+        assert len(c["p_ind"]) == c["p_ptr"][-1] and len(c["f_ind"]) == c["f_ptr"][-1]
+        assert c["s_ptr"][-1] == nnz and len(c["s_ptr"]) == c["padded_batch"] + 1
+        assert np.all(np.diff(c["f_ptr"]) == np.diff(c["s_ptr"]) + c["prefix_rows"])
+        for a in (c["p_ind"], c["f_ind"]):
+            assert a.min() >= 0 and a.max() < spec.pool
