@@ -504,7 +504,7 @@ def time_cascade(batch, dev, peaks):
     diff = (out - o_f).abs().max().item()
     res.update({"prefix_rows": Lp, "requests": Bn, "requests_per_prefix_pass": group,
                 "max_abs_diff_cascade_vs_flat": diff,
-                "note": "shared prefix of 4096 rows in front of each context; cascade = prefix pass with the query "
+                "note": f"shared prefix of {Lp} rows in front of each context; cascade = prefix pass with the query "
                         "rows of 128 // H requests as one pseudo-request's heads + suffix pass + mla_merge_two_states; "
                         "CUDA-graph replays; L2 not flushed (the prefix rows are reused by design)"})
     return res
