@@ -179,16 +179,20 @@ int mla_merge_states(const float* v_partial, const float* s_partial, const int32
  *
  *   - The first call on a device looks the buffer's device address up for
  *     that device (a runtime query, no allocation); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is cached per device and per
+ *     CUDA context: after cudaDeviceReset (or anything else that replaces
+ *     the device's context) the next call looks it up again, so that call,
+ *     too, must not be inside a stream capture.
  *   - Plans whose partial states do not fit (256 B + P*H*513*4 bytes larger
  *     than MLA_NOALLOC_SCRATCH_BYTES) are rejected with MLA_ERR_WORKSPACE
  *     and nothing is launched.
  *   - Every call shares the one buffer: calls that overlap on the GPU (on
  *     different streams, or from different threads) race and corrupt each
  *     other's partial states.  Serialise them on one stream.
- *   - Each call clears the buffer's status word before its kernels run;
- *     device-side status (bad slot indices, timeouts) of this variant is not
- *     readable by the caller.
+ *   - The buffer's status word starts at zero (static initialisation) and,
+ *     like a caller workspace's, keeps the first device-side error (bad slot
+ *     index, timeout, plan mismatch) of any call until
+ *     mla_noalloc_check_errors reads and clears it.
  *   - Nothing here calls cudaMalloc, cudaFree or an allocating routine. */
 #define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
 int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* plan_dev,
@@ -197,6 +201,17 @@ int mla_decode_run_noalloc(const int32_t* plan_host, const int32_t* plan_dev,
                            const int32_t* kv_indptr, const int32_t* kv_indices,
                            float sm_scale, void* out, int32_t out_dtype, float* lse,
                            void* stream);
+
+/* mla_noalloc_check_errors -- the device status of mla_decode_run_noalloc.
+ *
+ * Synchronises `stream`, then reads the status word of the static buffer on
+ * the current device and clears it when it is non-zero (the same contract as
+ * mla_check_errors on a caller workspace).  Returns MLA_OK, the first
+ * MLA_ERR_* a kernel recorded since the last read, or MLA_ERR_CUDA when the
+ * stream or the copy failed.  It allocates nothing: the word is copied into a
+ * host int.  Like the entry point it reports on, it has no counterpart on the
+ * pages. */
+int mla_noalloc_check_errors(void* stream);
 
 /* mla_merge_two_states -- asynchronous on `stream`.
  *

@@ -26,7 +26,7 @@ EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decod
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
            "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query",
            "mla_merge_two_states", "mla_decode_fp8_workspace_bytes", "mla_decode_run_fp8", "mla_append_kv_fp8",
-           "mla_decode_graph_sizes", "mla_decode_run_graph")
+           "mla_decode_graph_sizes", "mla_decode_run_graph", "mla_noalloc_check_errors")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -58,6 +58,8 @@ _lib.mla_decode_run_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64,
                                         ctypes.c_int32, _vp, _vp]
 _lib.mla_check_errors.restype = ctypes.c_int
 _lib.mla_check_errors.argtypes = [_vp, _vp]
+_lib.mla_noalloc_check_errors.restype = ctypes.c_int
+_lib.mla_noalloc_check_errors.argtypes = [_vp]
 _lib.mla_absorb_query.restype = ctypes.c_int
 _lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]
 _lib.mla_decode_run_multi_query.restype = ctypes.c_int
@@ -141,6 +143,35 @@ def decode_plan(kv_indptr_host, num_heads: int, num_sms: int = 0):
     return plan, int(ws.value)
 
 
+_H_BATCH, _H_WORKERS, _H_ITEMS = 2, 6, 8      # plan header words (include/mla_decode.h)
+
+
+def plan_nnz(plan_host) -> int:
+    """Token count a plan covers: the largest kv_end of its work items (the
+    items tile [0, kv_indptr[batch]) exactly), 0 when it has none."""
+    h = np.asarray(plan_host)
+    n = int(h[_H_ITEMS])
+    if n <= 0:
+        return 0
+    off = 16 + int(h[_H_WORKERS]) + 1
+    return int(h[off + 2: off + 4 * n: 4].max())
+
+
+def _check_csr(plan_host, kv_indptr, kv_indices, where) -> None:
+    """The kernels trust kv_indptr to hold batch + 1 entries and kv_indices
+    the slots kv_indptr names (the ABI passes no lengths); with the host plan
+    both sizes are checked here, before any launch."""
+    h = np.asarray(plan_host)
+    batch = int(h[_H_BATCH])
+    if kv_indptr is None or kv_indptr.numel() != batch + 1:
+        n = 0 if kv_indptr is None else kv_indptr.numel()
+        raise ValueError(f"{where}: kv_indptr has {n} entries, the plan was built for {batch + 1}")
+    nnz = plan_nnz(h)
+    if nnz > 0 and (kv_indices is None or kv_indices.numel() < nnz):
+        n = 0 if kv_indices is None else kv_indices.numel()
+        raise ValueError(f"{where}: kv_indices has {n} entries, the plan's items reach {nnz}")
+
+
 def _out_dtype(out, where):
     import torch
     code = {torch.float32: 0, torch.bfloat16: 1}.get(out.dtype)
@@ -157,6 +188,7 @@ def decode_run(plan_host: np.ndarray, plan_dev, q_nope, q_rope, kv_cache, kv_ind
     None, workspace uint8 (zero-filled before first use)."""
     out_dtype = _out_dtype(out, _entry)
     plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    _check_csr(plan_host, kv_indptr, kv_indices, _entry)
     st = getattr(_lib, _entry)(plan_host.ctypes.data, _ptr(plan_dev), _ptr(q_nope), _ptr(q_rope),
                              _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(kv_indptr), _ptr(kv_indices),
                              float(sm_scale), _ptr(out), out_dtype, _ptr(lse), _ptr(workspace),
@@ -190,11 +222,18 @@ def decode_run_noalloc(plan_host, plan_dev, q_nope, q_rope, kv_cache, kv_indptr,
     device buffer, shared by every call -- calls must not overlap on the GPU."""
     out_dtype = _out_dtype(out, "mla_decode_run_noalloc")
     plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    _check_csr(plan_host, kv_indptr, kv_indices, "mla_decode_run_noalloc")
     st = _lib.mla_decode_run_noalloc(plan_host.ctypes.data, _ptr(plan_dev), _ptr(q_nope), _ptr(q_rope),
                                      _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(kv_indptr), _ptr(kv_indices),
                                      float(sm_scale), _ptr(out), out_dtype, _ptr(lse), _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_decode_run_noalloc")
+
+
+def noalloc_check_errors(stream=None) -> int:
+    """Synchronise, read and clear the status word of the static buffer that
+    mla_decode_run_noalloc uses on the current device."""
+    return int(_lib.mla_noalloc_check_errors(_stream_handle(stream)))
 
 
 def merge_states(v_partial, s_partial, merge_indptr, out, lse, stream=None) -> None:
@@ -248,6 +287,8 @@ def decode_run_graph(plan_dev, max_batch, num_heads, num_sms, q_nope, q_rope, kv
     """Decode reading its plan only from the device buffer plan_dev (int32, capacity words), so a captured
     graph can be replayed after a new plan (and new CSR arrays) are copied into the same buffers."""
     out_dtype = _out_dtype(out, "mla_decode_run_graph")
+    if kv_indptr is None or kv_indptr.numel() != int(max_batch) + 1:
+        raise ValueError(f"mla_decode_run_graph: kv_indptr must hold max_batch + 1 = {int(max_batch) + 1} entries")
     st = _lib.mla_decode_run_graph(_ptr(plan_dev), int(plan_dev.numel()), int(max_batch), int(num_heads),
                                    int(num_sms), _ptr(q_nope), _ptr(q_rope), _ptr(kv_cache), int(kv_cache.shape[0]),
                                    _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out), out_dtype,
@@ -273,6 +314,7 @@ def decode_run_fp8(plan_host, plan_dev, q_nope, q_rope, kv_cache, kv_scale, kv_i
     other tensors as for decode_run; workspace of decode_fp8_workspace_bytes(plan) bytes, zero-filled once."""
     out_dtype = _out_dtype(out, "mla_decode_run_fp8")
     plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    _check_csr(plan_host, kv_indptr, kv_indices, "mla_decode_run_fp8")
     st = _lib.mla_decode_run_fp8(plan_host.ctypes.data, _ptr(plan_dev), _ptr(q_nope), _ptr(q_rope), _ptr(kv_cache),
                                  int(kv_cache.shape[0]), float(kv_scale), _ptr(kv_indptr), _ptr(kv_indices),
                                  float(sm_scale), _ptr(out), out_dtype, _ptr(lse), _ptr(workspace),
@@ -294,6 +336,7 @@ def decode_run_multi_query(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache,
     """q_len draft tokens per request in one pass: q [B, q_len, H, 576 split], out [B, q_len, H, 512]."""
     out_dtype = _out_dtype(out, "mla_decode_run_multi_query")
     plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    _check_csr(plan_host, kv_indptr, kv_indices, "mla_decode_run_multi_query")
     st = _lib.mla_decode_run_multi_query(plan_host.ctypes.data, _ptr(plan_dev), int(q_len), _ptr(q_nope),
                                          _ptr(q_rope), _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(kv_indptr),
                                          _ptr(kv_indices), float(sm_scale), _ptr(out), out_dtype, _ptr(lse),
@@ -323,6 +366,9 @@ def decode_step_host(q_nope, q_rope, kv_indptr, kv_indices, kv_cache, sm_scale, 
     `plan` is a host int32 tensor with room for the plan words."""
     out_dtype = _out_dtype(out, "mla_decode_step_host")
     B, H = int(q_nope.shape[0]), int(q_nope.shape[1])
+    if kv_indptr.numel() != B + 1 or kv_indices.numel() < int(kv_indptr[-1]):
+        raise ValueError("mla_decode_step_host: kv_indptr must hold batch + 1 entries and kv_indices the "
+                         "kv_indptr[batch] slots it names")
     st = _lib.mla_decode_step_host(_ptr(q_nope), _ptr(q_rope), _ptr(kv_indptr), _ptr(kv_indices), B, H,
                                    _ptr(kv_cache), int(kv_cache.shape[0]), float(sm_scale), _ptr(out), out_dtype,
                                    _ptr(lse), _ptr(plan), int(plan.numel()), _ptr(staging), int(staging.numel()),
@@ -350,26 +396,15 @@ class Decoder:
         self.batch = int(np.asarray(kv_indptr_host).shape[0]) - 1
         self.nnz = int(np.asarray(kv_indptr_host)[-1])
 
-    def _check_csr(self, kv_indptr, kv_indices):
-        # the kernels trust kv_indices to hold kv_indptr[batch] slots; the
-        # plan's host copy of kv_indptr lets this be checked before a launch
-        if kv_indptr.numel() != self.batch + 1:
-            raise ValueError(f"kv_indptr has {kv_indptr.numel()} entries, the plan was built for {self.batch + 1}")
-        if self.nnz > 0 and (kv_indices is None or kv_indices.numel() < self.nnz):
-            n = 0 if kv_indices is None else kv_indices.numel()
-            raise ValueError(f"kv_indices has {n} entries, the plan's kv_indptr ends at {self.nnz}")
-
     @property
     def header(self):
         return self.plan_host[:16]
 
     def run(self, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse, stream=None):
-        self._check_csr(kv_indptr, kv_indices)
         decode_run(self.plan_host, self.plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
                    sm_scale, out, lse, self.workspace, stream)
 
     def attend(self, q_nope, q_rope, kv_cache, kv_indptr, kv_indices, sm_scale, out, lse, stream=None):
-        self._check_csr(kv_indptr, kv_indices)
         decode_attend(self.plan_host, self.plan_dev, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
                       sm_scale, out, lse, self.workspace, stream)
 

@@ -2,6 +2,7 @@
 // checks, the host plan, TMA descriptor encoding and kernel dispatch.  Nothing
 // here allocates device memory or synchronises except mla_check_errors.
 #include <algorithm>
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -97,21 +98,24 @@ int mla_decode_plan(const int32_t* kv_indptr, int32_t batch, int32_t num_heads, 
   if (!variant_for_heads(num_heads, &T, &cpw)) return MLA_ERR_UNSUPPORTED;
   if (num_sms < 0) return MLA_ERR_INVALID_ARG;
   if (num_sms == 0) {
-    // the SM count of the current device, queried once per device
-    static int sms_of[64] = {};
+    // the SM count of the current device, queried once per device; plans
+    // may be built from several host threads at once, so the cache entries
+    // are atomics (a race only repeats the query)
+    static std::atomic<int> sms_of[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_CUDA;
     }
-    if (dev >= 0 && dev < 64 && sms_of[dev] > 0) {
-      num_sms = sms_of[dev];
+    const int cached = (dev >= 0 && dev < 64) ? sms_of[dev].load(std::memory_order_relaxed) : 0;
+    if (cached > 0) {
+      num_sms = cached;
     } else {
       if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();
         return MLA_ERR_CUDA;
       }
-      if (dev >= 0 && dev < 64) sms_of[dev] = num_sms;
+      if (dev >= 0 && dev < 64) sms_of[dev].store(num_sms, std::memory_order_relaxed);
     }
   }
   std::vector<int32_t> words;

@@ -14,8 +14,9 @@
 //   PV (per CTA):           O_c[128 h x 256] += P[128 x 64 tok] . V[64 tok x D_c]
 //
 // so no product is computed twice and no latent byte is loaded twice.
-// ("实现差距：MLA 与 DeepSeek V3", section 2.4: s = (s_nope + s_pe) * sm_scale,
-// FA2-style online softmax, kv_c reused as the value; "Attention backends",
+// ("实现差距：MLA 与 DeepSeek V3", section 2.4: the latent and rope dot products
+// are summed and scaled by sm_scale, FA2-style online softmax, the latent rows
+// reused as the values; "Attention backends",
 // paragraph "MLA": every KV byte used by all 128 heads.)
 //
 // The exchange is the narrow path: an SM moves only about 9 bytes per cycle

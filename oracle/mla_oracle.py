@@ -18,9 +18,11 @@ to rounding order):
 
 Sources, by page and section:
   * "实现差距：MLA 与 DeepSeek V3", section 2.4 "MLA Pallas Kernel (V2 生产版本)",
-    core computation: s = (s_nope + s_pe) * sm_scale, an FA2-style online
-    softmax, then p times kv_c with kv_c serving as the value.  The oracle
-    takes the softmax in one pass (max, then exp) instead of online.
+    core computation: the latent-path and rope-path dot products are added
+    and the sum is multiplied by sm_scale (s_t above), an FA2-style online
+    softmax follows, and the softmax weights multiply the latent rows, which
+    serve as the values.  The oracle takes the softmax in one pass (max, then
+    exp) instead of online.
   * same page, section 2.1 "Absorbed MLA 投影流程": kv_a_proj_with_mqa gives a
     576-wide row split as kv_latent (512) then k_rope (64) -- the row layout.
   * "Attention backends", paragraph "MLA": one 576-wide vector per token, 576

@@ -21,6 +21,29 @@ def B():
     return binding
 
 
+_FAKE = {}
+
+
+def _fake_ptr():
+    """A device address for the rejection tests.  Every case below must fail
+    its host check before any launch; should a check regress, what a kernel
+    would get is a zero-filled 16 MiB device buffer when a GPU is present
+    (every pointer below, with its small offsets, stays inside it), and on a
+    machine without a GPU nothing can launch at all."""
+    if "p" not in _FAKE:
+        try:
+            import torch
+            have = torch.cuda.is_available()
+        except Exception:
+            have = False
+        if have:
+            _FAKE["buf"] = torch.zeros(16 << 20, dtype=torch.uint8, device="cuda")
+            _FAKE["p"] = int(_FAKE["buf"].data_ptr())
+        else:
+            _FAKE["p"] = 1 << 20
+    return _FAKE["p"]
+
+
 def _declared_functions():
     names = []
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
@@ -110,7 +133,7 @@ def test_plan_rejects_bad_input(B):
 def test_run_rejects_bad_arguments_before_launch(B):
     lib = B.library()
     plan, ws_bytes = B.decode_plan(np.array([0, 100, 300], dtype=np.int32), 16, num_sms=152)
-    fake = 1 << 20   # never dereferenced: every case below fails its host check first
+    fake = _fake_ptr()   # never dereferenced: every case below fails its host check first
 
     def run(plan_host=plan, plan_dev=fake, ws=fake, ws_bytes=ws_bytes, out_dtype=0, slots=1000, q=fake,
             scale=0.1):
@@ -145,7 +168,7 @@ def test_merge_rejects_bad_arguments(B):
 
 def test_head_products_reject_bad_arguments(B):
     lib = B.library()
-    fake = 1 << 20
+    fake = _fake_ptr()
     # unsupported head dims, then bad sizes and pointers; all before any launch
     assert lib.mla_absorb_query(fake, fake, fake, 4, 16, 64, None, None) == 2
     assert lib.mla_absorb_query(fake, fake, fake, -1, 16, 128, None, None) == 1
@@ -164,7 +187,7 @@ def test_head_products_reject_bad_arguments(B):
 
 def test_append_rejects_bad_arguments(B):
     lib = B.library()
-    fake = 1 << 20
+    fake = _fake_ptr()
     assert lib.mla_append_kv(fake, 100, fake, fake, -1, None, None) == 1
     assert lib.mla_append_kv(fake, 0, fake, fake, 2, None, None) == 1
     assert lib.mla_append_kv(None, 100, fake, fake, 2, None, None) == 1
@@ -174,7 +197,7 @@ def test_append_rejects_bad_arguments(B):
 
 def test_merge_two_rejects_bad_arguments(B):
     lib = B.library()
-    fake = 1 << 20
+    fake = _fake_ptr()
     assert lib.mla_merge_two_states(fake, fake, fake, fake, 4, fake, 2, None, None) == 2
     assert lib.mla_merge_two_states(fake, fake, fake, fake, -1, fake, 0, None, None) == 1
     assert lib.mla_merge_two_states(None, fake, fake, fake, 4, fake, 0, None, None) == 1
@@ -184,7 +207,7 @@ def test_merge_two_rejects_bad_arguments(B):
 
 def test_fp8_entry_points_reject_bad_arguments(B):
     lib = B.library()
-    fake = 1 << 20
+    fake = _fake_ptr()
     plan, ws_bytes = B.decode_plan(np.array([0, 100, 300], dtype=np.int32), 16, num_sms=152)
     need = B.decode_fp8_workspace_bytes(plan)
     # plan workspace + two 18 KB query images + 2 x 16 factors, 256-byte aligned regions
@@ -238,7 +261,7 @@ def test_graph_capacities_hold_every_plan_they_promise(B):
 
 def test_graph_run_rejects_bad_arguments(B):
     lib = B.library()
-    fake = 1 << 20
+    fake = _fake_ptr()
     words, ws = B.decode_graph_sizes(8, 16, 152)
 
     def run(pw=words, wsb=ws, q=fake, heads=16, out_dtype=0, plan=fake):
@@ -268,7 +291,7 @@ def test_empty_batch_run_checks_arguments_and_launches_nothing(B):
     lib = B.library()
     plan, ws_bytes = B.decode_plan(np.array([0], dtype=np.int32), 16, num_sms=152)
     assert plan[2] == 0
-    fake = 1 << 20   # never dereferenced
+    fake = _fake_ptr()   # never dereferenced
     ph = np.ascontiguousarray(plan, dtype=np.int32)
 
     def run(plan_dev=fake, ws=fake):
@@ -280,14 +303,29 @@ def test_empty_batch_run_checks_arguments_and_launches_nothing(B):
     assert run(ws=None) == 1
 
 
-def test_decoder_refuses_index_arrays_shorter_than_its_plan(B):
-    # the kernels trust kv_indices to hold kv_indptr[batch] slots: the
-    # convenience holder checks that on the host before any launch
+def test_wrappers_refuse_index_arrays_shorter_than_the_plan(B):
+    # the kernels trust kv_indices to hold the slots kv_indptr names (the ABI
+    # passes no lengths): every binding wrapper with a host plan checks both
+    # sizes against the plan before any launch
     import torch
-    dec = B.Decoder(np.array([0, 100, 300], dtype=np.int32), 16, device="cpu", num_sms=152)
+    plan, _ = B.decode_plan(np.array([0, 100, 300], dtype=np.int32), 16, num_sms=152)
+    assert B.plan_nnz(plan) == 300
     ok_ptr, ok_idx = torch.zeros(3, dtype=torch.int32), torch.zeros(300, dtype=torch.int32)
-    dec._check_csr(ok_ptr, ok_idx)
+    B._check_csr(plan, ok_ptr, ok_idx, "t")
     with pytest.raises(ValueError, match="kv_indices has 299 entries"):
-        dec._check_csr(ok_ptr, torch.zeros(299, dtype=torch.int32))
+        B._check_csr(plan, ok_ptr, torch.zeros(299, dtype=torch.int32), "t")
     with pytest.raises(ValueError, match="kv_indptr has 4 entries"):
-        dec._check_csr(torch.zeros(4, dtype=torch.int32), ok_idx)
+        B._check_csr(plan, torch.zeros(4, dtype=torch.int32), ok_idx, "t")
+    # the wrappers raise before touching the library (CPU tensors stand in)
+    x = torch.zeros(4, dtype=torch.float32)
+    short = torch.zeros(299, dtype=torch.int32)
+    for call in (lambda: B.decode_run(plan, x, x, x, x, ok_ptr, short, 0.1, x, None, x),
+                 lambda: B.decode_attend(plan, x, x, x, x, ok_ptr, short, 0.1, x, None, x),
+                 lambda: B.decode_run_noalloc(plan, x, x, x, x, ok_ptr, short, 0.1, x, None),
+                 lambda: B.decode_run_fp8(plan, x, x, x, x, 0.03, ok_ptr, short, 0.1, x, None, x),
+                 lambda: B.decode_run_multi_query(plan, x, 1, x, x, x, ok_ptr, short, 0.1, x, None, x)):
+        with pytest.raises(ValueError, match="kv_indices has 299 entries"):
+            call()
+    # an empty batch covers no tokens
+    empty, _ = B.decode_plan(np.array([0], dtype=np.int32), 16, num_sms=152)
+    assert B.plan_nnz(empty) == 0

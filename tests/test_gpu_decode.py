@@ -227,8 +227,16 @@ def test_plan_item_outside_its_request_is_reported_not_faulted(H):
     bad[items_off + 4 * (n_items - 1) + 2] = bt.nnz + 64      # last item reaches past kv_indices
     out = torch.zeros((bt.batch, H, 512), device="cuda")
     lse = torch.zeros((bt.batch, H), device="cuda")
-    binding.decode_run(bad, torch.from_numpy(bad).cuda(), dev["q_nope"], dev["q_rope"], dev["kv_cache"],
-                       dev["kv_indptr"], dev["kv_indices"], bt.sm_scale, out, lse, dec.workspace)
+    # straight through the C ABI: the binding would refuse this plan on the
+    # host (its last item reaches past kv_indices); the kernels must cope too
+    import ctypes
+    bad_d = torch.from_numpy(bad).cuda()
+    st = binding.library().mla_decode_run(
+        bad.ctypes.data, bad_d.data_ptr(), dev["q_nope"].data_ptr(), dev["q_rope"].data_ptr(),
+        dev["kv_cache"].data_ptr(), bt.pool, dev["kv_indptr"].data_ptr(), dev["kv_indices"].data_ptr(),
+        ctypes.c_float(bt.sm_scale), out.data_ptr(), 0, lse.data_ptr(), dec.workspace.data_ptr(),
+        dec.workspace.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
     assert dec.check() == 7          # MLA_ERR_PLAN_MISMATCH
     dec.workspace.zero_()
     (o2, l2), _ = run_gpu(bt, dev=dev)
