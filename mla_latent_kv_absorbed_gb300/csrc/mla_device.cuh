@@ -216,6 +216,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory to the shared memory of another CTA of the cluster
+// (dst and bar are that CTA's addresses, from mapa), completing `bytes` of
+// transaction count on that CTA's mbarrier.  The copy runs in the async
+// proxy: generic writes of the source must be fenced before it is issued.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+
 // Brings `bytes` (multiple of 16, 16-byte aligned) of global memory into L2
 // as one bulk request; completes asynchronously, nothing to wait on.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
