@@ -186,12 +186,10 @@ int launch_decode(const DecodeParams& p, int variant, const void* q_nope, const 
       return MLA_ERR_CUDA;
     return launch_swab(H, tm_kv, tm_qn, tm_qr, p, p.num_workers, st);
   }
-  // the pair kernel's CTAs each take half of the rope dims (64-byte rows)
-  // and load the rope query as two boxes of H/2 rows: this CTA's heads, then
-  // the peer's
+  // the pair kernel's CTAs each take half of the rope dims: 64-byte rows
   CUtensorMap tm_kr;
   if (!make_map(&tm_kr, kv_cache, kRow, static_cast<uint64_t>(p.num_slots), 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&tm_qr, q_rope, kRope, qrows, 32, static_cast<uint32_t>(H / 2), CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map(&tm_qr, q_rope, kRope, qrows, 32, static_cast<uint32_t>(H), CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
   return launch_pair(H, tm_kv, tm_kr, tm_qr, p, p.num_workers, st);
 }

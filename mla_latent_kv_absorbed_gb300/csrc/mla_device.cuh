@@ -329,6 +329,10 @@ __device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uin
 __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
+// Two floats as an E5M2 pair (low byte = a), round to nearest, saturating.
+__device__ __forceinline__ uint32_t e5m2x2(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2));
+}
 // The two values of an E4M3 pair, exactly.
 __device__ __forceinline__ float2 e4m3x2_value(uint32_t v) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFFu), __NV_E4M3);
@@ -459,11 +463,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0
-// in bits 7-9 and 10-12) and an fp32 accumulator; other fields as above.
+// Instruction descriptor for kind::f8f6f4 with an fp32 accumulator: the A
+// and B formats are independent (bits 7-9 and 10-12; E4M3 = 0, E5M2 = 1);
+// other fields as above.
+constexpr uint32_t kFmtE4M3 = 0, kFmtE5M2 = 1;
+__host__ __device__ constexpr uint32_t idesc_f8(uint32_t a_fmt, uint32_t b_fmt, int M, int N, bool a_mn_major,
+                                                bool b_mn_major) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// E4M3 A and B.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc_f8(kFmtE4M3, kFmtE4M3, M, N, a_mn_major, b_mn_major);
 }
 
 // ---------------------------------------------------------------- cluster --

@@ -4,75 +4,70 @@
 // one SM cannot hold the whole problem: the fp32 output O[128 heads x 512]
 // alone is all 512 TMEM columns.  So a worker is a cluster of two CTAs that
 // split the latent dimensions: CTA c owns latent dims D_c = [256c, 256c+256)
-// of every row and half of the rope key, and the softmax of half the heads.
+// of every row and half of the rope key.
 //
 //   QK (per CTA, partial):  S_c[128 h x 64 tok] = Q[:, D_c] . K[:, D_c]^T  (+ its rope half)
-//   exchange 1:             each CTA sends its fp32 partial of the PEER's heads
-//                           to the peer (distributed shared memory)
-//   softmax (own heads):    s = S_c + S_peer, an fp32 sum of the two halves,
-//                           online softmax, P as bf16
-//   exchange 2:             each CTA copies its heads' P rows to the peer
+//   exchange:               each CTA sends its partial row of every head to
+//                           the other through distributed shared memory
+//   combine:                S = S_c + decoded S_(1-c)
+//   softmax:                each CTA its own P and row sums
 //   PV (per CTA):           O_c[128 h x 256] += P[128 x 64 tok] . V[64 tok x D_c]
 //
-// so no product is computed twice, no latent byte is loaded twice, and no
-// score is held in less than fp32 on the way.  ("实现差距：MLA 与 DeepSeek V3",
-// section 2.4: the latent and rope dot products are summed and scaled by
-// sm_scale, FA2-style online softmax, the latent rows reused as the values;
-// "Attention backends", paragraph "MLA": every KV byte used by all 128 heads.)
+// so no product is computed twice and no latent byte is loaded twice.
+// ("实现差距：MLA 与 DeepSeek V3", section 2.4: the latent and rope dot products
+// are summed and scaled by sm_scale, FA2-style online softmax, the latent rows
+// reused as the values; "Attention backends",
+// paragraph "MLA": every KV byte used by all 128 heads.)
 //
 // The exchange is the narrow path: an SM moves only about 9 bytes per cycle
-// to its cluster peer.  Per 64-token tile each CTA sends 64 heads x 64
-// partial scores x 4 B (16 KB) and 64 rows x 128 B of P (8 KB); the softmax
-// of a head runs in one CTA only, so neither it nor the scores are
-// duplicated.
-//
-// Rows.  In CTA c, TMEM lane / P row / O row r < H/2 is this CTA's head
-// c*H/2 + r ("own"), and row 64 + r is the peer's head (1-c)*H/2 + r; other
-// rows are padding (zero query).  Own rows sit in lane quadrants 0-1, peer
-// rows in quadrants 2-3, so the warps of quadrants 0-1 take the softmax and
-// those of quadrants 2-3 the exchange of the peer's rows.
+// to its cluster peer, so the partial rows travel as 23-bit fixed point (3
+// bytes) with a power-of-two step per row and 32-token half (32 scores: 96 B
+// + a 4-byte exponent), 25 KB per tile in each direction.  With s_max the
+// largest |partial| of the half row, the rounding error is at most 2^-22
+// s_max per partial, about what fp32 itself loses summing the 288 products,
+// at any query magnitude.  Each CTA adds its own EXACT partial to the peer's
+// decoded one, so a score carries one rounding (the peer's), not two.  The two
+// CTAs' scores may then differ in their last bits; that is harmless because
+// each CTA normalises its own half of O with its own row sum (softmax weights
+// and normaliser from the same scores), and only CTA 0 writes the lse.
 //
 // TMEM (512 columns per CTA): O_c [0,256) fp32; the query's latent half
-// [256,384) as packed bf16 (A operand of QK); two score buffers [384,448),
-// [448,512) holding this CTA's raw fp32 partial.
+// [256,384) as packed bf16 (A operand of QK, read from TMEM); two score
+// buffers [384,448), [448,512) that hold this CTA's fp32 partial.
 //
 // Shared memory per CTA: a ring of 4 latent blocks (64 tokens x 256 dims,
-// 32 KB, TMA gather4), 4 rope atoms (4 KB: this CTA's 32 rope dims, 64-byte
-// swizzle), the rope query (8 KB), 2 P slots (128 rows x 64 tokens bf16, the
-// A operand of PV: rows 0-63 written here, rows 64-127 copied in by the
-// peer), 2 receive slots (the peer's fp32 partials of this CTA's heads,
-// 16 KB), 2 side slots (the peer's rescale factors and row sums), reduction
-// buffers.
+// 32 KB, gathered with TMA gather4), 4 rope atoms (4 KB: this CTA's 32 rope
+// dims, 64-byte swizzle), the rope query (8 KB), 2 exchange slots (16 KB
+// each: the high parts of the peer's partial rows, later overwritten in place
+// by P as bf16, the A operand of PV), their low-byte blocks (8 KB each), the
+// peer's exponents and the softmax warps' reduction buffers.
 //
-// Warp roles per CTA (800 threads).  Row warp w < 16 sits on lane quadrant
-// w & 3 and takes tokens 16(w >> 2)..+15 of every tile and latent columns
-// 64(w >> 2)..+63 of O:
-//   quadrants 0-1 (own rows)  softmax: add the peer's partial, row maximum
-//               over the four warps of the quadrant, lazy reference, P, row
-//               sums; rescale and write out their rows of O
-//   quadrants 2-3 (peer rows) pushers: push this CTA's partial of the peer's
-//               rows (st.async); write those rows of O out after an item
+// Warp roles per CTA (736 threads).  Warp w of the sixteen score warps owns
+// heads 32(w%4)..+31 (TMEM lane h = head h) and tokens 32((w/4)%2)..+31 of
+// every tile; the sender and the softmax warp of the same heads and tokens
+// hand the S buffer over in place:
+//   warps 8-15  senders: load this CTA's latent half of the query into TMEM;
+//               for tile g quantise their part of this CTA's partial and push
+//               the codes into the peer's exchange slot (st.async)
+//   warps 0-7   softmax: add the peer's decoded partial to this CTA's, take the
+//               softmax (the row maximum is combined with the partner warp of
+//               the other token half), write P over the peer's rows; after an
+//               item's last tile, the epilogue (1/l, O, lse)
 //   warp 16     QK issuer and rope-query loader (one thread)
-//   warp 17     TMEM allocator and PV issuer (one thread), which also copies
-//               this CTA's P rows to the peer (bulk copy)
-//   warps 18-19 takers (lane quadrants 2, 3): once the peer's P rows of a
-//               tile have landed, apply its rescale factors to the peer's
-//               rows of O, then release the tile's PV.  Kept apart from the
-//               pushers so that no push ever waits for a P exchange.
-//   warps 20-24 gather producers: latent atoms 0-3 of the CTA's half, rope
+//   warp 17     TMEM allocator and PV issuer (one thread)
+//   warps 18-22 gather producers: latent atoms 0-3 of the CTA's half, rope;
+//               each loads its tile's slot numbers itself
+// Splitting senders from softmax lets tile g+1 be quantised and pushed while
+// tile g is still in its softmax, so the exchange latency is hidden.
 //
-// Per tile g (S buffer, receive slot and P slot g mod 2): QK(g) -> pushers
-// push the peer's rows, softmax warps read their own rows (freeing the S
-// buffer for QK(g+2)) -> the peer's partials land -> softmax, own P rows ->
-// the PV issuer copies them to the peer -> the peer's P rows land, the
-// takers apply the peer's rescale factors -> PV(g), which frees the latent
-// block and P slot g mod 2.  An item's output is written after the next
-// item's first tile has been pushed and taken through its softmax.
-//
-// The reference maximum moves lazily: only when a tile's maximum exceeds it
-// by more than 64 (log2 units), so O is rescaled rarely.  P stays below 2^64
-// and O, l below 2^100, well inside fp32; a score more than 126 below the
-// reference flushes to zero, at less than 2^-126 of the largest weight.
+// Per tile g (S buffer g mod 2, exchange slot g mod 2): QK(g) -> the senders
+// and the softmax warps both read the buffer (freeing it for QK(g+2)); the
+// senders quantise and push, the softmax warps add the peer's rows when they
+// land and write P -> PV(g) frees the latent block
+// and, through a multicast commit, tells the PEER that its rows for tile g+2
+// may land in this slot.
+// The softmax moves its reference maximum lazily (threshold 8 in log2
+// units) as in the few-heads kernel.
 #include "mla_device.cuh"
 #include "mla_launch.h"
 
@@ -80,37 +75,33 @@ namespace mla {
 namespace pair {
 
 constexpr int T = 64;                        // tokens per tile
-constexpr int kGroup = 16;                   // tokens of a tile per row warp
-constexpr int kRowWarps = 16;                // warps 0-15
-constexpr int kOwnWarps = 8;                 // the row warps of quadrants 0-1
-constexpr int kMmaWarp = 16, kPvWarp = 17;
-constexpr int kTakeWarp0 = 18, kTakeWarps = 2;   // lane quadrants 2 and 3: the peer's rows of O
-constexpr int kProducerWarp0 = kTakeWarp0 + kTakeWarps;
+constexpr int TH = 32;                       // tokens of a tile per row warp
+constexpr int kRowWarps = 8;                 // softmax warps 0-7 and sender warps 8-15 alike
 constexpr int kProducers = 5;                // latent atoms 0-3 and the rope
-constexpr int kCopyWarp = kProducerWarp0 + kProducers;   // copies this CTA's P rows to the peer
-constexpr int kThreads = 32 * (kCopyWarp + 1);
-constexpr int kLatBlocks = 4;                // ring of latent blocks
+constexpr int kSendWarp0 = 8, kMmaWarp = 16, kLoaderWarp = 17, kProducerWarp0 = 18;
+constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
+// A latent block is held from its gathers until its PV, the whole life of a
+// tile in the pipeline, so the ring is as deep as shared memory allows.
+constexpr int kLatBlocks = 4;                // ring of latent blocks (every latent producer fills every block)
 constexpr int kRopeSlots = 4;
+constexpr int kXSlots = 2;                   // exchange slots
 constexpr int kLead = 3;                     // a producer issues tile g once tile g - kLead has landed
-constexpr int kXSlots = 2;                   // receive slots
-constexpr int kPSlots = 2;                   // P slots (also the parity of "PV(g) done")
 constexpr int kAtom = T * 128;               // 8 KB: 64 tokens x 64 dims
 constexpr int kLatBlock = 4 * kAtom;         // 32 KB: 64 tokens x 256 dims
 constexpr int kRopeAtom = T * 64;            // 4 KB: 64 tokens x this CTA's 32 rope dims (64-byte swizzle)
 constexpr int kQRBytes = 128 * 64;           // rope query: 128 rows x this CTA's 32 rope dims
-constexpr int kPSlot = 128 * 128;            // 128 rows x 64 tokens bf16 (K-major, 128-byte swizzle)
-constexpr int kXSlot = 64 * T * 4;           // 64 own rows x 64 tokens fp32 (256-byte rows)
-constexpr int kSideSlot = 2 * 64 * 4;        // [64] rescale factors, [64] row sums
+constexpr int kXSlot = 128 * 128;            // 128 rows x 128 B (64 int16 scores, then 64 bf16 P)
+constexpr int kXLoSlot = 128 * 64;           // the codes' low bytes: [4 chunks (half, part)][128 rows] x 16 B
+constexpr int kXeSlot = 2 * 128 * 4;         // [2 token halves][128 rows] int32 exponents
+constexpr int kXBytes = kXSlot + kXLoSlot + kXeSlot;   // bytes the peer sends per tile
 constexpr int kOffLat = 0;
 constexpr int kOffRope = kOffLat + kLatBlocks * kLatBlock;
-constexpr int kOffQR = kOffRope + kRopeSlots * kRopeAtom;
-constexpr int kOffP = kOffQR + kQRBytes;
-constexpr int kOffX = kOffP + kPSlots * kPSlot;
-constexpr int kOffSide = kOffX + kXSlots * kXSlot;              // the peer's rescale factors / row sums
-constexpr int kOffSideOut = kOffSide + kPSlots * kSideSlot;     // this CTA's, copied to the peer with P
-constexpr int kOffRed = kOffSideOut + kPSlots * kSideSlot;   // [2][4][64] tile maxima, [4][64] row sums
-constexpr int kOffLPeer = kOffRed + (2 * 4 * 64 + 4 * 64) * 4;   // [2 items][64] the peer's row sums, kept by the takers
-constexpr int kOffBar = kOffLPeer + 2 * 64 * 4;
+constexpr int kOffQR = kOffRope + kRopeSlots * kRopeAtom;   // rope query (K-major SW64)
+constexpr int kOffX = kOffQR + kQRBytes;
+constexpr int kOffXLo = kOffX + kXSlots * kXSlot;       // [kXSlots] low-byte blocks from the peer
+constexpr int kOffXE = kOffXLo + kXSlots * kXLoSlot;    // [kXSlots] exponent blocks from the peer
+constexpr int kOffRed = kOffXE + kXSlots * kXeSlot;     // [2 bufs][2 halves][128] row maxima, [2][128] row sums
+constexpr int kOffBar = kOffRed + (2 * 2 * 128 + 2 * 128) * 4;
 // barriers
 constexpr int bLatFull = 0;
 constexpr int bLatEmpty = bLatFull + kLatBlocks;
@@ -119,33 +110,28 @@ constexpr int bRopeEmpty = bRopeFull + kRopeSlots;
 constexpr int bQFull = bRopeEmpty + kRopeSlots;
 constexpr int bQEmpty = bQFull + 1;
 constexpr int bSFull = bQEmpty + 1;          // [2] this CTA's partial is in the S buffer
-constexpr int bSFree = bSFull + 2;           // [2] every row warp has read the S buffer
-constexpr int bXFull = bSFree + 2;           // [kXSlots] the peer's partials have landed here
-constexpr int bXFree = bXFull + kXSlots;     // [kXSlots] the PEER's receive slot may take this CTA's next partials
-constexpr int bPFull = bXFree + kXSlots;     // [kPSlots] the own P rows are written
-constexpr int bPeerP = bPFull + kPSlots;     // [kPSlots] the peer's P rows and side values have landed here
-constexpr int bPeerOK = bPeerP + kPSlots;    // [kPSlots] the senders have applied the peer's rescale factors
-constexpr int bPSlotMine = bPeerOK + kPSlots;   // [kPSlots] this CTA's PV of the slot's tile is done
-constexpr int bPSlotPeer = bPSlotMine + kPSlots;  // [kPSlots] the PEER's PV of the slot's tile is done
-constexpr int bOFull = bPSlotPeer + kPSlots;
+constexpr int bSFree = bSFull + 2;           // [2] the senders and the softmax warps have read the S buffer
+constexpr int bPFull = bSFree + 2;           // [kXSlots] P is in the exchange slot
+constexpr int bPvDone = bPFull + kXSlots;    // [2] PV(g) has completed (buffer g mod 2)
+constexpr int bOFull = bPvDone + 2;
 constexpr int bOEmpty = bOFull + 1;
-constexpr int bDrain = bOEmpty + 1;
+constexpr int bXFull = bOEmpty + 1;          // [kXSlots] the peer's rows have landed in this CTA's slot
+constexpr int bXFree = bXFull + kXSlots;     // [kXSlots] the PEER's slot may take this CTA's next rows
+constexpr int bDrain = bXFree + kXSlots;
 constexpr int kNumBars = bDrain + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffLast = kOffMisc + 16;      // [kLatBlocks + kRopeSlots] last armed use
 constexpr int kSmemBytes = kOffLast + 4 * (kLatBlocks + kRopeSlots) + 1024;
 constexpr int kTmO = 0, kTmQ = 256, kTmS = 384;
-constexpr uint32_t kIdescQK = idesc_bf16(128, T, false, false);     // M=128 rows, N=64 tokens
+constexpr uint32_t kIdescQK = idesc_bf16(128, T, false, false);     // M=128 heads, N=64 tokens
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // N=256 dims, B (V) MN-major
 static_assert(kProducers == 5, "producers 0-3 gather the latent atoms, producer 4 the rope");
-static_assert(kThreads == 832, "26 warps (registers are budgeted as for 28)");
-static_assert(kTakeWarp0 % 4 == 2, "the taker warps sit on lane quadrants 2 and 3");
+static_assert(kThreads == 736, "23 warps");
 static_assert(kLead < kLatBlocks && kLead <= kRopeSlots, "a ring slot's phase must not be lapped while waited on");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffP % 1024 == 0 && kOffX % 1024 == 0 &&
-                  kOffSide % 16 == 0 && kOffBar % 8 == 0,
+static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 1024 == 0 && kXSlot % 1024 == 0 &&
+                  kOffXE % 16 == 0 && kOffBar % 8 == 0,
               "alignment");
-static_assert(kPSlots == 2, "bPSlotMine doubles as the 'PV(g) done' barrier of parity g mod 2");
 
 // Items every role processes: a request in range and a token range inside
 // kv_indices (so no access can leave the arrays).  Whether the range also
@@ -166,11 +152,30 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Head of row r in CTA `cta` for H = 2 Hh heads, or -1 for a padding row.
-__device__ __forceinline__ int row_head(int r, uint32_t cta, int Hh) {
-  if (r < 64) return r < Hh ? static_cast<int>(cta) * Hh + r : -1;
-  return r - 64 < Hh ? static_cast<int>(cta ^ 1u) * Hh + (r - 64) : -1;
-}
+// 2^k as a float, for -126 <= k <= 127.
+__device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
+
+// Partial scores travel as 23-bit fixed point with a power-of-two step per
+// row and 32-token half: with e the exponent of the half row's largest
+// |partial| (nudged up by 2^-21 so that no code reaches 2^22), the step is
+// 2^(e-21), so a code q = rint(partial / step) has |q| < 2^22 and the
+// rounding error is at most 2^-22 of the largest |partial|, about fp32's own
+// rounding of a sum of 288 products.  The code goes as offset binary
+// u = q + 2^22 in 23 bits: its high 16 bits (u >> 8) in the slot's 128-byte
+// rows (the bytes P later overwrites in place), its low 8 bits in a side
+// block.  Rounding and decoding use full-rate float arithmetic:
+//   encode: partial / step + 1.5 * 2^23 rounds to the nearest integer (ties to
+//           even) and leaves u in the low 23 bits of the float;
+//   decode: the bits 0x4B000000 | x are the float 2^23 + x, so with
+//           fh = 2^23 + (u >> 8) and fl = 2^23 + (u & 255),
+//           fh * 256 step + fl * step - (2^31 + 2^23 + 2^22) step = q * step,
+//           exactly, as two FMAs whose results are representable.
+// Both the sender (from its own codes) and the receiver (from the peer's)
+// form q * step exactly and then multiply by the same factor once, so the
+// two CTAs hold the same scaled partials and, after one commutative add,
+// the same scores.
+constexpr float kEncBias = 12582912.0f;      // 1.5 * 2^23
+constexpr float kDecHi = 2160066560.0f;      // 2^31 + 2^23 + 2^22 = 515 * 2^22 (exact in fp32)
 
 __global__ void __launch_bounds__(kThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kr,
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t cta = cluster_ctarank();        // 0 or 1: which latent half, which heads
+  const uint32_t cta = cluster_ctarank();        // 0 or 1: which latent half
   const uint32_t peer = cta ^ 1u;
   auto bar = [&](int i) -> uint32_t { return base + kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -190,7 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{abort_flag, p.status};
 #ifdef MLA_TRACE
   if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     MLA_TRACE_RAW(15, 0, static_cast<long long>(globaltimer()));
+    MLA_TRACE_RAW(15, 2, static_cast<long long>(smid));
     MLA_TRACE_RAW(15, 3, clock64());
   }
 #endif
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int it0, it1;
   plan_items(p, w, it0, it1);
   const int32_t* items = p.plan + p.items_off;
-  const int H = p.heads, Hh = H >> 1;
+  const int H = p.heads;
   const int nnz = __ldg(p.kv_indptr + p.batch);   // loaded alongside the plan words
 
   if (threadIdx.x == 0) {
@@ -208,20 +216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bQFull), kRowWarps + 1);       // the row warps (latent half) + the rope TMA
     mbar_init(bar(bQEmpty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(bSFull + i), 1);
-      mbar_init(bar(bSFree + i), kRowWarps);
+      mbar_init(bar(bSFull + i), 1); mbar_init(bar(bSFree + i), 2 * kRowWarps);
     }
     for (int i = 0; i < kXSlots; ++i) {
+      mbar_init(bar(bPFull + i), kRowWarps);
       mbar_init(bar(bXFull + i), 1);             // own expect_tx; the bytes come from the peer
-      mbar_init(bar(bXFree + i), 1);             // the peer's PV issuer (commit)
+      mbar_init(bar(bXFree + i), 1);             // the peer's PV commit
     }
-    for (int i = 0; i < kPSlots; ++i) {
-      mbar_init(bar(bPFull + i), kOwnWarps);
-      mbar_init(bar(bPeerP + i), 1);             // own expect_tx; the bytes come from the peer
-      mbar_init(bar(bPeerOK + i), kTakeWarps);
-      mbar_init(bar(bPSlotMine + i), 1);         // this CTA's PV commit
-      mbar_init(bar(bPSlotPeer + i), 1);         // the peer's PV commit
-    }
+    mbar_init(bar(bPvDone), 1);
+    mbar_init(bar(bPvDone + 1), 1);
     mbar_init(bar(bOFull), 1);
     mbar_init(bar(bOEmpty), kRowWarps);
     mbar_init(bar(bDrain), 2);                   // both issuers' final commits
@@ -229,10 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // rope-query rows of padding heads stay zero (each TMA box has H/2 rows)
+  // rope-query rows >= H stay zero (the TMA box has H rows)
   for (int i = threadIdx.x; i < kQRBytes / 16; i += blockDim.x)
     *reinterpret_cast<uint4*>(smem + kOffQR + 16 * i) = make_uint4(0, 0, 0, 0);
-  if (warp == kPvWarp) {
+  if (warp == kLoaderWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -243,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // the merge kernel may be launched now: it waits for this grid to finish
   griddep_launch_dependents();
-  bool aborted = false;                          // set by the row and taker warps only
+  bool aborted = false;                          // set by the softmax / sender warps only
 
-  if (warp >= kProducerWarp0 && warp < kCopyWarp) {
+  if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
     // A warp completes one gather4 only every ~70-110 cycles, so a tile's
     // landing time is set by how many gathers one warp issues for it.  The
@@ -258,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && pw == 0) tma_prefetch_desc(&tm_kv);
     if (lane == 0 && pw == 4) tma_prefetch_desc(&tm_kr);
     const uint64_t pol = l2_policy_evict_first();
+    // The slot numbers of the next tile are loaded while this tile waits for
+    // ring space and issues its gathers, so their latency is hidden.
     int it = it0, s = 0, n = 0;
     auto next_item = [&]() {                     // first usable item from `it` on
       for (; it < it1; ++it) {
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         t0 = 0;
       }
       if (it < it1) load_slots(t0, vn);
+      if (lane == 0 && pw == 0) MLA_TRACE_EVENT(0, g);
       {
         const bool rope = pw == 4;
         const uint32_t nslots = rope ? kRopeSlots : kLatBlocks;
@@ -313,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!e_ok) { ok = false; break; }
         if (rope) {
           if (lane == 0) mbar_arrive_expect_tx(full, kRopeAtom);
+          if (lane == 0) MLA_TRACE_EVENT(11, g);
           __syncwarp();
           if (lane < 16)
             tma_gather4(base + kOffRope + slot * kRopeAtom + lane * 256, &tm_kr, 512 + 32 * static_cast<int>(cta),
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_gather4(base + kOffLat + slot * kLatBlock + pw * kAtom + lane * 512, &tm_kv,
                         64 * (4 * static_cast<int>(cta) + pw), v[0], v[1], v[2], v[3], full, pol);
           if (lane == 0 && pw == 0) atomicMax(last_armed + slot, static_cast<int>(use));
-          if (lane == 0 && pw == 0) MLA_TRACE_EVENT(0, g);
+          if (lane == 0 && pw == 0) MLA_TRACE_EVENT(1, g);
         }
       }
       ++g;
@@ -335,43 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = last_armed[lane];
       const int bfull = lane < kLatBlocks ? bLatFull + lane : bRopeFull + (lane - kLatBlocks);
       if (u >= 0) drain_wait(bar(bfull), u & 1);
-    }
-    __syncwarp();
-  } else if (warp == kCopyWarp) {
-    // ------------------------------------------------------------- P copier
-    // Tile g: once the softmax warps have written their P rows (so they have
-    // also consumed the peer's partials of tile g), let the peer's pushers
-    // refill that receive slot, and once the peer's PV of tile g - kPSlots
-    // has freed the peer's P slot, copy the P rows and the side slot there.
-    if (lane == 0) {
-      // this CTA's rows 0..H/2-1 of a P slot are the peer's rows 64..64+H/2-1
-      const uint32_t peer_p = mapa_shared(base + kOffP + 64 * 128, peer);
-      const uint32_t peer_pbar = mapa_shared(bar(bPeerP), peer);
-      const uint32_t peer_side = mapa_shared(base + kOffSide, peer);
-      const uint32_t p_bytes = static_cast<uint32_t>(Hh) * 128u;
-      const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
-      uint32_t g = 0;
-      bool ok = true;
-      for (int it = it0; it < it1 && ok; ++it) {
-        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-        if (!item_ok(p, nnz, b, s, e)) continue;
-        const int nt = (e - s + T - 1) / T;
-        for (int j = 0; j < nt; ++j, ++g) {
-          const uint32_t ps = g % kPSlots, use = g / kPSlots;
-          if (!mbar_wait(bar(bPFull + ps), use & 1, wc)) { ok = false; break; }
-          // the arrive on the peer's barrier rides on a tensor-core commit: it
-          // tracks no MMA of this thread, and unlike a thread's remote arrive
-          // it does not queue behind the pushers' stores
-          umma_commit_mc(bar(bXFree + g % kXSlots), peer_mask);
-          if (g >= static_cast<uint32_t>(kPSlots) && !mbar_wait<true>(bar(bPSlotPeer + ps), (use - 1) & 1, wc)) {
-            ok = false;
-            break;
-          }
-          bulk_copy_to_peer(peer_p + ps * kPSlot, base + kOffP + ps * kPSlot, p_bytes, peer_pbar + 8u * ps);
-          bulk_copy_to_peer(peer_side + ps * kSideSlot, base + kOffSideOut + ps * kSideSlot, kSideSlot,
-                            peer_pbar + 8u * ps);
-        }
-      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -392,12 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = (e - s + T - 1) / T;
         // the rope query of this item replaces the previous one once its last QK is done
         if (nitem > 0 && !mbar_wait(bar(bQEmpty), (nitem - 1) & 1, wc)) break;
-        // rows 0..H/2-1: this CTA's heads; rows 64..64+H/2-1: the peer's
         mbar_arrive_expect_tx(bar(bQFull), H * 64);
-        tma_load_2d(base + kOffQR, &tm_qr, 32 * static_cast<int>(cta), b * H + static_cast<int>(cta) * Hh,
-                    bar(bQFull));
-        tma_load_2d(base + kOffQR + 64 * 64, &tm_qr, 32 * static_cast<int>(cta), b * H + static_cast<int>(peer) * Hh,
-                    bar(bQFull));
+        tma_load_2d(base + kOffQR, &tm_qr, 32 * static_cast<int>(cta), b * H, bar(bQFull));
         if (!mbar_wait(bar(bQFull), nitem & 1, wc)) break;     // + the latent half in TMEM
         for (int j = 0; j < nt; ++j, ++g) {
           const uint32_t d_s = tmem + kTmS + (g & 1) * 64;
@@ -410,8 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 16; ++k)            // 256 latent dims = 16 K-steps; A (query) from TMEM
             umma_ts(d_s, tmem + kTmQ + 8 * k, D(bk, (k >> 2) * kAtom + (k & 3) * 32), kIdescQK, k != 0 ? 1u : 0u);
+          MLA_TRACE_EVENT(10, g);
           if (!mbar_wait(bar(bRopeFull + rs), (g / kRopeSlots) & 1, wc)) { ok = false; break; }
           tc_fence_after();
+          MLA_TRACE_EVENT(12, g);
           const uint64_t br = D(dr, rs * kRopeAtom);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)          // this CTA's half of the rope dims: 2 K-steps of 16
@@ -427,11 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(bar(bDrain), 0);
     }
     __syncwarp();
-  } else if (warp == kPvWarp) {
-    // ------------------------------------------------- PV issuer + P copier
+  } else if (warp == kLoaderWarp) {
+    // ----------------------------------------------------------- PV issuer
     if (lane == 0) {
       const uint64_t dv = sdesc(base + kOffLat, kAtom, 1024);      // latent block 0, MN-major (B of PV)
-      const uint64_t dp = sdesc(base + kOffP, 16, 1024);           // P slot 0 (A of PV)
+      const uint64_t dp = sdesc(base + kOffX, 16, 1024);           // P in exchange slot 0 (A of PV)
       auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
       const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
       uint32_t g = 0, nitem = 0;
@@ -441,20 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!item_ok(p, nnz, b, s, e)) continue;
         const int nt = (e - s + T - 1) / T;
         for (int j = 0; j < nt; ++j, ++g) {
-          const uint32_t ps = g % kPSlots, blk = g % kLatBlocks, use = g / kPSlots;
-          if (!mbar_wait(bar(bPFull + ps), use & 1, wc)) { ok = false; break; }       // own P rows (and O rescaled)
-          MLA_TRACE_EVENT(4, g);
-          if (!mbar_wait(bar(bPeerOK + ps), use & 1, wc)) { ok = false; break; }      // the peer's P rows, applied
+          const uint32_t xs = g % kXSlots, blk = g % kLatBlocks;
+          if (!mbar_wait(bar(bPFull + xs), (g / kXSlots) & 1, wc)) { ok = false; break; }
           if (j == 0 && nitem > 0 && !mbar_wait(bar(bOEmpty), (nitem - 1) & 1, wc)) { ok = false; break; }
           tc_fence_after();
+          MLA_TRACE_EVENT(4, g);
           const uint64_t bv = D(dv, blk * kLatBlock);
-          const uint64_t ap = D(dp, ps * kPSlot);
+          const uint64_t ap = D(dp, xs * kXSlot);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)          // 64 tokens = 4 K-steps of 16
             umma_ss(tmem + kTmO, D(ap, ks * 32), D(bv, ks * 2048), kIdescPV, (j == 0 && ks == 0) ? 0u : 1u);
           umma_commit(bar(bLatEmpty + blk));
-          umma_commit(bar(bPSlotMine + ps));
-          umma_commit_mc(bar(bPSlotPeer + ps), peer_mask);     // in the peer: "the peer's PV of slot ps is done"
+          umma_commit_mc(bar(bXFree + xs), peer_mask);         // the peer may send into this slot again
+          umma_commit(bar(bPvDone + (g & 1)));
           if (j == nt - 1) umma_commit(bar(bOFull));
           MLA_TRACE_EVENT(5, g);
         }
@@ -465,392 +432,341 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------- row warps and takers
-    // Row warp w < 16: lane quadrant w & 3, token group / column quarter w >> 2.
-    // Taker warps 18 and 19: lane quadrants 2 and 3, all 256 columns.
-    const bool taker = warp >= kTakeWarp0;
-    const int q = warp & 3, kg = taker ? 0 : warp >> 2;
-    const bool own = q < 2;
-    const int r = 32 * q + lane;                 // TMEM lane, P row, O row
-    const int rl = own ? r : r - 64;             // row within the own or the peer half
-    const int h = row_head(r, cta, Hh);          // head of this row, -1 for padding
-    const bool row_ok = h >= 0;
+    // ----------------------------------------------- sender and softmax warps
+    const bool is_sender = warp >= kSendWarp0;
+    const int q = warp & 3, th = (warp >> 2) & 1;   // TMEM lane quadrant, token half of every tile
+    const int h = 32 * q + lane;                 // head == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    float* red_max = reinterpret_cast<float*>(smem + kOffRed);           // [2][4][64]
-    float* red_l = red_max + 2 * 4 * 64;                                 // [4][64]
-    const float* side = reinterpret_cast<const float*>(smem + kOffSide);
+    const bool head_ok = h < H;
+    const uint32_t sw = static_cast<uint32_t>(h & 7);      // 16-byte chunk c of row h sits at c ^ (h mod 8)
+    const uint32_t xrow_peer = mapa_shared(base + kOffX + h * 128, peer);
+    const uint32_t xe_peer = mapa_shared(base + kOffXE + (th * 128 + h) * 4, peer);
+    const uint32_t xlo_peer = mapa_shared(base + kOffXLo + h * 16, peer);
+    const uint32_t xfull_peer = mapa_shared(bar(bXFull), peer);
+    float* red_max = reinterpret_cast<float*>(smem + kOffRed);            // [2][2][128]
+    float* red_l = red_max + 2 * 2 * 128;                                 // [2 halves][128]
+    float m_ref = 0.f, l_sum = 0.f;
     auto wait = [&](uint32_t bb, uint32_t par, bool cluster_scope) {
       if (aborted) return;
-      bool ok = true;
-      if (lane == 0) ok = cluster_scope ? mbar_wait<true>(bb, par, wc) : mbar_wait(bb, par, wc);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) aborted = true;
-    };
-    // PV(g) has completed (this CTA)
-    auto wait_pv = [&](uint32_t g) { wait(bar(bPSlotMine + (g % kPSlots)), (g / kPSlots) & 1, false); };
-    // O row r, columns [c0, c0 + 16 n), times alpha (after PV(g-1))
-    auto rescale_o = [&](float alpha, int c0, int n) {
-      if (aborted) return;
-#pragma unroll 1
-      for (int c = 0; c < n; ++c) {
-        uint32_t o[16];
-        const uint32_t ta = tmem + lane_off + kTmO + c0 + 16 * c;
-        tmem_ld16(ta, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st16(ta, o);
-      }
-      tmem_wait_st();
-    };
-    // the usable items, walked by every role in the same order
-    auto next_ok = [&](int i) {
-      for (; i < it1; ++i) {
-        const int b = items[4 * i], s = items[4 * i + 1], e = items[4 * i + 2];
-        if (item_ok(p, nnz, b, s, e)) return i;
-      }
-      return it1;
+      bool r = true;
+      if (lane == 0) r = cluster_scope ? mbar_wait<true>(bb, par, wc) : mbar_wait(bb, par, wc);
+      r = __shfl_sync(0xffffffffu, r, 0);
+      if (!r) aborted = true;
     };
 
-    if (taker) {
-      // ---------------------------------------------------------- takers
-      // tile g: once the peer's P rows have landed, apply its rescale factors
-      // to these 32 rows of O (all 256 columns); PV(g) waits for this
-      // (an item's last tile also brings the peer's row sums: they are kept
-      // here, per item parity, for the pushers' write-out after its last PV)
-      float* l_peer = reinterpret_cast<float*>(smem + kOffLPeer);
-      uint32_t g = 0, nitem = 0;
-      for (int it = next_ok(it0); it < it1; it = next_ok(it + 1), ++nitem) {
-        const int s = items[4 * it + 1], e = items[4 * it + 2];
-        const int nt = (e - s + T - 1) / T;
-        for (int j = 0; j < nt; ++j, ++g) {
-          const uint32_t ps = g % kPSlots;
-          // arm the slot for the peer's P rows and side slot of tile g: by the
-          // taker that also waits on it, so never before tile g - 2's phase
-          // has completed (the bytes may land either side of the arm)
-          if (warp == kTakeWarp0 && lane == 0 && !aborted)
-            mbar_arrive_expect_tx(bar(bPeerP + ps), static_cast<uint32_t>(Hh) * 128u + kSideSlot);
-          wait(bar(bPeerP + ps), (g / kPSlots) & 1, true);
-          if (lane == 0 && warp == kTakeWarp0) MLA_TRACE_EVENT(13, g);
-          if (j == nt - 1 && row_ok && !aborted)
-            l_peer[(nitem & 1) * 64 + rl] = side[ps * (kSideSlot / 4) + 64 + rl];
-          const float alpha = (!aborted && row_ok) ? side[ps * (kSideSlot / 4) + rl] : 1.f;
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {   // never on an item's first tile
-            wait_pv(g - 1);
-            tc_fence_after();
-            rescale_o(alpha, 0, 16);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0 && !aborted) mbar_arrive(bar(bPeerOK + ps));
-        }
-      }
-    } else {
-      // -------------------------------------------------------- row warps
-      // -- this warp's 16 S columns of tile g (raw fp32 partial), then free the S buffer
-      auto read_s = [&](uint32_t g, uint32_t (&v)[16]) {
-        const uint32_t sb = g & 1;
-        wait(bar(bSFull + sb), (g >> 1) & 1, false);
+    // -- tile g of this CTA: quantise this warp's 32 partial scores of row h
+    //    and push the codes to the peer (the softmax warps read the same
+    //    partials from TMEM themselves)
+    auto send = [&](uint32_t g) {
+      const uint32_t sb = g & 1, xs = g % kXSlots;
+      const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64 + th * TH;
+      wait(bar(bSFull + sb), (g >> 1) & 1, false);
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(6, g);
+      tc_fence_after();
+      uint32_t qw[16], lb[16];
+      int e_own;
+      {
+        uint32_t r[32];
         if (!aborted) {
-          tc_fence_after();
-          tmem_ld16(tmem + lane_off + kTmS + sb * 64 + kg * kGroup, v);
+          tmem_ld16(tm_s, *reinterpret_cast<uint32_t(*)[16]>(r));
+          tmem_ld16(tm_s + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0;
+          for (int i = 0; i < 32; ++i) r[i] = 0;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(bar(bSFree + sb));
-      };
-
-      // -- the latent half of the query of request b for this warp's row and 64 dims, into TMEM
-      auto load_q = [&](int b) {
-        if (!aborted) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              p.q_nope + (static_cast<size_t>(b) * H + (row_ok ? h : 0)) * kLatent + 256 * cta + 64 * kg);
+        // the step is 2^(e-21), e the exponent of max|s| nudged up by 2^-21 so
+        // that no code rounds to 2^22
+        float mx = 0.f;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {          // 2 x 16 columns = 64 bf16
-            uint32_t v16[16];
+        for (int i = 0; i < 32; i += 2) mx = max3(mx, fabsf(__uint_as_float(r[i])), fabsf(__uint_as_float(r[i + 1])));
+        mx *= 1.000000476837158203125f;
+        e_own = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127, -100);
+        const float inv = pow2i(min(21 - e_own, 127));
+        const float2 inv2 = f2_pack(inv, inv), enc2 = f2_pack(kEncBias, kEncBias);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 t = f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), inv2, enc2);
+          qw[i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x6521);   // u >> 8, two codes
+          lb[i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);   // u & 255, two codes
+        }
+      }
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(13, g);
+      // push into the peer's slot xs once the peer's PV(g - kXSlots) has read it
+      if (g >= kXSlots) wait(bar(bXFree + xs), ((g / kXSlots) - 1) & 1, true);
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(14, g);
+      if (!aborted) {
+        const uint32_t fb = xfull_peer + 8u * xs;
+        const uint32_t dst = xrow_peer + xs * kXSlot;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t c = static_cast<uint32_t>(4 * th + k);
+          st_async_v4(dst + ((c ^ sw) << 4), qw[4 * k], qw[4 * k + 1], qw[4 * k + 2], qw[4 * k + 3], fb);
+        }
+        // low bytes: 32 codes of this row and half as 2 chunks of 16, chunk k
+        // of half th at row h of block (2 th + k)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w[i] = __byte_perm(lb[8 * k + 2 * i], lb[8 * k + 2 * i + 1], 0x5410);
+          st_async_v4(xlo_peer + xs * kXLoSlot + static_cast<uint32_t>((2 * th + k) * 128) * 16u, w[0], w[1], w[2], w[3],
+                      fb);
+        }
+        st_async_b32(xe_peer + xs * kXeSlot, static_cast<uint32_t>(e_own), fb);
+      }
+      if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(8, g);
+    };
+
+    // -- tile g (j-th of an item of n tokens): add the peer's rows, softmax, P
+    auto softmax = [&](uint32_t g, int j, int n) {
+      const uint32_t sb = g & 1, xs = g % kXSlots;
+      const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64 + th * TH;
+      // arm slot xs for the peer's rows of tile g: done here, by the warp that
+      // also waits on it, so the arm for tile g + kXSlots cannot come before
+      // this tile's phase has completed (the peer's bytes may land either side)
+      if (warp == 0 && lane == 0 && !aborted) mbar_arrive_expect_tx(bar(bXFull + xs), kXBytes);
+      wait(bar(bSFull + sb), (g >> 1) & 1, false);
+      uint32_t sv[32];
+      if (!aborted) {
+        tc_fence_after();
+        tmem_ld16(tm_s, *reinterpret_cast<uint32_t(*)[16]>(sv));
+        tmem_ld16(tm_s + 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16));
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[i] = 0;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(bar(bSFree + sb));
+      wait(bar(bXFull + xs), (g / kXSlots) & 1, true);
+      if (threadIdx.x == 0) MLA_TRACE_EVENT(9, g);
+      // s = (own exact partial + the peer's decoded one) in log2 units; -inf past the item end
+      uint8_t* xrow = smem + kOffX + xs * kXSlot + h * 128;
+      const int e_peer = !aborted ? *reinterpret_cast<const int*>(smem + kOffXE + xs * kXeSlot + (th * 128 + h) * 4)
+                                  : -100;
+      const float st_p = pow2i(max(e_peer - 21, -126));
+      const float2 st2 = f2_pack(st_p, st_p), sth2 = f2_pack(256.f * st_p, 256.f * st_p);
+      const float2 dec2 = f2_pack(-kDecHi * st_p, -kDecHi * st_p);
+      const float2 sl2 = f2_pack(p.scale_log2, p.scale_log2);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {            // 8 tokens per 16-byte chunk
+        const uint32_t c = static_cast<uint32_t>(4 * th + k);
+        uint4 pv = make_uint4(0x40004000u, 0x40004000u, 0x40004000u, 0x40004000u);   // code of 0 (u = 2^22)
+        uint4 lv = make_uint4(0, 0, 0, 0);
+        if (!aborted) {
+          pv = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) << 4));
+          // low bytes of tokens 8k..8k+7 of this half: bytes 8 (k & 1) .. of chunk (2 th + k / 2)
+          lv = *reinterpret_cast<const uint4*>(smem + kOffXLo + xs * kXLoSlot + ((2 * th + (k >> 1)) * 128 + h) * 16);
+        }
+        const uint32_t pq[4] = {pv.x, pv.y, pv.z, pv.w};
+        const uint32_t lw[2] = {(k & 1) ? lv.z : lv.x, (k & 1) ? lv.w : lv.y};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = 8 * k + 2 * i;
+          const float2 f = f2_pack(__uint_as_float(__byte_perm(pq[i], 0x4B000000u, 0x7610)),
+                                   __uint_as_float(__byte_perm(pq[i], 0x4B000000u, 0x7632)));
+          const uint32_t lo2 = lw[i >> 1] >> (16 * (i & 1));     // the two low bytes of tokens t, t + 1
+          const float2 fl = f2_pack(__uint_as_float(__byte_perm(lo2, 0x4B000000u, 0x7660)),
+                                    __uint_as_float(__byte_perm(lo2, 0x4B000000u, 0x7661)));
+          const float2 sp = f2_fma(fl, st2, f2_fma(f, sth2, dec2));
+          const float2 s2 = f2_mul(f2_add(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), sp), sl2);
+          sv[t] = __float_as_uint(s2.x);
+          sv[t + 1] = __float_as_uint(s2.y);
+        }
+      }
+      const int nvalid = n - j * T - th * TH;
+      if (nvalid < TH) {
+#pragma unroll
+        for (int t = 0; t < TH; ++t)
+          if (t >= nvalid) sv[t] = __float_as_uint(-INFINITY);
+      }
+      // the half row's maximum as a tree (short dependency chains)
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        mx8[i] = max3(__uint_as_float(sv[4 * i]), __uint_as_float(sv[4 * i + 1]),
+                      fmaxf(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])));
+      const float mh = fmaxf(max3(mx8[0], mx8[1], mx8[2]), max3(max3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+      // row maximum over the tile: combine with the partner warp (other token half)
+      float* rm = red_max + (g & 1) * 256;
+      rm[th * 128 + h] = mh;
+      named_bar_sync(1 + q, 64);
+      const float mt = fmaxf(rm[h], rm[128 + h]);
+      if (j == 0 || m_ref == -INFINITY) {
+        // an item's first tile sets the reference; so does the first tile
+        // with a valid score when a causal query row had none before (O and
+        // the row sum are still zero then)
+        m_ref = mt;
+        if (j == 0) l_sum = 0.f;
+      } else {
+        const bool need = mt > m_ref + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale this warp's half of O (128 columns) after the previous PV has
+          // landed.  PV(g-2) is complete here (the peer sent tile g only after
+          // this CTA's PV(g-2) had freed slot g mod 2), so the barrier of tile
+          // g-1 cannot be a lap behind.
+          wait(bar(bPvDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, false);
+          tc_fence_after();
+          const float alpha = need ? ex2_approx(m_ref - mt) : 1.f;
+          if (need) {
+            m_ref = mt;
+            l_sum *= alpha;
+          }
+          if (!aborted) {
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t o[16];
+              const uint32_t ta = tmem + lane_off + kTmO + 128 * th + 16 * c;
+              tmem_ld16(ta, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(ta, o);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+        }
+      }
+      // P = 2^(s - m_ref) as bf16, written over the peer's rows (K-major, 128-byte swizzle)
+      const float m_eff = m_ref == -INFINITY ? 0.f : m_ref;   // a row with no valid score yet: P = 0
+      const float2 nm2 = f2_pack(-m_eff, -m_eff);
+      float2 l4[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 d = f2_add(f2_pack(__uint_as_float(sv[8 * k + 2 * i]), __uint_as_float(sv[8 * k + 2 * i + 1])), nm2);
+          const float a = ex2_approx(d.x), e2 = ex2_approx(d.y);
+          l4[i] = f2_add(l4[i], f2_pack(a, e2));   // four independent sums
+          pk[i] = pack_bf16x2(a, e2);
+        }
+        const uint32_t c = static_cast<uint32_t>(4 * th + k);
+        if (!aborted) *reinterpret_cast<uint4*>(xrow + ((c ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      const float2 l2 = f2_add(f2_add(l4[0], l4[1]), f2_add(l4[2], l4[3]));
+      l_sum += l2.x + l2.y;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(bar(bPFull + xs));
+      if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
+    };
+
+    // -- after an item's last tile: 1/l, O (this warp's 128 columns) and lse
+    auto epilogue = [&](int b, int part, uint32_t nitem) {
+      if (threadIdx.x == 0 && nitem < 24) MLA_TRACE_RAW(15, 8 + 2 * nitem, clock64());
+      // the row sum over the tile halves, added in the same order by both warps
+      red_l[th * 128 + h] = l_sum;
+      named_bar_sync(1 + q, 64);
+      const float lsum = red_l[h] + red_l[128 + h];
+      wait(bar(bOFull), nitem & 1, false);
+      tc_fence_after();
+      const bool part_ok = part < p.max_partials;   // a device-only plan naming a partial past the workspace
+      if (!part_ok && threadIdx.x == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
+      if (!aborted && part_ok) {
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;     // no valid score: out = 0
+        float* dst_f = nullptr;
+        __nv_bfloat16* dst_h = nullptr;
+        const size_t col0 = 256 * static_cast<size_t>(cta) + 128 * th;
+        if (part < 0) {
+          const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + col0;
+          if (p.out_bf16) dst_h = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
+          else dst_f = reinterpret_cast<float*>(p.out) + o;
+        } else {
+          dst_f = p.part_o + (static_cast<size_t>(part) * H + h) * kLatent + col0;
+        }
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {          // 32 columns per TMEM round trip, 32-byte stores
+          uint32_t o[32];
+          {
+            uint32_t a[16], c[16];
+            tmem_ld16(tmem + lane_off + kTmO + 128 * th + 32 * cb, a);
+            tmem_ld16(tmem + lane_off + kTmO + 128 * th + 32 * cb + 16, c);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) { o[i] = a[i]; o[16 + i] = c[i]; }
+          }
+          if (head_ok) {
+            if (dst_f) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = __float_as_uint(__uint_as_float(o[8 * i + k]) * inv);
+                st_global_v8(dst_f + 32 * cb + 8 * i, v);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                uint32_t v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  v[k] = pack_bf16x2(__uint_as_float(o[16 * i + 2 * k]) * inv, __uint_as_float(o[16 * i + 2 * k + 1]) * inv);
+                st_global_v8(dst_h + 32 * cb + 16 * i, v);
+              }
+            }
+          }
+        }
+        if (cta == 0 && th == 0 && head_ok) {
+          const float l = lsum > 0.f ? (m_ref + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+          if (part < 0) { if (p.lse) p.lse[static_cast<size_t>(b) * H + h] = l; }
+          else p.part_lse[static_cast<size_t>(part) * H + h] = l;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(bar(bOEmpty));
+      if (threadIdx.x == 0 && nitem < 24) MLA_TRACE_RAW(15, 9 + 2 * nitem, clock64());
+    };
+
+    uint32_t g = 0, nitem = 0;
+    for (int it = it0; it < it1; ++it) {
+      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+      const int part = items[4 * it + 3];
+      if (!item_ok(p, nnz, b, s, e)) continue;
+      const int n = e - s, nt = (n + T - 1) / T;
+      if (is_sender) {
+        // -- query latent half of this item into TMEM (after the previous item's last QK)
+        if (nitem > 0) wait(bar(bQEmpty), (nitem - 1) & 1, false);
+        tc_fence_after();
+        if (!aborted) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(b) * H + h) * kLatent +
+                                                            256 * cta);
+#pragma unroll
+          for (int c = 4 * th; c < 4 * th + 4; ++c) {   // this warp's 4 x 16 columns = 128 bf16
+            uint32_t r[16];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint4 v = row_ok ? __ldg(src + 4 * c + k) : make_uint4(0, 0, 0, 0);
-              v16[4 * k] = v.x; v16[4 * k + 1] = v.y; v16[4 * k + 2] = v.z; v16[4 * k + 3] = v.w;
+              const uint4 v = head_ok ? __ldg(src + 4 * c + k) : make_uint4(0, 0, 0, 0);
+              r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
             }
-            tmem_st16(tmem + lane_off + kTmQ + 32 * kg + 16 * c, v16);
+            tmem_st16(tmem + lane_off + kTmQ + 16 * c, r);
           }
           tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(bar(bQFull));
-      };
-
-      // -- after an item's last PV: O row r (this warp's 64 columns) / l to out or a partial state
-      const float* l_peer = reinterpret_cast<const float*>(smem + kOffLPeer);
-      auto write_o = [&](int b, int part, uint32_t nitem, float lsum, float lse_val) {
-        wait(bar(bOFull), nitem & 1, false);
-        tc_fence_after();
-        // the peer's row sum of a peer row: stored by the takers before they
-        // released the item's last PV, which bOFull follows
-        if (!own) lsum = (!aborted && row_ok) ? l_peer[(nitem & 1) * 64 + rl] : 0.f;
-        const bool part_ok = part < p.max_partials;   // a device-only plan naming a partial past the workspace
-        if (!part_ok && threadIdx.x == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
-        if (!aborted && part_ok) {
-          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;     // no valid score: out = 0
-          float* dst_f = nullptr;
-          __nv_bfloat16* dst_h = nullptr;
-          const size_t col0 = 256 * static_cast<size_t>(cta) + 64 * kg;
-          const size_t hh = row_ok ? static_cast<size_t>(h) : 0;
-          if (part < 0) {
-            const size_t o = (static_cast<size_t>(b) * H + hh) * kLatent + col0;
-            if (p.out_bf16) dst_h = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
-            else dst_f = reinterpret_cast<float*>(p.out) + o;
-          } else {
-            dst_f = p.part_o + (static_cast<size_t>(part) * H + hh) * kLatent + col0;
-          }
-#pragma unroll 1
-          for (int cb = 0; cb < 2; ++cb) {        // 32 columns per TMEM round trip, 32-byte stores
-            uint32_t o[32];
-            {
-              uint32_t a[16], c[16];
-              tmem_ld16(tmem + lane_off + kTmO + 64 * kg + 32 * cb, a);
-              tmem_ld16(tmem + lane_off + kTmO + 64 * kg + 32 * cb + 16, c);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) { o[i] = a[i]; o[16 + i] = c[i]; }
-            }
-            if (row_ok) {
-              if (dst_f) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  uint32_t v[8];
-#pragma unroll
-                  for (int k = 0; k < 8; ++k) v[k] = __float_as_uint(__uint_as_float(o[8 * i + k]) * inv);
-                  st_global_v8(dst_f + 32 * cb + 8 * i, v);
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                  uint32_t v[8];
-#pragma unroll
-                  for (int k = 0; k < 8; ++k)
-                    v[k] = pack_bf16x2(__uint_as_float(o[16 * i + 2 * k]) * inv,
-                                       __uint_as_float(o[16 * i + 2 * k + 1]) * inv);
-                  st_global_v8(dst_h + 32 * cb + 16 * i, v);
-                }
-              }
-            }
-          }
-          if (own && kg == 0 && row_ok) {          // the owner of the head writes its lse
-            if (part < 0) { if (p.lse) p.lse[static_cast<size_t>(b) * H + h] = lse_val; }
-            else p.part_lse[static_cast<size_t>(part) * H + h] = lse_val;
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && !aborted) mbar_arrive(bar(bOEmpty));
-      };
-
-      // an item's output is written after the next item's first tile, so that
-      // the epilogue overlaps that tile's exchange instead of delaying it
-      struct Pending { int b, part; uint32_t nitem; float lsum, lse; };
-      Pending pend{-1, 0, 0, 0.f, 0.f};
-      auto flush = [&]() {
-        if (pend.b < 0) return;
-        write_o(pend.b, pend.part, pend.nitem, pend.lsum, pend.lse);
-        pend.b = -1;
-      };
-
-      int it = next_ok(it0);
-      if (it < it1) load_q(items[4 * it]);      // the first item's query
-      uint32_t g = 0, nitem = 0;
-
-      if (own) {
-        // ---------------------------------------------- softmax (own rows)
-        float* side_out = reinterpret_cast<float*>(smem + kOffSideOut);   // [kPSlots][alpha 64 | l 64]
-        float m_ref = 0.f, l_sum = 0.f, lsum = 0.f;
-        for (; it < it1; it = next_ok(it + 1)) {
-          const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2], part = items[4 * it + 3];
-          const int n = e - s, nt = (n + T - 1) / T;
-          // multi-query: head h is query h / (H / q_len) of its request, which
-          // sees the first L - q_len + 1 + i rows of the request's context
-          int n_row = n;
-          if (p.q_len > 1 && row_ok) {
-            const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
-            const int i = h / (H / p.q_len);
-            n_row = max(0, min(n, (hi - lo) - p.q_len + 1 + i - (s - lo)));
-          }
-          for (int j = 0; j < nt; ++j, ++g) {
-            const uint32_t xs = g % kXSlots, ps = g % kPSlots;
-            // arm the receive slot for the peer's partials of tile g: done here,
-            // by a warp that also waits on it, so the arm for tile g + kXSlots
-            // cannot come before this tile's phase has completed
-            if (warp == 0 && lane == 0 && !aborted)
-              mbar_arrive_expect_tx(bar(bXFull + xs), static_cast<uint32_t>(Hh) * T * 4u);
-            uint32_t sv[16];
-            read_s(g, sv);
-            if (threadIdx.x == 0) MLA_TRACE_EVENT(10, g);
-            wait(bar(bXFull + xs), (g / kXSlots) & 1, true);
-            if (threadIdx.x == 0) MLA_TRACE_EVENT(9, g);
-            // s = (own + peer) * sm_scale * log2(e): the full score as an fp32 sum of the two halves
-            {
-              const uint8_t* xrow = smem + kOffX + xs * kXSlot + rl * 256;
-              const float2 sl2 = f2_pack(p.scale_log2, p.scale_log2);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t c = static_cast<uint32_t>(4 * kg + i);
-                uint4 pv = make_uint4(0, 0, 0, 0);
-                if (!aborted) pv = *reinterpret_cast<const uint4*>(xrow + ((c ^ static_cast<uint32_t>(rl & 15)) << 4));
-                const float2 a = f2_mul(f2_add(f2_pack(__uint_as_float(sv[4 * i]), __uint_as_float(sv[4 * i + 1])),
-                                               f2_pack(__uint_as_float(pv.x), __uint_as_float(pv.y))), sl2);
-                const float2 c2 = f2_mul(f2_add(f2_pack(__uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3])),
-                                                f2_pack(__uint_as_float(pv.z), __uint_as_float(pv.w))), sl2);
-                sv[4 * i] = __float_as_uint(a.x);
-                sv[4 * i + 1] = __float_as_uint(a.y);
-                sv[4 * i + 2] = __float_as_uint(c2.x);
-                sv[4 * i + 3] = __float_as_uint(c2.y);
-              }
-            }
-            if (threadIdx.x == 0) MLA_TRACE_EVENT(1, g);
-            const int nvalid = n_row - j * T - kg * kGroup;
-            if (nvalid < kGroup) {
-#pragma unroll
-              for (int t = 0; t < kGroup; ++t)
-                if (t >= nvalid) sv[t] = __float_as_uint(-INFINITY);
-            }
-            const float mh =
-                fmaxf(max3(max3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2])),
-                           max3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5])),
-                           max3(__uint_as_float(sv[6]), __uint_as_float(sv[7]), __uint_as_float(sv[8]))),
-                      max3(max3(__uint_as_float(sv[9]), __uint_as_float(sv[10]), __uint_as_float(sv[11])),
-                           max3(__uint_as_float(sv[12]), __uint_as_float(sv[13]), __uint_as_float(sv[14])),
-                           __uint_as_float(sv[15])));
-            // row maximum over the tile: the four warps of the quadrant
-            float* rm = red_max + (g & 1) * 256;
-            rm[kg * 64 + r] = mh;
-            named_bar_sync(1 + q, 128);
-            const float mt = fmaxf(fmaxf(rm[r], rm[64 + r]), fmaxf(rm[128 + r], rm[192 + r]));
-            float alpha = 1.f;
-            if (j == 0 || m_ref == -INFINITY) {
-              // an item's first tile sets the reference; so does the first tile
-              // with a valid score when a causal query row had none before (O and
-              // the row sum are still zero then)
-              m_ref = mt;
-              if (j == 0) l_sum = 0.f;
-            } else {
-              const bool need = mt > m_ref + 64.f;
-              if (__any_sync(0xffffffffu, need)) {
-                wait_pv(g - 1);                      // PV(g-1) must have landed before O is rescaled
-                tc_fence_after();
-                if (need) {
-                  alpha = ex2_approx(m_ref - mt);
-                  m_ref = mt;
-                  l_sum *= alpha;
-                }
-                rescale_o(alpha, 64 * kg, 4);
-                tc_fence_before();
-              }
-            }
-            if (threadIdx.x == 0) MLA_TRACE_EVENT(11, g);
-            // P = 2^(s - m_ref) as bf16 into P slot ps (K-major, 128-byte swizzle),
-            // once both CTAs' PVs of tile g - kPSlots have read it (this CTA's
-            // own rows, and the peer's copy of them)
-            if (g >= static_cast<uint32_t>(kPSlots)) {
-              wait_pv(g - kPSlots);
-              wait(bar(bPSlotPeer + ps), ((g / kPSlots) - 1) & 1, true);
-            }
-            if (threadIdx.x == 0) MLA_TRACE_EVENT(12, g);
-            const float m_eff = m_ref == -INFINITY ? 0.f : m_ref;   // a row with no valid score yet: P = 0
-            const float2 nm2 = f2_pack(-m_eff, -m_eff);
-            float2 l4[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-            uint8_t* prow = smem + kOffP + ps * kPSlot + r * 128;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 d =
-                    f2_add(f2_pack(__uint_as_float(sv[8 * c + 2 * i]), __uint_as_float(sv[8 * c + 2 * i + 1])), nm2);
-                const float a0 = ex2_approx(d.x), a1 = ex2_approx(d.y);
-                l4[i & 1] = f2_add(l4[i & 1], f2_pack(a0, a1));
-                pk[i] = pack_bf16x2(a0, a1);
-              }
-              const uint32_t ch = static_cast<uint32_t>(2 * kg + c);
-              if (!aborted)
-                *reinterpret_cast<uint4*>(prow + ((ch ^ static_cast<uint32_t>(r & 7)) << 4)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-            const float2 l2 = f2_add(l4[0], l4[1]);
-            l_sum += l2.x + l2.y;
-            // this row's rescale factor and, after an item's last tile, its row
-            // sum (the four warps' parts added in a fixed order), for the
-            // peer's half of O: they travel with the P rows
-            if (kg == 0 && !aborted) side_out[ps * (kSideSlot / 4) + rl] = alpha;
-            if (j == nt - 1) {
-              red_l[kg * 64 + r] = l_sum;
-              named_bar_sync(1 + q, 128);
-              lsum = (red_l[r] + red_l[64 + r]) + (red_l[128 + r] + red_l[192 + r]);
-              if (kg == 0 && !aborted) side_out[ps * (kSideSlot / 4) + 64 + rl] = lsum;
-            }
-            if (threadIdx.x == 0) MLA_TRACE_EVENT(14, g);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && !aborted) mbar_arrive(bar(bPFull + ps));
-            if (threadIdx.x == 0) MLA_TRACE_EVENT(7, g);
-            if (j == 0) flush();                   // the previous item's output
-          }
-          // (red_l is rewritten at the next item's last tile, after at least one
-          // more tile-maximum barrier, so every warp has read it by then)
-          const float lse_val = lsum > 0.f ? (m_ref + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
-          // the next item's query, as soon as this item's last QK is done
-          const int nx = next_ok(it + 1);
-          if (nx < it1) {
-            wait(bar(bQEmpty), nitem & 1, false);
-            tc_fence_after();
-            load_q(items[4 * nx]);
-          }
-          pend = Pending{b, part, nitem, lsum, lse_val};
-          ++nitem;
-        }
-        flush();
+        for (int j = 0; j < nt; ++j, ++g) send(g);
       } else {
-        // ----------------------------------------- pushers (the peer's rows)
-        const uint32_t xrow_peer = mapa_shared(base + kOffX + rl * 256, peer);
-        const uint32_t xfull_peer = mapa_shared(bar(bXFull), peer);
-        for (; it < it1; it = next_ok(it + 1)) {
-          const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2], part = items[4 * it + 3];
-          const int nt = (e - s + T - 1) / T;
-          for (int j = 0; j < nt; ++j, ++g) {
-            // tile g: this CTA's partial of the peer's row into the peer's receive slot
-            const uint32_t xs = g % kXSlots;
-            uint32_t v[16];
-            read_s(g, v);
-            if (threadIdx.x == 64) MLA_TRACE_EVENT(6, g);
-            if (g >= static_cast<uint32_t>(kXSlots)) wait(bar(bXFree + xs), ((g / kXSlots) - 1) & 1, true);
-            if (row_ok && !aborted) {
-              const uint32_t dst = xrow_peer + xs * kXSlot, fb = xfull_peer + 8u * xs;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t c = static_cast<uint32_t>(4 * kg + i);
-                st_async_v4(dst + ((c ^ static_cast<uint32_t>(rl & 15)) << 4), v[4 * i], v[4 * i + 1], v[4 * i + 2],
-                            v[4 * i + 3], fb);
-              }
-            }
-            if (threadIdx.x == 64) MLA_TRACE_EVENT(8, g);
-            if (j == 0) flush();                   // the previous item's output
-          }
-          const int nx = next_ok(it + 1);
-          if (nx < it1) {
-            wait(bar(bQEmpty), nitem & 1, false);
-            tc_fence_after();
-            load_q(items[4 * nx]);
-          }
-          pend = Pending{b, part, nitem, 0.f, 0.f};
-          ++nitem;
+        // multi-query: row h is query h / (H / q_len) of its request, which
+        // sees the first L - q_len + 1 + i rows of the request's context
+        int n_row = n;
+        if (p.q_len > 1) {
+          const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
+          const int i = h / (H / p.q_len);
+          n_row = max(0, min(n, (hi - lo) - p.q_len + 1 + i - (s - lo)));
         }
-        flush();
+        for (int j = 0; j < nt; ++j, ++g) softmax(g, j, n_row);
+        epilogue(b, part, nitem);
       }
+      ++nitem;
     }
   }
 
@@ -869,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     MLA_TRACE_RAW(15, 1, static_cast<long long>(globaltimer()));
     MLA_TRACE_RAW(15, 4, clock64());
   }
-  if (warp == kPvWarp) tmem_dealloc(tmem, 512);
+  if (warp == kLoaderWarp) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace pair

@@ -4,44 +4,54 @@
 // kind::f8f6f4, K = 32 per instruction) and no dequantisation pass.
 // ("MLA and torch.compile: v0.3's two sources", section "MLA: starting from a
 // 439-line commit": the FP8 KV cache; "实现差距：MLA 与 DeepSeek V3", section
-// 2.4: dual-path score, FA2-style online softmax, kv_c reused as the value.)
+// 2.4: the latent and rope dot products summed and scaled, FA2-style online
+// softmax, the latent rows reused as the values.)
 //
 // As in the bf16 kernel a worker is a cluster of two CTAs, CTA c owning latent
 // dims [256c, 256c+256) and rope dims [32c, 32c+32); partial scores are
-// exchanged as 16-bit fixed point and both CTAs take the same softmax.  What
-// changes is the arithmetic of the two products:
+// exchanged as 23-bit fixed point (error at most 2^-22 of the half row's
+// largest partial, at any query magnitude), and each CTA adds its own exact
+// partial to the peer's decoded one and normalises its half of O with its own
+// row sum.  What changes is the arithmetic of the two products:
 //   - the cache rows stay E4M3 (value = code x kv_scale);
-//   - the query is carried as two E4M3 parts: per head, q' = q * 2^a with the
+//   - the query is carried as two 8-bit parts: per head, q' = q * 2^a with the
 //     power of two a that puts max |q'| over this CTA's 288 dims in [128, 256),
-//     hi = e4m3(q'), lo = e4m3(q' - hi).  Both parts are A operands from TMEM
-//     (4 codes per column) and accumulate into the same scores, so each
+//     hi = e4m3(q'), lo = e5m2(q' - hi).  The residual of a bf16 value after
+//     its 4 leading bits has at most 3 significant bits, which E5M2 holds, and
+//     its range reaches 2^-16, so hi + lo is q' exactly for |q'| >= 2^-6 (an
+//     E4M3 lo, unscaled in the shared accumulator, would lose the bits of
+//     every element below 2^-2: about 2e-6 of the row's largest partial).
+//     Both parts are A operands from TMEM (4 codes per column; the lo MMAs
+//     take A as E5M2, B as E4M3) and accumulate into the same scores, so each
 //     latent K-step of 32 dims takes 2 MMAs (the bf16 kernel takes 2 of 16);
-//     the senders multiply their partial by 2^-a before quantising it, so the
-//     two CTAs' partials are in the same units;
+//     partials are multiplied by 2^-a (the senders' before quantising, the
+//     softmax warps' own before adding the peer's), so the two CTAs' partials
+//     are in the same units;
 //   - P' = 2^(s - m_ref + 5) likewise (a reference that lags the maximum by at
 //     most 3, so P' <= 256 and the maximum's weight is >= 32): hi = e4m3(P'), lo = e4m3(P' - hi),
 //     written side by side in the exchange slot's 128-byte rows (bytes 0-63
 //     hi, 64-127 lo, one byte per token): 2 MMAs per 32-token K-step (the
 //     split takes the difference in f16: five instructions per pair).
-// hi + lo holds q' and P to about 8 significant bits (bf16 has 8), within
-// 2^-10 absolute for the small elements.  The epilogue multiplies O by
+// hi + lo holds P to about 8 significant bits (bf16 has 8), within 2^-10
+// absolute for the small weights.  The epilogue multiplies O by
 // kv_scale / l; the score decode multiplies by sm_scale * log2(e) * kv_scale.
 //
 // TMEM (512 columns per CTA): O_c [0,256) fp32; the query's hi part [256,320)
-// and lo part [320,384) (E4M3, 4 per column); two score buffers [384,512).
+// and lo part [320,384) (4 codes per column); two score buffers [384,512).
 //
 // Shared memory per CTA: a ring of 8 latent blocks (64 tokens x 256 dims,
 // 16 KB: two 128-dim atoms, 128-byte swizzle), 8 rope atoms (64 tokens x 32
 // dims, 2 KB, 32-byte swizzle), the rope query's hi and lo parts (128 rows x
-// 32 bytes each, 32-byte swizzle), 2 exchange slots (the peer's codes, then
-// P), the peer's exponents and the softmax warps' reduction buffers.
+// 32 bytes each, 32-byte swizzle), 2 exchange slots (the high parts of the
+// peer's codes, then P), their low-byte blocks, the peer's exponents and the
+// softmax warps' reduction buffers.
 //
 // Warp roles per CTA (736 threads), as in the bf16 kernel:
 //   warps 8-15  senders: at an item's start, load the head's query dims of
 //               this CTA, scale and split them into TMEM (latent) and shared
-//               memory (rope); per tile, quantise their part of the partial,
-//               leave the dequantised values in TMEM and push the codes
-//   warps 0-7   softmax: add the peer's codes, softmax, P (hi and lo) over the
+//               memory (rope); per tile, quantise their part of the partial
+//               and push the codes
+//   warps 0-7   softmax: add the peer's decoded partial to this CTA's, softmax, P (hi and lo) over the
 //               peer's rows; the epilogue
 //   warp 16     QK issuer (one thread)
 //   warp 17     TMEM allocator and PV issuer (one thread)
@@ -72,13 +82,15 @@ constexpr int kRopeAtom = T * 32;            // 2 KB: 64 tokens x this CTA's 32 
 constexpr int kQRPlane = 128 * 32;           // rope query part: 128 rows x 32 E4M3 (32-byte swizzle)
 constexpr int kQRBytes = 2 * kQRPlane;       // hi, then lo
 constexpr int kXSlot = 128 * 128;            // 128 rows x 128 B (64 int16 scores, then P: 64 hi and 64 lo E4M3)
+constexpr int kXLoSlot = 128 * 64;           // the codes' low bytes: [4 chunks (half, part)][128 rows] x 16 B
 constexpr int kXeSlot = 2 * 128 * 4;         // [2 token halves][128 rows] int32 exponents
-constexpr int kXBytes = kXSlot + kXeSlot;    // bytes the peer sends per tile
+constexpr int kXBytes = kXSlot + kXLoSlot + kXeSlot;   // bytes the peer sends per tile
 constexpr int kOffLat = 0;
 constexpr int kOffRope = kOffLat + kLatBlocks * kLatBlock;
 constexpr int kOffQR = kOffRope + kRopeSlots * kRopeAtom;   // rope query hi | lo (K-major SW32)
 constexpr int kOffX = kOffQR + kQRBytes;
-constexpr int kOffXE = kOffX + kXSlots * kXSlot;        // [kXSlots] exponent blocks from the peer
+constexpr int kOffXLo = kOffX + kXSlots * kXSlot;       // [kXSlots] low-byte blocks from the peer
+constexpr int kOffXE = kOffXLo + kXSlots * kXLoSlot;    // [kXSlots] exponent blocks from the peer
 constexpr int kOffRed = kOffXE + kXSlots * kXeSlot;     // [2 bufs][2 halves][128] row maxima, [2][128] row sums
 constexpr int kOffBar = kOffRed + (2 * 2 * 128 + 2 * 128) * 4;
 // barriers
@@ -89,8 +101,7 @@ constexpr int bRopeEmpty = bRopeFull + kRopeSlots;
 constexpr int bQFull = bRopeEmpty + kRopeSlots;
 constexpr int bQEmpty = bQFull + 1;
 constexpr int bSFull = bQEmpty + 1;          // [2] this CTA's partial is in the S buffer
-constexpr int bSQuant = bSFull + 2;          // [2] the senders left the dequantised row in the S buffer
-constexpr int bSFree = bSQuant + 2;          // [2] the softmax warps have read the S buffer
+constexpr int bSFree = bSFull + 2;           // [2] the senders and the softmax warps have read the S buffer
 constexpr int bPFull = bSFree + 2;           // [kXSlots] P is in the exchange slot
 constexpr int bPvDone = bPFull + kXSlots;    // [2] PV(g) has completed (buffer g mod 2)
 constexpr int bOFull = bPvDone + 2;
@@ -104,6 +115,7 @@ constexpr int kOffLast = kOffMisc + 16;      // [kLatBlocks + kRopeSlots] last a
 constexpr int kSmemBytes = kOffLast + 4 * (kLatBlocks + kRopeSlots) + 1024;
 constexpr int kTmO = 0, kTmQHi = 256, kTmQLo = 320, kTmS = 384;
 constexpr uint32_t kIdescQK = idesc_e4m3(128, T, false, false);     // M=128 heads, N=64 tokens
+constexpr uint32_t kIdescQKLo = idesc_f8(kFmtE5M2, kFmtE4M3, 128, T, false, false);   // the query's E5M2 low part
 constexpr uint32_t kIdescPV = idesc_e4m3(128, 256, false, true);    // N=256 dims, B (V) MN-major
 static_assert(kProducers == 5, "producers 0-3 gather the latent atoms, producer 4 the rope");
 static_assert(kThreads == 736, "23 warps");
@@ -135,18 +147,27 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // 2^k as a float, for -126 <= k <= 127.
 __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
 
-// 16-bit codes are offset binary: u = q + 32768 for the integer q in [-32767, 32767].
-// Rounding and decoding use full-rate float arithmetic, not conversions:
-//   encode: v + (1.5 * 2^23 + 32768) rounds v to the nearest integer (ties to
-//           even) and leaves u in the low 16 bits of the float;
-//   decode: the bits 0x4B000000 | u are the float 2^23 + u, so
-//           (2^23 + u) * step - (2^23 + 32768) * step = q * step exactly.
+// Partial scores travel as 23-bit fixed point with a power-of-two step per
+// row and 32-token half: with e the exponent of the half row's largest
+// |partial| (nudged up by 2^-21 so that no code reaches 2^22), the step is
+// 2^(e-21), so a code q = rint(partial / step) has |q| < 2^22 and the
+// rounding error is at most 2^-22 of the largest |partial|, about fp32's own
+// rounding of a sum of 288 products.  The code goes as offset binary
+// u = q + 2^22 in 23 bits: its high 16 bits (u >> 8) in the slot's 128-byte
+// rows (the bytes P later overwrites in place), its low 8 bits in a side
+// block.  Rounding and decoding use full-rate float arithmetic:
+//   encode: partial / step + 1.5 * 2^23 rounds to the nearest integer (ties to
+//           even) and leaves u in the low 23 bits of the float;
+//   decode: the bits 0x4B000000 | x are the float 2^23 + x, so with
+//           fh = 2^23 + (u >> 8) and fl = 2^23 + (u & 255),
+//           fh * 256 step + fl * step - (2^31 + 2^23 + 2^22) step = q * step,
+//           exactly, as two FMAs whose results are representable.
 // Both the sender (from its own codes) and the receiver (from the peer's)
-// form q * step exactly and then multiply by sm_scale * log2(e) once, so the
+// form q * step exactly and then multiply by the same factor once, so the
 // two CTAs hold the same scaled partials and, after one commutative add,
 // the same scores.
-constexpr float kEncBias = 12615680.0f;      // 1.5 * 2^23 + 32768
-constexpr float kDecBias = 8421376.0f;       // 2^23 + 32768
+constexpr float kEncBias = 12582912.0f;      // 1.5 * 2^23
+constexpr float kDecHi = 2160066560.0f;      // 2^31 + 2^23 + 2^22 = 515 * 2^22 (exact in fp32)
 
 __global__ void __launch_bounds__(kThreads, 1)
     pair8_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kr,
@@ -186,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bQFull), kRowWarps);           // the sender warps (latent parts in TMEM, rope parts in smem)
     mbar_init(bar(bQEmpty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(bSFull + i), 1); mbar_init(bar(bSQuant + i), kRowWarps); mbar_init(bar(bSFree + i), kRowWarps);
+      mbar_init(bar(bSFull + i), 1); mbar_init(bar(bSFree + i), 2 * kRowWarps);
     }
     for (int i = 0; i < kXSlots; ++i) {
       mbar_init(bar(bPFull + i), kRowWarps);
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {           // 256 latent dims = 8 K-steps of 32; A (query hi, lo) from TMEM
             umma_ts_f8(d_s, tmem + kTmQHi + 8 * k, D(bk, (k >> 2) * kAtom + (k & 3) * 32), kIdescQK, k != 0 ? 1u : 0u);
-            umma_ts_f8(d_s, tmem + kTmQLo + 8 * k, D(bk, (k >> 2) * kAtom + (k & 3) * 32), kIdescQK, 1u);
+            umma_ts_f8(d_s, tmem + kTmQLo + 8 * k, D(bk, (k >> 2) * kAtom + (k & 3) * 32), kIdescQKLo, 1u);
           }
           MLA_TRACE_EVENT(10, g);
           if (!mbar_wait(bar(bRopeFull + rs), (g / kRopeSlots) & 1, wc)) { ok = false; break; }
@@ -349,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t br = D(dr, rs * kRopeAtom);
           // this CTA's 32 rope dims: one K-step, query hi then lo
           umma_ss_f8(d_s, dqr, br, kIdescQK, 1u);
-          umma_ss_f8(d_s, D(dqr, kQRPlane), br, kIdescQK, 1u);
+          umma_ss_f8(d_s, D(dqr, kQRPlane), br, kIdescQKLo, 1u);
           umma_commit(bar(bRopeEmpty + rs));
           umma_commit(bar(bSFull + (g & 1)));
           if (j == nt - 1) umma_commit(bar(bQEmpty));
@@ -409,11 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sw = static_cast<uint32_t>(h & 7);      // 16-byte chunk c of row h sits at c ^ (h mod 8)
     const uint32_t xrow_peer = mapa_shared(base + kOffX + h * 128, peer);
     const uint32_t xe_peer = mapa_shared(base + kOffXE + (th * 128 + h) * 4, peer);
+    const uint32_t xlo_peer = mapa_shared(base + kOffXLo + h * 16, peer);
     const uint32_t xfull_peer = mapa_shared(bar(bXFull), peer);
     float* red_max = reinterpret_cast<float*>(smem + kOffRed);            // [2][2][128]
     float* red_l = red_max + 2 * 2 * 128;                                 // [2 halves][128]
     float m_ref = 0.f, l_sum = 0.f;
-    float q_fac = 1.f;                           // senders: 2^-a of this item's head scaling
+    float q_fac = 1.f;                           // 2^-a of this item's head scaling (senders and softmax)
     const float sl_kv = p.scale_log2 * kv_scale; // decoded partials in log2 units of the true scores
     auto wait = [&](uint32_t bb, uint32_t par, bool cluster_scope) {
       if (aborted) return;
@@ -423,15 +445,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!r) aborted = true;
     };
 
-    // -- tile g of this CTA: quantise this warp's 32 partial scores of row h,
-    //    keep the dequantised (scaled) values in TMEM, push the codes to the peer
+    // -- tile g of this CTA: quantise this warp's 32 partial scores of row h
+    //    and push the codes to the peer (the softmax warps read the same
+    //    partials from TMEM themselves)
     auto send = [&](uint32_t g) {
       const uint32_t sb = g & 1, xs = g % kXSlots;
       const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64 + th * TH;
       wait(bar(bSFull + sb), (g >> 1) & 1, false);
       if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(6, g);
       tc_fence_after();
-      uint32_t qw[16];
+      uint32_t qw[16], lb[16];
       int e_own;
       {
         uint32_t r[32];
@@ -443,6 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0;
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !aborted) mbar_arrive(bar(bSFree + sb));
         // this CTA's partial in the units both CTAs share: times 2^-a (exact)
         {
           const float2 qf2 = f2_pack(q_fac, q_fac);
@@ -453,36 +479,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             r[i + 1] = __float_as_uint(v.y);
           }
         }
-        // the step is 2^(e-14), e the exponent of max|s| nudged up by 2^-15 so
-        // that no code rounds to 32768
+        // the step is 2^(e-21), e the exponent of max|s| nudged up by 2^-21 so
+        // that no code rounds to 2^22
         float mx = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; i += 2) mx = max3(mx, fabsf(__uint_as_float(r[i])), fabsf(__uint_as_float(r[i + 1])));
-        mx *= 1.000030517578125f;
+        mx *= 1.000000476837158203125f;
         e_own = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127, -100);
-        const float inv = pow2i(min(14 - e_own, 127)), st = pow2i(max(e_own - 14, -126));
+        const float inv = pow2i(min(21 - e_own, 127));
         const float2 inv2 = f2_pack(inv, inv), enc2 = f2_pack(kEncBias, kEncBias);
-        const float2 st2 = f2_pack(st, st), dec2 = f2_pack(-kEncBias * st, -kEncBias * st);
-        const float2 sl2 = f2_pack(sl_kv, sl_kv);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o16[16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 t = f2_fma(f2_pack(__uint_as_float(r[16 * c + 2 * i]), __uint_as_float(r[16 * c + 2 * i + 1])),
-                                    inv2, enc2);
-            qw[8 * c + i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x5410);
-            const float2 d = f2_mul(f2_fma(t, st2, dec2), sl2);
-            o16[2 * i] = __float_as_uint(d.x);
-            o16[2 * i + 1] = __float_as_uint(d.y);
-          }
-          if (!aborted) tmem_st16(tm_s + 16 * c, o16);
+        for (int i = 0; i < 16; ++i) {
+          const float2 t = f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), inv2, enc2);
+          qw[i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x6521);   // u >> 8, two codes
+          lb[i] = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);   // u & 255, two codes
         }
-        if (!aborted) tmem_wait_st();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && !aborted) mbar_arrive(bar(bSQuant + sb));
       if (threadIdx.x == 32 * kSendWarp0) MLA_TRACE_EVENT(13, g);
       // push into the peer's slot xs once the peer's PV(g - kXSlots) has read it
       if (g >= kXSlots) wait(bar(bXFree + xs), ((g / kXSlots) - 1) & 1, true);
@@ -494,6 +506,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 4; ++k) {
           const uint32_t c = static_cast<uint32_t>(4 * th + k);
           st_async_v4(dst + ((c ^ sw) << 4), qw[4 * k], qw[4 * k + 1], qw[4 * k + 2], qw[4 * k + 3], fb);
+        }
+        // low bytes: 32 codes of this row and half as 2 chunks of 16, chunk k
+        // of half th at row h of block (2 th + k)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w[i] = __byte_perm(lb[8 * k + 2 * i], lb[8 * k + 2 * i + 1], 0x5410);
+          st_async_v4(xlo_peer + xs * kXLoSlot + static_cast<uint32_t>((2 * th + k) * 128) * 16u, w[0], w[1], w[2], w[3],
+                      fb);
         }
         st_async_b32(xe_peer + xs * kXeSlot, static_cast<uint32_t>(e_own), fb);
       }
@@ -508,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // also waits on it, so the arm for tile g + kXSlots cannot come before
       // this tile's phase has completed (the peer's bytes may land either side)
       if (warp == 0 && lane == 0 && !aborted) mbar_arrive_expect_tx(bar(bXFull + xs), kXBytes);
-      wait(bar(bSQuant + sb), (g >> 1) & 1, false);
+      wait(bar(bSFull + sb), (g >> 1) & 1, false);
       uint32_t sv[32];
       if (!aborted) {
         tc_fence_after();
@@ -524,26 +546,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && !aborted) mbar_arrive(bar(bSFree + sb));
       wait(bar(bXFull + xs), (g / kXSlots) & 1, true);
       if (threadIdx.x == 0) MLA_TRACE_EVENT(9, g);
-      // s = own + peer (log2 units), the same in both CTAs; -inf past the item end
+      // s = (own exact partial x 2^-a + the peer's decoded one) in log2 units; -inf past the item end
       uint8_t* xrow = smem + kOffX + xs * kXSlot + h * 128;
       const int e_peer = !aborted ? *reinterpret_cast<const int*>(smem + kOffXE + xs * kXeSlot + (th * 128 + h) * 4)
                                   : -100;
-      const float st_p = pow2i(max(e_peer - 14, -126));
-      const float2 st2 = f2_pack(st_p, st_p), dec2 = f2_pack(-kDecBias * st_p, -kDecBias * st_p);
-      const float2 sl2 = f2_pack(sl_kv, sl_kv);
+      const float st_p = pow2i(max(e_peer - 21, -126));
+      const float2 st2 = f2_pack(st_p, st_p), sth2 = f2_pack(256.f * st_p, 256.f * st_p);
+      const float2 dec2 = f2_pack(-kDecHi * st_p, -kDecHi * st_p);
+      const float2 sl2 = f2_pack(sl_kv, sl_kv), qf2 = f2_pack(q_fac, q_fac);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {            // 8 tokens per 16-byte chunk
         const uint32_t c = static_cast<uint32_t>(4 * th + k);
-        uint4 pv = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);   // code of 0
-        if (!aborted) pv = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) << 4));
+        uint4 pv = make_uint4(0x40004000u, 0x40004000u, 0x40004000u, 0x40004000u);   // code of 0 (u = 2^22)
+        uint4 lv = make_uint4(0, 0, 0, 0);
+        if (!aborted) {
+          pv = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) << 4));
+          // low bytes of tokens 8k..8k+7 of this half: bytes 8 (k & 1) .. of chunk (2 th + k / 2)
+          lv = *reinterpret_cast<const uint4*>(smem + kOffXLo + xs * kXLoSlot + ((2 * th + (k >> 1)) * 128 + h) * 16);
+        }
         const uint32_t pq[4] = {pv.x, pv.y, pv.z, pv.w};
+        const uint32_t lw[2] = {(k & 1) ? lv.z : lv.x, (k & 1) ? lv.w : lv.y};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int t = 8 * k + 2 * i;
           const float2 f = f2_pack(__uint_as_float(__byte_perm(pq[i], 0x4B000000u, 0x7610)),
                                    __uint_as_float(__byte_perm(pq[i], 0x4B000000u, 0x7632)));
-          const float2 sp = f2_mul(f2_fma(f, st2, dec2), sl2);
-          const float2 s2 = f2_add(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), sp);
+          const uint32_t lo2 = lw[i >> 1] >> (16 * (i & 1));     // the two low bytes of tokens t, t + 1
+          const float2 fl = f2_pack(__uint_as_float(__byte_perm(lo2, 0x4B000000u, 0x7660)),
+                                    __uint_as_float(__byte_perm(lo2, 0x4B000000u, 0x7661)));
+          const float2 sp = f2_fma(fl, st2, f2_fma(f, sth2, dec2));
+          const float2 s2 = f2_mul(f2_fma(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), qf2, sp), sl2);
           sv[t] = __float_as_uint(s2.x);
           sv[t + 1] = __float_as_uint(s2.y);
         }
@@ -715,6 +747,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == 0 && nitem < 24) MLA_TRACE_RAW(15, 9 + 2 * nitem, clock64());
     };
 
+    // the head's scale a: max |q 2^a| over this CTA's 256 latent + 32 rope
+    // dims in [128, 256).  Senders and softmax warps each compute it from the
+    // query, with the same code, so both hold the same 2^-a.
+    auto head_exp = [&](int b) -> int {
+      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(b) * H + h) * kLatent + 256 * cta);
+      const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + (static_cast<size_t>(b) * H + h) * kRope + 32 * cta);
+      auto absmax8 = [](const uint4& v, float m) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        return m;
+      };
+      float amax = 0.f;
+      if (head_ok) {
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) amax = absmax8(__ldg(qn + i), amax);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) amax = absmax8(__ldg(qr + i), amax);
+      }
+      int a = 0;
+      if (amax > 0.f && amax <= 3.0e38f) {
+        int e;
+        frexpf(amax, &e);
+        a = min(126, max(-126, 8 - e));
+      }
+      return a;
+    };
+
     uint32_t g = 0, nitem = 0;
     for (int it = it0; it < it1; ++it) {
       const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
@@ -733,29 +794,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                            256 * cta);
           const uint4* qr = reinterpret_cast<const uint4*>(p.q_rope + (static_cast<size_t>(b) * H + h) * kRope +
                                                            32 * cta);
-          auto absmax8 = [](const uint4& v, float m) {
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
-            return m;
-          };
-          float amax = 0.f;
-          if (head_ok) {
-#pragma unroll 4
-            for (int i = 0; i < 32; ++i) amax = absmax8(__ldg(qn + i), amax);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) amax = absmax8(__ldg(qr + i), amax);
-          }
-          int a = 0;                               // max |q 2^a| in [128, 256)
-          if (amax > 0.f && amax <= 3.0e38f) {
-            int e;
-            frexpf(amax, &e);
-            a = min(126, max(-126, 8 - e));
-          }
+          const int a = head_exp(b);
           q_fac = ldexpf(1.f, -a);
           const float up = ldexpf(1.f, a);
-          // 8 bf16 -> 2 words of E4M3 hi and 2 of lo
+          // 8 bf16 -> 2 words of E4M3 hi and 2 of E5M2 lo
           auto split8 = [&](const uint4& v, uint32_t& h0, uint32_t& h1, uint32_t& l0, uint32_t& l1) {
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t hh[4], ll[4];
@@ -764,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float u0 = __uint_as_float(w[i] << 16) * up, u1 = __uint_as_float(w[i] & 0xFFFF0000u) * up;
               hh[i] = e4m3x2(u0, u1);
               const float2 hv = e4m3x2_value(hh[i]);
-              ll[i] = e4m3x2(u0 - hv.x, u1 - hv.y);
+              ll[i] = e5m2x2(u0 - hv.x, u1 - hv.y);   // the difference is exact in fp32
             }
             h0 = hh[0] | (hh[1] << 16);
             h1 = hh[2] | (hh[3] << 16);
@@ -812,6 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int i = h / (H / p.q_len);
           n_row = max(0, min(n, (hi - lo) - p.q_len + 1 + i - (s - lo)));
         }
+        q_fac = ldexpf(1.f, -head_exp(b));
         for (int j = 0; j < nt; ++j, ++g) softmax(g, j, n_row);
         epilogue(b, part, nitem);
       }

@@ -13,7 +13,7 @@ held to the same bar as the unit-scale tests, |dout| <= 1e-2 + 1e-2|ref| and
     N(0,1) q_pre and w_kc of gain 1 (entries N(0, 1/128)) or 11.3 (N(0, 1));
     the oracle's fp64 product, rounded to bf16, feeds both sides; at gain 1
     the query mla_absorb_query makes on the GPU is decoded too.
-Few-heads (H = 16, 32) and two-CTA (H = 64, 128) kernels, bf16 cache.
+Few-heads (H = 16, 32) and two-CTA (H = 64, 128) kernels, bf16 and FP8 caches.
 """
 import numpy as np
 import pytest
@@ -118,3 +118,53 @@ def test_absorbed_queries(H, gain):
         dec.run(q_gpu, dev["q_rope"], dev["kv_cache"], dev["kv_indptr"], dev["kv_indices"], bt.sm_scale, o, l)
         assert dec.check() == 0
         assert_close(o.cpu().numpy(), l.cpu().numpy(), ro, rl)
+
+
+# ------------------------------------------------------------- FP8 cache
+
+def _fp8_case(H, seed, q_factor):
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    bt = _batch(H, seed)
+    codes = W.make_fp8_cache(bt.pool, seed + 2)
+    qn, qr = _scale_bits(bt.q_nope, q_factor), _scale_bits(bt.q_rope, q_factor)
+    return bt, qn, qr, codes
+
+
+def _run_fp8(bt, qn, qr, codes, kv_scale):
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding
+    H, B = bt.heads, bt.batch
+    plan, _ = binding.decode_plan(bt.kv_indptr, H)
+    plan_d = torch.from_numpy(plan).cuda()
+    ws = torch.zeros(binding.decode_fp8_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    out = torch.full((B, H, 512), float("nan"), device="cuda")
+    lse = torch.full((B, H), float("nan"), device="cuda")
+    binding.decode_run_fp8(plan, plan_d, bf(qn), bf(qr), torch.from_numpy(codes).cuda(), kv_scale,
+                           torch.from_numpy(bt.kv_indptr.astype(np.int32)).cuda(),
+                           torch.from_numpy(bt.kv_indices.astype(np.int32)).cuda(), bt.sm_scale, out, lse, ws)
+    st = binding.check_errors(ws)
+    assert st == 0, binding.status_string(st)
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+@pytest.mark.parametrize("scale", [1, 8, 32, 128])
+def test_fp8_query_scale(H, scale):
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    from oracle import mla_oracle as O
+    bt, qn, qr, codes = _fp8_case(H, 900 + H + scale, scale)
+    out, lse = _run_fp8(bt, qn, qr, codes, W.FP8_KV_SCALE)
+    ro, rl = O.decode_attention_fp8(qn, qr, codes, W.FP8_KV_SCALE, bt.kv_indptr, bt.kv_indices, bt.sm_scale)
+    assert_close(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("H", [64, 128])
+def test_fp8_per_head_query_scales(H):
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    from oracle import mla_oracle as O
+    bt, qn, qr, codes = _fp8_case(H, 950 + H, _per_head_scales(H))
+    for kv_scale in (W.FP8_KV_SCALE, 0.0123):
+        out, lse = _run_fp8(bt, qn, qr, codes, kv_scale)
+        ro, rl = O.decode_attention_fp8(qn, qr, codes, kv_scale, bt.kv_indptr, bt.kv_indices, bt.sm_scale)
+        assert_close(out, lse, ro, rl)
