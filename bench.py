@@ -3,8 +3,12 @@
 
 A step is one whole decode pass (mla_decode_attend + mla_decode_merge) over one
 synthetic batch whose inputs are already resident in HBM.  Default workload:
-the DeepSeek-V2-Lite-shaped batch (B=64, H=16, contexts uniform in
-[512, 4096], page size 1, 2^19-slot pool); ``--workload 1..5`` picks another.
+the ragged serving batch (B=256, H=128, contexts lognormal around 1500 clipped
+to [16, 32768], page size 1, 2^20-slot pool); ``--workload 1..5`` picks another.
+The other >= 4k-context workloads of the family (V2-Lite B=64/H=16, V3
+B=128/H=128 at 4096, long B=2/H=128 at 64k + 128k) are measured in the same
+run under ``per_config`` (step and decode kernel alone, each one CUDA-graph
+replay over rotating input sets), with their side legs.
 
 Timing: W untimed warm-up steps, then exactly K steps run back to back (as a
 decode loop runs them) between two CUDA events on the launching stream,
@@ -13,8 +17,9 @@ over ranks is reported.  L2 cannot help: step k reads input set k mod R, and
 the R sets (each with its own KV pool, query, indices) are chosen so that the
 cache bytes the other R-1 steps stream in between exceed 4x the L2 size.
 The decode kernel's own time (the roofline's "achieved") is taken in a second
-pass with CUDA events around each decode launch, and a third pass reports the
-step with a 256 MiB L2-flushing write (outside the events) before each step.
+pass: K decode launches alone (no merge) over the same rotation, captured as
+one CUDA graph and timed as one replay; a third pass reports the step with a
+256 MiB L2-flushing write (outside the events) before each step.
 ``--gpus N`` under torchrun runs N independent replicas (the path needs no
 collective).  ``--impl reference`` times the fp64 CPU oracle instead.
 """
@@ -250,7 +255,7 @@ def run_reference(args, batch, rank, pg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(batch, args),
+        "config": workload_config(batch, args, host=True),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -258,9 +263,12 @@ def run_reference(args, batch, rank, pg):
     return 0
 
 
-def workload_config(batch, args, rotate=None):
+def workload_config(batch, args, rotate=None, host=False):
     spec = batch.spec
-    if rotate and rotate[0] > 1:
+    if host:
+        l2 = ("not applicable: the fp64 oracle runs on the host CPU from host memory (numpy); no GPU cache "
+              "is involved")
+    elif rotate and rotate[0] > 1:
         l2 = ("inputs larger than L2: step k reads input set k mod %d (own KV pool, q, indices), "
               "the other sets stream %.0f MB of cache in between" % rotate)
     elif rotate:
@@ -512,7 +520,8 @@ def time_cascade(batch, dev, peaks):
 
 def time_fp8(batch, dev, peaks, step_us_bf16, indptr_d, indices_d):
     """The same decode over an FP8 (E4M3) copy of the cache (mla_decode_run_fp8:
-    query prep, decode, merge), H <= 32 only.  Synthetic codes with kv_scale
+    at H <= 32 a query-prep kernel, the few-heads FP8 decode and the merge; at
+    H >= 48 the two-CTA FP8 decode and the merge).  Synthetic codes with kv_scale
     2^-5; R pool copies whose touched bytes exceed 4x L2 are rotated inside one
     captured CUDA graph, replayed after warm-up.  Flops as for bf16 (the
     roofline takes the larger of the byte and flop times)."""
@@ -572,7 +581,138 @@ def time_fp8(batch, dev, peaks, step_us_bf16, indptr_d, indices_d):
             "latent_kv_gbs": batch.nnz * 576 / (us * 1e-6) / 1e9, "speedup_vs_bf16_step": step_us_bf16 / us,
             "kv_scale": W.FP8_KV_SCALE,
             "note": "FP8 (E4M3) cache, one byte per value; decode (tcgen05 kind::f8f6f4; H <= 32 after a query-prep "
-                    "kernel) + merge per step; synthetic codes; R KV copies > 4x L2 rotated inside one CUDA graph"}
+                    "kernel, H >= 48 the two-CTA kernel) + merge per step; synthetic codes; R KV copies > 4x L2 "
+                    "rotated inside one CUDA graph"}
+
+
+def graph_ms_per_call(fn, n, stream, dev):
+    """Capture n calls fn(k, stream) as one CUDA graph, replay it once
+    untimed, then time one replay with events on `stream`: milliseconds per
+    call."""
+    import torch
+    cap = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for k in range(n):
+                fn(k, cap)
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / n
+
+
+class DecodeInputs:
+    """One workload on the device: R input sets (KV pool, q, indices) such
+    that the other R-1 steps of a back-to-back run stream more than 4x L2 of
+    cache rows, the decoder (plan + workspace) and the outputs."""
+
+    def __init__(self, batch, dev, args):
+        import numpy as np
+        import torch
+        from mla_latent_kv_absorbed_gb300 import binding
+        self.batch, self.dev = batch, dev
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        q_nope, q_rope, self.kv = bf(batch.q_nope), bf(batch.q_rope), bf(batch.kv_cache)
+        self.indptr_d = torch.from_numpy(batch.kv_indptr).to(dev)
+        self.indices_d = torch.from_numpy(batch.kv_indices).to(dev)
+        Bn, H = batch.batch, batch.heads
+        self.out = torch.empty((Bn, H, 512), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((Bn, H), dtype=torch.float32, device=dev)
+        self.dec = binding.Decoder(batch.kv_indptr, H, device=dev)
+        l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.step_kv_bytes = batch.nnz * 1152
+        self.R = args.sets if args.sets > 0 else max(2, math.ceil(4 * l2_bytes / self.step_kv_bytes) + 1)
+        self.sets = [(q_nope, q_rope, self.kv, self.indices_d)]
+        for _ in range(self.R - 1):
+            self.sets.append((q_nope.clone(), q_rope.clone(), self.kv.clone(), self.indices_d.clone()))
+
+    def attend(self, k, st):
+        qn, qr, kvc, ind = self.sets[k % self.R]
+        self.dec.attend(qn, qr, kvc, self.indptr_d, ind, self.batch.sm_scale, self.out, self.lse, st)
+
+    def step(self, k, st):
+        self.attend(k, st)
+        self.dec.merge(self.out, self.lse, st)
+
+    def check(self, stream, where):
+        from mla_latent_kv_absorbed_gb300 import binding
+        st = self.dec.check(stream)
+        if st != 0:
+            raise RuntimeError(f"device status {where}: {binding.status_string(st)}")
+
+    @property
+    def rotate(self):
+        return (self.R, (self.R - 1) * self.step_kv_bytes / 1e6)
+
+
+def roofline_of(batch, peaks, peak_src, kernel_ms, step_ms):
+    """The decode kernel against the roofline of this workload's algorithmic
+    bytes and flops (the slower of the two at the measured peaks)."""
+    bytes_alg, flops_alg = algorithmic_work(batch)
+    t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops_alg / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = bytes_alg / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = flops_alg / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    kernel = "swab" if batch.heads <= 32 else "pair"
+    roof["traffic"] = ncu_traffic(batch.spec.name if batch.spec else "custom", kernel)
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = f"mla_decode ({kernel})"
+    roof["kernel_ms"] = kernel_ms
+    roof["kernel_timing"] = "decode launches alone (no merge), rotating the input sets, one CUDA-graph replay"
+    roof["algorithmic_bytes"] = bytes_alg
+    roof["algorithmic_flops"] = flops_alg
+    roof["roofline_us"] = max(t_hbm, t_tc) * 1e6
+    roof["step_frac_of_roofline"] = max(t_hbm, t_tc) * 1e3 / step_ms
+    return roof
+
+
+def measure_config(batch, dev, args, peaks, peak_src, legs=()):
+    """A workload besides the headline one, from the same run: its step
+    (decode + merge) and its decode kernel alone, each timed as one CUDA-graph
+    replay of K launches over the rotating input sets, plus the side legs
+    named in `legs`."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    x = DecodeInputs(batch, dev, args)
+    for k in range(max(args.warmup, x.R)):
+        x.step(k, stream)
+    x.check(stream, "after warm-up")
+    step_ms = graph_ms_per_call(x.step, args.steps, stream, dev)
+    kernel_ms = graph_ms_per_call(x.attend, args.steps, stream, dev)
+    x.check(stream, "after timing")
+    roof = roofline_of(batch, peaks, peak_src, kernel_ms, step_ms)
+    res = {"workload": batch.spec.name, "batch": batch.batch, "heads": batch.heads, "nnz": batch.nnz,
+           "step_us": step_ms * 1e3, "kernel_us": kernel_ms * 1e3, "frac": roof["frac"],
+           "step_frac_of_roofline": roof["step_frac_of_roofline"], "traffic": roof["traffic"],
+           "roofline_us": roof["roofline_us"], "bound": roof["bound"],
+           "latent_kv_gbs": batch.nnz * 1152 / (step_ms * 1e-3) / 1e9,
+           "latent_kv_gbs_kernel": batch.nnz * 1152 / (kernel_ms * 1e-3) / 1e9,
+           "kernel": roof["kernel"], "input_sets": x.R}
+    if "fp8" in legs:
+        res["fp8_cache"] = time_fp8(batch, dev, peaks, step_ms * 1e3, x.indptr_d, x.indices_d)
+    if "multi_query" in legs:
+        res["multi_query"] = time_multi_query(batch, dev, peaks, x.kv, x.indptr_d, x.indices_d)
+    if "cascade" in legs:
+        res["cascade"] = time_cascade(batch, dev, peaks)
+    if "head_products" in legs:
+        res["head_products"] = time_head_products(batch, dev, peaks)
+    del x
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, batch, world, rank, local, pg):
@@ -584,41 +724,19 @@ def run_ours(args, batch, world, rank, local, pg):
     if pg is not None:
         pg.barrier()
     B.build()
-    from mla_latent_kv_absorbed_gb300 import binding
+    from mla_latent_kv_absorbed_gb300 import binding, workloads
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-    q_nope, q_rope, kv = bf(batch.q_nope), bf(batch.q_rope), bf(batch.kv_cache)
-    indptr_d = torch.from_numpy(batch.kv_indptr).to(dev)
-    indices_d = torch.from_numpy(batch.kv_indices).to(dev)
-    Bn, H = batch.batch, batch.heads
-    out = torch.empty((Bn, H, 512), dtype=torch.float32, device=dev)
-    lse = torch.empty((Bn, H), dtype=torch.float32, device=dev)
-    dec = binding.Decoder(batch.kv_indptr, H, device=dev)
+    x = DecodeInputs(batch, dev, args)
+    dec, kv, Bn, H = x.dec, x.kv, batch.batch, batch.heads
     plan_us = host_plan_us(binding, batch.kv_indptr, H, dec.plan_host.size)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    # input sets for back-to-back steps: R copies (KV pool, q, indices) such
-    # that the other R-1 steps stream more than 4x L2 of cache rows
-    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    step_kv_bytes = batch.nnz * 1152
-    R = args.sets if args.sets > 0 else max(2, math.ceil(4 * l2_bytes / step_kv_bytes) + 1)
-    sets = [(q_nope, q_rope, kv, indices_d)]
-    for _ in range(R - 1):
-        sets.append((q_nope.clone(), q_rope.clone(), kv.clone(), indices_d.clone()))
-
-    def step(k, st=stream):
-        qn, qr, kvc, ind = sets[k % R]
-        dec.attend(qn, qr, kvc, indptr_d, ind, batch.sm_scale, out, lse, st)
-        dec.merge(out, lse, st)
-
-    for k in range(max(args.warmup, R)):
-        step(k)
-    st = dec.check(stream)
-    if st != 0:
-        raise RuntimeError(f"device status after warm-up: {binding.status_string(st)}")
+    for k in range(max(args.warmup, x.R)):
+        x.step(k, stream)
+    x.check(stream, "after warm-up")
 
     # the K timed steps captured once as a CUDA graph (decode loops replay
     # graphs: no host work between the steps' launches); one untimed replay
@@ -628,7 +746,7 @@ def run_ours(args, batch, world, rank, local, pg):
     with torch.cuda.stream(cap):
         with torch.cuda.graph(graph, stream=cap):
             for k in range(args.steps):
-                step(k, cap)
+                x.step(k, cap)
     stream.wait_stream(cap)
     graph.replay()
     torch.cuda.synchronize()
@@ -647,33 +765,23 @@ def run_ours(args, batch, world, rank, local, pg):
         wall = time.perf_counter() - wall0
     if pg is not None:
         pg.barrier()
-    st = dec.check(stream)
-    if st != 0:
-        raise RuntimeError(f"device status after timing: {binding.status_string(st)}")
+    x.check(stream, "after timing")
     ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, pg, dev)
     del graph
+
+    # ---- the decode kernel alone: K decode launches (no merge) over the same
+    # rotation, one graph replay, so that it is timed like the step
+    attend_ms = max_over_ranks(graph_ms_per_call(x.attend, args.steps, stream, dev), pg, dev)
 
     # the same K steps launched one call at a time from the host (for reference)
     torch.cuda.synchronize()
     e0h, e1h = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0h.record(stream)
     for k in range(args.steps):
-        step(k)
+        x.step(k, stream)
     e1h.record(stream)
     torch.cuda.synchronize()
     host_launched_ms = max_over_ranks(e0h.elapsed_time(e1h) / args.steps, pg, dev)
-
-    # ---- the decode kernel alone: events around each attend launch, same rotation
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for k in range(args.steps):
-        qn, qr, kvc, ind = sets[k % R]
-        evs[k][0].record(stream)
-        dec.attend(qn, qr, kvc, indptr_d, ind, batch.sm_scale, out, lse, stream)
-        evs[k][1].record(stream)
-        dec.merge(out, lse, stream)
-    torch.cuda.synchronize()
-    attend_avg = max_over_ranks(statistics.mean(a.elapsed_time(b_) for a, b_ in evs), pg, dev)
 
     # ---- per-step timing with an L2-flushing write before each step (for reference)
     fl = []
@@ -681,15 +789,12 @@ def run_ours(args, batch, world, rank, local, pg):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        step(k)
+        x.step(k, stream)
         e1.record(stream)
         fl.append((e0, e1))
     torch.cuda.synchronize()
     flushed_ms = max_over_ranks(statistics.mean(a.elapsed_time(b_) for a, b_ in fl), pg, dev)
-    st = dec.check(stream)
-    if st != 0:
-        raise RuntimeError(f"device status after timing: {binding.status_string(st)}")
-    rotate = (R, (R - 1) * step_kv_bytes / 1e6)
+    x.check(stream, "after timing")
 
     # ---------------------------------------------------------------- e2e
     # Public API end to end from host buffers (mla_decode_step_host): every
@@ -700,107 +805,103 @@ def run_ours(args, batch, world, rank, local, pg):
     h_ptr = torch.from_numpy(batch.kv_indptr.astype(np.int32)).pin_memory()
     h_idx = torch.from_numpy(batch.kv_indices.astype(np.int32)).pin_memory()
     pw = int(dec.plan_host.shape[0])
-    stage_bytes = binding.step_staging_bytes(Bn, H, batch.nnz, pw, 0)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    bufs = []
-    for j in range(2):
-        bufs.append(dict(plan=torch.empty(pw, dtype=torch.int32).pin_memory(),
-                         staging=torch.empty(stage_bytes, dtype=torch.uint8, device=dev),
-                         h_out=torch.empty((Bn, H, 512), dtype=torch.float32).pin_memory(),
-                         h_lse=torch.empty((Bn, H), dtype=torch.float32).pin_memory(),
-                         done=torch.cuda.Event(), in_done=torch.cuda.Event(), run_done=torch.cuda.Event()))
 
-    def host_step(j, pipelined):
-        b = bufs[j]
-        binding.decode_step_host(h_qn, h_qr, h_ptr, h_idx, kv, batch.sm_scale, b["h_out"], b["h_lse"], b["plan"],
-                                 b["staging"], dec.workspace, stream, s_in if pipelined else None,
-                                 s_out if pipelined else None)
-        b["done"].record(s_out if pipelined else stream)
-        if pipelined:
-            b["in_done"].record(s_in)
-            b["run_done"].record(stream)
+    def e2e_run(out_dtype):
+        code = 0 if out_dtype == torch.float32 else 1
+        stage_bytes = binding.step_staging_bytes(Bn, H, batch.nnz, pw, code)
+        bufs = []
+        for j in range(2):
+            bufs.append(dict(plan=torch.empty(pw, dtype=torch.int32).pin_memory(),
+                             staging=torch.empty(stage_bytes, dtype=torch.uint8, device=dev),
+                             h_out=torch.empty((Bn, H, 512), dtype=out_dtype).pin_memory(),
+                             h_lse=torch.empty((Bn, H), dtype=torch.float32).pin_memory(),
+                             done=torch.cuda.Event(), in_done=torch.cuda.Event(), run_done=torch.cuda.Event()))
 
-    # (1) one step at a time, everything on one stream: the latency of a step
-    for _ in range(max(2, args.warmup)):
-        host_step(0, False)
-        bufs[0]["done"].synchronize()
-    e2e_times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        host_step(0, False)
-        bufs[0]["done"].synchronize()
-        e2e_times.append(time.perf_counter() - t0)
-    e2e_serial_us = max_over_ranks(statistics.mean(e2e_times) * 1e6, pg, dev)
-    serial_out = bufs[0]["h_out"].clone()
-
-    # (2) steps pipelined as a serving loop runs them: kernels in order on the
-    # compute stream, copies in and out on their own streams, two staging
-    # buffers in turn, so step k's copies in and step k-1's copies out overlap
-    # the kernels (the host waits only for the step two back before reusing
-    # its pinned plan buffer)
-    def pipelined(n):
-        for k in range(n):
-            j = k % 2
+        def host_step(j, pipelined):
             b = bufs[j]
-            if k >= 2:
-                b["in_done"].synchronize()         # step k-2's plan words have left the pinned buffer
-                s_in.wait_event(b["run_done"])     # its kernels are done reading this staging buffer
-                stream.wait_event(b["done"])       # its result has been copied out of it
-            host_step(j, True)
-        torch.cuda.synchronize()
+            binding.decode_step_host(h_qn, h_qr, h_ptr, h_idx, kv, batch.sm_scale, b["h_out"], b["h_lse"], b["plan"],
+                                     b["staging"], dec.workspace, stream, s_in if pipelined else None,
+                                     s_out if pipelined else None)
+            b["done"].record(s_out if pipelined else stream)
+            if pipelined:
+                b["in_done"].record(s_in)
+                b["run_done"].record(stream)
 
-    pipelined(max(2, args.warmup))
-    t0 = time.perf_counter()
-    pipelined(args.steps)
-    e2e_us = max_over_ranks((time.perf_counter() - t0) / args.steps * 1e6, pg, dev)
-    e2e_ok = bool(torch.equal(bufs[0]["h_out"], serial_out) and torch.equal(bufs[1]["h_out"], serial_out))
-    ph = bufs[0]["plan"].numpy()
-    h_out = bufs[0]["h_out"]
-    h_lse = bufs[0]["h_lse"]
-    h2d = (h_qn.numel() * 2 + h_qr.numel() * 2 + h_ptr.numel() * 4 + h_idx.numel() * 4 + ph.shape[0] * 4)
-    d2h = h_out.numel() * 4 + h_lse.numel() * 4
-    st = dec.check(stream)
-    if st != 0:
-        raise RuntimeError(f"device status after e2e: {binding.status_string(st)}")
+        # (1) one step at a time, everything on one stream: the latency of a step
+        for _ in range(max(2, args.warmup)):
+            host_step(0, False)
+            bufs[0]["done"].synchronize()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            host_step(0, False)
+            bufs[0]["done"].synchronize()
+            times.append(time.perf_counter() - t0)
+        serial_us = max_over_ranks(statistics.mean(times) * 1e6, pg, dev)
+        serial_out = bufs[0]["h_out"].clone()
+
+        # (2) steps pipelined as a serving loop runs them: kernels in order on
+        # the compute stream, copies in and out on their own streams, two
+        # staging buffers in turn, so step k's copies in and step k-1's copies
+        # out overlap the kernels (the host waits only for the step two back
+        # before reusing its pinned plan buffer)
+        def pipelined(n):
+            for k in range(n):
+                j = k % 2
+                b = bufs[j]
+                if k >= 2:
+                    b["in_done"].synchronize()         # step k-2's plan words have left the pinned buffer
+                    s_in.wait_event(b["run_done"])     # its kernels are done reading this staging buffer
+                    stream.wait_event(b["done"])       # its result has been copied out of it
+                host_step(j, True)
+            torch.cuda.synchronize()
+
+        pipelined(max(2, args.warmup))
+        t0 = time.perf_counter()
+        pipelined(args.steps)
+        us = max_over_ranks((time.perf_counter() - t0) / args.steps * 1e6, pg, dev)
+        ok = bool(torch.equal(bufs[0]["h_out"], serial_out) and torch.equal(bufs[1]["h_out"], serial_out))
+        h2d = (h_qn.numel() * 2 + h_qr.numel() * 2 + h_ptr.numel() * 4 + h_idx.numel() * 4 + pw * 4)
+        d2h = bufs[0]["h_out"].numel() * bufs[0]["h_out"].element_size() + bufs[0]["h_lse"].numel() * 4
+        return us, serial_us, ok, h2d, d2h
+
+    e2e_us, e2e_serial_us, e2e_ok, h2d, d2h = e2e_run(torch.float32)
+    e2e_bf16_us, e2e_bf16_serial_us, e2e_bf16_ok, _, d2h_bf16 = e2e_run(torch.bfloat16)
+    x.check(stream, "after e2e")
 
     if rank != 0:
         return 0
     peaks, peak_src = load_peaks()
-    bytes_alg, flops_alg = algorithmic_work(batch)
-    gbs_attend = bytes_alg / (attend_avg * 1e-3) / 1e9
-    tflops_attend = flops_alg / (attend_avg * 1e-3) / 1e12
-    t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flops_alg / (peaks["bf16_tflops"] * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": gbs_attend, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs_attend / peaks["hbm_gbs"]}
-    else:
-        roof = {"bound": "tensor", "achieved": tflops_attend, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": tflops_attend / peaks["bf16_tflops"]}
-    kernel = "swab" if H <= 32 else "pair"
-    roof["traffic"] = ncu_traffic(batch.spec.name if batch.spec else "custom", kernel)
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
-    roof["kernel"] = "mla_decode (swab)" if H <= 32 else "mla_decode (pair)"
-    roof["kernel_ms"] = attend_avg
-    roof["algorithmic_bytes"] = bytes_alg
-    roof["algorithmic_flops"] = flops_alg
-    roof["roofline_us"] = max(t_hbm, t_tc) * 1e6
-    roof["step_frac_of_roofline"] = max(t_hbm, t_tc) * 1e3 / ms
+    roof = roofline_of(batch, peaks, peak_src, attend_ms, ms)
 
     head_products = time_head_products(batch, dev, peaks)
-    multi_query = time_multi_query(batch, dev, peaks, kv, indptr_d, indices_d)
+    multi_query = time_multi_query(batch, dev, peaks, kv, x.indptr_d, x.indices_d)
     cascade = time_cascade(batch, dev, peaks)
-    fp8 = time_fp8(batch, dev, peaks, ms * 1e3, indptr_d, indices_d)
+    fp8 = time_fp8(batch, dev, peaks, ms * 1e3, x.indptr_d, x.indices_d)
+    rotate = x.rotate
+    launches = args.steps * (1 + (1 if dec.has_merge else 0))
+    del x
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads of the same family, from the same run
+    per_config = {}
+    if not args.no_per_config:
+        legs_of = {2: ("fp8", "multi_query", "cascade", "head_products"), 3: ("fp8",), 5: ()}
+        for n in (2, 3, 4, 5):
+            if n == args.workload:
+                continue
+            b = workloads.make_workload(n)
+            per_config[b.spec.name] = measure_config(b, dev, args, peaks, peak_src, legs_of.get(n, ()))
+            del b
 
     cpu = None
     if not args.no_cpu_baseline:
         us, nreq, tok = cpu_oracle_sample(batch, args.cpu_budget_s)
         cpu = {"value": us, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
                "sample": f"first {nreq} requests ({tok} of {batch.nnz} tokens), fp64 numpy, scaled by tokens"}
-    launches = args.steps * (1 + (1 if dec.has_merge else 0))
     line = {
         "metric": METRIC, "value": ms * 1e3, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
@@ -813,6 +914,7 @@ def run_ours(args, batch, world, rank, local, pg):
                   "as above), replayed once between the events; step_us_host_launched: the same steps issued one "
                   "call at a time from Python",
         "roofline": roof,
+        "per_config": per_config,
         "head_products": head_products,
         "multi_query": multi_query,
         "cascade": cascade,
@@ -820,9 +922,12 @@ def run_ours(args, batch, world, rank, local, pg):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "includes": "mla_decode_step_host: host plan + pinned H2D (q, indptr, indices, plan) + kernels + D2H "
-                            "(out, lse) every step; steps pipelined with copies on copy-in / copy-out streams and two staging buffers "
-                            "(value), one at a time on one stream (serial_us)",
-                "serial_us": e2e_serial_us, "pipelined_result_matches_serial": e2e_ok},
+                            "(out fp32, lse) every step; steps pipelined with copies on copy-in / copy-out streams and "
+                            "two staging buffers (value), one at a time on one stream (serial_us)",
+                "serial_us": e2e_serial_us, "pipelined_result_matches_serial": e2e_ok,
+                "bf16_out": {"value": e2e_bf16_us, "serial_us": e2e_bf16_serial_us, "d2h_bytes_per_step": int(d2h_bf16),
+                             "pipelined_result_matches_serial": e2e_bf16_ok,
+                             "note": "the same loop with the output written and copied back as bf16"}},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "plan_us_host": plan_us,
@@ -838,8 +943,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the chosen workload (per_config stays empty)")
     ap.add_argument("--sets", type=int, default=0,
                     help="input sets rotated over the back-to-back steps (0: enough to defeat L2; 1 for profiling)")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
