@@ -39,7 +39,8 @@ Sources, by page and section:
     absorbing and decompressing paths -- ``mac_counts``.
   * "[sglang] EAGLE 트리 검증 어텐션 최적화", section "들어가며": draft tokens
     verified in one pass, each attending to the shared prefix and its
-    ancestors -- ``decode_attention_multi_query`` (chain-shaped drafts).
+    ancestors -- ``decode_attention_multi_query`` (chain-shaped drafts),
+    ``tree_ancestors`` and ``decode_attention_tree`` (topk > 1: a tree).
   * "MLA and torch.compile", section "MLA: starting from a 439-line commit"
     (FP8 KV cache; FP8 tensors are float8_e4m3fn) and "实现差距", section 2.4
     (FP8 packing of new rows) -- ``e4m3_to_f64``, ``f32_to_e4m3``,
@@ -52,14 +53,19 @@ invariance under relabelling cache slots; all-equal rows and q = 0 closed
 forms; the MAC counts printed in exercise 1 (tests/golden/); the E4M3 code
 table and rounding against torch's float8_e4m3fn conversions plus closed-form
 codes, ties and saturation; FP8 decode against the bf16 decode of the same
-(exactly representable) values.  Every function here is pinned by at least
-one of them.
+(exactly representable) values; the draft tree against a brute-force masked
+softmax whose visibility comes from a transitive closure of the parent
+relation, against the chain and the star (every draft a child of the
+context), a hand-made three-draft tree, and relabellings of sibling
+subtrees.  Every function here is pinned by at least one of them.
 
 Readings taken where the pages are silent: the rope key sits at columns
 [512, 576) of a row; the LSE is natural-log and of the scaled scores; an empty
 request gives out = 0 and lse = -inf; merging skips partials whose lse is -inf;
 a slot named twice in one request counts twice; an FP8 cache holds E4M3
-codes with one float32 scale for the whole cache.
+codes with one float32 scale for the whole cache; a draft tree lists its
+drafts in generation order (a parent before its children, -1 for a child of
+the verified context), and its drafts are the last W rows of the context.
 """
 from __future__ import annotations
 
@@ -150,6 +156,61 @@ def decode_attention_multi_query(q_nope_bits, q_rope_bits, kv_cache_bits, kv_ind
         assert hi - lo >= q_len, "a context holds at least its new tokens"
         for i in range(Q):
             rows = gather_rows(kv_cache_bits, kv_indices, lo, hi - q_len + i + 1)
+            o, l = partial_state(bf16_bits_to_f64(qn[b, i]), bf16_bits_to_f64(qr[b, i]), rows, sm_scale)
+            out[b, i], lse[b, i] = o, l
+    return out, lse
+
+
+def tree_ancestors(parents) -> list:
+    """Ancestor-or-self sets of a draft tree.
+
+    parents [W] (ints): parents[i] is the draft that draft i extends, or -1
+    when it extends the verified context directly.  The drafts are listed in
+    the order they were generated, so a parent comes before its children
+    (parents[i] < i); anything else is rejected with ValueError.  Returns, for
+    every i, the sorted list of i, its parent, its parent's parent, ... .
+    ("[sglang] EAGLE 트리 검증 어텐션 최적화", section "들어가며": with topk > 1
+    the drafts form a tree, and each query token attends only to its own
+    ancestor chain among them.)
+    """
+    par = [int(x) for x in np.asarray(parents).reshape(-1)]
+    out = []
+    for i, pi in enumerate(par):
+        if not -1 <= pi < i:
+            raise ValueError(f"draft {i}: parent {pi} is not an earlier draft or -1")
+        chain = [i] if pi < 0 else out[pi] + [i]
+        out.append(sorted(chain))
+    return out
+
+
+def decode_attention_tree(q_nope_bits, q_rope_bits, kv_cache_bits, kv_indptr, kv_indices, sm_scale, parents):
+    """Verification of a tree of W draft tokens per request in one pass.
+
+    q_nope [B, W, H, 512], q_rope [B, W, H, 64] (bf16 bits); request b's
+    context of L_b rows ends with its W drafts in their generation order,
+    parents [B, W] as in ``tree_ancestors``.  Query i sees the first L_b - W
+    rows (the verified context, shared by every draft) and, among the drafts,
+    exactly its ancestors and itself ("[sglang] EAGLE 트리 검증 어텐션 최적화",
+    section "들어가며").  A chain (parents[i] = i - 1) is
+    ``decode_attention_multi_query``.  Returns (out [B, W, H, 512],
+    lse [B, W, H]).
+    """
+    qn = np.asarray(q_nope_bits)
+    qr = np.asarray(q_rope_bits)
+    B, W, H = qn.shape[0], qn.shape[1], qn.shape[2]
+    parents = np.asarray(parents).reshape(B, W)
+    out = np.empty((B, W, H, KV_LORA_RANK))
+    lse = np.empty((B, W, H))
+    for b in range(B):
+        lo, hi = int(kv_indptr[b]), int(kv_indptr[b + 1])
+        if hi - lo < W:
+            raise ValueError("a context holds at least its draft tokens")
+        first = hi - W                                   # the first draft's position in kv_indices
+        anc = tree_ancestors(parents[b])
+        for i in range(W):
+            slots = np.concatenate([np.asarray(kv_indices[lo:first], dtype=np.int64),
+                                    np.asarray([kv_indices[first + a] for a in anc[i]], dtype=np.int64)])
+            rows = bf16_bits_to_f64(kv_cache_bits[slots])
             o, l = partial_state(bf16_bits_to_f64(qn[b, i]), bf16_bits_to_f64(qr[b, i]), rows, sm_scale)
             out[b, i], lse[b, i] = o, l
     return out, lse
