@@ -408,6 +408,85 @@ def time_multi_query(batch, dev, peaks, kv, indptr_d, indices_d):
     return res
 
 
+def topk_tree_parents(width, topk=2):
+    """Parent array of a draft tree grown breadth first, every draft getting
+    `topk` children until `width` drafts exist (-1: a child of the verified
+    context).  topk = 2, width = 8: [-1, 0, 0, 1, 1, 2, 2, 3], depth 4."""
+    par = [-1]
+    node = 0
+    while len(par) < width:
+        for _ in range(topk):
+            if len(par) < width:
+                par.append(node)
+        node += 1
+    return par
+
+
+def time_tree(batch, dev, peaks, kv, indptr_d, indices_d):
+    """Tree-shaped draft verification (mla_decode_run_tree) at this
+    workload's contexts: a top-2 tree of W = 128 // H drafts per request
+    (every query sees the context and its ancestors), and for comparison the
+    chain of W drafts (mla_decode_run_multi_query), each over back-to-back
+    launches that rotate KV copies larger than 4x L2.  Only for H <= 32."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding
+    Bn, H = batch.batch, batch.heads
+    if H > 32:
+        return None
+    W = 128 // H
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(4 * l2 / (batch.nnz * 1152)) + 1)
+    kvs = [kv] + [kv.clone() for _ in range(R - 1)]
+    par_host = np.tile(np.array(topk_tree_parents(W), dtype=np.int32), (Bn, 1))
+    parents = torch.from_numpy(par_host).to(dev)
+    masks = torch.zeros((Bn, W), dtype=torch.int64, device=dev)
+    qn = torch.randn((Bn, W, H, 512), device=dev).to(torch.bfloat16)
+    qr = torch.randn((Bn, W, H, 64), device=dev).to(torch.bfloat16)
+    plan, ws_bytes = binding.decode_plan(batch.kv_indptr, W * H)
+    plan_d = torch.from_numpy(plan).to(dev)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty((Bn, W, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((Bn, W, H), dtype=torch.float32, device=dev)
+    runs = {
+        "tree": lambda k: binding.decode_run_tree(plan, plan_d, parents, masks, qn, qr, kvs[k % R], indptr_d,
+                                                  indices_d, batch.sm_scale, out, lse, ws),
+        "chain": lambda k: binding.decode_run_multi_query(plan, plan_d, W, qn, qr, kvs[k % R], indptr_d, indices_d,
+                                                          batch.sm_scale, out, lse, ws),
+    }
+    res = {"drafts": W, "topk": 2, "parents": topk_tree_parents(W), "heads_per_query": H}
+    anc = []
+    for i, p_ in enumerate(res["parents"]):
+        anc.append(1 if p_ < 0 else anc[p_] + 1)          # drafts each query sees (its depth)
+    for name, run in runs.items():
+        for k in range(3):
+            run(k)
+        torch.cuda.synchronize()
+        n = max(20, R)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(n):
+            run(k)
+        e1.record()
+        torch.cuda.synchronize()
+        st = binding.check_errors(ws)
+        if st != 0:
+            raise RuntimeError(f"device status after the {name} verification: {binding.status_string(st)}")
+        us = e0.elapsed_time(e1) * 1e3 / n
+        rows = Bn * W * H
+        bytes_alg = batch.nnz * 1152 + batch.nnz * 4 + rows * (576 * 2 + 512 * 4 + 4) + (Bn + 1) * 4
+        seen = anc if name == "tree" else [i + 1 for i in range(W)]
+        flops = 2176 * H * sum(max(0, int(L) - W) + d for L in batch.lengths for d in seen)
+        t = max(bytes_alg / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+        res[name] = {"us": us, "roofline_us": t, "frac": t / us}
+    res["note"] = ("W draft tokens per request verified in one pass over this workload's contexts; tree: a top-2 "
+                   "breadth-first tree (parents as listed), each query seeing the context and its ancestors "
+                   "(ancestor masks built by a small kernel every call); chain: the same W drafts in a line; "
+                   "synthetic queries; back-to-back launches over KV copies > 4x L2")
+    del kvs
+    return res
+
+
 def cascade_csr(batch):
     """Host CSR arrays of the shared-prefix leg (H <= 32): a prefix of
     min(4096, pool) distinct slots; G pseudo-requests of 128 // H requests'
@@ -708,6 +787,8 @@ def measure_config(batch, dev, args, peaks, peak_src, legs=()):
         res["multi_query"] = time_multi_query(batch, dev, peaks, x.kv, x.indptr_d, x.indices_d)
     if "cascade" in legs:
         res["cascade"] = time_cascade(batch, dev, peaks)
+    if "tree" in legs:
+        res["tree_verify"] = time_tree(batch, dev, peaks, x.kv, x.indptr_d, x.indices_d)
     if "head_products" in legs:
         res["head_products"] = time_head_products(batch, dev, peaks)
     del x
@@ -880,6 +961,7 @@ def run_ours(args, batch, world, rank, local, pg):
     head_products = time_head_products(batch, dev, peaks)
     multi_query = time_multi_query(batch, dev, peaks, kv, x.indptr_d, x.indices_d)
     cascade = time_cascade(batch, dev, peaks)
+    tree = time_tree(batch, dev, peaks, kv, x.indptr_d, x.indices_d)
     fp8 = time_fp8(batch, dev, peaks, ms * 1e3, x.indptr_d, x.indices_d)
     rotate = x.rotate
     launches = args.steps * (1 + (1 if dec.has_merge else 0))
@@ -889,7 +971,7 @@ def run_ours(args, batch, world, rank, local, pg):
     # ---- the other workloads of the same family, from the same run
     per_config = {}
     if not args.no_per_config:
-        legs_of = {2: ("fp8", "multi_query", "cascade", "head_products"), 3: ("fp8",), 5: ()}
+        legs_of = {2: ("fp8", "multi_query", "cascade", "tree", "head_products"), 3: ("fp8",), 5: ()}
         for n in (2, 3, 4, 5):
             if n == args.workload:
                 continue
@@ -918,6 +1000,7 @@ def run_ours(args, batch, world, rank, local, pg):
         "head_products": head_products,
         "multi_query": multi_query,
         "cascade": cascade,
+        "tree_verify": tree,
         "fp8_cache": fp8,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

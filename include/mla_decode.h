@@ -51,7 +51,9 @@ typedef enum {
   MLA_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, attribute, device query) */
   MLA_ERR_TIMEOUT = 5,       /* a device-side wait exceeded its limit (~1 s); the kernel returned early */
   MLA_ERR_INDEX_OOB = 6,     /* a kv_indices value was outside [0, num_slots); row 0 was read instead */
-  MLA_ERR_PLAN_MISMATCH = 7  /* a plan work item does not lie inside its request's kv_indptr range */
+  MLA_ERR_PLAN_MISMATCH = 7, /* a plan work item does not lie inside its request's kv_indptr range */
+  MLA_ERR_TREE = 8           /* a draft tree names a parent that is not an earlier draft or -1; that draft
+                                was verified as a child of the context */
 } mla_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -255,6 +257,37 @@ int mla_decode_run_multi_query(const int32_t* plan_host, const int32_t* plan_dev
                                const int32_t* kv_indptr, const int32_t* kv_indices, float sm_scale, void* out,
                                int32_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/* mla_decode_run_tree -- asynchronous on `stream`.
+ *
+ * Verification of a TREE of W = q_len draft tokens per request in one pass
+ * ("[sglang] EAGLE 트리 검증 어텐션 최적화", section "들어가며": with topk > 1
+ * the drafts form a tree, and each query token attends to the verified
+ * context and to its own ancestor chain among the drafts).  Request b's
+ * context of L_b rows ends with its W drafts in generation order; query i
+ * sees the first L_b - W rows and, among the last W, the drafts on its path
+ * to the root and itself.  Layouts and plan as for mla_decode_run_multi_query
+ * (the W x H query rows are the heads of one request, each cache row is
+ * gathered once for all of them), plus:
+ *   tree_parents  device int32 [B, W]: parents[b][i] = the draft that draft i
+ *                 extends (0 <= parent < i), or -1 for a child of the context.
+ *                 Read only.  An entry outside [-1, i) records MLA_ERR_TREE
+ *                 (mla_check_errors) and draft i is verified as a child of
+ *                 the context.
+ *   tree_masks    device uint64 [B, W], 8-byte aligned, caller-owned scratch:
+ *                 the call writes each draft's ancestor-or-self bits there
+ *                 (a small kernel on `stream`) and the decode kernels read
+ *                 them; it must stay allocated until the call's work is done.
+ * W = 1 is mla_decode_run.  Both decode kernels apply the masks (W * H of 16
+ * or 32: one CTA per worker; 48..128: a two-CTA cluster).
+ * Errors: MLA_ERR_INVALID_ARG when W < 1, the plan's head count is not a
+ * multiple of W, or tree_parents / tree_masks is null or misaligned;
+ * MLA_ERR_UNSUPPORTED when W > 64; otherwise as for mla_decode_run. */
+int mla_decode_run_tree(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len,
+                        const int32_t* tree_parents, uint64_t* tree_masks, const void* q_nope, const void* q_rope,
+                        const void* kv_cache, int64_t num_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
+                        float sm_scale, void* out, int32_t out_dtype, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /* mla_decode_step_host -- one decode step from HOST buffers, asynchronous on `stream`.
  *

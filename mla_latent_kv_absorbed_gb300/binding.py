@@ -20,13 +20,14 @@ MLA_OK = 0
 STATUS_NAMES = {
     0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
     4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT", 6: "MLA_ERR_INDEX_OOB", 7: "MLA_ERR_PLAN_MISMATCH",
+    8: "MLA_ERR_TREE",
 }
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decode_run",
            "mla_decode_attend", "mla_decode_merge", "mla_merge_states", "mla_check_errors",
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
            "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query",
            "mla_merge_two_states", "mla_decode_fp8_workspace_bytes", "mla_decode_run_fp8", "mla_append_kv_fp8",
-           "mla_decode_graph_sizes", "mla_decode_run_graph", "mla_noalloc_check_errors")
+           "mla_decode_graph_sizes", "mla_decode_run_graph", "mla_noalloc_check_errors", "mla_decode_run_tree")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -65,6 +66,9 @@ _lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
 _lib.mla_decode_run_multi_query.restype = ctypes.c_int
 _lib.mla_decode_run_multi_query.argtypes = [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp,
                                             ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.mla_decode_run_tree.restype = ctypes.c_int
+_lib.mla_decode_run_tree.argtypes = [_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, _vp,
+                                     ctypes.c_float, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
 _lib.mla_merge_two_states.restype = ctypes.c_int
 _lib.mla_merge_two_states.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_int32, _vp, _vp]
 _lib.mla_step_staging_bytes.restype = ctypes.c_size_t
@@ -344,6 +348,25 @@ def decode_run_multi_query(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache,
                                          _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_decode_run_multi_query")
+
+
+def decode_run_tree(plan_host, plan_dev, parents, tree_masks, q_nope, q_rope, kv_cache, kv_indptr, kv_indices,
+                    sm_scale, out, lse, workspace, stream=None) -> None:
+    """A tree of W draft tokens per request in one pass: parents device int32 [B, W] (each draft's parent, an
+    earlier draft, or -1), tree_masks device int64 [B, W] scratch; q [B, W, H, 576 split], out [B, W, H, 512]."""
+    out_dtype = _out_dtype(out, "mla_decode_run_tree")
+    plan_host = np.ascontiguousarray(plan_host, dtype=np.int32)
+    _check_csr(plan_host, kv_indptr, kv_indices, "mla_decode_run_tree")
+    W = int(parents.shape[-1])
+    if tree_masks.numel() < parents.numel() or tree_masks.element_size() != 8:
+        raise MLAError(1, "mla_decode_run_tree: tree_masks must hold one 8-byte word per draft")
+    st = _lib.mla_decode_run_tree(plan_host.ctypes.data, _ptr(plan_dev), W, _ptr(parents), _ptr(tree_masks),
+                                  _ptr(q_nope), _ptr(q_rope), _ptr(kv_cache), int(kv_cache.shape[0]),
+                                  _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out), out_dtype,
+                                  _ptr(lse), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                  _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_run_tree")
 
 
 def merge_two_states(o_a, lse_a, o_b, lse_b, out, lse, stream=None) -> None:

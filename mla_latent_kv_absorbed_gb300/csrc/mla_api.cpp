@@ -81,6 +81,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
     case MLA_ERR_INDEX_OOB: return "MLA_ERR_INDEX_OOB";
     case MLA_ERR_PLAN_MISMATCH: return "MLA_ERR_PLAN_MISMATCH";
+    case MLA_ERR_TREE: return "MLA_ERR_TREE";
     default: return "MLA_ERR_UNKNOWN";
   }
 }
@@ -148,7 +149,8 @@ namespace {
 int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len, const void* q_nope,
                 const void* q_rope, const void* kv_cache, int64_t num_slots, const int32_t* kv_indptr,
                 const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
-                void* workspace, size_t workspace_bytes, void* stream);
+                void* workspace, size_t workspace_bytes, void* stream,
+                const unsigned long long* tree_masks = nullptr);
 }  // namespace
 
 int mla_decode_attend(const int32_t* plan_host, const int32_t* plan_dev, const void* q_nope,
@@ -167,6 +169,32 @@ int mla_decode_run_multi_query(const int32_t* plan_host, const int32_t* plan_dev
                                void* stream) {
   const int rc = attend_impl(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache, num_slots, kv_indptr,
                              kv_indices, sm_scale, out, out_dtype, lse, workspace, workspace_bytes, stream);
+  if (rc != MLA_OK) return rc;
+  return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_run_tree(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len,
+                        const int32_t* tree_parents, uint64_t* tree_masks, const void* q_nope, const void* q_rope,
+                        const void* kv_cache, int64_t num_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
+                        float sm_scale, void* out, int32_t out_dtype, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  const int rc0 = check_run_args(plan_host, plan_dev, out_dtype, workspace, workspace_bytes);
+  if (rc0 != MLA_OK) return rc0;
+  const int B = plan_host[kHBatch], H = plan_host[kHHeads];
+  if (q_len < 1 || H % q_len != 0) return MLA_ERR_INVALID_ARG;
+  if (q_len > 64) return MLA_ERR_UNSUPPORTED;
+  if (q_len == 1)
+    return mla_decode_run(plan_host, plan_dev, q_nope, q_rope, kv_cache, num_slots, kv_indptr, kv_indices, sm_scale,
+                          out, out_dtype, lse, workspace, workspace_bytes, stream);
+  if (!tree_parents || !tree_masks || (reinterpret_cast<uintptr_t>(tree_masks) & 7u) != 0 ||
+      (reinterpret_cast<uintptr_t>(tree_parents) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned long long* masks = reinterpret_cast<unsigned long long*>(tree_masks);
+  const int rm = launch_tree_masks(tree_parents, B, q_len, masks, static_cast<int*>(workspace), st);
+  if (rm != MLA_OK) return rm;
+  const int rc = attend_impl(plan_host, plan_dev, q_len, q_nope, q_rope, kv_cache, num_slots, kv_indptr,
+                             kv_indices, sm_scale, out, out_dtype, lse, workspace, workspace_bytes, stream, masks);
   if (rc != MLA_OK) return rc;
   return mla_decode_merge(plan_host, plan_dev, out, out_dtype, lse, workspace, workspace_bytes, stream);
 }
@@ -197,7 +225,7 @@ int launch_decode(const DecodeParams& p, int variant, const void* q_nope, const 
 int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len, const void* q_nope,
                 const void* q_rope, const void* kv_cache, int64_t num_slots, const int32_t* kv_indptr,
                 const int32_t* kv_indices, float sm_scale, void* out, int32_t out_dtype, float* lse,
-                void* workspace, size_t workspace_bytes, void* stream) {
+                void* workspace, size_t workspace_bytes, void* stream, const unsigned long long* tree_masks) {
   const int rc0 = check_run_args(plan_host, plan_dev, out_dtype, workspace, workspace_bytes);
   if (rc0 != MLA_OK) return rc0;
   if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
@@ -234,6 +262,7 @@ int attend_impl(const int32_t* plan_host, const int32_t* plan_dev, int32_t q_len
   // both decode kernels apply the per-row causal limit
   if (q_len < 1 || H % q_len != 0) return MLA_ERR_INVALID_ARG;
   p.q_len = q_len;
+  p.tree_masks = q_len > 1 ? tree_masks : nullptr;   // draft trees: ancestor masks instead of the chain's limit
   return launch_decode(p, plan_host[kHVariant], q_nope, q_rope, kv_cache, st);
 }
 }  // namespace

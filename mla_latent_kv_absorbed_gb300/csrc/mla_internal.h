@@ -58,6 +58,8 @@ struct DecodeParams {
   int plan_cap_words;         // > 0: a device-only plan (graph replays) of at most this many words, checked
                               // and clamped by the kernels; 0: a plan the host has checked
   int max_partials;           // partial states the workspace holds; an item naming another writes nothing
+  const unsigned long long* tree_masks;   // q_len > 1: per request and draft [B, q_len] the ancestor-or-self
+                                          // bits of a draft tree, or null for a chain of drafts
 };
 
 struct MergeParams {

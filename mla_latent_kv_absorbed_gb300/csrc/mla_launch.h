@@ -33,6 +33,11 @@ int launch_project(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadG
 int launch_merge_two(const float* o_a, const float* l_a, const float* o_b, const float* l_b, void* out, int out_bf16,
                      float* lse, long long rows, cudaStream_t stream);
 
+// Ancestor-or-self masks of B draft trees of W <= 64 drafts (parents [B, W]
+// int32 -> masks [B, W] uint64); a bad parent records MLA_ERR_TREE in status.
+int launch_tree_masks(const int32_t* parents, int batch, int width, unsigned long long* masks, int* status,
+                      cudaStream_t stream);
+
 // Cache append of a step's new rows.
 int launch_append(const AppendParams& p, cudaStream_t stream);
 

@@ -177,6 +177,10 @@ __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_ca
 constexpr float kEncBias = 12582912.0f;      // 1.5 * 2^23
 constexpr float kDecHi = 2160066560.0f;      // 2^31 + 2^23 + 2^22 = 515 * 2^22 (exact in fp32)
 
+// kMQ: several query tokens per request (q_len > 1: a chain or a tree of
+// drafts), each row with its own visible tokens; the single-query
+// instantiation carries none of it.
+template <bool kMQ>
 __global__ void __launch_bounds__(kThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kr,
                 const __grid_constant__ CUtensorMap tm_qr,
@@ -522,6 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // -- tile g (j-th of an item of n tokens): add the peer's rows, softmax, P
+    // draft trees: this row's ancestor-or-self mask over the item's draft
+    // tokens, which start at item position t_d0 (far past the end otherwise)
+    uint64_t t_anc = 0;
+    int t_d0 = 0x3FFFFFFF;
     auto softmax = [&](uint32_t g, int j, int n) {
       const uint32_t sb = g & 1, xs = g % kXSlots;
       const uint32_t tm_s = tmem + lane_off + kTmS + sb * 64 + th * TH;
@@ -580,10 +588,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int nvalid = n - j * T - th * TH;
-      if (nvalid < TH) {
+      const int dz = t_d0 - j * T - th * TH;     // the first draft token's place in this half tile
+      if (nvalid < TH || dz < TH) {
+        // bit t: token t lies before the item end and, if it is a draft
+        // token, is an ancestor of this row's query or the query itself
+        uint32_t vis = nvalid >= TH ? 0xFFFFFFFFu : (nvalid <= 0 ? 0u : (1u << nvalid) - 1u);
+        if (dz < TH) {
+          const uint64_t a = dz >= 0 ? (t_anc << dz) | ((1ull << dz) - 1ull) : (-dz >= 64 ? 0ull : t_anc >> -dz);
+          vis &= static_cast<uint32_t>(a);
+        }
 #pragma unroll
         for (int t = 0; t < TH; ++t)
-          if (t >= nvalid) sv[t] = __float_as_uint(-INFINITY);
+          if (!((vis >> t) & 1u)) sv[t] = __float_as_uint(-INFINITY);
       }
       // the half row's maximum as a tree (short dependency chains)
       float mx8[8];
@@ -755,13 +771,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !aborted) mbar_arrive(bar(bQFull));
         for (int j = 0; j < nt; ++j, ++g) send(g);
       } else {
-        // multi-query: row h is query h / (H / q_len) of its request, which
-        // sees the first L - q_len + 1 + i rows of the request's context
+        // multi-query: row h is query i = h / (H / q_len) of its request.  A
+        // chain of drafts sees the first L - q_len + 1 + i rows of the
+        // request's context; a tree sees the first L - q_len rows and, among
+        // the last q_len, the ancestors of draft i and draft i itself
         int n_row = n;
-        if (p.q_len > 1) {
+        if (kMQ && p.q_len > 1) {
           const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
           const int i = h / (H / p.q_len);
-          n_row = max(0, min(n, (hi - lo) - p.q_len + 1 + i - (s - lo)));
+          if (p.tree_masks) {
+            t_anc = head_ok ? __ldg(p.tree_masks + static_cast<size_t>(b) * p.q_len + i) : 0ull;
+            t_d0 = (hi - lo) - p.q_len - (s - lo);
+          } else {
+            n_row = max(0, min(n, (hi - lo) - p.q_len + 1 + i - (s - lo)));
+          }
         }
         for (int j = 0; j < nt; ++j, ++g) softmax(g, j, n_row);
         epilogue(b, part, nitem);
@@ -793,12 +816,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kv_rope, const CUtensorMap& tm_qr,
                 const DecodeParams& p, int workers, cudaStream_t stream) {
   if (heads < 48 || heads > 128 || heads % 16 != 0) return MLA_ERR_UNSUPPORTED;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(pair::pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) !=
-        cudaSuccess)
+  const bool mq = p.q_len > 1;
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[mq]) {
+    if (cudaFuncSetAttribute(mq ? pair::pair_kernel<true> : pair::pair_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess)
       return MLA_ERR_CUDA;
-    attr_done = true;
+    attr_done[mq] = true;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * workers, 1, 1);
@@ -812,7 +836,9 @@ int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kv_ro
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pair::pair_kernel, tm_kv, tm_kv_rope, tm_qr, p) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, mq ? pair::pair_kernel<true> : pair::pair_kernel<false>, tm_kv, tm_kv_rope, tm_qr, p) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -486,16 +486,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int part = items[4 * it + 3];
       if (!item_ok(p, nnz, b, s, e)) continue;
       const int n = e - s, nt = (n + T - 1) / T;
-      // multi-query: head row h is query i = h / (NH / q_len) of its request,
-      // which sees the first L - q_len + 1 + i rows of the request's context,
-      // i.e. the item's first mq_base + i tokens
+      // multi-query: head row h is query i = h / (NH / q_len) of its request.
+      // A chain of drafts sees the first L - q_len + 1 + i rows of the
+      // request's context, i.e. the item's first mq_base + i tokens; a tree
+      // sees the item's tokens before mq_d0 (the first draft) and, among the
+      // drafts, the ancestors of draft i and draft i itself
       constexpr bool mq = kMQ;
-      int mq_base = n, mq_heads = NH;
+      int mq_base = n, mq_heads = NH, mq_d0 = 0x3FFFFFFF;
+      const bool tree = kMQ && p.tree_masks != nullptr;
       if (mq) {
         const int lo = __ldg(p.kv_indptr + b), hi = __ldg(p.kv_indptr + b + 1);
-        mq_base = (hi - lo) - p.q_len + 1 - (s - lo);
         mq_heads = NH / p.q_len;
+        if (tree) mq_d0 = (hi - lo) - p.q_len - (s - lo);
+        else mq_base = (hi - lo) - p.q_len + 1 - (s - lo);
       }
+      const unsigned long long* anc_b = tree ? p.tree_masks + static_cast<size_t>(b) * p.q_len : nullptr;
       for (int j = 0; j < nt; ++j, ++g) {
         const uint32_t buf = g & 1;
         wait(bar(C::bSFull + buf), (g >> 1) & 1);
@@ -521,10 +526,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(kBarSm, 128);
         float sv[kHalf];
+        const int kd = j * T + t - mq_d0;       // this token's draft index (tree), < 0 for the shared context
 #pragma unroll
         for (int k = 0; k < kHalf; ++k) {
           const int lim = mq ? max(0, min(n, mq_base + (pair * kHalf + k) / mq_heads)) : n;
-          sv[k] = t < lim - j * T ? (own[k] + X[((1 - pair) * kHalf + k) * T + t]) * p.scale_log2 : -INFINITY;
+          bool ok = t < lim - j * T;
+          if (kMQ && kd >= 0)                     // only a tree's draft tokens: an ancestor of this row's query?
+            ok = ok && kd < 64 && ((__ldg(anc_b + (pair * kHalf + k) / mq_heads) >> kd) & 1ull);
+          sv[k] = ok ? (own[k] + X[((1 - pair) * kHalf + k) * T + t]) * p.scale_log2 : -INFINITY;
         }
         if (j == 0) {
 #pragma unroll

@@ -157,6 +157,30 @@ def test_run_rejects_bad_arguments_before_launch(B):
     assert run(scale=float("nan")) == 1
 
 
+def test_tree_run_rejects_bad_arguments_before_launch(B):
+    # draft trees: width, head multiple, parents and mask scratch are checked
+    # on the host before the mask kernel or the decode is launched
+    lib = B.library()
+    fake = _fake_ptr()
+    plan, ws_bytes = B.decode_plan(np.array([0, 100, 300], dtype=np.int32), 16 * 4, num_sms=152)
+    ph = np.ascontiguousarray(plan, dtype=np.int32)
+
+    def run(W=4, parents=fake, masks=fake):
+        return lib.mla_decode_run_tree(ph.ctypes.data, fake, W, parents, masks, fake, fake, fake, 1000, fake, fake,
+                                       ctypes.c_float(0.1), fake, 0, fake, fake, ws_bytes, None)
+
+    assert run(W=0) == 1
+    assert run(W=3) == 1                                 # 64 rows are not a multiple of 3
+    assert run(parents=None) == 1
+    assert run(masks=None) == 1
+    assert run(masks=fake + 4) == 1                      # mask words are 8-byte aligned
+    assert run(parents=fake + 2) == 1
+    plan128, ws128 = B.decode_plan(np.array([0, 100], dtype=np.int32), 128, num_sms=152)
+    ph128 = np.ascontiguousarray(plan128, dtype=np.int32)
+    assert lib.mla_decode_run_tree(ph128.ctypes.data, fake, 128, fake, fake, fake, fake, fake, 1000, fake, fake,
+                                   ctypes.c_float(0.1), fake, 0, fake, fake, ws128, None) == 2   # W > 64
+
+
 def test_merge_rejects_bad_arguments(B):
     lib = B.library()
     assert lib.mla_merge_states(None, None, None, -1, 16, None, 0, None, None) == 1
@@ -323,7 +347,10 @@ def test_wrappers_refuse_index_arrays_shorter_than_the_plan(B):
                  lambda: B.decode_attend(plan, x, x, x, x, ok_ptr, short, 0.1, x, None, x),
                  lambda: B.decode_run_noalloc(plan, x, x, x, x, ok_ptr, short, 0.1, x, None),
                  lambda: B.decode_run_fp8(plan, x, x, x, x, 0.03, ok_ptr, short, 0.1, x, None, x),
-                 lambda: B.decode_run_multi_query(plan, x, 1, x, x, x, ok_ptr, short, 0.1, x, None, x)):
+                 lambda: B.decode_run_multi_query(plan, x, 1, x, x, x, ok_ptr, short, 0.1, x, None, x),
+                 lambda: B.decode_run_tree(plan, x, torch.zeros((2, 1), dtype=torch.int32),
+                                           torch.zeros((2, 1), dtype=torch.int64), x, x, x, ok_ptr, short, 0.1, x,
+                                           None, x)):
         with pytest.raises(ValueError, match="kv_indices has 299 entries"):
             call()
     # an empty batch covers no tokens

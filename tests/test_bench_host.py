@@ -60,3 +60,15 @@ def test_cascade_leg_index_arrays_match_their_kv_indptr():
         assert np.all(np.diff(c["f_ptr"]) == np.diff(c["s_ptr"]) + c["prefix_rows"])
         for a in (c["p_ind"], c["f_ind"]):
             assert a.min() >= 0 and a.max() < spec.pool
+
+
+def test_topk_tree_parents_is_a_valid_breadth_first_tree():
+    # the bench's draft tree: a parent before its children, top-2 fan-out,
+    # drafts of depth 1..4 for eight drafts
+    from oracle import mla_oracle as O
+    import bench
+    par = bench.topk_tree_parents(8)
+    anc = O.tree_ancestors(par)
+    assert par == [-1, 0, 0, 1, 1, 2, 2, 3]
+    assert [len(a) for a in anc] == [1, 2, 2, 3, 3, 3, 3, 4]
+    assert all(par.count(i) <= 2 for i in range(8))
