@@ -732,6 +732,58 @@ class DecodeInputs:
         return (self.R, (self.R - 1) * self.step_kv_bytes / 1e6)
 
 
+def time_absorbing_step(x, dev, args, peaks, decode_step_ms):
+    """A whole absorbing decode step at this workload's shape, timed as one
+    CUDA-graph replay of K steps over the rotating input sets: query
+    absorption (q_pre . w_kc -> the decode's q_nope), the append of one new
+    cache row per request (its context's last slot), the decode and merge
+    (bf16 output) and the output projection (o_lat . w_vc -> fp32).  Every
+    launch is a programmatic dependent of the one before it, so each kernel's
+    setup overlaps its predecessor's tail."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding, workloads
+    b = x.batch
+    Bn, H = b.batch, b.heads
+    stream = torch.cuda.current_stream(dev)
+    hp = workloads.make_head_product_inputs(Bn, H, seed=workloads.SEED_BASE + 901)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    q_pre, w_kc, w_vc = bf(hp.q_pre), bf(hp.w_kc), bf(hp.w_vc)
+    lengths = np.diff(b.kv_indptr)
+    if (lengths < 1).any():
+        return None
+    slots = torch.from_numpy(b.kv_indices[b.kv_indptr[1:] - 1].astype(np.int32)).to(dev)
+    new_rows = torch.randn((Bn, 576), device=dev).to(torch.bfloat16)
+    o_lat = torch.empty((Bn, H, 512), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((Bn, H, 128), dtype=torch.float32, device=dev)
+
+    def step(k, st):
+        qn, qr, kvc, ind = x.sets[k % x.R]
+        binding.absorb_query(q_pre, w_kc, qn, stream=st)
+        binding.append_kv(kvc, slots, new_rows, stream=st)
+        x.dec.attend(qn, qr, kvc, x.indptr_d, ind, b.sm_scale, o_lat, x.lse, st)
+        x.dec.merge(o_lat, x.lse, st)
+        binding.project_output(o_lat, w_vc, out, stream=st)
+
+    for k in range(max(3, x.R)):
+        step(k, stream)
+    x.check(stream, "after the absorbing step")
+    ms = graph_ms_per_call(step, args.steps, stream, dev)
+    x.check(stream, "after the absorbing step")
+    dec_bytes, dec_flops = algorithmic_work(b)
+    dec_bytes -= Bn * H * 512 * 2                     # bf16 output instead of fp32
+    head_bytes = 2 * H * 128 * 512 * 2 + Bn * H * (128 * 2 + 512 * 2) + Bn * H * (512 * 2 + 128 * 4)
+    app_bytes = Bn * (576 * 2 * 2 + 4)
+    bytes_alg = dec_bytes + head_bytes + app_bytes
+    flops = dec_flops + 4 * Bn * H * 128 * 512
+    t = max(bytes_alg / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+    return {"us": ms * 1e3, "decode_step_us": decode_step_ms * 1e3, "roofline_us": t, "frac": t / (ms * 1e3),
+            "algorithmic_bytes": bytes_alg,
+            "note": "absorb (q_pre . w_kc) + append (one row per request) + decode + merge (bf16 out) + project "
+                    "(o_lat . w_vc, fp32 out) per step, each launch a programmatic dependent of the one before; "
+                    "K steps as one CUDA-graph replay over the rotating input sets; synthetic weights"}
+
+
 def roofline_of(batch, peaks, peak_src, kernel_ms, step_ms):
     """The decode kernel against the roofline of this workload's algorithmic
     bytes and flops (the slower of the two at the measured peaks)."""
@@ -774,6 +826,7 @@ def measure_config(batch, dev, args, peaks, peak_src, legs=()):
     kernel_ms = graph_ms_per_call(x.attend, args.steps, stream, dev)
     x.check(stream, "after timing")
     roof = roofline_of(batch, peaks, peak_src, kernel_ms, step_ms)
+    absorbing = time_absorbing_step(x, dev, args, peaks, step_ms) if "absorbing_step" in legs else None
     res = {"workload": batch.spec.name, "batch": batch.batch, "heads": batch.heads, "nnz": batch.nnz,
            "step_us": step_ms * 1e3, "kernel_us": kernel_ms * 1e3, "frac": roof["frac"],
            "step_frac_of_roofline": roof["step_frac_of_roofline"], "traffic": roof["traffic"],
@@ -781,6 +834,8 @@ def measure_config(batch, dev, args, peaks, peak_src, legs=()):
            "latent_kv_gbs": batch.nnz * 1152 / (step_ms * 1e-3) / 1e9,
            "latent_kv_gbs_kernel": batch.nnz * 1152 / (kernel_ms * 1e-3) / 1e9,
            "kernel": roof["kernel"], "input_sets": x.R}
+    if absorbing is not None:
+        res["absorbing_step"] = absorbing
     if "fp8" in legs:
         res["fp8_cache"] = time_fp8(batch, dev, peaks, step_ms * 1e3, x.indptr_d, x.indices_d)
     if "multi_query" in legs:
@@ -959,6 +1014,7 @@ def run_ours(args, batch, world, rank, local, pg):
     roof = roofline_of(batch, peaks, peak_src, attend_ms, ms)
 
     head_products = time_head_products(batch, dev, peaks)
+    absorbing = time_absorbing_step(x, dev, args, peaks, ms)
     multi_query = time_multi_query(batch, dev, peaks, kv, x.indptr_d, x.indices_d)
     cascade = time_cascade(batch, dev, peaks)
     tree = time_tree(batch, dev, peaks, kv, x.indptr_d, x.indices_d)
@@ -971,7 +1027,8 @@ def run_ours(args, batch, world, rank, local, pg):
     # ---- the other workloads of the same family, from the same run
     per_config = {}
     if not args.no_per_config:
-        legs_of = {2: ("fp8", "multi_query", "cascade", "tree", "head_products"), 3: ("fp8",), 5: ()}
+        legs_of = {2: ("fp8", "multi_query", "cascade", "tree", "head_products", "absorbing_step"),
+                   3: ("fp8", "absorbing_step"), 5: ()}
         for n in (2, 3, 4, 5):
             if n == args.workload:
                 continue
@@ -998,6 +1055,7 @@ def run_ours(args, batch, world, rank, local, pg):
         "roofline": roof,
         "per_config": per_config,
         "head_products": head_products,
+        "absorbing_step": absorbing,
         "multi_query": multi_query,
         "cascade": cascade,
         "tree_verify": tree,

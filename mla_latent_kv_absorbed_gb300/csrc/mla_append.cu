@@ -16,6 +16,10 @@ constexpr int kAppendRows = 4;
 __global__ void __launch_bounds__(kAppendPieces * kAppendRows) append_kernel(const AppendParams p) {
   const int r = blockIdx.x * kAppendRows + threadIdx.x / kAppendPieces;
   const int piece = threadIdx.x % kAppendPieces;
+  // a programmatic dependent of the previous kernel in the stream: read and
+  // write only once it has finished, and let the next one be scheduled
+  griddep_wait();
+  griddep_launch_dependents();
   if (r >= p.rows) return;
   const long long slot = __ldg(p.slots + r);
   if (slot < 0 || slot >= p.num_slots) {
@@ -29,7 +33,16 @@ __global__ void __launch_bounds__(kAppendPieces * kAppendRows) append_kernel(con
 int launch_append(const AppendParams& p, cudaStream_t stream) {
   if (p.rows <= 0) return MLA_OK;
   const int blocks = (p.rows + kAppendRows - 1) / kAppendRows;
-  append_kernel<<<blocks, kAppendPieces * kAppendRows, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(kAppendPieces * kAppendRows, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, append_kernel, p) != cudaSuccess) return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -105,6 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // a programmatic dependent of the previous kernel in the stream (the setup
+  // above overlapped its tail): its results are read only once it has
+  // finished; the next kernel may be scheduled from here on
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -228,7 +233,17 @@ int launch(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGemmParam
   }
   const int tiles = p.heads * ((p.rows + BM - 1) / BM) * (N / C::NT);
   const int grid = tiles < sms ? tiles : sms;
-  head_gemm_kernel<K, N, NT, OutT><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_a, tm_w, p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // setup overlaps the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, head_gemm_kernel<K, N, NT, OutT>, tm_a, tm_w, p) != cudaSuccess) return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -37,6 +37,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   __shared__ float s_wsum[kMergeGroups - 1];
   const int e = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int G = static_cast<int>(blockDim.x >> 7), grp = tid >> 7, t = tid & 127;
+  // the next kernel in the stream may be scheduled now; it waits for this
+  // grid before it touches what this grid reads or writes
+  griddep_launch_dependents();
   const int nthreads = static_cast<int>(blockDim.x);
   int b, p0, p1;
   if (p.plan) {

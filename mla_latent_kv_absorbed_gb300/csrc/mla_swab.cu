@@ -218,10 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 
   const int w = blockIdx.x;
-  int it0, it1;
-  plan_items(p, w, it0, it1);
-  const int32_t* items = p.plan + p.items_off;
-  const int nnz = __ldg(p.kv_indptr + p.batch);   // loaded alongside the plan words
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kLatUnits; ++i) { mbar_init(bar(C::bLatFull + i), 1); mbar_init(bar(C::bLatEmpty + i), 1); }
@@ -246,6 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent of the previous kernel in the
+  // stream: everything above overlapped its tail; its results (the plan,
+  // indices, query, cache rows) are read only after it has finished
+  griddep_wait();
+  int it0, it1;
+  plan_items(p, w, it0, it1);
+  const int32_t* items = p.plan + p.items_off;
+  const int nnz = __ldg(p.kv_indptr + p.batch);
   if (threadIdx.x == 0) MLA_TRACE_RAW(15, 5, clock64());
   // the merge kernel may be launched now: it waits for this grid to finish
   griddep_launch_dependents();
@@ -735,7 +739,17 @@ int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap
       return MLA_ERR_CUDA;
     attr_done = true;
   }
-  swab_kernel<NH, kMQ><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_qn, tm_qr, p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // the prologue overlaps the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, swab_kernel<NH, kMQ>, tm_kv, tm_qn, tm_qr, p) != cudaSuccess) return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
