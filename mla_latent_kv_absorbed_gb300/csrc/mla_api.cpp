@@ -208,16 +208,18 @@ int launch_decode(const DecodeParams& p, int variant, const void* q_nope, const 
   CUtensorMap tm_kv, tm_qn, tm_qr;
   const uint64_t qrows = static_cast<uint64_t>(p.batch) * H;
   if (!make_map(&tm_kv, kv_cache, kRow, static_cast<uint64_t>(p.num_slots), 64, 1)) return MLA_ERR_CUDA;
+  // the rope as 32-dim halves (64-byte rows): the few-heads kernel's two
+  // folded score halves, the pair kernel's two CTAs
+  CUtensorMap tm_kr;
+  if (!make_map(&tm_kr, kv_cache, kRow, static_cast<uint64_t>(p.num_slots), 32, 1, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MLA_ERR_CUDA;
   if (variant == kVariantSwab) {
     if (!make_map(&tm_qr, q_rope, kRope, qrows, 64, static_cast<uint32_t>(H)) ||
         !make_map(&tm_qn, q_nope, kLatent, qrows, 64, static_cast<uint32_t>(H)))
       return MLA_ERR_CUDA;
-    return launch_swab(H, tm_kv, tm_qn, tm_qr, p, p.num_workers, st);
+    return launch_swab(H, tm_kv, tm_kr, tm_qn, tm_qr, p, p.num_workers, st);
   }
-  // the pair kernel's CTAs each take half of the rope dims: 64-byte rows
-  CUtensorMap tm_kr;
-  if (!make_map(&tm_kr, kv_cache, kRow, static_cast<uint64_t>(p.num_slots), 32, 1, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&tm_qr, q_rope, kRope, qrows, 32, static_cast<uint32_t>(H), CU_TENSOR_MAP_SWIZZLE_64B))
+  if (!make_map(&tm_qr, q_rope, kRope, qrows, 32, static_cast<uint32_t>(H), CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
   return launch_pair(H, tm_kv, tm_kr, tm_qr, p, p.num_workers, st);
 }

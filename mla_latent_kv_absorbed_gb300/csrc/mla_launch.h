@@ -8,8 +8,10 @@
 
 namespace mla {
 
-// Decode kernel for H in {16, 32}; grid = plan workers.
-int launch_swab(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_qn,
+// Decode kernel for H in {16, 32}; grid = plan workers.  tm_kv: bf16 rows, box
+// {64, 1}, 128-byte swizzle; tm_kr: the same rows, box {32, 1}, 64-byte swizzle
+// (the rope halves).
+int launch_swab(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kr, const CUtensorMap& tm_qn,
                 const CUtensorMap& tm_qr, const DecodeParams& p, int grid, cudaStream_t stream);
 
 // Decode kernel for H in 48..128 (a two-CTA cluster per worker); grid = 2 * workers.

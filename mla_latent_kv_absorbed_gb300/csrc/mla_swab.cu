@@ -20,8 +20,9 @@
 // tokens x 64 dims (8 KB).  A tile lands in three ring units: latent unit A
 // holds atoms {0, 4, 1, 5}, unit B atoms {2, 6, 3, 7} (so atom c+4 follows
 // atom c and one 128-row descriptor covers both halves), and the rope unit
-// holds the rope atom followed by the rope shifted by 32 dims (dims 544-607;
-// the 32 past the row end are the TMA's zero fill).  Each latent byte is read
+// holds rope dims 0-31 then 32-63 as two atoms of 64 tokens x 32 dims (64-byte
+// rows, 64-byte swizzle), so one 128-row descriptor covers the rope of both
+// halves too and no byte past the row is gathered.  Each latent byte is read
 // by the tensor core twice -- in the key (score over 576) and as the value
 // (the latent reused as V) -- and its unit is released after its PVs, so
 // every cache byte crosses HBM once.
@@ -56,11 +57,12 @@ namespace swab {
 
 constexpr int T = 64;                      // tokens per tile
 constexpr int kQkWarp = 4, kPvWarp = 5, kProducerWarp0 = 6;
-constexpr int kProducers = 10;             // latent atoms 0-7, rope, shifted rope
+constexpr int kProducers = 10;             // latent atoms 0-7, rope dims 0-31, rope dims 32-63
 constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
 constexpr int kAtom = T * 128;             // 8 KB: 64 tokens x 64 dims
 constexpr int kUnit = 4 * kAtom;           // latent unit: atoms {c, c+4, c+1, c+5}
-constexpr int kRopeUnit = 2 * kAtom;       // rope atom, then the rope shifted by 32 dims
+constexpr int kRopeAtom = T * 64;          // 4 KB: 64 tokens x 32 rope dims (64-byte swizzle)
+constexpr int kRopeUnit = 2 * kRopeAtom;   // rope dims 0-31, then 32-63
 constexpr int kRopeUnits = 2;
 #ifndef MLA_SWAB_LEAD_UNITS
 #define MLA_SWAB_LEAD_UNITS 4
@@ -193,8 +195,9 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
 // causal limit; the single-query instantiation carries none of it.
 template <int NH, bool kMQ>
 __global__ void __launch_bounds__(kThreads, 1)
-    swab_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qn,
-                const __grid_constant__ CUtensorMap tm_qr, const DecodeParams p) {
+    swab_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kr,
+                const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
+                const DecodeParams p) {
   using C = Cfg<NH>;
   constexpr int kHalf = C::kHalf;
   extern __shared__ uint8_t smem_raw[];
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // landing time is set by how many gathers one warp issues for it: each
     // producer owns one of the tile's ten gather jobs (16 gather4 each).
     // Job k < 8 is latent atom k (unit (k >> 1) & 1, position 2(k & 1) + (k >> 2));
-    // job 8 the rope atom (dims 512..575), job 9 the rope shifted by 32 dims.
+    // jobs 8 and 9 rope dims 0-31 and 32-63 (row dims 512..543, 544..575).
     // Jobs 0, 2 and 8 arm their unit's full barrier with the unit's bytes.
     // Slot numbers come straight from kv_indices (lane l < 16 loads tokens
     // 4l..4l+3, issued before the wait for ring space so the load overlaps
@@ -268,10 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the ragged tail repeats the last valid slot (its scores are masked).
     const int job = warp - kProducerWarp0;
     if (lane == 0 && job == 0) tma_prefetch_desc(&tm_kv);
+    if (lane == 0 && job == 8) tma_prefetch_desc(&tm_kr);
     const bool rope = job >= 8;
     const int u = (job >> 1) & 1;
-    const int x = rope ? (job == 8 ? kLatent : kLatent + 32) : 64 * job;
-    const uint32_t pos_off = rope ? (job - 8) * kAtom : ((job & 1) * 2 + (job >> 2)) * kAtom;
+    const int x = rope ? kLatent + 32 * (job - 8) : 64 * job;
+    const uint32_t pos_off = rope ? (job - 8) * kRopeAtom : ((job & 1) * 2 + (job >> 2)) * kAtom;
+    const CUtensorMap* tmap = rope ? &tm_kr : &tm_kv;
+    const uint32_t row_bytes = rope ? 64u : 128u;            // per gathered row
     const bool arms = rope ? job == 8 : (job == 0 || job == 2);
     const uint32_t arm_bytes = rope ? kRopeUnit : kUnit;
     const uint64_t pol = l2_policy_evict_first();
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!e_ok) { ok = false; break; }
         if (lane == 0 && arms) mbar_arrive_expect_tx(full, arm_bytes);
         __syncwarp();
-        if (lane < 16) tma_gather4(addr + pos_off + lane * 512, &tm_kv, x, v[0], v[1], v[2], v[3], full, pol);
+        if (lane < 16) tma_gather4(addr + pos_off + lane * 4 * row_bytes, tmap, x, v[0], v[1], v[2], v[3], full, pol);
         if (lane == 0 && arms) atomicMax(last_armed + last_idx, static_cast<int>(use));
         if (lane == 0 && job == 0) MLA_TRACE_EVENT(1, g);
       }
@@ -358,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_qr);
       const uint64_t dq = sdesc(base + C::kOffQ, 16, 1024);      // Q pair 0 (B of QK)
       const uint64_t dk = sdesc(base + C::kOffLat, 16, 1024);    // latent unit slot 0 (A of QK)
-      const uint64_t dr = sdesc(base + C::kOffRope, 16, 1024);   // rope unit slot 0 (A of QK)
+      const uint64_t dr = sdesc(base + C::kOffRope, 16, 512, kLayoutSw64);   // rope unit slot 0 (A of QK)
       auto D = [](uint64_t d, uint32_t byte_off) -> uint64_t { return d + (byte_off >> 4); };
       const uint32_t qbase = base + C::kOffQ;
       uint32_t g = 0, nitem = 0, ls = 0, lph = 0, rs = 0, rph = 0;
@@ -729,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int NH, bool kMQ>
-int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap& tm_qr,
+int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_kr, const CUtensorMap& tm_qn, const CUtensorMap& tm_qr,
            const DecodeParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<NH>;
   static bool attr_done = false;   // the attribute is per function, set once per process
@@ -749,19 +755,20 @@ int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_qn, const CUtensorMap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, swab_kernel<NH, kMQ>, tm_kv, tm_qn, tm_qr, p) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, swab_kernel<NH, kMQ>, tm_kv, tm_kr, tm_qn, tm_qr, p) != cudaSuccess)
+    return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace swab
 
-int launch_swab(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_qn,
+int launch_swab(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kr, const CUtensorMap& tm_qn,
                 const CUtensorMap& tm_qr, const DecodeParams& p, int grid, cudaStream_t stream) {
   const bool mq = p.q_len > 1;
-  if (heads == 16) return mq ? swab::launch<16, true>(tm_kv, tm_qn, tm_qr, p, grid, stream)
-                             : swab::launch<16, false>(tm_kv, tm_qn, tm_qr, p, grid, stream);
-  if (heads == 32) return mq ? swab::launch<32, true>(tm_kv, tm_qn, tm_qr, p, grid, stream)
-                             : swab::launch<32, false>(tm_kv, tm_qn, tm_qr, p, grid, stream);
+  if (heads == 16) return mq ? swab::launch<16, true>(tm_kv, tm_kr, tm_qn, tm_qr, p, grid, stream)
+                             : swab::launch<16, false>(tm_kv, tm_kr, tm_qn, tm_qr, p, grid, stream);
+  if (heads == 32) return mq ? swab::launch<32, true>(tm_kv, tm_kr, tm_qn, tm_qr, p, grid, stream)
+                             : swab::launch<32, false>(tm_kv, tm_kr, tm_qn, tm_qr, p, grid, stream);
   return MLA_ERR_UNSUPPORTED;
 }
 
