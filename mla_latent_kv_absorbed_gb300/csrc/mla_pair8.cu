@@ -195,11 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
 
   const int w = blockIdx.x >> 1;
-  int it0, it1;
-  plan_items(p, w, it0, it1);
-  const int32_t* items = p.plan + p.items_off;
   const int H = p.heads;
-  const int nnz = __ldg(p.kv_indptr + p.batch);   // loaded alongside the plan words
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLatBlocks; ++i) { mbar_init(bar(bLatFull + i), 1); mbar_init(bar(bLatEmpty + i), 1); }
@@ -232,6 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();                            // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent of the previous kernel in the
+  // stream: everything above overlapped its tail; its results (the plan,
+  // indices, query, cache rows) are read only after it has finished
+  griddep_wait();
+  int it0, it1;
+  plan_items(p, w, it0, it1);
+  const int32_t* items = p.plan + p.items_off;
+  const int nnz = __ldg(p.kv_indptr + p.batch);
   // the merge kernel may be launched now: it waits for this grid to finish
   griddep_launch_dependents();
   bool aborted = false;                          // set by the softmax / sender warps only
@@ -897,13 +901,15 @@ int launch_pair8(int heads, const CUtensorMap& tm_lat, const CUtensorMap& tm_rop
   cfg.blockDim = dim3(pair8::kThreads, 1, 1);
   cfg.dynamicSmemBytes = pair8::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // the prologue overlaps the previous kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, pair8::pair8_kernel, tm_lat, tm_rope, p, kv_scale) != cudaSuccess) return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

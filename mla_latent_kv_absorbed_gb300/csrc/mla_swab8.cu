@@ -724,6 +724,10 @@ constexpr int kAppendRows = 8;
 __global__ void __launch_bounds__(kAppendPieces * kAppendRows) append_fp8_kernel(const AppendFp8Params p) {
   const int r = blockIdx.x * kAppendRows + threadIdx.x / kAppendPieces;
   const int piece = threadIdx.x % kAppendPieces;
+  // a programmatic dependent of the previous kernel in the stream: read and
+  // write only once it has finished, and let the next one be scheduled
+  griddep_wait();
+  griddep_launch_dependents();
   if (r >= p.rows) return;
   const long long slot = __ldg(p.slots + r);
   if (slot < 0 || slot >= p.num_slots) {
@@ -757,6 +761,9 @@ int launch(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const DecodePa
     attr_done = true;
   }
   const int warps = pp.rows;
+  // a plain launch (full stream order): the decode kernel below, its
+  // programmatic dependent, starts gathering cache rows before it waits, which
+  // is safe only because everything before the prep kernel has finished
   q8_prep_kernel<NH><<<(warps + 7) / 8, 256, 0, stream>>>(pp);
   if (cudaPeekAtLastError() != cudaSuccess) return MLA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -790,7 +797,16 @@ size_t fp8_image_bytes(int heads) { return static_cast<size_t>(4) * heads * 288;
 int launch_append_fp8(const AppendFp8Params& p, cudaStream_t stream) {
   if (p.rows <= 0) return MLA_OK;
   const int blocks = (p.rows + swab8::kAppendRows - 1) / swab8::kAppendRows;
-  swab8::append_fp8_kernel<<<blocks, swab8::kAppendPieces * swab8::kAppendRows, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(swab8::kAppendPieces * swab8::kAppendRows, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, swab8::append_fp8_kernel, p) != cudaSuccess) return MLA_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
