@@ -134,8 +134,11 @@ def test_absorbing_step_eager_and_in_a_cuda_graph(H):
     check(*inp2)
 
 
-@pytest.mark.parametrize("H,out_dtype", [(16, "f32"), (128, "bf16")])
-def test_host_buffer_step_equals_device_run(H, out_dtype):
+@pytest.mark.parametrize("H,out_dtype,pinned_out", [(16, "f32", True), (128, "bf16", True), (128, "f32", True),
+                                                    (16, "f32", False), (128, "bf16", False)])
+def test_host_buffer_step_equals_device_run(H, out_dtype, pinned_out):
+    # the result copied back into page-locked or pageable host buffers: the
+    # device run's bits either way
     import torch
     from mla_latent_kv_absorbed_gb300 import binding, workloads as W
     from tests._helpers import to_device
@@ -151,8 +154,10 @@ def test_host_buffer_step_equals_device_run(H, out_dtype):
     hq = pin(bt.q_nope.view(np.int16)).view(torch.bfloat16)
     hr = pin(bt.q_rope.view(np.int16)).view(torch.bfloat16)
     hp, hi = pin(bt.kv_indptr.astype(np.int32)), pin(bt.kv_indices.astype(np.int32))
-    out = torch.empty((bt.batch, H, 512), dtype=dt).pin_memory()
-    lse = torch.empty((bt.batch, H), dtype=torch.float32).pin_memory()
+    out = torch.empty((bt.batch, H, 512), dtype=dt)
+    lse = torch.empty((bt.batch, H), dtype=torch.float32)
+    if pinned_out:
+        out, lse = out.pin_memory(), lse.pin_memory()
     plan = torch.empty(dec.plan_host.shape[0], dtype=torch.int32).pin_memory()
     staging = torch.empty(binding.step_staging_bytes(bt.batch, H, bt.nnz, plan.numel(), 0 if dt == torch.float32 else 1),
                           dtype=torch.uint8, device="cuda")
