@@ -99,25 +99,10 @@ int mla_decode_plan(const int32_t* kv_indptr, int32_t batch, int32_t num_heads, 
   if (!variant_for_heads(num_heads, &T, &cpw)) return MLA_ERR_UNSUPPORTED;
   if (num_sms < 0) return MLA_ERR_INVALID_ARG;
   if (num_sms == 0) {
-    // the SM count of the current device, queried once per device; plans
-    // may be built from several host threads at once, so the cache entries
-    // are atomics (a race only repeats the query)
-    static std::atomic<int> sms_of[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-      cudaGetLastError();
-      return MLA_ERR_CUDA;
-    }
-    const int cached = (dev >= 0 && dev < 64) ? sms_of[dev].load(std::memory_order_relaxed) : 0;
-    if (cached > 0) {
-      num_sms = cached;
-    } else {
-      if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return MLA_ERR_CUDA;
-      }
-      if (dev >= 0 && dev < 64) sms_of[dev].store(num_sms, std::memory_order_relaxed);
-    }
+    // the SM count of the current device (cached per device; plans may be
+    // built from several host threads at once)
+    num_sms = device_sm_count();
+    if (num_sms < 1) return MLA_ERR_CUDA;
   }
   std::vector<int32_t> words;
   size_t ws = 0;

@@ -217,20 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int K, int N, int NT, typename OutT>
 int launch(const CUtensorMap& tm_a, const CUtensorMap& tm_w, const HeadGemmParams& p, cudaStream_t stream) {
   using C = Cfg<K, N, NT>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(head_gemm_kernel<K, N, NT, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    attr_done = true;
-  }
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-      return MLA_ERR_CUDA;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&head_gemm_kernel<K, N, NT, OutT>), C::kSmemBytes))
+    return MLA_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms < 1) return MLA_ERR_CUDA;
   const int tiles = p.heads * ((p.rows + BM - 1) / BM) * (N / C::NT);
   const int grid = tiles < sms ? tiles : sms;
   cudaLaunchConfig_t cfg{};

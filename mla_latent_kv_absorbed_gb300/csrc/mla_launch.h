@@ -8,6 +8,14 @@
 
 namespace mla {
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` in the current
+// context (once per kernel and context; later calls return at once).  false:
+// the CUDA call failed.
+bool set_smem_limit(const void* func, int bytes);
+
+// SM count of the current device (cached per device), or 0 on an error.
+int device_sm_count();
+
 // Decode kernel for H in {16, 32}; grid = plan workers.  tm_kv: bf16 rows, box
 // {64, 1}, 128-byte swizzle; tm_kr: the same rows, box {32, 1}, 64-byte swizzle
 // (the rope halves).

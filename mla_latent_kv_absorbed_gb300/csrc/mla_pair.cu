@@ -821,13 +821,10 @@ int launch_pair(int heads, const CUtensorMap& tm_kv, const CUtensorMap& tm_kv_ro
                 const DecodeParams& p, int workers, cudaStream_t stream) {
   if (heads < 48 || heads > 128 || heads % 16 != 0) return MLA_ERR_UNSUPPORTED;
   const bool mq = p.q_len > 1;
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[mq]) {
-    if (cudaFuncSetAttribute(mq ? pair::pair_kernel<true> : pair::pair_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    attr_done[mq] = true;
-  }
+  if (!set_smem_limit(mq ? reinterpret_cast<const void*>(&pair::pair_kernel<true>)
+                          : reinterpret_cast<const void*>(&pair::pair_kernel<false>),
+                       pair::kSmemBytes))
+    return MLA_ERR_CUDA;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * workers, 1, 1);
   cfg.blockDim = dim3(pair::kThreads, 1, 1);

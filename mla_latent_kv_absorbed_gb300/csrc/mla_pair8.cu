@@ -889,13 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 int launch_pair8(int heads, const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const DecodeParams& p,
                  float kv_scale, int workers, cudaStream_t stream) {
   if (heads < 48 || heads > 128 || heads % 16 != 0) return MLA_ERR_UNSUPPORTED;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(pair8::pair8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pair8::kSmemBytes) !=
-        cudaSuccess)
-      return MLA_ERR_CUDA;
-    attr_done = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&pair8::pair8_kernel), pair8::kSmemBytes)) return MLA_ERR_CUDA;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * workers, 1, 1);
   cfg.blockDim = dim3(pair8::kThreads, 1, 1);

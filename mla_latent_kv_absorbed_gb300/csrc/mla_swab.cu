@@ -738,13 +738,7 @@ template <int NH, bool kMQ>
 int launch(const CUtensorMap& tm_kv, const CUtensorMap& tm_kr, const CUtensorMap& tm_qn, const CUtensorMap& tm_qr,
            const DecodeParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<NH>;
-  static bool attr_done = false;   // the attribute is per function, set once per process
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(swab_kernel<NH, kMQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    attr_done = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&swab_kernel<NH, kMQ>), C::kSmemBytes)) return MLA_ERR_CUDA;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -753,13 +753,7 @@ template <int NH>
 int launch(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const DecodeParams& p, const Fp8Params& p8,
            const Fp8PrepParams& pp, int grid, cudaStream_t stream) {
   using C = Cfg<NH>;
-  static bool attr_done = false;   // per function, once per process
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(swab8_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
-      return MLA_ERR_CUDA;
-    attr_done = true;
-  }
+  if (!set_smem_limit(reinterpret_cast<const void*>(&swab8_kernel<NH>), C::kSmemBytes)) return MLA_ERR_CUDA;
   const int warps = pp.rows;
   // a plain launch (full stream order): the decode kernel below, its
   // programmatic dependent, starts gathering cache rows before it waits, which
