@@ -170,10 +170,11 @@ __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_ca
 //           fh = 2^23 + (u >> 8) and fl = 2^23 + (u & 255),
 //           fh * 256 step + fl * step - (2^31 + 2^23 + 2^22) step = q * step,
 //           exactly, as two FMAs whose results are representable.
-// Both the sender (from its own codes) and the receiver (from the peer's)
-// form q * step exactly and then multiply by the same factor once, so the
-// two CTAs hold the same scaled partials and, after one commutative add,
-// the same scores.
+// The receiver forms q * step exactly from the peer's codes, adds it to its
+// own exact partial and multiplies the sum by the score scale once.  The two
+// CTAs' scores may then differ in their last bits (each rounds only the
+// other's partial); that is harmless, as each CTA normalises its own half of
+// O with row sums of its own scores.
 constexpr float kEncBias = 12582912.0f;      // 1.5 * 2^23
 constexpr float kDecHi = 2160066560.0f;      // 2^31 + 2^23 + 2^22 = 515 * 2^22 (exact in fp32)
 
