@@ -92,3 +92,25 @@ def test_multi_query_short_context_rows_on_both_kernels():
     # a q_len that does not divide the plan's rows is refused
     with pytest.raises(binding.MLAError):
         _run(bt2, 3, 4)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("q_len,H", [(4, 16), (2, 16)])
+def test_multi_query_full_size_v2lite_sampled(q_len, H):
+    # the bench's draft-verification shapes at the V2-Lite contexts (64
+    # requests, 512..4096 rows): 64 rows on the two-CTA kernel, 32 on the
+    # few-heads kernel, the plan of the whole batch; a sample of requests
+    # (as their own CSR batch) against the oracle
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    from oracle import mla_oracle as O
+    ref = W.make_workload(2)
+    bt = W.make_batch([int(x) for x in ref.lengths], heads=q_len * H, pool=ref.pool, seed=1800 + q_len)
+    out, lse, _ = _run(bt, q_len, H)
+    req = sorted(set([0, bt.batch - 1] + list(range(0, bt.batch, 9))))
+    lens = [int(bt.kv_indptr[b + 1] - bt.kv_indptr[b]) for b in req]
+    ptr = np.concatenate([[0], np.cumsum(lens)])
+    ind = np.concatenate([bt.kv_indices[bt.kv_indptr[b]:bt.kv_indptr[b + 1]] for b in req])
+    qn = bt.q_nope[req].reshape(len(req), q_len, H, 512)
+    qr = bt.q_rope[req].reshape(len(req), q_len, H, 64)
+    ro, rl = O.decode_attention_multi_query(qn, qr, bt.kv_cache, ptr, ind, bt.sm_scale, q_len)
+    _check(out[req], lse[req], ro, rl)

@@ -156,3 +156,37 @@ def test_bad_parent_is_reported_and_verified_as_a_child_of_the_context(W, Hq):
     ro, rl = _oracle(bt, W, fixed)
     assert_close(out.reshape(bt.batch, -1, 512), lse.reshape(bt.batch, -1), ro.reshape(bt.batch, -1, 512),
                  rl.reshape(bt.batch, -1))
+
+
+def _sub_batch(bt, W, requests):
+    """The given requests of a batch as their own CSR batch (their rows, their
+    queries), for the oracle."""
+    import copy
+    sub = copy.copy(bt)
+    lens = [int(bt.kv_indptr[b + 1] - bt.kv_indptr[b]) for b in requests]
+    sub.kv_indptr = np.concatenate([[0], np.cumsum(lens)]).astype(bt.kv_indptr.dtype)
+    sub.kv_indices = np.concatenate([bt.kv_indices[bt.kv_indptr[b]:bt.kv_indptr[b + 1]] for b in requests])
+    sub.q_nope, sub.q_rope = bt.q_nope[requests], bt.q_rope[requests]
+    sub.lengths = np.asarray(lens, dtype=bt.lengths.dtype)
+    return sub
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape", ["topk2", "chain"])
+def test_tree_full_size_v2lite_sampled(shape):
+    # the bench's draft-verification shape: the V2-Lite contexts (64 requests,
+    # 512..4096 rows), 8 drafts of 16 heads (128 rows, the two-CTA kernel),
+    # the plan of the whole batch; a sample of requests against the oracle
+    from mla_latent_kv_absorbed_gb300 import workloads as Wl
+    W, Hq = 8, 16
+    ref = Wl.make_workload(2)
+    bt = Wl.make_batch([int(x) for x in ref.lengths], heads=W * Hq, pool=ref.pool, seed=1700)
+    parents = np.tile(_topk_tree(W) if shape == "topk2" else np.arange(-1, W - 1, dtype=np.int32),
+                      (bt.batch, 1)).astype(np.int32)
+    out, lse, _ = _run(bt, W, parents)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    req = sorted(set([0, bt.batch - 1] + list(range(0, bt.batch, 9))))
+    sub = _sub_batch(bt, W, req)
+    ro, rl = _oracle(sub, W, parents[req])
+    assert_close(out[req].reshape(len(req), -1, 512), lse[req].reshape(len(req), -1),
+                 ro.reshape(len(req), -1, 512), rl.reshape(len(req), -1))
