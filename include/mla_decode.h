@@ -442,8 +442,9 @@ int mla_decode_fp8_workspace_bytes(const int32_t* plan_host, size_t* workspace_b
  * mla_decode_run over an FP8 cache: the same out / lse as the bf16 decode of
  * the cache values (code value x kv_scale), with the bf16 query used as is.
  * Every head count of mla_decode_plan is supported (16 or 32: one CTA per
- * worker; 48..128: a two-CTA cluster, whose partial-score exchange bounds a
- * score's error at 2^-15 of the largest partial in its 32-token half row).
+ * worker; 48..128: a two-CTA cluster; each CTA keeps its own partial score
+ * exact and receives its peer's with an error of at most 2^-22 of the largest
+ * partial in its 32-token half row).
  *
  *   kv_cache   device uint8 [num_slots, 576] E4M3 codes.
  *   kv_scale   finite, > 0.

@@ -83,9 +83,10 @@ constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
 // A latent block is held from its gathers until its PV, the whole life of a
 // tile in the pipeline, so the ring is as deep as shared memory allows.
 constexpr int kLatBlocks = 4;                // ring of latent blocks (every latent producer fills every block)
-constexpr int kRopeSlots = 4;
-constexpr int kXSlots = 2;                   // exchange slots
+constexpr int kRopeSlots = 2;               // a rope slot is free again once QK has read it
+constexpr int kXSlots = 3;                   // exchange slots
 constexpr int kLead = 3;                     // a producer issues tile g once tile g - kLead has landed
+constexpr int kRopeLead = kLead < kRopeSlots ? kLead : kRopeSlots;   // the same for the rope
 constexpr int kAtom = T * 128;               // 8 KB: 64 tokens x 64 dims
 constexpr int kLatBlock = 4 * kAtom;         // 32 KB: 64 tokens x 256 dims
 constexpr int kRopeAtom = T * 64;            // 4 KB: 64 tokens x this CTA's 32 rope dims (64-byte swizzle)
@@ -127,7 +128,7 @@ constexpr uint32_t kIdescQK = idesc_bf16(128, T, false, false);     // M=128 hea
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // N=256 dims, B (V) MN-major
 static_assert(kProducers == 5, "producers 0-3 gather the latent atoms, producer 4 the rope");
 static_assert(kThreads == 736, "23 warps");
-static_assert(kLead < kLatBlocks && kLead <= kRopeSlots, "a ring slot's phase must not be lapped while waited on");
+static_assert(kLead < kLatBlocks && kRopeLead <= kRopeSlots, "a ring slot's phase must not be lapped while waited on");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 1024 == 0 && kXSlot % 1024 == 0 &&
                   kOffXE % 16 == 0 && kOffBar % 8 == 0,
@@ -320,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t full = bar((rope ? bRopeFull : bLatFull) + slot);
         bool e_ok = true;
         if (lane == 0 && use > 0) e_ok = mbar_wait(bar((rope ? bRopeEmpty : bLatEmpty) + slot), (use - 1) & 1, wc);
-        if (lane == 0 && e_ok && g >= static_cast<uint32_t>(kLead)) {   // pace: tile g - kLead has landed
-          const uint32_t gp = g - kLead;
+        const uint32_t lead = rope ? kRopeLead : kLead;
+        if (lane == 0 && e_ok && g >= lead) {   // pace: tile g - lead has landed
+          const uint32_t gp = g - lead;
           e_ok = mbar_wait(bar((rope ? bRopeFull : bLatFull) + gp % nslots), (gp / nslots) & 1, wc);
         }
         e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
