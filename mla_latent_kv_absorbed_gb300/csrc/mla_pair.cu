@@ -60,11 +60,11 @@
 // Splitting senders from softmax lets tile g+1 be quantised and pushed while
 // tile g is still in its softmax, so the exchange latency is hidden.
 //
-// Per tile g (S buffer g mod 2, exchange slot g mod 2): QK(g) -> the senders
+// Per tile g (S buffer g mod 2, exchange slot g mod 3): QK(g) -> the senders
 // and the softmax warps both read the buffer (freeing it for QK(g+2)); the
 // senders quantise and push, the softmax warps add the peer's rows when they
 // land and write P -> PV(g) frees the latent block
-// and, through a multicast commit, tells the PEER that its rows for tile g+2
+// and, through a multicast commit, tells the PEER that its rows for tile g+3
 // may land in this slot.
 // The softmax moves its reference maximum lazily (threshold 8 in log2
 // units) as in the few-heads kernel.
@@ -130,6 +130,7 @@ static_assert(kProducers == 5, "producers 0-3 gather the latent atoms, producer 
 static_assert(kThreads == 736, "23 warps");
 static_assert(kLead < kLatBlocks && kRopeLead <= kRopeSlots, "a ring slot's phase must not be lapped while waited on");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kXSlots <= 3, "the rescale's wait on PV(g-1) relies on PV(g-3) being complete");
 static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 1024 == 0 && kXSlot % 1024 == 0 &&
                   kOffXE % 16 == 0 && kOffBar % 8 == 0,
               "alignment");
@@ -630,9 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = mt > m_ref + 8.f;
         if (__any_sync(0xffffffffu, need)) {
           // rescale this warp's half of O (128 columns) after the previous PV has
-          // landed.  PV(g-2) is complete here (the peer sent tile g only after
-          // this CTA's PV(g-2) had freed slot g mod 2), so the barrier of tile
-          // g-1 cannot be a lap behind.
+          // landed.  PV(g-3) is complete here (the peer sent tile g only after
+          // this CTA's PV(g - kXSlots) had freed slot g mod kXSlots, and
+          // kXSlots <= 3), so the barrier of tile g-1 cannot be a lap behind.
           wait(bar(bPvDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, false);
           tc_fence_after();
           const float alpha = need ? ex2_approx(m_ref - mt) : 1.f;

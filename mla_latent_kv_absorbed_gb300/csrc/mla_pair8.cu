@@ -73,9 +73,10 @@ constexpr int kThreads = 32 * (kProducerWarp0 + kProducers);
 // A latent block is held from its gathers until its PV, the whole life of a
 // tile in the pipeline, so the ring is as deep as shared memory allows.
 constexpr int kLatBlocks = 8;                // ring of latent blocks (every latent producer fills every block)
-constexpr int kRopeSlots = 8;
-constexpr int kXSlots = 2;                   // exchange slots
+constexpr int kRopeSlots = 4;               // a rope slot is free again once QK has read it
+constexpr int kXSlots = 3;                   // exchange slots
 constexpr int kLead = 6;                     // a producer issues tile g once tile g - kLead has landed
+constexpr int kRopeLead = kLead < kRopeSlots ? kLead : kRopeSlots;   // the same for the rope
 constexpr int kAtom = T * 128;               // 8 KB: 64 tokens x 128 E4M3 dims
 constexpr int kLatBlock = 2 * kAtom;         // 16 KB: 64 tokens x 256 dims
 constexpr int kRopeAtom = T * 32;            // 2 KB: 64 tokens x this CTA's 32 rope dims (32-byte swizzle)
@@ -119,8 +120,9 @@ constexpr uint32_t kIdescQKLo = idesc_f8(kFmtE5M2, kFmtE4M3, 128, T, false, fals
 constexpr uint32_t kIdescPV = idesc_e4m3(128, 256, false, true);    // N=256 dims, B (V) MN-major
 static_assert(kProducers == 5, "producers 0-3 gather the latent atoms, producer 4 the rope");
 static_assert(kThreads == 736, "23 warps");
-static_assert(kLead < kLatBlocks && kLead <= kRopeSlots, "a ring slot's phase must not be lapped while waited on");
+static_assert(kLead < kLatBlocks && kRopeLead <= kRopeSlots, "a ring slot's phase must not be lapped while waited on");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kXSlots <= 3, "the rescale's wait on PV(g-1) relies on PV(g-3) being complete");
 static_assert(kOffRope % 1024 == 0 && kOffQR % 1024 == 0 && kOffX % 1024 == 0 && kXSlot % 1024 == 0 &&
                   kOffXE % 16 == 0 && kOffBar % 8 == 0,
               "alignment");
@@ -305,8 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t full = bar((rope ? bRopeFull : bLatFull) + slot);
         bool e_ok = true;
         if (lane == 0 && use > 0) e_ok = mbar_wait(bar((rope ? bRopeEmpty : bLatEmpty) + slot), (use - 1) & 1, wc);
-        if (lane == 0 && e_ok && g >= static_cast<uint32_t>(kLead)) {   // pace: tile g - kLead has landed
-          const uint32_t gp = g - kLead;
+        const uint32_t lead = rope ? kRopeLead : kLead;
+        if (lane == 0 && e_ok && g >= lead) {   // pace: tile g - lead has landed
+          const uint32_t gp = g - lead;
           e_ok = mbar_wait(bar((rope ? bRopeFull : bLatFull) + gp % nslots), (gp / nslots) & 1, wc);
         }
         e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
@@ -613,9 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = mt > m_ref + 3.f;   // P' <= 2^8 (see below)
         if (__any_sync(0xffffffffu, need)) {
           // rescale this warp's half of O (128 columns) after the previous PV has
-          // landed.  PV(g-2) is complete here (the peer sent tile g only after
-          // this CTA's PV(g-2) had freed slot g mod 2), so the barrier of tile
-          // g-1 cannot be a lap behind.
+          // landed.  PV(g-3) is complete here (the peer sent tile g only after
+          // this CTA's PV(g - kXSlots) had freed slot g mod kXSlots, and
+          // kXSlots <= 3), so the barrier of tile g-1 cannot be a lap behind.
           wait(bar(bPvDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, false);
           tc_fence_after();
           const float alpha = need ? ex2_approx(m_ref - mt) : 1.f;
