@@ -9,13 +9,15 @@
 // Partials with lse_i = -inf weigh nothing; no live partial gives out = 0,
 // lse = -inf (an empty request).
 //
-// One block per (entry, head) of G groups of 128 threads (G = 1, 2 or 4, from
-// the most pieces an entry has).  The partial LSEs are loaded in parallel and
-// their weights go through shared memory; then thread t of group k owns latent
-// dims 4t..4t+3 and streams the partials k, k+G, k+2G, ... as float4, four at a
-// time, so 4G partial rows per dim are in flight and a request cut into tens of
-// pieces costs a few memory round trips.  The groups' sums are added in a
-// fixed order.
+// A block of 8 warps covers 8 / S heads of one entry; the S warps of a head
+// split its partials (warp k takes partials k, k + S, k + 2S, ...), S = 1, 2,
+// 4 or 8 from the most pieces an entry has.  A lane owns 16 latent dims (4
+// float4 at float4 index 32c + lane of the row, so each load instruction of a
+// warp reads 512 contiguous bytes); a warp keeps two partial rows in flight
+// while it adds the previous two, and its first two rows are loaded together
+// with the LSEs.  A warp's partial LSEs are loaded one per lane, their maximum
+// and weights never leave the warp; the S warps of a head are combined in a
+// fixed order (each rescaled to the head's maximum) through shared memory.
 // The kernel is launched as a programmatic dependent of the decode kernel:
 // its blocks are scheduled while the decode kernel drains and wait
 // (griddepcontrol.wait) until its partial states are complete and visible.
@@ -26,35 +28,54 @@
 
 namespace mla {
 
-constexpr int kMergeGroups = 4;                      // at most
-constexpr int kMergeThreads = 128 * kMergeGroups;
-constexpr int kMergeChunk = 1024;   // partials whose weights one pass keeps in shared memory
+constexpr int kMergeWarps = 8;
+constexpr int kMergeThreads = 32 * kMergeWarps;
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-  __shared__ float s_w[kMergeChunk];
-  __shared__ float s_red[kMergeThreads / 32];
-  __shared__ float4 s_acc[kMergeGroups - 1][128];
-  __shared__ float s_wsum[kMergeGroups - 1];
-  const int e = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const int G = static_cast<int>(blockDim.x >> 7), grp = tid >> 7, t = tid & 127;
+__device__ __forceinline__ void ld_row4(float4 (&v)[4], const float4* src) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) v[c] = __ldcg(src + 32 * c);
+}
+__device__ __forceinline__ void fma_row4(float4 (&acc)[4], float w, const float4 (&v)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    acc[c].x = fmaf(w, v[c].x, acc[c].x);
+    acc[c].y = fmaf(w, v[c].y, acc[c].y);
+    acc[c].z = fmaf(w, v[c].z, acc[c].z);
+    acc[c].w = fmaf(w, v[c].w, acc[c].w);
+  }
+}
+__device__ __forceinline__ void scale_row4(float4 (&acc)[4], float a) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    acc[c].x *= a;
+    acc[c].y *= a;
+    acc[c].z *= a;
+    acc[c].w *= a;
+  }
+}
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p, const int S) {
+  __shared__ float4 s_acc[kMergeWarps][4][32];
+  __shared__ float s_m[kMergeWarps], s_ws[kMergeWarps];
+  const int e = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = static_cast<int>(blockIdx.y) * (kMergeWarps / S) + warp / S, sub = warp % S;
   // the next kernel in the stream may be scheduled now; it waits for this
   // grid before it touches what this grid reads or writes
   griddep_launch_dependents();
-  const int nthreads = static_cast<int>(blockDim.x);
   int b, p0, p1;
   if (p.plan) {
     // device-only plan (graph replays): the entry count, the list and its
     // bounds come from the plan words; the grid covers every possible entry
-    const int32_t* h = p.plan;
-    const int W = h[kHWorkers], n_items = h[kHItems], n_merges = h[kHMerges];
+    const int32_t* hw = p.plan;
+    const int W = hw[kHWorkers], n_items = hw[kHItems], n_merges = hw[kHMerges];
     const long long off = kHeaderWords + static_cast<long long>(W) + 1 + 4ll * n_items;
-    const bool good = h[kHMagic] == kPlanMagic && h[kHVersion] == kPlanVersion && h[kHHeads] == p.heads &&
+    const bool good = hw[kHMagic] == kPlanMagic && hw[kHVersion] == kPlanVersion && hw[kHHeads] == p.heads &&
                       W == p.workers &&
                       n_items >= 0 && n_merges >= 0 && off + 3ll * n_merges <= p.plan_cap_words;
     if (!good || e >= n_merges) return;
-    b = h[off + 3 * e];
-    p0 = h[off + 3 * e + 1];
-    p1 = h[off + 3 * e + 2];
+    b = hw[off + 3 * e];
+    p0 = hw[off + 3 * e + 1];
+    p1 = hw[off + 3 * e + 2];
     if (b < 0 || b >= p.batch || p0 < 0 || p1 < p0 || p1 > p.max_partials) {
       if (tid == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
       return;
@@ -70,88 +91,113 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   }
   griddep_wait();
   const int H = p.heads;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool live = h < H;
+  float4 acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f, M = -INFINITY;
-  for (int c0 = p0; c0 < p1; c0 += kMergeChunk) {
-    // this chunk's partials: LSEs in parallel, then the chunk maximum
-    const int nc = min(kMergeChunk, p1 - c0);
-    float m = -INFINITY;
-    for (int i = tid; i < nc; i += nthreads) {
-      const float l = __ldcg(p.part_lse + static_cast<size_t>(c0 + i) * H + h);
-      s_w[i] = l;
-      m = fmaxf(m, l);
-    }
+  if (live) {
+    const int n = p1 - p0;
+    const int nw = n > sub ? (n - sub + S - 1) / S : 0;     // this warp's partials
+    const size_t step = static_cast<size_t>(S) * H * (kLatent / 4);   // float4 between them
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(p0 + sub) * H + h) * kLatent) +
+                        lane;
+    float4 va[4], vb[4];
+    if (nw > 0) ld_row4(va, src);
+    if (nw > 1) ld_row4(vb, src + step);
+    for (int c0 = 0; c0 < nw; c0 += 32) {
+      const int nc = min(32, nw - c0);
+      if (c0 > 0) {
+        ld_row4(va, src + c0 * step);
+        if (nc > 1) ld_row4(vb, src + (c0 + 1) * step);
+      }
+      // this chunk's LSEs (one per lane), their maximum, the running state
+      const float l = lane < nc ? __ldcg(p.part_lse + static_cast<size_t>(p0 + sub + (c0 + lane) * S) * H + h)
+                                : -INFINITY;
+      float mc = l;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((tid & 31) == 0) s_red[tid >> 5] = m;
-    __syncthreads();
-    float mc = s_red[0];
-    for (int w = 1; w < nthreads / 32; ++w) mc = fmaxf(mc, s_red[w]);
-    // fold the chunk into the running state (one chunk unless a request has
-    // more than kMergeChunk partials)
-    const float mn = fmaxf(M, mc);
-    if (mn > -INFINITY && M > -INFINITY && mn != M) {
-      const float a = expf(M - mn);
-      wsum *= a;
-      acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
-    }
-    M = mn;
-    for (int i = tid; i < nc; i += nthreads) {
-      const float l = s_w[i];
-      s_w[i] = (l == -INFINITY || M == -INFINITY) ? 0.f : expf(l - M);
-    }
-    __syncthreads();
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(c0) * H + h) * kLatent) + t;
-    const size_t stride = static_cast<size_t>(H) * kLatent / 4;   // float4 per partial
-    int i = grp;
-    for (; i + 3 * G < nc; i += 4 * G) {
-      float4 v[4];
+      for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+      const float mn = fmaxf(M, mc);
+      if (mn > -INFINITY && M > -INFINITY && mn != M) {
+        const float a = expf(M - mn);
+        wsum *= a;
+        scale_row4(acc, a);
+      }
+      M = mn;
+      const float wl = (l == -INFINITY || M == -INFINITY) ? 0.f : expf(l - M);
+      for (int j = 0; j < nc; j += 2) {
+        float4 vc[4], vd[4];
+        const bool more = j + 2 < nc;
+        if (more) {
+          ld_row4(vc, src + (c0 + j + 2) * step);
+          if (j + 3 < nc) ld_row4(vd, src + (c0 + j + 3) * step);
+        }
+        const float w0 = __shfl_sync(0xffffffffu, wl, j);
+        const float w1 = __shfl_sync(0xffffffffu, wl, (j + 1) & 31);
+        wsum += w0;
+        fma_row4(acc, w0, va);
+        if (j + 1 < nc) {
+          wsum += w1;
+          fma_row4(acc, w1, vb);
+        }
+        if (more) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = __ldcg(src + (i + q * G) * stride);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float w = s_w[i + q * G];
-        wsum += w;
-        acc.x = fmaf(w, v[q].x, acc.x);
-        acc.y = fmaf(w, v[q].y, acc.y);
-        acc.z = fmaf(w, v[q].z, acc.z);
-        acc.w = fmaf(w, v[q].w, acc.w);
+          for (int c = 0; c < 4; ++c) {
+            va[c] = vc[c];
+            vb[c] = vd[c];
+          }
+        }
       }
     }
-    for (; i < nc; i += G) {
-      const float4 v = __ldcg(src + i * stride);
-      const float w = s_w[i];
-      wsum += w;
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+  }
+  if (S > 1) {
+    // the head's S warps, added in a fixed order at the head's maximum
+#pragma unroll
+    for (int c = 0; c < 4; ++c) s_acc[warp][c][lane] = acc[c];
+    if (lane == 0) {
+      s_m[warp] = M;
+      s_ws[warp] = wsum;
     }
-    __syncthreads();   // s_w and s_red are reused by the next chunk
+    __syncthreads();
+    if (sub != 0 || !live) return;
+    float mh = -INFINITY;
+    for (int k = 0; k < S; ++k) mh = fmaxf(mh, s_m[warp + k]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    wsum = 0.f;
+    for (int k = 0; k < S; ++k) {
+      const float mk = s_m[warp + k];
+      const float a = mk == -INFINITY ? 0.f : expf(mk - mh);
+      wsum = fmaf(a, s_ws[warp + k], wsum);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 v = s_acc[warp + k][c][lane];
+        acc[c].x = fmaf(a, v.x, acc[c].x);
+        acc[c].y = fmaf(a, v.y, acc[c].y);
+        acc[c].z = fmaf(a, v.z, acc[c].z);
+        acc[c].w = fmaf(a, v.w, acc[c].w);
+      }
+    }
+    M = mh;
   }
-  // add the groups' sums in a fixed order
-  if (grp > 0) {
-    s_acc[grp - 1][t] = acc;
-    if (t == 0) s_wsum[grp - 1] = wsum;
-  }
-  __syncthreads();
-  if (grp != 0) return;
-  for (int k = 0; k < G - 1; ++k) {
-    const float4 a = s_acc[k][t];
-    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
-    wsum += s_wsum[k];
-  }
+  if (!live) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + 4 * t;
+  const size_t o = (static_cast<size_t>(b) * H + h) * kLatent;
   if (p.out_bf16) {
-    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
-    dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o) + lane;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[c].x * inv, acc[c].y * inv);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[c].z * inv, acc[c].w * inv);
+      dst[32 * c] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
   } else {
-    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) + lane;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      dst[32 * c] = make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv);
   }
-  if (t == 0 && p.lse) p.lse[static_cast<size_t>(b) * H + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  if (lane == 0 && p.lse) p.lse[static_cast<size_t>(b) * H + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
 // Two states per row, same layout ([rows, 512] and [rows]): the merge of a
@@ -191,10 +237,12 @@ int launch_merge_two(const float* o_a, const float* l_a, const float* o_b, const
 
 int launch_merge(const MergeParams& p, int entries, int max_pieces, cudaStream_t stream) {
   if (entries <= 0) return MLA_OK;
-  const int groups = max_pieces >= 16 ? 4 : max_pieces >= 8 ? 2 : 1;
+  // warps per head: a warp takes up to about four partials
+  const int S = max_pieces > 16 ? 8 : max_pieces > 8 ? 4 : max_pieces > 4 ? 2 : 1;
+  const int heads_per_block = kMergeWarps / S;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(entries, p.heads);
-  cfg.blockDim = dim3(128 * groups);
+  cfg.gridDim = dim3(entries, (p.heads + heads_per_block - 1) / heads_per_block);
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -202,7 +250,7 @@ int launch_merge(const MergeParams& p, int entries, int max_pieces, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, merge_kernel, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, merge_kernel, p, S) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }
