@@ -24,7 +24,11 @@ enum PlanHeader : int {
 };
 constexpr int kVariantSwab = 1;  // H in {16, 32}: one CTA per worker, 64-token tiles
 constexpr int kVariantPair = 2;  // H in 48..128: a 2-CTA cluster per worker, 64-token tiles
-constexpr int kItemOverheadTokens = 32;   // plan cost of one work item (its epilogue), in tokens
+// plan cost of one work item beyond its tiles, in tokens: the item's epilogue
+// and the pipeline refill behind it (measured: about half a tile for the
+// one-CTA kernel, about four tiles for the two-CTA kernel, whose epilogue
+// writes 128 heads x 256 dims per CTA while the next item's softmax waits)
+constexpr int item_overhead_tokens(int variant) { return variant == kVariantPair ? 256 : 32; }
 constexpr int kMinPieceTokens = 64;       // no cut piece is shorter
 constexpr int kCapStepTokens = 8;         // the budget grows in these steps until the fill fits
 constexpr size_t kWsHeaderBytes = 256;

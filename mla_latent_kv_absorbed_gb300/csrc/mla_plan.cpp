@@ -7,8 +7,10 @@
 //   * variant by head count: H in {16, 32} -> one CTA per worker; H in
 //     48..128 (step 16) -> a 2-CTA cluster per worker; 64-token tiles for both;
 //   * W workers = SMs / CTAs-per-worker; loads are counted in tokens, an item
-//     of n tokens costs its tiles, roundup(n, 64), plus kItemOverheadTokens
-//     (its epilogue): a worker's time follows its tiles, ragged or not;
+//     of n tokens costs its tiles, roundup(n, 64), plus the variant's item
+//     overhead (its epilogue and the refill behind it: 32 tokens for one-CTA
+//     workers, 256 for two-CTA workers): a worker's time follows its tiles,
+//     ragged or not, and its items;
 //   * wrap-around fill: requests, in order, are poured into workers 0, 1, ...
 //     each up to a load budget cap, so a request is cut only where a worker
 //     is full (at most W - 1 cuts, hence few partial states to merge), at a
@@ -43,7 +45,7 @@ inline long long round_up_tile(long long n) { return ceil_div(n, kTileTokens) * 
 // Wrap-around fill with load budget cap (tokens); false when W workers do not
 // suffice.  Pieces come out in worker order (the fill only moves forward), so
 // one flat list holds them all: no allocation per attempt once it has grown.
-bool fill(const std::vector<long long>& len, int W, long long cap, std::vector<Piece>& pieces) {
+bool fill(const std::vector<long long>& len, int W, long long cap, long long ov, std::vector<Piece>& pieces) {
   pieces.clear();
   int w = 0;
   long long used = 0;
@@ -53,7 +55,7 @@ bool fill(const std::vector<long long>& len, int W, long long cap, std::vector<P
     while (k0 < L) {
       if (w == W) return false;
       const long long rem = L - k0;
-      const long long space = cap - used - kItemOverheadTokens;
+      const long long space = cap - used - ov;
       const long long fit = space / kTileTokens * kTileTokens;   // whole tiles that fit
       long long take;
       if (round_up_tile(rem) <= space || (fit >= kTileTokens && rem - fit < kMinPieceTokens)) {
@@ -66,7 +68,7 @@ bool fill(const std::vector<long long>& len, int W, long long cap, std::vector<P
         continue;
       }
       pieces.push_back({w, static_cast<int>(b), k0, take});
-      used += round_up_tile(take) + kItemOverheadTokens;
+      used += round_up_tile(take) + ov;
       k0 += take;
     }
   }
@@ -108,8 +110,9 @@ int build_plan(const int32_t* indptr, int B, int H, int num_sms, std::vector<int
   std::vector<Piece> pieces;
   pieces.reserve(static_cast<size_t>(B) + W);
   if (total > 0) {
-    cap = ceil_div(total + (nonempty + W - 1) * kItemOverheadTokens, W);
-    while (!fill(len, W, cap, pieces)) cap += kCapStepTokens;
+    const long long ov = item_overhead_tokens(variant);
+    cap = ceil_div(total + (nonempty + W - 1) * ov, W);
+    while (!fill(len, W, cap, ov, pieces)) cap += kCapStepTokens;
   }
 
   // per request: pieces, first partial index, pieces numbered so far (one allocation)

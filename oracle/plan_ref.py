@@ -14,8 +14,9 @@ contexts across SMs.  They give no rule, so this is the one the library uses:
     work in 64-token tiles;
   * W workers = SMs (swab) or SMs // 2 (pair);
   * loads are counted in tokens: a work item of n tokens costs its tiles,
-    ceil(n / T) * T, plus ITEM_OVERHEAD; total = sum over requests of
-    ceil(L_b / T) * T;
+    ceil(n / T) * T, plus the variant's ITEM_OVERHEAD (32 tokens for swab,
+    256 for pair: a cost-model figure, measured per kernel); total = sum over
+    requests of ceil(L_b / T) * T;
   * wrap-around fill: requests are walked in b order and poured into workers
     0, 1, ... in turn, each worker up to a load budget cap; a request is cut
     only where a worker is full, at a tile boundary of the request (so only
@@ -23,7 +24,7 @@ contexts across SMs.  They give no rule, so this is the one the library uses:
   * no cut piece is shorter than MIN_PIECE tokens: with space < MIN_PIECE left
     the worker is closed, and a tail shorter than MIN_PIECE stays with the
     head piece (the worker then overshoots cap by < MIN_PIECE);
-  * cap starts at ceil((total + (nonempty + W - 1) * ITEM_OVERHEAD) / W) and
+  * cap starts at ceil((total + (nonempty + W - 1) * overhead) / W) and
     grows by CAP_STEP tokens until the fill fits on the W workers;
   * partial slots are numbered over the cut requests in (b, piece) order; an
     uncut request's item writes out/lse directly (partial = -1);
@@ -39,7 +40,6 @@ from __future__ import annotations
 PLAN_MAGIC = 0x4D4C4131
 PLAN_VERSION = 1
 HEADER_WORDS = 16
-ITEM_OVERHEAD = 32    # tokens
 MIN_PIECE = 64        # tokens
 CAP_STEP = 8          # tokens
 WS_HEADER_BYTES = 256
@@ -47,6 +47,7 @@ D_LATENT = 512
 
 VARIANT_SWAB = 1
 VARIANT_PAIR = 2
+ITEM_OVERHEAD = {VARIANT_SWAB: 32, VARIANT_PAIR: 256}   # tokens per work item
 
 
 def variant_for_heads(H: int):
@@ -69,7 +70,7 @@ def _round_up(n: int) -> int:
     return _ceil_div(n, TILE) * TILE
 
 
-def _fill(lengths, W, cap):
+def _fill(lengths, W, cap, overhead):
     """Wrap-around fill with load budget cap: per-worker lists of
     (b, first token, tokens), or None when W workers do not suffice."""
     lists = [[] for _ in range(W)]
@@ -80,7 +81,7 @@ def _fill(lengths, W, cap):
             if w == W:
                 return None
             rem = t - k0
-            space = cap - used - ITEM_OVERHEAD
+            space = cap - used - overhead
             fit = (space // TILE) * TILE if space > 0 else 0      # whole tiles that fit
             if _round_up(rem) <= space or (fit >= TILE and rem - fit < MIN_PIECE):
                 take = rem
@@ -90,7 +91,7 @@ def _fill(lengths, W, cap):
                 w, used = w + 1, 0
                 continue
             lists[w].append((b, k0, take))
-            used += _round_up(take) + ITEM_OVERHEAD
+            used += _round_up(take) + overhead
             k0 += take
     return lists
 
@@ -109,10 +110,11 @@ def build_plan(kv_indptr, H: int, num_sms: int):
     total = sum(_round_up(L) for L in lengths)
     nonempty = sum(1 for L in lengths if L > 0)
 
+    overhead = ITEM_OVERHEAD[variant]
     if total > 0:
-        cap = _ceil_div(total + (nonempty + W - 1) * ITEM_OVERHEAD, W)
+        cap = _ceil_div(total + (nonempty + W - 1) * overhead, W)
         while True:
-            lists = _fill(lengths, W, cap)
+            lists = _fill(lengths, W, cap, overhead)
             if lists is not None:
                 break
             cap += CAP_STEP

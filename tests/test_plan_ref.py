@@ -36,7 +36,8 @@ def _check(indptr, H, sms):
     T, c = d["T"], d["c"]
     assert d["wptr"][0] == 0 and d["wptr"][-1] == d["n"]
     assert all(a <= b for a, b in zip(d["wptr"], d["wptr"][1:]))
-    items_max = c - PR.ITEM_OVERHEAD + PR.MIN_PIECE if c else 0   # tokens
+    ov = PR.ITEM_OVERHEAD[d["variant"]]
+    items_max = c - ov + PR.MIN_PIECE if c else 0   # tokens
     # exact coverage of each request's keys
     cover = {b: [] for b in range(B)}
     parts = {}
@@ -76,12 +77,12 @@ def _check(indptr, H, sms):
     loads = []
     for w in range(d["W"]):
         its = d["items"][d["wptr"][w]:d["wptr"][w + 1]]
-        loads.append(sum(rup(e - s) + PR.ITEM_OVERHEAD for (_, s, e, _) in its))
+        loads.append(sum(rup(e - s) + ov for (_, s, e, _) in its))
     for b in range(B):
         for (s, e) in sorted(cover[b])[:-1]:
             assert (e - s) % T == 0                      # only a request's last piece is ragged
     if total:
-        ideal = -(-(total + (nonempty + d["W"] - 1) * PR.ITEM_OVERHEAD) // d["W"])
+        ideal = -(-(total + (nonempty + d["W"] - 1) * ov) // d["W"])
         assert ideal <= c <= ideal + 2 * PR.MIN_PIECE + PR.CAP_STEP
         assert max(loads) <= c + PR.MIN_PIECE
         cuts = sum(len(cover[b]) - 1 for b in range(B) if lengths[b] > 0)
@@ -124,7 +125,7 @@ def test_long_request_is_split_over_workers():
     W = d["W"]
     tokens = [sum(e - s for (_, s, e, _) in d["items"][d["wptr"][w]:d["wptr"][w + 1]]) for w in range(W)]
     perfect = -(-196608 // W)
-    assert max(tokens) <= perfect + 2 * PR.ITEM_OVERHEAD + PR.MIN_PIECE + PR.CAP_STEP   # within ~2 tiles of perfect
+    assert max(tokens) <= perfect + 2 * PR.ITEM_OVERHEAD[d["variant"]] + PR.MIN_PIECE + PR.CAP_STEP
 
 
 def test_uniform_batch_cuts_few_requests():
