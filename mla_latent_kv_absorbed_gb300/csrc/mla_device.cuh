@@ -552,6 +552,35 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
                : "memory");
 }
 
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Transpose of N-word blocks among each group of 4 lanes: on entry lane i of
+// a group holds blocks 0..3 of its own row (block j = v[N j .. N j + N - 1]);
+// on exit it holds block i of the group's rows 0..3 (block k = row k's block
+// i).  Two exchange stages, lane distance 2 then 1: in each, a lane keeps the
+// blocks whose index agrees with its own lane index in that bit and swaps the
+// others with its partner's.
+template <int N>
+__device__ __forceinline__ void transpose4_blocks(uint32_t (&v)[4 * N], int lane) {
+#pragma unroll
+  for (int d = 2; d >= 1; d >>= 1) {
+    const bool up = (lane & d) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j & d) continue;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const uint32_t send = up ? v[N * j + e] : v[N * (j ^ d) + e];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, d);
+        if (up) v[N * j + e] = recv;
+        else v[N * (j ^ d) + e] = recv;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

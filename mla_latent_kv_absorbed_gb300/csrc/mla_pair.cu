@@ -695,18 +695,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!part_ok && threadIdx.x == 0) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
       if (!aborted && part_ok) {
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;     // no valid score: out = 0
+        // rows of this warp's lane group (4 lanes): after the block transpose
+        // lane i of group m holds columns 8i..8i+7 (fp32) of rows 4m..4m+3 of
+        // the warp's 32, so each store instruction writes whole 128-byte lines
+        const int h4 = 32 * q + 4 * (lane >> 2), bi = lane & 3;
+        const size_t col0 = 256 * static_cast<size_t>(cta) + 128 * th;
+        const size_t row0 = part < 0 ? static_cast<size_t>(b) * H : static_cast<size_t>(part) * H;
         float* dst_f = nullptr;
         __nv_bfloat16* dst_h = nullptr;
-        const size_t col0 = 256 * static_cast<size_t>(cta) + 128 * th;
-        if (part < 0) {
-          const size_t o = (static_cast<size_t>(b) * H + h) * kLatent + col0;
-          if (p.out_bf16) dst_h = reinterpret_cast<__nv_bfloat16*>(p.out) + o;
-          else dst_f = reinterpret_cast<float*>(p.out) + o;
-        } else {
-          dst_f = p.part_o + (static_cast<size_t>(part) * H + h) * kLatent + col0;
-        }
+        if (part >= 0) dst_f = p.part_o + row0 * kLatent + col0;
+        else if (p.out_bf16) dst_h = reinterpret_cast<__nv_bfloat16*>(p.out) + row0 * kLatent + col0;
+        else dst_f = reinterpret_cast<float*>(p.out) + row0 * kLatent + col0;
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {          // 32 columns per TMEM round trip, 32-byte stores
+        for (int cb = 0; cb < 4; ++cb) {          // 32 columns per TMEM round trip
           uint32_t o[32];
           {
             uint32_t a[16], c[16];
@@ -716,25 +717,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) { o[i] = a[i]; o[16 + i] = c[i]; }
           }
-          if (head_ok) {
-            if (dst_f) {
+          if (dst_f) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t v[8];
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
+            transpose4_blocks<8>(o, lane);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = __float_as_uint(__uint_as_float(o[8 * i + k]) * inv);
-                st_global_v8(dst_f + 32 * cb + 8 * i, v);
-              }
-            } else {
+            for (int k = 0; k < 4; ++k) {
+              uint32_t v[8];
 #pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                uint32_t v[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  v[k] = pack_bf16x2(__uint_as_float(o[16 * i + 2 * k]) * inv, __uint_as_float(o[16 * i + 2 * k + 1]) * inv);
-                st_global_v8(dst_h + 32 * cb + 16 * i, v);
-              }
+              for (int e = 0; e < 8; ++e) v[e] = o[8 * k + e];
+              if (h4 + k < H) st_global_v8(dst_f + static_cast<size_t>(h4 + k) * kLatent + 32 * cb + 8 * bi, v);
             }
+          } else {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            transpose4_blocks<4>(w, lane);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (h4 + k < H)
+                st_global_v4(dst_h + static_cast<size_t>(h4 + k) * kLatent + 32 * cb + 8 * bi, w[4 * k], w[4 * k + 1],
+                             w[4 * k + 2], w[4 * k + 3]);
           }
         }
         if (cta == 0 && th == 0 && head_ok) {
@@ -756,21 +760,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!item_ok(p, nnz, b, s, e)) continue;
       const int n = e - s, nt = (n + T - 1) / T;
       if (is_sender) {
-        // -- query latent half of this item into TMEM (after the previous item's last QK)
+        // -- query latent half of this item into TMEM (after the previous item's
+        //    last QK).  The first half of the row is read before that wait, and
+        //    the next item's row is prefetched into L2 now: an item's first QK
+        //    waits on this load.
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(b) * H + h) * kLatent +
+                                                          256 * cta) + 16 * th;
+        const bool q_ok = head_ok && !aborted;
+        uint4 qv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qv[k] = q_ok ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+        if (it + 1 < it1 && head_ok) {
+          const int bn = items[4 * (it + 1)];
+          if (bn >= 0 && bn < p.batch) {
+            const uint4* nsrc = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(bn) * H + h) * kLatent +
+                                                               256 * cta) + 16 * th;
+            prefetch_l2_line(nsrc);
+            prefetch_l2_line(nsrc + 8);
+          }
+        }
         if (nitem > 0) wait(bar(bQEmpty), (nitem - 1) & 1, false);
         tc_fence_after();
         if (!aborted) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(b) * H + h) * kLatent +
-                                                            256 * cta);
 #pragma unroll
-          for (int c = 4 * th; c < 4 * th + 4; ++c) {   // this warp's 4 x 16 columns = 128 bf16
-            uint32_t r[16];
+          for (int hf = 0; hf < 2; ++hf) {        // this warp's 2 x 2 x 16 columns = 128 bf16
+            if (hf == 1) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint4 v = head_ok ? __ldg(src + 4 * c + k) : make_uint4(0, 0, 0, 0);
-              r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
+              for (int k = 0; k < 8; ++k) qv[k] = q_ok ? __ldg(src + 8 + k) : make_uint4(0, 0, 0, 0);
             }
-            tmem_st16(tmem + lane_off + kTmQ + 16 * c, r);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t r[16];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint4 v = qv[4 * c + k];
+                r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
+              }
+              tmem_st16(tmem + lane_off + kTmQ + 16 * (4 * th + 2 * hf + c), r);
+            }
           }
           tmem_wait_st();
         }
