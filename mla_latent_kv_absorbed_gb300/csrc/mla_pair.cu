@@ -122,7 +122,9 @@ constexpr int bDrain = bXFree + kXSlots;
 constexpr int kNumBars = bDrain + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffLast = kOffMisc + 16;      // [kLatBlocks + kRopeSlots] last armed use
-constexpr int kSmemBytes = kOffLast + 4 * (kLatBlocks + kRopeSlots) + 1024;
+constexpr int kItemCache = 64;              // this CTA's first work items, copied to shared memory
+constexpr int kOffItems = (kOffLast + 4 * (kLatBlocks + kRopeSlots) + 15) / 16 * 16;
+constexpr int kSmemBytes = kOffItems + 16 * kItemCache + 1024;
 constexpr int kTmO = 0, kTmQ = 256, kTmS = 384;
 constexpr uint32_t kIdescQK = idesc_bf16(128, T, false, false);     // M=128 heads, N=64 tokens
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // N=256 dims, B (V) MN-major
@@ -254,6 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   int it0, it1;
   plan_items(p, w, it0, it1);
   const int32_t* items = p.plan + p.items_off;
+  // this CTA's first kItemCache items, read once: no warp waits on the plan
+  // in global memory at an item start
+  int32_t* s_items = reinterpret_cast<int32_t*>(smem + kOffItems);
+  const int n_cached = min(max(it1 - it0, 0), kItemCache);
+  for (int i = threadIdx.x; i < 4 * n_cached; i += blockDim.x) s_items[i] = items[4 * it0 + i];
+  __syncthreads();
+  auto item_w = [&](int it, int k) -> int {
+    return it - it0 < kItemCache ? s_items[4 * (it - it0) + k] : items[4 * it + k];
+  };
   const int nnz = __ldg(p.kv_indptr + p.batch);
   // the merge kernel may be launched now: it waits for this grid to finish
   griddep_launch_dependents();
@@ -277,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = it0, s = 0, n = 0;
     auto next_item = [&]() {                     // first usable item from `it` on
       for (; it < it1; ++it) {
-        const int b = items[4 * it], s0 = items[4 * it + 1], e = items[4 * it + 2];
+        const int b = item_w(it, 0), s0 = item_w(it, 1), e = item_w(it, 2);
         if (item_ok(p, nnz, b, s0, e)) {
           if (pw == 0 && lane == 0 && !item_in_request(p, b, s0, e)) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
           s = s0;
@@ -369,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0, nitem = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
-        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+        const int b = item_w(it, 0), s = item_w(it, 1), e = item_w(it, 2);
         if (!item_ok(p, nnz, b, s, e)) continue;
         const int nt = (e - s + T - 1) / T;
         // the rope query of this item replaces the previous one once its last QK is done
@@ -417,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0, nitem = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
-        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+        const int b = item_w(it, 0), s = item_w(it, 1), e = item_w(it, 2);
         if (!item_ok(p, nnz, b, s, e)) continue;
         const int nt = (e - s + T - 1) / T;
         for (int j = 0; j < nt; ++j, ++g) {
@@ -755,30 +766,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t g = 0, nitem = 0;
     for (int it = it0; it < it1; ++it) {
-      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      const int part = items[4 * it + 3];
+      const int b = item_w(it, 0), s = item_w(it, 1), e = item_w(it, 2);
+      const int part = item_w(it, 3);
       if (!item_ok(p, nnz, b, s, e)) continue;
       const int n = e - s, nt = (n + T - 1) / T;
       if (is_sender) {
         // -- query latent half of this item into TMEM (after the previous item's
-        //    last QK).  The first half of the row is read before that wait, and
-        //    the next item's row is prefetched into L2 now: an item's first QK
-        //    waits on this load.
+        //    last QK).  The first half of the row is read before that wait: an
+        //    item's first QK waits on this load.
         const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(b) * H + h) * kLatent +
                                                           256 * cta) + 16 * th;
         const bool q_ok = head_ok && !aborted;
         uint4 qv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) qv[k] = q_ok ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
-        if (it + 1 < it1 && head_ok) {
-          const int bn = items[4 * (it + 1)];
-          if (bn >= 0 && bn < p.batch) {
-            const uint4* nsrc = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(bn) * H + h) * kLatent +
-                                                               256 * cta) + 16 * th;
-            prefetch_l2_line(nsrc);
-            prefetch_l2_line(nsrc + 8);
-          }
-        }
         if (nitem > 0) wait(bar(bQEmpty), (nitem - 1) & 1, false);
         tc_fence_after();
         if (!aborted) {

@@ -113,7 +113,9 @@ constexpr int bDrain = bXFree + kXSlots;
 constexpr int kNumBars = bDrain + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffLast = kOffMisc + 16;      // [kLatBlocks + kRopeSlots] last armed use
-constexpr int kSmemBytes = kOffLast + 4 * (kLatBlocks + kRopeSlots) + 1024;
+constexpr int kItemCache = 64;              // this CTA's first work items, copied to shared memory
+constexpr int kOffItems = (kOffLast + 4 * (kLatBlocks + kRopeSlots) + 15) / 16 * 16;
+constexpr int kSmemBytes = kOffItems + 16 * kItemCache + 1024;
 constexpr int kTmO = 0, kTmQHi = 256, kTmQLo = 320, kTmS = 384;
 constexpr uint32_t kIdescQK = idesc_e4m3(128, T, false, false);     // M=128 heads, N=64 tokens
 constexpr uint32_t kIdescQKLo = idesc_f8(kFmtE5M2, kFmtE4M3, 128, T, false, false);   // the query's E5M2 low part
@@ -238,6 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   int it0, it1;
   plan_items(p, w, it0, it1);
   const int32_t* items = p.plan + p.items_off;
+  // this CTA's first kItemCache items, read once: no warp waits on the plan
+  // in global memory at an item start
+  int32_t* s_items = reinterpret_cast<int32_t*>(smem + kOffItems);
+  const int n_cached = min(max(it1 - it0, 0), kItemCache);
+  for (int i = threadIdx.x; i < 4 * n_cached; i += blockDim.x) s_items[i] = items[4 * it0 + i];
+  __syncthreads();
+  auto item_w = [&](int it, int k) -> int {
+    return it - it0 < kItemCache ? s_items[4 * (it - it0) + k] : items[4 * it + k];
+  };
   const int nnz = __ldg(p.kv_indptr + p.batch);
   // the merge kernel may be launched now: it waits for this grid to finish
   griddep_launch_dependents();
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = it0, s = 0, n = 0;
     auto next_item = [&]() {                     // first usable item from `it` on
       for (; it < it1; ++it) {
-        const int b = items[4 * it], s0 = items[4 * it + 1], e = items[4 * it + 2];
+        const int b = item_w(it, 0), s0 = item_w(it, 1), e = item_w(it, 2);
         if (item_ok(p, nnz, b, s0, e)) {
           if (pw == 0 && lane == 0 && !item_in_request(p, b, s0, e)) record_status(p.status, MLA_ERR_PLAN_MISMATCH);
           s = s0;
@@ -353,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0, nitem = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
-        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+        const int b = item_w(it, 0), s = item_w(it, 1), e = item_w(it, 2);
         if (!item_ok(p, nnz, b, s, e)) continue;
         const int nt = (e - s + T - 1) / T;
         // the senders load this item's query parts once its previous item's last QK is done
@@ -400,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0, nitem = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
-        const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
+        const int b = item_w(it, 0), s = item_w(it, 1), e = item_w(it, 2);
         if (!item_ok(p, nnz, b, s, e)) continue;
         const int nt = (e - s + T - 1) / T;
         for (int j = 0; j < nt; ++j, ++g) {
@@ -790,28 +801,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t g = 0, nitem = 0;
     for (int it = it0; it < it1; ++it) {
-      const int b = items[4 * it], s = items[4 * it + 1], e = items[4 * it + 2];
-      const int part = items[4 * it + 3];
+      const int b = item_w(it, 0), s = item_w(it, 1), e = item_w(it, 2);
+      const int part = item_w(it, 3);
       if (!item_ok(p, nnz, b, s, e)) continue;
       const int n = e - s, nt = (n + T - 1) / T;
       if (is_sender) {
         // -- this item's query parts: the head's scale a from this CTA's 256
         //    latent + 32 rope dims (read before the wait for the previous item's
-        //    last QK, while the next item's rows are prefetched into L2: an
-        //    item's first QK waits on this work), then, after that wait, this
-        //    warp's 128 latent dims as hi / lo into TMEM and (token-half-0
-        //    warps) the 32 rope dims as hi / lo into shared memory
+        //    last QK: an item's first QK waits on this work), then, after that
+        //    wait, this warp's 128 latent dims as hi / lo into TMEM and
+        //    (token-half-0 warps) the 32 rope dims as hi / lo into shared memory
         const int a = !aborted ? head_exp(b) : 0;
-        if (it + 1 < it1 && head_ok) {
-          const int bn = items[4 * (it + 1)];
-          if (bn >= 0 && bn < p.batch) {
-            const uint4* nq = reinterpret_cast<const uint4*>(p.q_nope + (static_cast<size_t>(bn) * H + h) * kLatent +
-                                                             256 * cta);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) prefetch_l2_line(nq + 8 * k);
-            prefetch_l2_line(p.q_rope + (static_cast<size_t>(bn) * H + h) * kRope + 32 * cta);
-          }
-        }
         if (nitem > 0) wait(bar(bQEmpty), (nitem - 1) & 1, false);
         tc_fence_after();
         if (!aborted) {
