@@ -36,11 +36,12 @@
 // buffers [384,448), [448,512) that hold this CTA's fp32 partial.
 //
 // Shared memory per CTA: a ring of 4 latent blocks (64 tokens x 256 dims,
-// 32 KB, gathered with TMA gather4), 4 rope atoms (4 KB: this CTA's 32 rope
-// dims, 64-byte swizzle), the rope query (8 KB), 2 exchange slots (16 KB
+// 32 KB, gathered with TMA gather4), 2 rope atoms (4 KB: this CTA's 32 rope
+// dims, 64-byte swizzle), the rope query (8 KB), 3 exchange slots (16 KB
 // each: the high parts of the peer's partial rows, later overwritten in place
 // by P as bf16, the A operand of PV), their low-byte blocks (8 KB each), the
-// peer's exponents and the softmax warps' reduction buffers.
+// peer's exponents, the softmax warps' reduction buffers and the CTA's first
+// work items.
 //
 // Warp roles per CTA (736 threads).  Warp w of the sixteen score warps owns
 // heads 32(w%4)..+31 (TMEM lane h = head h) and tokens 32((w/4)%2)..+31 of

@@ -40,11 +40,11 @@
 // and lo part [320,384) (4 codes per column); two score buffers [384,512).
 //
 // Shared memory per CTA: a ring of 8 latent blocks (64 tokens x 256 dims,
-// 16 KB: two 128-dim atoms, 128-byte swizzle), 8 rope atoms (64 tokens x 32
+// 16 KB: two 128-dim atoms, 128-byte swizzle), 4 rope atoms (64 tokens x 32
 // dims, 2 KB, 32-byte swizzle), the rope query's hi and lo parts (128 rows x
-// 32 bytes each, 32-byte swizzle), 2 exchange slots (the high parts of the
-// peer's codes, then P), their low-byte blocks, the peer's exponents and the
-// softmax warps' reduction buffers.
+// 32 bytes each, 32-byte swizzle), 3 exchange slots (the high parts of the
+// peer's codes, then P), their low-byte blocks, the peer's exponents, the
+// softmax warps' reduction buffers and the CTA's first work items.
 //
 // Warp roles per CTA (736 threads), as in the bf16 kernel:
 //   warps 8-15  senders: at an item's start, load the head's query dims of
