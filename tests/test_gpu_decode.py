@@ -246,3 +246,20 @@ def test_plan_item_outside_its_request_is_reported_not_faulted(H):
     (o2, l2), _ = run_gpu(bt, dev=dev)
     ro, rl = oracle(bt)
     assert_close(o2, l2, ro, rl)
+
+
+@pytest.mark.parametrize("H,num_sms", [(128, 8), (16, 4)])
+def test_many_items_per_worker(H, num_sms):
+    # hundreds of short requests on a handful of workers: a worker's items go
+    # past the two-CTA kernel's 64-item shared-memory copy (the rest are read
+    # from the plan in global memory), with empty and one-token requests mixed in
+    rng = np.random.default_rng(2000 + H)
+    lengths = [int(x) for x in rng.integers(0, 6, size=700)]
+    lengths[5] = 300
+    bt = _batch(lengths, H, pool=sum(lengths) + 50, seed=21)
+    (out, lse), dec = run_gpu(bt, num_sms=num_sms)
+    W = dec.header[6]
+    items = dec.header[8]
+    assert items / W > 64                        # the fallback is exercised
+    ro, rl = oracle(bt)
+    assert_close(out, lse, ro, rl)
