@@ -27,6 +27,12 @@
 namespace mla {
 namespace hg {
 
+// L2 prefetch of one box of a tiled tensor map (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+
 constexpr int kThreads = 256;
 constexpr int BM = 128, BK = 64;
 constexpr int kEpiWarp0 = 4;
@@ -105,6 +111,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // While the previous kernel drains, this CTA's first two tiles (weights and
+  // rows) are prefetched into L2.  Only prefetched: the rows may still be
+  // written by that kernel, and L2 is where every write lands, so the loads
+  // after the wait below still see the final data; the prefetch only takes
+  // the DRAM latency off the chain that follows the wait.
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_w);
+    for (int t = blockIdx.x, n = 0; t < tiles && n < 2; t += gridDim.x, ++n) {
+      int h, m0, n0;
+      tile_of(t, h, m0, n0);
+      for (int k = 0; k < C::kChunks; ++k) {
+        tma_prefetch_l2_2d(&tm_a, h * K + k * BK, m0);
+#pragma unroll
+        for (int j = 0; j < C::kBBlocks; ++j) tma_prefetch_l2_2d(&tm_w, n0 + 64 * j, h * K + k * BK);
+      }
+    }
+  }
   // a programmatic dependent of the previous kernel in the stream (the setup
   // above overlapped its tail): its results are read only once it has
   // finished; the next kernel may be scheduled from here on
@@ -114,8 +138,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_a);
-      tma_prefetch_desc(&tm_w);
       uint32_t c = 0;                              // chunk count over all tiles
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
