@@ -15,8 +15,11 @@
 //     each up to a load budget cap, so a request is cut only where a worker
 //     is full (at most W - 1 cuts, hence few partial states to merge), at a
 //     tile boundary of the request (only its last piece has a ragged tile);
-//   * no cut piece is shorter than kMinPieceTokens: with less space left the
-//     worker is closed, and a shorter tail stays with its head piece;
+//   * no cut piece is shorter than kMinPieceTokens and no worker's load
+//     exceeds cap: where the tail after the whole tiles that fit would be
+//     shorter, the cut moves one tile earlier (the tail piece then holds a
+//     whole tile besides its ragged one; a worker one tile over cap would be
+//     the step's slowest); with less space than that the worker is closed;
 //   * cap starts at ceil((total + (nonempty + W - 1) * overhead) / W) tokens,
 //     total counting every request in whole tiles, and grows by
 //     kCapStepTokens until the fill fits on W workers.
@@ -58,10 +61,12 @@ bool fill(const std::vector<long long>& len, int W, long long cap, long long ov,
       const long long space = cap - used - ov;
       const long long fit = space / kTileTokens * kTileTokens;   // whole tiles that fit
       long long take;
-      if (round_up_tile(rem) <= space || (fit >= kTileTokens && rem - fit < kMinPieceTokens)) {
+      if (round_up_tile(rem) <= space) {
         take = rem;
-      } else if (fit >= kMinPieceTokens) {
+      } else if (fit >= kMinPieceTokens && rem - fit >= kMinPieceTokens) {
         take = fit;
+      } else if (fit - kTileTokens >= kMinPieceTokens) {
+        take = fit - kTileTokens;                                  // the tail keeps a whole tile
       } else {
         ++w;
         used = 0;

@@ -21,9 +21,11 @@ contexts across SMs.  They give no rule, so this is the one the library uses:
     0, 1, ... in turn, each worker up to a load budget cap; a request is cut
     only where a worker is full, at a tile boundary of the request (so only
     its last piece can be ragged), and there are at most W - 1 cuts;
-  * no cut piece is shorter than MIN_PIECE tokens: with space < MIN_PIECE left
-    the worker is closed, and a tail shorter than MIN_PIECE stays with the
-    head piece (the worker then overshoots cap by < MIN_PIECE);
+  * no cut piece is shorter than MIN_PIECE tokens and no worker's load
+    exceeds cap: where the tail after the whole tiles that fit would be
+    shorter than MIN_PIECE, the cut moves one tile earlier (the tail piece
+    then holds a whole tile besides its ragged one); with less space than
+    that the worker is closed;
   * cap starts at ceil((total + (nonempty + W - 1) * overhead) / W) and
     grows by CAP_STEP tokens until the fill fits on the W workers;
   * partial slots are numbered over the cut requests in (b, piece) order; an
@@ -83,10 +85,12 @@ def _fill(lengths, W, cap, overhead):
             rem = t - k0
             space = cap - used - overhead
             fit = (space // TILE) * TILE if space > 0 else 0      # whole tiles that fit
-            if _round_up(rem) <= space or (fit >= TILE and rem - fit < MIN_PIECE):
+            if _round_up(rem) <= space:
                 take = rem
-            elif fit >= MIN_PIECE:
+            elif fit >= MIN_PIECE and rem - fit >= MIN_PIECE:
                 take = fit
+            elif fit - TILE >= MIN_PIECE:
+                take = fit - TILE                                  # the tail keeps a whole tile
             else:
                 w, used = w + 1, 0
                 continue

@@ -3,8 +3,8 @@
 The pages fix no chunking rule, only its job (cover every key once, balance
 long and short contexts across SMs), so these pins check that job: exact
 coverage, partial numbering, the merge list, and the wrap-around fill's
-bounds (in tokens, pieces costed in whole tiles): every worker's load within
-MIN_PIECE of the budget cap, cap within 2 MIN_PIECE + CAP_STEP of the ideal
+bounds (in tokens, pieces costed in whole tiles): no worker's load above the
+budget cap, cap within 2 MIN_PIECE + CAP_STEP of the ideal
 ceil((total + items) / W), cuts only at tile boundaries of the request, no
 cut piece shorter than MIN_PIECE, and at most W - 1 cuts.
 """
@@ -37,7 +37,7 @@ def _check(indptr, H, sms):
     assert d["wptr"][0] == 0 and d["wptr"][-1] == d["n"]
     assert all(a <= b for a, b in zip(d["wptr"], d["wptr"][1:]))
     ov = PR.ITEM_OVERHEAD[d["variant"]]
-    items_max = c - ov + PR.MIN_PIECE if c else 0   # tokens
+    items_max = c - ov if c else 0                 # tokens
     # exact coverage of each request's keys
     cover = {b: [] for b in range(B)}
     parts = {}
@@ -84,7 +84,7 @@ def _check(indptr, H, sms):
     if total:
         ideal = -(-(total + (nonempty + d["W"] - 1) * ov) // d["W"])
         assert ideal <= c <= ideal + 2 * PR.MIN_PIECE + PR.CAP_STEP
-        assert max(loads) <= c + PR.MIN_PIECE
+        assert max(loads) <= c
         cuts = sum(len(cover[b]) - 1 for b in range(B) if lengths[b] > 0)
         assert cuts <= d["W"] - 1 and d["P"] <= 2 * cuts
         for b in range(B):
