@@ -483,6 +483,23 @@ int mla_append_kv_fp8(void* kv_cache, int64_t num_slots, const int32_t* slots, c
  * MLA_ERR_CUDA if the stream reports a CUDA error. */
 int mla_check_errors(void* workspace, void* stream);
 
+/* mla_probe_wait_limit -- asynchronous on `stream`.  A diagnostic of the
+ * failure handling, not part of a decode.
+ *
+ * Every device-side wait of the kernels above is bounded: after about 1 s of
+ * wall time it gives up, the kernel records MLA_ERR_TIMEOUT in the workspace
+ * status word and returns, so a stalled pipeline becomes a status code, not a
+ * hung GPU.  This launches one warp whose first thread waits, with that same
+ * bounded wait, on a shared-memory barrier that nothing completes: after the
+ * limit the status word holds MLA_ERR_TIMEOUT (read and clear it with
+ * mla_check_errors) and the context stays usable.  Nothing but the status
+ * word is written.
+ *
+ *   workspace  device, at least 4 bytes, 16-byte aligned (a decode workspace).
+ * Errors: MLA_ERR_INVALID_ARG for a null or misaligned workspace; nothing is
+ * launched then. */
+int mla_probe_wait_limit(void* workspace, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,8 @@ EXPORTS = ("mla_status_string", "mla_abi_version", "mla_decode_plan", "mla_decod
            "mla_decode_run_noalloc", "mla_absorb_query", "mla_project_output",
            "mla_append_kv", "mla_step_staging_bytes", "mla_decode_step_host", "mla_decode_run_multi_query",
            "mla_merge_two_states", "mla_decode_fp8_workspace_bytes", "mla_decode_run_fp8", "mla_append_kv_fp8",
-           "mla_decode_graph_sizes", "mla_decode_run_graph", "mla_noalloc_check_errors", "mla_decode_run_tree")
+           "mla_decode_graph_sizes", "mla_decode_run_graph", "mla_noalloc_check_errors", "mla_decode_run_tree",
+           "mla_probe_wait_limit")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 if not os.path.exists(LIB_PATH):
@@ -61,6 +62,8 @@ _lib.mla_check_errors.restype = ctypes.c_int
 _lib.mla_check_errors.argtypes = [_vp, _vp]
 _lib.mla_noalloc_check_errors.restype = ctypes.c_int
 _lib.mla_noalloc_check_errors.argtypes = [_vp]
+_lib.mla_probe_wait_limit.restype = ctypes.c_int
+_lib.mla_probe_wait_limit.argtypes = [_vp, _vp]
 _lib.mla_absorb_query.restype = ctypes.c_int
 _lib.mla_absorb_query.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]
 _lib.mla_decode_run_multi_query.restype = ctypes.c_int
@@ -405,6 +408,14 @@ def decode_step_host(q_nope, q_rope, kv_indptr, kv_indices, kv_cache, sm_scale, 
 def check_errors(workspace, stream=None) -> int:
     """Synchronise, read and clear the device status; returns the status code."""
     return int(_lib.mla_check_errors(_ptr(workspace), _stream_handle(stream)))
+
+
+def probe_wait_limit(workspace, stream=None) -> None:
+    """Launch the bounded-wait diagnostic: a wait that nothing completes gives up
+    after the kernels' wait limit and leaves MLA_ERR_TIMEOUT in the status word."""
+    st = _lib.mla_probe_wait_limit(_ptr(workspace), _stream_handle(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_probe_wait_limit")
 
 
 class Decoder:

@@ -219,6 +219,14 @@ def test_append_rejects_bad_arguments(B):
     assert lib.mla_append_kv(None, 100, None, None, 0, None, None) == 0
 
 
+def test_wait_probe_rejects_bad_arguments(B):
+    lib = B.library()
+    lib.mla_probe_wait_limit.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    fake = _fake_ptr()
+    assert lib.mla_probe_wait_limit(None, None) == 1
+    assert lib.mla_probe_wait_limit(fake + 4, None) == 1
+
+
 def test_merge_two_rejects_bad_arguments(B):
     lib = B.library()
     fake = _fake_ptr()
