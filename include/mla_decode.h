@@ -486,8 +486,8 @@ int mla_check_errors(void* workspace, void* stream);
 /* mla_probe_wait_limit -- asynchronous on `stream`.  A diagnostic of the
  * failure handling, not part of a decode.
  *
- * Every device-side wait of the kernels above is bounded: after about 1 s of
- * wall time it gives up, the kernel records MLA_ERR_TIMEOUT in the workspace
+ * Every mbarrier wait of the decode and head-product kernels above is bounded:
+ * after about 1 s of wall time it gives up, the kernel records MLA_ERR_TIMEOUT in the workspace
  * status word and returns, so a stalled pipeline becomes a status code, not a
  * hung GPU.  This launches one warp whose first thread waits, with that same
  * bounded wait, on a shared-memory barrier that nothing completes: after the

@@ -1,5 +1,5 @@
-// The failure path of the kernels' bounded waits, on its own.  Every decode,
-// merge and head-product kernel waits on its mbarriers through mbar_wait,
+// The failure path of the kernels' bounded waits, on its own.  Every decode
+// and head-product kernel waits on its mbarriers through mbar_wait,
 // which gives up after MLA_WAIT_LIMIT_NS of wall time, records
 // MLA_ERR_TIMEOUT in the workspace status word and lets the kernel return, so
 // a stalled pipeline ends as a status code instead of a hung GPU.  In those
