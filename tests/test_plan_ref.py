@@ -140,3 +140,18 @@ def test_unsupported_heads():
     for H in (0, 8, 24, 136, 256):
         with pytest.raises(ValueError):
             PR.build_plan([0, 5], H, 152)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_benchmark_workload_plans(n):
+    # the five workloads the bench and the parity tests use, at 152 SMs: every
+    # pin above, and the tiles per worker never above the budget's whole tiles
+    from mla_latent_kv_absorbed_gb300 import workloads
+    b = workloads.make_workload(n)
+    d = _check([int(x) for x in b.kv_indptr], b.heads, 152)
+    W, T = d["W"], d["T"]
+    ov = PR.ITEM_OVERHEAD[d["variant"]]
+    for w in range(W):
+        its = d["items"][d["wptr"][w]:d["wptr"][w + 1]]
+        tiles = sum(-(-(e - s) // T) for (_, s, e, _) in its)
+        assert tiles * T + len(its) * ov <= d["c"]
