@@ -31,7 +31,7 @@ def test_tiny_workload_full():
     assert dec.header[4] == 1   # few-heads kernel variant ran
 
 
-@pytest.mark.parametrize("H", [16, 32, 48, 64, 112, 128])
+@pytest.mark.parametrize("H", [16, 32, 48, 64, 80, 96, 112, 128])
 def test_ragged_tails_small(H):
     # lengths around the 128-token tile edges, plus an empty request
     bt = _batch([1, 2, 3, 127, 128, 129, 0, 255, 256, 257, 1000, 64], H, seed=H)

@@ -64,7 +64,7 @@ def test_fp8_every_request_empty(H):
     assert np.all(out == 0) and np.all(np.isneginf(lse))
 
 
-@pytest.mark.parametrize("H", [16, 32, 64, 128])
+@pytest.mark.parametrize("H", [16, 32, 48, 64, 96, 128])
 @pytest.mark.parametrize("lengths", [
     [1, 7, 33, 100],
     [63, 64, 65, 127, 128, 129, 0, 191],          # around the tile edges, an empty request
