@@ -263,3 +263,32 @@ def test_many_items_per_worker(H, num_sms):
     assert items / W > 64                        # the fallback is exercised
     ro, rl = oracle(bt)
     assert_close(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_rows_past_4_gib_of_the_pool(H):
+    # every row the batch reads sits above slot 2^22 of a 4.8 GB pool (byte
+    # offsets past 2^32); the result equals the oracle on the compact pool
+    # (the slot numbers are only names), and an append past 2^22 lands exactly
+    import torch
+    from mla_latent_kv_absorbed_gb300 import binding
+    bt = _batch([300, 5, 1000, 64], H, seed=77 + H)
+    dev = to_device(bt)
+    base, big = 1 << 22, (1 << 22) + 4096
+    used = np.unique(bt.kv_indices)
+    assert used.size < big - base
+    mapping = np.full(bt.kv_cache.shape[0], -1, dtype=np.int64)
+    mapping[used] = base + np.arange(used.size)
+    pool = torch.zeros((big, 576), dtype=torch.bfloat16, device="cuda")
+    pool[torch.from_numpy(mapping[used]).cuda()] = dev["kv_cache"][torch.from_numpy(used.astype(np.int64)).cuda()]
+    moved = dict(dev, kv_cache=pool, kv_indices=torch.from_numpy(mapping[bt.kv_indices].astype(np.int32)).cuda())
+    (out, lse), _ = run_gpu(bt, dev=moved)
+    ro, rl = oracle(bt)
+    assert_close(out, lse, ro, rl)
+
+    rows = torch.randn((2, 576), device="cuda").to(torch.bfloat16)
+    slots = torch.tensor([big - 1, base + used.size], dtype=torch.int32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    binding.append_kv(pool, slots, rows, ws)
+    assert binding.check_errors(ws) == 0
+    assert torch.equal(pool[big - 1], rows[0]) and torch.equal(pool[base + used.size], rows[1])

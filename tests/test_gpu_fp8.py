@@ -27,7 +27,7 @@ def _bf16_to_f32(bits):
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def _run_fp8(bt, qn, qr, codes, indices, kv_scale, out_dtype="f32", repeat=1, num_sms=0):
+def _run_fp8(bt, qn, qr, codes, indices, kv_scale, out_dtype="f32", repeat=1, num_sms=0, kv_dev=None):
     import torch
     from mla_latent_kv_absorbed_gb300 import binding
     H, B = bt.heads, bt.batch
@@ -35,7 +35,7 @@ def _run_fp8(bt, qn, qr, codes, indices, kv_scale, out_dtype="f32", repeat=1, nu
     plan_d = torch.from_numpy(plan).cuda()
     ws = torch.zeros(binding.decode_fp8_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-    kv = torch.from_numpy(np.ascontiguousarray(codes)).cuda()
+    kv = kv_dev if kv_dev is not None else torch.from_numpy(np.ascontiguousarray(codes)).cuda()
     ptr = torch.from_numpy(bt.kv_indptr.astype(np.int32)).cuda()
     idx = torch.from_numpy(indices if indices.size else np.zeros(1, np.int32)).cuda()
     q_n, q_r = bf(qn), bf(qr)
@@ -191,3 +191,22 @@ def test_fp8_full_size_v3_sampled():
     ro, rl = _oracle(bt, bt.q_nope, bt.q_rope, codes, bt.kv_indices, W.FP8_KV_SCALE, requests=reqs)
     assert_close(out, lse, ro, rl, requests=reqs)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_fp8_rows_past_4_gib_of_the_pool(H):
+    # every row the batch reads sits above slot 2^23 of a 4.8 GB FP8 pool (byte
+    # offsets past 2^32); the result equals the oracle on the compact pool
+    import torch
+    from mla_latent_kv_absorbed_gb300 import workloads as W
+    bt, qn, qr, codes, idx = _fp8_case([300, 5, 1000, 64], H, seed=610 + H)
+    base, big = 1 << 23, (1 << 23) + 4096
+    used = np.unique(idx)
+    assert used.size < big - base
+    mapping = np.full(codes.shape[0], -1, dtype=np.int64)
+    mapping[used] = base + np.arange(used.size)
+    pool = torch.zeros((big, 576), dtype=torch.uint8, device="cuda")
+    pool[torch.from_numpy(mapping[used]).cuda()] = torch.from_numpy(np.ascontiguousarray(codes[used])).cuda()
+    out, lse = _run_fp8(bt, qn, qr, codes, mapping[idx].astype(np.int32), W.FP8_KV_SCALE, kv_dev=pool)
+    ro, rl = _oracle(bt, qn, qr, codes, idx, W.FP8_KV_SCALE)
+    assert_close(out, lse, ro, rl)
